@@ -1,0 +1,336 @@
+/*
+ * moe_oracle.c -- plain, slow, CPU reference of the MoE tree-verification layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg may load this library. It shares no code, header
+ * or table with the CUDA path, and the CUDA path never calls it.
+ *
+ * Sources (page title + section):
+ *   [LAYER]  "MoE and speculative decoding: joint optimisation of compute,
+ *            communication and acceptance" (blog), section "starting from one MoE
+ *            layer": E(x) = TopR(softmax(W_r x)), y = sum_{e in E(x)} g_e(x) E_e(x),
+ *            and the router -> permute/group -> grouped GEMM -> unpermute+combine
+ *            pipeline.
+ *   [UNION]  same blog, section "dense vs MoE verification": the working set of a
+ *            verification is the union of the experts chosen by its tokens.
+ *   [ACCEPT] "AcceptMoE" news article, section 02: commitment probability per draft
+ *            position weights the target router scores; the root node's natural
+ *            top-k is kept (root anchor); the set size follows the effective rank of
+ *            the demand distribution; residency-aware pruning removes low-demand
+ *            non-resident experts within a rerouting budget and a minimum set size.
+ *   [ABS]    AcceptMoE abstract (arXiv 2608.02989): a verifier-side selector that
+ *            combines target-router scores with offline commitment probabilities,
+ *            sizes the eligible set per verification block, and constrains
+ *            target-expert eligibility (re-route inside the eligible set).
+ *
+ * The pages give the method in prose only. Where a step is left open, the reading
+ * taken is stated at the step (demand D_e = sum_n c(depth_n) softmax(l_n)_e,
+ * m = max(k, ceil(exp H)) capped at the pool size, pool = natural union, prune in
+ * ascending demand with a count budget, gates renormalised over the chosen k).
+ *
+ * Precision: every floating-point step runs in fp64 on inputs upcast exactly from
+ * fp32/bf16. Decisions that compare router logits (top-k) take them in fp32, the
+ * precision the logits have on the device, so both sides decide on equal values.
+ *
+ * Parity unpinned: the exact integer rounding of exp(H) and the candidate-pool rule
+ * used by the AcceptMoE authors (the pages print no worked selection example).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_API __attribute__((visibility("default")))
+
+enum { ORC_NATURAL = 0, ORC_ACCEPT = 1, ORC_FIXED_B = 2 };
+
+/* bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word. */
+static double elem(const void *p, int dtype, size_t i) {
+    if (dtype == 0) return (double)((const float *)p)[i];
+    uint32_t u = ((uint32_t)((const uint16_t *)p)[i]) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* [LAYER] router scores l = W_r x, one row per token; no bias. */
+ORC_API void oracle_router(const void *x, const void *Wr, int dtype, int R, int d, int E,
+                           double *logits) {
+    for (int n = 0; n < R; ++n)
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int i = 0; i < d; ++i)
+                s += elem(x, dtype, (size_t)n * d + i) * elem(Wr, dtype, (size_t)e * d + i);
+            logits[(size_t)n * E + e] = s;
+        }
+}
+
+/* [LAYER] TopR: the k largest scores of one row, in descending order, ties to the
+ * lower expert id. softmax is monotone, so top-k of the probabilities is top-k of
+ * the logits. `allowed` (may be NULL) restricts the candidates. Returns the gap
+ * between the k-th chosen score and the best score left out (+inf if none left). */
+static double topk_row(const float *l, int E, int k, const unsigned char *allowed, int *out) {
+    unsigned char taken[1024];
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            if ((allowed && !allowed[e]) || taken[e]) continue;
+            if (best < 0 || l[e] > l[best]) best = e;
+        }
+        out[j] = best;
+        if (best >= 0) taken[best] = 1;
+    }
+    int rest = -1;
+    for (int e = 0; e < E; ++e) {
+        if ((allowed && !allowed[e]) || taken[e]) continue;
+        if (rest < 0 || l[e] > l[rest]) rest = e;
+    }
+    if (rest < 0 || out[k - 1] < 0) return INFINITY;
+    return (double)l[out[k - 1]] - (double)l[rest];
+}
+
+ORC_API double oracle_topk(const float *logits, int R, int E, int k, int *idx) {
+    double margin = INFINITY;
+    for (int n = 0; n < R; ++n) {
+        double g = topk_row(logits + (size_t)n * E, E, k, NULL, idx + (size_t)n * k);
+        if (g < margin) margin = g;
+    }
+    return margin;
+}
+
+/* softmax of one row of fp32 logits in fp64: exp(l_e - max) / sum_e' exp(l_e' - max),
+ * the sum taken in ascending expert order. */
+static void softmax_row(const float *l, int E, double *p) {
+    double mx = l[0], s = 0.0;
+    for (int e = 1; e < E; ++e)
+        if (l[e] > mx) mx = l[e];
+    for (int e = 0; e < E; ++e) {
+        p[e] = exp((double)l[e] - mx);
+        s += p[e];
+    }
+    for (int e = 0; e < E; ++e) p[e] /= s;
+}
+
+/* Order used by the fill and by pruning: a before b when D_a > D_b (descending), or
+ * equal demand and lower id. */
+static int before_desc(const double *D, int a, int b) {
+    return D[a] > D[b] || (D[a] == D[b] && a < b);
+}
+
+/* Selection for one draft tree of N nodes (node 0 is the root).
+ *
+ * Steps ([ACCEPT] + [ABS]):
+ *  1. natural top-k per node; natural union U.
+ *  2. demand D_e = sum_n c(depth_n) * softmax(l_n)_e, nodes in ascending order;
+ *     c(depth) beyond the table repeats the last entry.
+ *  3. effective rank r = exp(H(D / sum D)), H = -sum q ln q over all E experts.
+ *     m = max(k, ceil(r)) (a value within 1e-9 relative of an integer counts as that
+ *     integer), capped at the pool size. FIXED_B takes m = max(k, fixed_B) instead.
+ *  4. root anchor A = natural top-k of node 0 (when `anchor`); S = A plus the best
+ *     m - |A| experts of pool \ A in (D desc, id asc) order. pool = U, or all experts.
+ *  5. residency-aware pruning (when `prune`): members of S \ A that are not resident
+ *     are removed in (D asc, id asc) order while fewer than `budget` have been
+ *     removed and |S| > max(min_set, k).
+ *  6. restricted top-k: each node takes its k best logits inside S, gates are the
+ *     softmax over the k chosen logits. NATURAL: S = all experts.
+ *
+ * info[0..3] = |U|, |union of restricted choices|, |S| after step 4 (m), removed.
+ * margins[0] = smallest top-k gap (fp32 logits, natural), margins[1] = relative
+ * distance of r to the nearest integer, margins[2] = relative demand gap at the
+ * fill cut, margins[3] = relative demand gap at the prune cut, margins[4] =
+ * smallest restricted top-k gap. Returns 0, or -1 on bad arguments. */
+ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int E, int k,
+                               const double *c, int n_c, int mode, int pool_all, int anchor,
+                               int prune, const unsigned char *resident, int budget,
+                               int min_set, int fixed_B, int *idx, double *gates,
+                               unsigned char *eligible, int *info, double *D, double *margins) {
+    if (N < 1 || E < 1 || E > 1024 || k < 1 || k > E || n_c < 1) return -1;
+    int *nat = (int *)malloc(sizeof(int) * (size_t)N * k);
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    unsigned char inU[1024], inS[1024], inA[1024];
+    for (int m = 0; m < 5; ++m) margins[m] = INFINITY;
+
+    /* 1. natural top-k and union */
+    memset(inU, 0, (size_t)E);
+    for (int n = 0; n < N; ++n) {
+        double g = topk_row(logits + (size_t)n * E, E, k, NULL, nat + (size_t)n * k);
+        if (g < margins[0]) margins[0] = g;
+        for (int j = 0; j < k; ++j) inU[nat[(size_t)n * k + j]] = 1;
+    }
+    int U = 0;
+    for (int e = 0; e < E; ++e) U += inU[e];
+    info[0] = U;
+    info[3] = 0;
+
+    if (mode == ORC_NATURAL) {
+        memset(inS, 1, (size_t)E);
+        info[2] = E;
+    } else {
+        /* 2. commitment-weighted demand */
+        for (int e = 0; e < E; ++e) D[e] = 0.0;
+        for (int n = 0; n < N; ++n) {
+            int t = depth[n] < n_c ? depth[n] : n_c - 1;
+            softmax_row(logits + (size_t)n * E, E, p);
+            for (int e = 0; e < E; ++e) D[e] += c[t] * p[e];
+        }
+        /* 3. effective rank and set size */
+        int pool = pool_all ? E : U;
+        int m;
+        if (mode == ORC_ACCEPT) {
+            double sum = 0.0, H = 0.0;
+            for (int e = 0; e < E; ++e) sum += D[e];
+            for (int e = 0; e < E; ++e) {
+                double q = D[e] / sum;
+                if (q > 0.0) H -= q * log(q);
+            }
+            double r = exp(H);
+            double rn = nearbyint(r);
+            margins[1] = fabs(r - rn) / r;
+            m = (fabs(r - rn) <= 1e-9 * r) ? (int)rn : (int)ceil(r);
+        } else {
+            m = fixed_B;
+        }
+        if (m < k) m = k;
+        if (m > pool) m = pool;
+        /* 4. anchor + fill */
+        memset(inA, 0, (size_t)E);
+        memset(inS, 0, (size_t)E);
+        int size = 0;
+        if (anchor)
+            for (int j = 0; j < k; ++j) {
+                inA[nat[j]] = 1;
+                inS[nat[j]] = 1;
+            }
+        for (int e = 0; e < E; ++e) size += inS[e];
+        int last = -1;
+        while (size < m) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (inS[e] || !(pool_all || inU[e])) continue;
+                if (best < 0 || before_desc(D, e, best)) best = e;
+            }
+            inS[best] = 1;
+            last = best;
+            ++size;
+        }
+        if (last >= 0) {
+            int next = -1;
+            for (int e = 0; e < E; ++e) {
+                if (inS[e] || !(pool_all || inU[e])) continue;
+                if (next < 0 || before_desc(D, e, next)) next = e;
+            }
+            if (next >= 0) margins[2] = (D[last] - D[next]) / D[last];
+        }
+        info[2] = size;
+        /* 5. residency-aware pruning */
+        if (prune && resident) {
+            int floor_ = min_set > k ? min_set : k;
+            int removed = 0, lastr = -1;
+            for (;;) {
+                int worst = -1;
+                for (int e = 0; e < E; ++e) {
+                    if (!inS[e] || inA[e] || resident[e]) continue;
+                    if (worst < 0 || before_desc(D, worst, e)) worst = e;
+                }
+                if (worst < 0) break;
+                if (removed >= budget || size <= floor_) {
+                    if (lastr >= 0) margins[3] = (D[worst] - D[lastr]) / D[worst];
+                    break;
+                }
+                inS[worst] = 0;
+                --size;
+                ++removed;
+                lastr = worst;
+            }
+            info[3] = removed;
+        }
+    }
+
+    /* 6. restricted top-k and renormalised gates */
+    memset(inU, 0, (size_t)E);
+    for (int n = 0; n < N; ++n) {
+        const float *l = logits + (size_t)n * E;
+        int *o = idx + (size_t)n * k;
+        double g = topk_row(l, E, k, inS, o);
+        if (g < margins[4]) margins[4] = g;
+        double mx = l[o[0]], s = 0.0;
+        for (int j = 0; j < k; ++j) {
+            gates[(size_t)n * k + j] = exp((double)l[o[j]] - mx);
+            s += gates[(size_t)n * k + j];
+        }
+        for (int j = 0; j < k; ++j) gates[(size_t)n * k + j] /= s;
+        for (int j = 0; j < k; ++j) inU[o[j]] = 1;
+    }
+    int Us = 0;
+    for (int e = 0; e < E; ++e) Us += inU[e];
+    info[1] = Us;
+    for (int e = 0; e < E; ++e) eligible[e] = inS[e];
+    free(nat);
+    free(p);
+    return 0;
+}
+
+/* [LAYER] permute / group by expert: a stable counting sort of the assignments
+ * (row r, slot j) -> expert idx[r*k+j] with key (expert, row, slot). counts[e] is the
+ * number of assignments of expert e, offsets[e] its exclusive prefix (offsets[E] =
+ * R*k), perm[p] the assignment id r*k+j at permuted position p. */
+ORC_API void oracle_permute(const int *idx, int R, int k, int E, int *counts, int *offsets,
+                            int *perm) {
+    int *cur = (int *)calloc((size_t)E, sizeof(int));
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int a = 0; a < R * k; ++a) counts[idx[a]]++;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    for (int r = 0; r < R; ++r)
+        for (int j = 0; j < k; ++j) {
+            int e = idx[r * k + j];
+            perm[offsets[e] + cur[e]++] = r * k + j;
+        }
+    free(cur);
+}
+
+/* [LAYER] one routed expert E_e(x) as a SwiGLU FFN:
+ *   a = W_gate[e] x, b = W_up[e] x, h = silu(a) * b, out = W_down[e] h,
+ * silu(a) = a / (1 + exp(-a)). W_gate, W_up are [E, f, d]; W_down is [E, d, f]. */
+ORC_API void oracle_expert_ffn(const double *x, int e, const void *Wg, const void *Wu,
+                               const void *Wd, int dtype, int d, int f, double *out) {
+    double *h = (double *)malloc(sizeof(double) * (size_t)f);
+    size_t base_gu = (size_t)e * f * d, base_d = (size_t)e * d * f;
+    for (int i = 0; i < f; ++i) {
+        double a = 0.0, b = 0.0;
+        for (int t = 0; t < d; ++t) {
+            a += elem(Wg, dtype, base_gu + (size_t)i * d + t) * x[t];
+            b += elem(Wu, dtype, base_gu + (size_t)i * d + t) * x[t];
+        }
+        h[i] = a / (1.0 + exp(-a)) * b;
+    }
+    for (int t = 0; t < d; ++t) {
+        double s = 0.0;
+        for (int i = 0; i < f; ++i) s += elem(Wd, dtype, base_d + (size_t)t * f + i) * h[i];
+        out[t] = s;
+    }
+    free(h);
+}
+
+/* [LAYER] y_r = sum_j g_{r,j} E_{idx_{r,j}}(x_r), slots in ascending order, for the
+ * rows listed in `rows` (all R rows when rows == NULL). y is [n_rows, d]. */
+ORC_API void oracle_moe_combine(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                                int dtype, int d, int f, const int *idx, const double *gates,
+                                int k, const int *rows, int n_rows, double *y) {
+    double *xr = (double *)malloc(sizeof(double) * (size_t)d);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int q = 0; q < n_rows; ++q) {
+        int r = rows ? rows[q] : q;
+        for (int t = 0; t < d; ++t) xr[t] = elem(x, dtype, (size_t)r * d + t);
+        double *yr = y + (size_t)q * d;
+        for (int t = 0; t < d; ++t) yr[t] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            oracle_expert_ffn(xr, idx[(size_t)r * k + j], Wg, Wu, Wd, dtype, d, f, o);
+            double g = gates[(size_t)r * k + j];
+            for (int t = 0; t < d; ++t) yr[t] += g * o[t];
+        }
+    }
+    free(xr);
+    free(o);
+}

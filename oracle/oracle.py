@@ -1,0 +1,200 @@
+"""ctypes wrapper around the plain-C oracle (moe_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package smoke check and
+by the benchmark's CPU-baseline leg. The product path never imports it.
+
+The wrapper only marshals numpy arrays into the C functions and composes them in
+the layer's order (router -> top-k -> selection per tree -> permute -> experts ->
+combine); all arithmetic is in moe_oracle.c.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "moe_oracle.c")
+LIB = os.path.join(HERE, "libmoe_oracle.so")
+
+NATURAL, ACCEPT, FIXED_B = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with plain gcc (no fast-math, no vectorisation flags)."""
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fvisibility=hidden",
+                        "-o", tmp, SRC, "-lm"], check=True)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = C.CDLL(build())
+        P = C.c_void_p
+        i = C.c_int
+        _lib.oracle_router.argtypes = [P, P, i, i, i, i, P]
+        _lib.oracle_router.restype = None
+        _lib.oracle_topk.argtypes = [P, i, i, i, P]
+        _lib.oracle_topk.restype = C.c_double
+        _lib.oracle_select_tree.argtypes = [P, P, i, i, i, P, i, i, i, i, i, P, i, i, i,
+                                            P, P, P, P, P, P]
+        _lib.oracle_select_tree.restype = i
+        _lib.oracle_permute.argtypes = [P, i, i, i, P, P, P]
+        _lib.oracle_permute.restype = None
+        _lib.oracle_expert_ffn.argtypes = [P, i, P, P, P, i, i, i, P]
+        _lib.oracle_expert_ffn.restype = None
+        _lib.oracle_moe_combine.argtypes = [P, P, P, P, i, i, i, P, P, i, P, i, P]
+        _lib.oracle_moe_combine.restype = None
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _raw(t):
+    """A C-contiguous numpy view of a torch tensor or numpy array plus its dtype code
+    (0 = fp32, 1 = bf16 as raw uint16 bits)."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().cpu().contiguous()
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16), 1
+            return t.to(torch.float32).numpy(), 0
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(t)
+    if a.dtype == np.uint16:
+        return a, 1
+    return a.astype(np.float32, copy=False), 0
+
+
+def router(x, Wr) -> np.ndarray:
+    """fp64 router logits [R, E]."""
+    xa, dt = _raw(x)
+    wa, dt2 = _raw(Wr)
+    assert dt == dt2
+    R, d = xa.shape
+    E = wa.shape[0]
+    out = np.empty((R, E), dtype=np.float64)
+    lib().oracle_router(_p(xa), _p(wa), dt, R, d, E, _p(out))
+    return out
+
+
+def topk(logits: np.ndarray, k: int):
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    R, E = l.shape
+    idx = np.empty((R, k), dtype=np.int32)
+    margin = lib().oracle_topk(_p(l), R, E, k, _p(idx))
+    return idx, margin
+
+
+def select_tree(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float],
+                mode: int = ACCEPT, pool_all: bool = False, anchor: bool = True,
+                prune: bool = False, resident: Optional[np.ndarray] = None,
+                budget: int = 8, min_set: int = 16, fixed_B: int = 0) -> Dict:
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    N, E = l.shape
+    dep = np.ascontiguousarray(depth, dtype=np.int32)
+    cc = np.ascontiguousarray(np.asarray(c, dtype=np.float64))
+    res = None if resident is None else np.ascontiguousarray(resident, dtype=np.uint8)
+    idx = np.empty((N, k), dtype=np.int32)
+    gates = np.empty((N, k), dtype=np.float64)
+    elig = np.empty(E, dtype=np.uint8)
+    info = np.empty(4, dtype=np.int32)
+    D = np.zeros(E, dtype=np.float64)
+    margins = np.empty(5, dtype=np.float64)
+    rc = lib().oracle_select_tree(_p(l), _p(dep), N, E, k, _p(cc), len(cc), mode,
+                                  int(pool_all), int(anchor), int(prune), _p(res), budget,
+                                  min_set, fixed_B, _p(idx), _p(gates), _p(elig), _p(info),
+                                  _p(D), _p(margins))
+    if rc != 0:
+        raise ValueError("oracle_select_tree: bad arguments")
+    return dict(idx=idx, gates=gates, eligible=elig, union_nat=int(info[0]),
+                union_sel=int(info[1]), m=int(info[2]), pruned=int(info[3]), D=D,
+                margin_topk=margins[0], margin_rank=margins[1], margin_fill=margins[2],
+                margin_prune=margins[3], margin_restricted=margins[4])
+
+
+def select_block(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float],
+                 **kw) -> Dict:
+    """Selection for B trees: logits [B*N, E], depth [B, N]. Per-tree results stacked."""
+    dep = np.atleast_2d(depth)
+    B, N = dep.shape
+    outs = [select_tree(logits[b * N:(b + 1) * N], dep[b], k, c, **kw) for b in range(B)]
+    res = dict(idx=np.concatenate([o["idx"] for o in outs]),
+               gates=np.concatenate([o["gates"] for o in outs]),
+               eligible=np.stack([o["eligible"] for o in outs]))
+    for key in ("union_nat", "union_sel", "m", "pruned"):
+        res[key] = np.array([o[key] for o in outs], dtype=np.int32)
+    for key in ("margin_topk", "margin_rank", "margin_fill", "margin_prune", "margin_restricted"):
+        res[key] = min(o[key] for o in outs)
+    res["D"] = np.stack([o["D"] for o in outs])
+    return res
+
+
+def permute(idx: np.ndarray, E: int):
+    a = np.ascontiguousarray(idx, dtype=np.int32)
+    R, k = a.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    perm = np.empty(R * k, dtype=np.int32)
+    lib().oracle_permute(_p(a), R, k, E, _p(counts), _p(offsets), _p(perm))
+    return counts, offsets, perm
+
+
+def expert_ffn(x_row: np.ndarray, e: int, Wg, Wu, Wd) -> np.ndarray:
+    g, dt = _raw(Wg)
+    u, _ = _raw(Wu)
+    w, _ = _raw(Wd)
+    E, f, d = g.shape
+    xr = np.ascontiguousarray(x_row, dtype=np.float64)
+    out = np.empty(d, dtype=np.float64)
+    lib().oracle_expert_ffn(_p(xr), e, _p(g), _p(u), _p(w), dt, d, f, _p(out))
+    return out
+
+
+def moe_combine(x, Wg, Wu, Wd, idx: np.ndarray, gates: np.ndarray,
+                rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """y [n_rows, d] (fp64) for the given routing."""
+    xa, dt = _raw(x)
+    g, dt2 = _raw(Wg)
+    u, _ = _raw(Wu)
+    w, _ = _raw(Wd)
+    assert dt == dt2
+    R, d = xa.shape
+    f = g.shape[1]
+    k = idx.shape[1]
+    ia = np.ascontiguousarray(idx, dtype=np.int32)
+    ga = np.ascontiguousarray(gates, dtype=np.float64)
+    ra = None if rows is None else np.ascontiguousarray(np.asarray(rows), dtype=np.int32)
+    n = R if rows is None else len(ra)
+    y = np.empty((n, d), dtype=np.float64)
+    lib().oracle_moe_combine(_p(xa), _p(g), _p(u), _p(w), dt, d, f, _p(ia), _p(ga), k, _p(ra),
+                             n, _p(y))
+    return y
+
+
+def forward(x, Wr, Wg, Wu, Wd, depth: np.ndarray, k: int, c: Sequence[float],
+            rows: Optional[Sequence[int]] = None, **select_kw) -> Dict:
+    """The whole layer: router (fp64, rounded to fp32 for the decisions) ->
+    per-tree selection -> permute -> gated expert outputs for `rows`."""
+    logits64 = router(x, Wr)
+    l32 = logits64.astype(np.float32)
+    E = l32.shape[1]
+    sel = select_block(l32, depth, k, c, **select_kw)
+    counts, offsets, perm = permute(sel["idx"], E)
+    y = moe_combine(x, Wg, Wu, Wd, sel["idx"], sel["gates"], rows=rows)
+    sel.update(logits=logits64, logits32=l32, counts=counts, offsets=offsets, perm=perm, y=y)
+    return sel

@@ -1,0 +1,339 @@
+"""Pins for the CPU oracle: worked examples, closed forms, brute force, invariants.
+
+Each check ties the oracle to something other than itself: values printed on the
+pages (tests/golden), closed forms (MoESD notes section 5.3, softmax/entropy of
+structured inputs), library routines (torch fp64 matmul, torch silu, scipy
+softmax), and brute-force enumeration on tiny inputs.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax as sp_softmax
+
+from expert_select_gb300 import workload as W
+from oracle import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read(name):
+    out = []
+    with open(os.path.join(GOLD, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append(line.split())
+    return out
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_worked_example_a_union_counts_reuse():
+    rows = _read("worked_example_a.txt")
+    E = int(next(r[1] for r in rows if r[0] == "E"))
+    k = int(next(r[1] for r in rows if r[0] == "k"))
+    sets = [[int(v) for v in r[1:]] for r in rows if r[0] == "row"]
+    idx, _ = O.topk(W.routing_from_sets(sets, E), k)
+    for r, s in enumerate(sets):
+        assert sorted(idx[r].tolist()) == sorted(s)
+    counts, offsets, perm = O.permute(idx, E)
+    union = int((counts > 0).sum())
+    assert int(counts.sum()) == int(next(r[1] for r in rows if r[0] == "expect_assignments"))
+    assert union == int(next(r[1] for r in rows if r[0] == "expect_union"))
+    for r in rows:
+        if r[0] == "expect_count":
+            assert counts[int(r[1])] == int(r[2])
+    reuse = 1.0 - union / float(idx.size)
+    assert reuse == pytest.approx(float(next(r[1] for r in rows if r[0] == "expect_reuse")))
+    # the natural-mode selection reports the same union
+    sel = O.select_tree(W.routing_from_sets(sets, E), np.array([0, 1, 1, 1]), k, [1.0],
+                        mode=O.NATURAL)
+    assert sel["union_nat"] == union == sel["union_sel"]
+    dis = [[int(v) for v in r[1:]] for r in rows if r[0] == "disjoint_row"]
+    didx, _ = O.topk(W.routing_from_sets(dis, E), k)
+    dc, _, _ = O.permute(didx, E)
+    assert int((dc > 0).sum()) == int(next(r[1] for r in rows if r[0] == "expect_disjoint_union"))
+
+
+def test_worked_example_b_tree_union():
+    rows = _read("worked_example_b.txt")
+    E = int(next(r[1] for r in rows if r[0] == "E"))
+    k = int(next(r[1] for r in rows if r[0] == "k"))
+    nodes = [r for r in rows if r[0] == "node"]
+    sets = [[int(v) for v in r[3:]] for r in nodes]
+    idx, _ = O.topk(W.routing_from_sets(sets, E), k)
+    counts, _, _ = O.permute(idx, E)
+    assert int((counts > 0).sum()) == int(next(r[1] for r in rows if r[0] == "expect_union"))
+    for r in rows:
+        if r[0] == "expect_count":
+            assert counts[int(r[1])] == int(r[2])
+
+
+# ------------------------------------------------------------------ closed forms
+
+@pytest.mark.parametrize("E,K,t", [(16, 2, 4), (16, 2, 5), (16, 2, 9), (128, 8, 65), (128, 4, 65)])
+def test_union_expectation_closed_form(E, K, t):
+    """MoESD notes section 5.3: with every token choosing K of E experts uniformly,
+    the expected number of distinct experts after t tokens is E[1-((E-K)/E)^t].
+    i.i.d. Gaussian logits make each natural top-K a uniform K-subset."""
+    trials = 3000 if E == 16 else 600
+    rng = np.random.Generator(np.random.PCG64(1234 + E + K + t))
+    logits = rng.standard_normal((trials * t, E)).astype(np.float32)
+    unions = np.empty(trials)
+    for i in range(trials):
+        sel = O.select_tree(logits[i * t:(i + 1) * t], np.zeros(t, np.int32), K, [1.0],
+                            mode=O.NATURAL)
+        unions[i] = sel["union_nat"]
+    expect = E * (1.0 - ((E - K) / E) ** t)
+    se = unions.std(ddof=1) / math.sqrt(trials)
+    assert abs(unions.mean() - expect) < 4.0 * se + 1e-9, (unions.mean(), expect, se)
+
+
+def test_router_matches_torch_fp64():
+    g = torch.Generator().manual_seed(7)
+    for dt in (torch.float32, torch.bfloat16):
+        x = torch.randn(7, 96, generator=g).to(dt)
+        w = (torch.randn(12, 96, generator=g) * 0.05).to(dt)
+        ref = (x.double() @ w.double().T).numpy()
+        got = O.router(x, w)
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.Generator(np.random.PCG64(5))
+    for trial in range(50):
+        E, k = int(rng.integers(3, 24)), None
+        k = int(rng.integers(1, E + 1))
+        # coarse values force ties; ties must go to the lower expert id
+        l = np.round(rng.standard_normal((6, E)) * 2) .astype(np.float32)
+        idx, _ = O.topk(l, k)
+        for r in range(6):
+            ref = sorted(range(E), key=lambda e: (-float(l[r, e]), e))[:k]
+            assert idx[r].tolist() == ref
+
+
+def _one_hot_logits(hot, E):
+    """Rows whose softmax is exactly one-hot in fp64 (exp(-1000) underflows to 0)."""
+    l = np.full((len(hot), E), -1000.0, dtype=np.float32)
+    for r, e in enumerate(hot):
+        l[r, e] = 0.0
+    return l
+
+
+def test_demand_one_hot_closed_form_and_depth_table():
+    """One-hot routing makes D_e = sum of c(depth_n) over the nodes routed to e,
+    and depths past the end of the commitment table use its last entry."""
+    E, k = 12, 1
+    c = [1.0, 0.5, 0.25]
+    depth = np.array([0, 1, 1, 2, 3, 7, 2], dtype=np.int32)
+    hot = [3, 5, 5, 3, 9, 9, 0]
+    sel = O.select_tree(_one_hot_logits(hot, E), depth, k, c, mode=O.ACCEPT, pool_all=True)
+    ct = [c[min(t, 2)] for t in depth]
+    expect = np.zeros(E)
+    for n, e in enumerate(hot):
+        expect[e] += ct[n]
+    np.testing.assert_array_equal(sel["D"], expect)
+    q = expect[expect > 0] / expect.sum()
+    rank = math.exp(-(q * np.log(q)).sum())
+    assert sel["m"] == max(k, math.ceil(rank - 1e-12))
+
+
+@pytest.mark.parametrize("j", [1, 3, 8, 13])
+def test_uniform_demand_effective_rank_is_j(j):
+    """D uniform over j experts has entropy ln j, so exp(H) = j and m = max(k, j)."""
+    E, k = 16, 2
+    l = np.full((5, E), -1000.0, dtype=np.float32)
+    l[:, :j] = 0.0
+    sel = O.select_tree(l, np.array([0, 1, 1, 2, 2]), k, [1.0, 0.6, 0.3], mode=O.ACCEPT,
+                        pool_all=True)
+    assert sel["m"] == max(k, j)
+    assert sel["margin_rank"] < 1e-12
+
+
+def test_root_only_commitment_gives_root_softmax():
+    rng = np.random.Generator(np.random.PCG64(9))
+    l = rng.standard_normal((9, 16)).astype(np.float32)
+    sel = O.select_tree(l, W.tiny_tree().depth, 2, [1.0, 0.0], mode=O.ACCEPT)
+    np.testing.assert_allclose(sel["D"], sp_softmax(l[0].astype(np.float64)), rtol=1e-14)
+
+
+def test_all_equal_logits_selected_equals_natural():
+    E, k = 16, 2
+    l = np.zeros((9, E), dtype=np.float32)
+    sel = O.select_tree(l, W.tiny_tree().depth, k, W.C_TINY, mode=O.ACCEPT)
+    nat = O.select_tree(l, W.tiny_tree().depth, k, W.C_TINY, mode=O.NATURAL)
+    # demand is uniform over all E, exp(H) = E, so m is capped at the pool (= U)
+    assert sel["m"] == sel["union_nat"] == k
+    np.testing.assert_array_equal(sel["idx"], nat["idx"])
+
+
+def test_gates_are_softmax_of_chosen_logits():
+    rng = np.random.Generator(np.random.PCG64(11))
+    t = W.eagle_tree(3)
+    l = W.synthetic_logits(4, t.parent, 32, 3.0)
+    for mode in (O.NATURAL, O.ACCEPT):
+        sel = O.select_tree(l, t.depth, 4, W.C_EAGLE, mode=mode)
+        for n in range(t.N):
+            ref = sp_softmax(l[n, sel["idx"][n]].astype(np.float64))
+            np.testing.assert_allclose(sel["gates"][n], ref, rtol=1e-13)
+
+
+# ----------------------------------------------------------------- brute force
+
+def _tiny_case(seed, E=16, k=2, scale=3.0):
+    t = W.tiny_tree()
+    return W.synthetic_logits(seed, t.parent, E, scale), t.depth
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_anchor_fill_brute_force(seed):
+    """S is the unique size-m superset of the root's natural top-k inside the pool
+    that maximises the summed demand (distinct demands)."""
+    k = 2
+    l, depth = _tiny_case(seed)
+    sel = O.select_tree(l, depth, k, W.C_TINY, mode=O.ACCEPT)
+    nat, _ = O.topk(l, k)
+    anchor = set(nat[0].tolist())
+    pool = sorted(set(nat.ravel().tolist()))
+    D = sel["D"]
+    m = sel["m"]
+    rest = [e for e in pool if e not in anchor]
+    best, best_sum = None, -1.0
+    for comb in itertools.combinations(rest, m - k):
+        s = sum(D[e] for e in comb)
+        if s > best_sum:
+            best, best_sum = set(comb) | anchor, s
+    assert set(np.flatnonzero(sel["eligible"]).tolist()) == best
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_prune_brute_force_and_invariants(seed):
+    k, budget, min_set = 2, 3, 4
+    t = W.eagle_tree(seed)
+    l = W.synthetic_logits(seed, t.parent, 16, 1.5)
+    res = W.residency_mask(seed, 16, 6)
+    base = O.select_tree(l, t.depth, k, W.C_EAGLE, mode=O.ACCEPT)
+    sel = O.select_tree(l, t.depth, k, W.C_EAGLE, mode=O.ACCEPT, prune=True, resident=res,
+                        budget=budget, min_set=min_set)
+    S0 = set(np.flatnonzero(base["eligible"]).tolist())
+    S1 = set(np.flatnonzero(sel["eligible"]).tolist())
+    anchor = set(O.topk(l[:1], k)[0][0].tolist())
+    removed = S0 - S1
+    assert S1 <= S0 and anchor <= S1
+    assert len(removed) == sel["pruned"] <= budget
+    assert all(res[e] == 0 for e in removed)
+    assert len(S1) >= min(len(S0), max(min_set, k))
+    removable = [e for e in S0 - anchor if res[e] == 0]
+    r = min(budget, max(0, len(S0) - max(min_set, k)), len(removable))
+    D = sel["D"]
+    best = min(itertools.combinations(removable, r), key=lambda cmb: sum(D[e] for e in cmb))
+    assert removed == set(best)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_restricted_topk_brute_force(seed):
+    k = 2
+    l, depth = _tiny_case(seed, scale=2.0)
+    sel = O.select_tree(l, depth, k, W.C_TINY, mode=O.ACCEPT)
+    S = np.flatnonzero(sel["eligible"]).tolist()
+    nat, _ = O.topk(l, k)
+    for n in range(l.shape[0]):
+        cands = [T for T in itertools.combinations(S, k)
+                 if min(l[n, list(T)]) > max([l[n, e] for e in S if e not in T], default=-np.inf)]
+        assert len(cands) == 1
+        got = sel["idx"][n].tolist()
+        assert set(got) == set(cands[0])
+        assert all(l[n, got[i]] >= l[n, got[i + 1]] for i in range(k - 1))
+        if set(nat[n].tolist()) <= set(S):
+            assert got == nat[n].tolist()
+
+
+def test_fixed_budget_mode_sets_size():
+    t = W.eagle_tree(2)
+    l = W.synthetic_logits(2, t.parent, 64, 3.0)
+    for B in (4, 10, 30, 1000):
+        sel = O.select_tree(l, t.depth, 4, W.C_EAGLE, mode=O.FIXED_B, fixed_B=B)
+        assert sel["m"] == min(max(B, 4), sel["union_nat"])
+        assert int(sel["eligible"].sum()) == sel["m"]
+
+
+@pytest.mark.parametrize("scale", [1.0, 4.5])
+def test_invariants_on_eagle_trees(scale):
+    """Root's natural experts always eligible, |S| >= k, and the selected union
+    never exceeds the natural union (it lies inside S, which lies inside U)."""
+    E, k = 128, 8
+    for seed in range(8):
+        t = W.eagle_tree(100 + seed)
+        l = W.synthetic_logits(seed, t.parent, E, scale)
+        sel = O.select_tree(l, t.depth, k, W.C_EAGLE, mode=O.ACCEPT)
+        nat, _ = O.topk(l, k)
+        S = set(np.flatnonzero(sel["eligible"]).tolist())
+        assert set(nat[0].tolist()) <= S
+        assert len(S) >= k
+        assert set(np.unique(sel["idx"]).tolist()) <= S <= set(np.unique(nat).tolist())
+        assert sel["union_sel"] <= sel["union_nat"]
+
+
+def test_permute_brute_force():
+    for seed, (R, E, k, skew) in enumerate([(65, 128, 8, 0.0), (9, 16, 2, 1.0), (300, 32, 4, 1.2)]):
+        idx = W.random_assignments(seed, R, E, k, skew)
+        counts, offsets, perm = O.permute(idx, E)
+        keys = sorted((int(idx[r, j]), r, j) for r in range(R) for j in range(k))
+        assert perm.tolist() == [r * k + j for (_, r, j) in keys]
+        np.testing.assert_array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+        assert offsets[0] == 0 and offsets[-1] == R * k
+        np.testing.assert_array_equal(np.diff(offsets), counts)
+
+
+# ---------------------------------------------------------------- expert math
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_single_expert_is_dense_swiglu(dt):
+    """k = 1 reduces the layer to one dense SwiGLU FFN per token:
+    y = W_down (silu(W_gate x) * (W_up x)), checked with torch fp64 + F.silu.
+    f != d catches a transposed operand."""
+    shape = W.LayerShape(d=48, E=3, k=1, f=20, dtype="fp32" if dt == torch.float32 else "bf16")
+    wg, wu, wd = W.expert_weights(1, shape, std=0.2)
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(5, 48, generator=g).to(dt)
+    idx = np.array([[0], [2], [1], [2], [0]], dtype=np.int32)
+    got = O.moe_combine(x, wg, wu, wd, idx, np.ones((5, 1)))
+    xd = x.double()
+    for r in range(5):
+        e = int(idx[r, 0])
+        h = torch.nn.functional.silu(wg[e].double() @ xd[r]) * (wu[e].double() @ xd[r])
+        np.testing.assert_allclose(got[r], (wd[e].double() @ h).numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_gated_combine_weights_slots():
+    shape = W.LayerShape(d=32, E=4, k=2, f=24, dtype="fp32")
+    wg, wu, wd = W.expert_weights(2, shape, std=0.3)
+    x = torch.randn(3, 32, generator=torch.Generator().manual_seed(1))
+    idx = np.array([[1, 3], [0, 1], [2, 0]], dtype=np.int32)
+    gates = np.array([[0.7, 0.3], [0.5, 0.5], [0.1, 0.9]])
+    got = O.moe_combine(x, wg, wu, wd, idx, gates, rows=[2, 0])
+    for q, r in enumerate([2, 0]):
+        ref = np.zeros(32)
+        for j in range(2):
+            e = int(idx[r, j])
+            h = torch.nn.functional.silu(wg[e].double() @ x[r].double()) * (wu[e].double() @ x[r].double())
+            ref += gates[r, j] * (wd[e].double() @ h).numpy()
+        np.testing.assert_allclose(got[q], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_forward_composes_router_selection_and_experts():
+    shape = W.TINY
+    t = W.tiny_tree()
+    x = W.hidden_states(1, t.parent, shape.d, torch.float32)
+    wr = W.router_weight(2, shape, std=0.1)
+    wg, wu, wd = W.expert_weights(3, shape)
+    out = O.forward(x, wr, wg, wu, wd, t.depth, shape.k, W.C_TINY, mode=O.ACCEPT)
+    np.testing.assert_allclose(out["logits"], (x.double() @ wr.double().T).numpy(), rtol=1e-12)
+    sel = O.select_tree(out["logits32"], t.depth, shape.k, W.C_TINY, mode=O.ACCEPT)
+    np.testing.assert_array_equal(out["idx"], sel["idx"])
+    y = O.moe_combine(x, wg, wu, wd, sel["idx"], sel["gates"])
+    np.testing.assert_array_equal(out["y"], y)
