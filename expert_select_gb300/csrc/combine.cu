@@ -1,0 +1,87 @@
+// Unpermute + weighted combine ("MoE and speculative decoding" blog, pipeline step
+// "unpermute + weighted combine"): y[r] = sum_j gates[r, j] O[pos(r, j)], slots in
+// ascending j, fp32 accumulation, rounded once to the layer dtype.
+//
+// Also holds the small kernel that publishes a residency table to the device.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename TO>
+__device__ __forceinline__ void store4(TO *y, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float *y, float4 v) {
+    *reinterpret_cast<float4 *>(y) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *y, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&lo);
+    u.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(y) = u;
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
+               const float *__restrict__ gates, int d, int k, TO *__restrict__ y) {
+    const int r = blockIdx.x;
+    const int c = (blockIdx.y * kThreads + threadIdx.x) * 4;
+    if (c >= d) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const int p = pos[r * k + j];
+        if (p < 0) continue;
+        const float g = gates[r * k + j];
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(o + (size_t)p * d + c));
+        acc.x = fmaf(g, v.x, acc.x);
+        acc.y = fmaf(g, v.y, acc.y);
+        acc.z = fmaf(g, v.z, acc.z);
+        acc.w = fmaf(g, v.w, acc.w);
+    }
+    store4<TO>(y + (size_t)r * d + c, acc);
+}
+
+struct PublishArgs {
+    int slot[kMaxE];
+    uint8_t res[kMaxE];
+};
+
+__global__ void publish_kernel(PublishArgs p, int E, int *slot, uint8_t *res) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (slot) slot[e] = p.slot[e];
+        if (res) res[e] = p.res[e];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
+                           const float *gates, int R, void *y, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    dim3 grid(R, (L.d / 4 + kThreads - 1) / kThreads);
+    if (L.dtype == MOE_DTYPE_BF16)
+        combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(o, pos, gates, L.d, L.k,
+                                                                (__nv_bfloat16 *)y);
+    else
+        combine_kernel<float><<<grid, kThreads, 0, s>>>(o, pos, gates, L.d, L.k, (float *)y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,
+                           uint8_t *res_dev, cudaStream_t s) {
+    PublishArgs p;
+    for (int e = 0; e < E; ++e) {
+        p.slot[e] = slot_host[e];
+        p.res[e] = res_host[e];
+    }
+    publish_kernel<<<1, 256, 0, s>>>(p, E, slot_dev, res_dev);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

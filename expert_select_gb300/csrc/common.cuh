@@ -1,0 +1,122 @@
+// Internal declarations shared by the libmoetree translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "moetree.h"
+
+namespace moe {
+
+// Bits of the kernel-side check word (first int of the workspace).
+enum : int { FLAG_BAD_EXPERT = 1, FLAG_WAIT_TIMEOUT = 2 };
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kMaxD = 6144;  // SIMT experts stage 8 rows of d (or f) fp32 in shared memory
+
+// Byte offsets of the scratch arrays inside one workspace.
+struct Workspace {
+    size_t flags;     // int32[64]: [0] check word, the rest scheduler counters
+    size_t logits;    // f32 [R, E]
+    size_t idx;       // i32 [R, k]
+    size_t gates;     // f32 [R, k]
+    size_t elig;      // u8  [B, E]
+    size_t info;      // i32 [B, 4]
+    size_t counts;    // i32 [E]
+    size_t offsets;   // i32 [E + 1]
+    size_t perm;      // i32 [A]  permuted position -> assignment id
+    size_t pos;       // i32 [A]  assignment id -> permuted position (-1 = skipped)
+    size_t active;    // i32 [E + 1]  [0] = n_active, then active experts ascending
+    size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
+    size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)
+    size_t o;         // f32 [A, d]  expert outputs in permuted order
+    size_t total;
+};
+
+Workspace workspace_layout(const moe_layer_desc &L, int B, int N);
+
+inline size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+// ---- launchers (each returns the launch's cudaError_t) ----
+cudaError_t launch_router(const moe_layer_desc &L, const void *x, const void *Wr, int R,
+                          float *logits, cudaStream_t s);
+
+struct SelectArgs {
+    int mode, n_c, pool_all, anchor, prune, budget, min_set, fixed_B;
+    float c[MOE_MAX_DEPTHS];
+};
+cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
+                          const int *depth, int B, int N, const uint8_t *resident, int *idx,
+                          float *gates, uint8_t *elig, int *info, cudaStream_t s);
+
+cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
+                           int *offsets, int *perm, int *pos, int *active, int *flags,
+                           cudaStream_t s);
+size_t permute_smem_bytes(int R, int E);
+
+struct FfnArgs {
+    const void *x;       // [R, d]
+    const void *Wg, *Wu; // [S, f, d]
+    const void *Wd;      // [S, d, f]
+    const int *slot;     // [E] or nullptr
+    const int *counts, *offsets, *perm, *active;
+    int R, d, f, E, k, dtype;
+    int *flags;
+    void *xp;            // gathered x (tensor-core path)
+    void *h;             // activations
+    float *o;            // expert outputs, permuted order
+};
+cudaError_t launch_ffn_simt(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s);
+bool ffn_tc_supported(const moe_layer_desc &L);
+
+cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
+                           const float *gates, int R, void *y, cudaStream_t s);
+
+cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,
+                           uint8_t *res_dev, cudaStream_t s);
+
+// ---- device helpers ----
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Loads 8 consecutive elements starting at element `i` of a row as fp32.
+// bf16: one 16-byte load; fp32: two 16-byte loads. `p` must be 16-byte aligned at i.
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float v[8]) {
+        uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+        v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+    }
+};
+template <> struct Vec8<float> {
+    __device__ __forceinline__ static void load(const float *p, float v[8]) {
+        float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+// Sums 32 per-lane values across a warp; afterwards lane L holds the total of
+// value index L (a transpose-reduction: 31 shuffles for 32 sums).
+__device__ __forceinline__ float warp_transpose_sum32(float v[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            float send = up ? v[i] : v[i + s];
+            float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+}  // namespace moe

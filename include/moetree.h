@@ -1,0 +1,242 @@
+/*
+ * moetree.h -- C ABI of libmoetree: a GB300 (sm_103a) MoE layer run over one
+ * speculative-decoding verification block (a draft tree verified in one pass),
+ * with AcceptMoE-style verifier-side expert selection.
+ *
+ * What the operations compute (page title + section):
+ *   - "MoE and speculative decoding" blog, section "starting from one MoE layer":
+ *     the layer E(x) = TopR(softmax(W_r x)), y = sum_{e in E(x)} g_e(x) E_e(x), run
+ *     as router -> permute/group by expert -> grouped GEMM over the active experts
+ *     -> unpermute + weighted combine.
+ *   - "AcceptMoE" news article, section 02, and the AcceptMoE abstract (arXiv
+ *     2608.02989): commitment-weighted demand, root anchor, self-sizing by the
+ *     effective rank of the demand, residency-aware pruning, and re-routing every
+ *     node inside the eligible set.
+ *   - same article, section 03 and the abstract: expert offload with 48 expert
+ *     slots per layer and host-to-device uploads of non-resident experts.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are plain pointers, row-major, densely packed. "device" means
+ *     CUDA device memory of the current device; "host" means CPU memory. The
+ *     caller owns every buffer and every stream; the library allocates nothing
+ *     except the residency table's host metadata.
+ *   - Work is enqueued on the caller's stream and returns without waiting, unless
+ *     an entry point says otherwise. Arguments are checked on the host before any
+ *     launch; a bad argument returns MOE_ERR_ARG and enqueues nothing.
+ *   - x, W_r and expert weights share the layer dtype (fp32 or bf16). Router
+ *     logits and gates are fp32. Expert ids and indices are int32.
+ *   - `workspace` is device memory of at least moe_workspace_bytes() bytes, 256-byte
+ *     aligned. It is scratch: its contents on entry are ignored and on return are
+ *     unspecified. Two calls that overlap in time must use different workspaces.
+ *   - No C++ exception crosses this ABI; every failure is a moe_status.
+ */
+#ifndef MOETREE_H
+#define MOETREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t (NULL = legacy default) */
+typedef struct CUevent_st *moe_event_t;   /* a cudaEvent_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,          /* bad argument; nothing was enqueued */
+    MOE_ERR_CUDA = -2,         /* a CUDA runtime/driver call failed */
+    MOE_ERR_NOSLOT = -3,       /* more experts needed at once than the layer has slots */
+    MOE_ERR_TIMEOUT = -4,      /* a bounded wait gave up */
+    MOE_ERR_DEVICE_CHECK = -5, /* a kernel-side check failed (see moe_workspace_check) */
+    MOE_ERR_UNSUPPORTED = -6   /* shape or dtype outside what the kernels support */
+} moe_status;
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* Routing modes. NATURAL is plain top-k routing (the pages' "Standard SD");
+ * ACCEPT is AcceptMoE selection; FIXED_B keeps the demand ranking but takes the
+ * set size from `fixed_B` instead of the effective rank (AcceptMoE-B; with a
+ * uniform commitment table and no anchor it is the MoE-Spec budget rule). */
+typedef enum { MOE_ROUTE_NATURAL = 0, MOE_ROUTE_ACCEPT = 1, MOE_ROUTE_FIXED_B = 2 } moe_route_mode;
+
+/* Which grouped-expert kernel runs. AUTO picks by dtype and shape. */
+typedef enum { MOE_FFN_AUTO = 0, MOE_FFN_SIMT = 1, MOE_FFN_TCGEN05 = 2 } moe_ffn_path;
+
+/* One MoE layer: hidden size d, E routed experts, top-k, SwiGLU width f.
+ * Limits: 1 <= k <= 16, k <= E <= 256, d and f multiples of 8 and at most 6144
+ * (multiples of 64 for the tcgen05 expert kernel). */
+typedef struct {
+    int d, E, k, f;
+    int dtype; /* moe_dtype */
+} moe_layer_desc;
+
+#define MOE_MAX_DEPTHS 16
+
+/* Expert-selection parameters ("AcceptMoE" news article, section 02).
+ *   c_by_depth[t]  commitment probability of a node at draft depth t (root = 0);
+ *                  depths >= n_c use c_by_depth[n_c-1].
+ *   pool_all       0: fill candidates come from the natural union of the tree
+ *                  (default); 1: from all E experts.
+ *   anchor         1: the root's natural top-k is always eligible (default).
+ *   prune          1: residency-aware pruning against `resident` (needs resident).
+ *   reroute_budget most experts pruning may remove from a tree's eligible set.
+ *   min_set        pruning stops when the set has max(min_set, k) experts.
+ *   fixed_B        set size for MOE_ROUTE_FIXED_B. */
+typedef struct {
+    int mode; /* moe_route_mode */
+    int n_c;
+    double c_by_depth[MOE_MAX_DEPTHS];
+    int pool_all;
+    int anchor;
+    int prune;
+    int reroute_budget;
+    int min_set;
+    int fixed_B;
+} moe_select_params;
+
+/* Per-tree counters written by selection, int32 [B][MOE_INFO_FIELDS] in device memory:
+ * natural union, selected union, eligible-set size m before pruning, pruned count. */
+#define MOE_INFO_FIELDS 4
+
+/* Optional device outputs of moe_tree_forward; any member may be NULL. */
+typedef struct {
+    float *logits;    /* [R, E] router logits */
+    int *topk_idx;    /* [R, k] routed experts (after selection) */
+    float *gates;     /* [R, k] renormalised gate weights */
+    uint8_t *eligible;/* [B, E] eligible set per tree */
+    int *info;        /* [B, MOE_INFO_FIELDS] */
+    int *counts;      /* [E] assignments per expert */
+    int *offsets;     /* [E+1] exclusive prefix of counts */
+    int *perm;        /* [R*k] permuted order of assignment ids r*k+j */
+} moe_tree_outputs;
+
+/* Run options; pass NULL for defaults. If both events are non-NULL they are
+ * recorded on the stream immediately before and after the grouped-expert kernel
+ * (for timing the dominant kernel with CUDA events). */
+typedef struct {
+    int ffn_path; /* moe_ffn_path */
+    moe_event_t ffn_begin;
+    moe_event_t ffn_end;
+} moe_run_opts;
+
+/* Text for a status code. Never NULL. */
+const char *moe_status_str(int status);
+
+/* ABI version of this header (major*100 + minor). */
+int moe_abi_version(void);
+
+/* Bytes of workspace needed for blocks of up to B trees of N nodes (R = B*N rows). */
+size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N);
+
+/* Router scores ("MoE and speculative decoding" blog, "starting from one MoE layer",
+ * the W_r x inside E(x) = TopR(softmax(W_r x))): logits[r, e] = sum_i x[r, i] W_r[e, i],
+ * fp32 accumulation, no bias.
+ *   x [R, d] and W_r [E, d] device, layer dtype; logits [R, E] device fp32. */
+moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void *W_r, int R,
+                             float *logits, moe_stream_t stream);
+
+/* Expert selection for B trees of N nodes from router logits ("AcceptMoE" news
+ * article, section 02; AcceptMoE abstract). Per tree: natural top-k of every node,
+ * demand D_e = sum_n c(depth_n) softmax(logits_n)_e (fp32, nodes in order), set
+ * size m = max(k, ceil(exp(H(D / sum D)))) capped at the pool (FIXED_B: fixed_B),
+ * root anchor + fill by (D desc, id asc), optional residency-aware pruning, then
+ * each node's top-k restricted to the eligible set, gates = softmax over the k
+ * chosen logits. NATURAL mode: plain top-k with the same renormalised gates.
+ *   logits   [B*N, E] device fp32, node n of tree b at row b*N + n, node 0 = root.
+ *   depth    [B*N] device int32, draft depth of each node (root 0).
+ *   resident [E] device uint8 (1 = expert resident) or NULL; required if P->prune.
+ *   topk_idx [B*N, k] device int32, descending logit order, ties to the lower id.
+ *   gates    [B*N, k] device fp32.
+ *   eligible [B, E] device uint8 or NULL; info [B, 4] device int32 or NULL. */
+moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
+                           const float *logits, const int *depth, int B, int N,
+                           const uint8_t *resident, int *topk_idx, float *gates,
+                           uint8_t *eligible, int *info, moe_stream_t stream);
+
+/* Permute / group by expert ("MoE and speculative decoding" blog, pipeline step
+ * "permute / group by expert"): stable counting sort of the assignments (r, j) by
+ * (expert, row, slot).
+ *   topk_idx [R, k] device int32; counts [E], offsets [E+1], perm [R*k] device int32
+ *   (perm[p] = r*k + j of the assignment at permuted position p). Expert ids out of
+ *   range are counted as a device-check failure and skipped. */
+moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int R, int *counts,
+                              int *offsets, int *perm, void *workspace, moe_stream_t stream);
+
+/* Grouped SwiGLU experts + gated combine for a given routing ("MoE and speculative
+ * decoding" blog, "grouped GEMM for active experts" and "unpermute + weighted
+ * combine"): y[r] = sum_j gates[r, j] W_down[e] (silu(W_gate[e] x_r) * (W_up[e] x_r)),
+ * e = topk_idx[r, j], slots summed in ascending j. Each expert with at least one
+ * assignment streams its weights from HBM once per launch (a token count above 256
+ * re-streams them once per 256 tokens).
+ *   x [R, d] device; y [R, d] device, layer dtype.
+ *   W_gate, W_up [S, f, d] and W_down [S, d, f] device: a pool of S expert slots.
+ *   slot_of_expert [E] device int32 maps expert -> slot, or NULL for slot = expert.
+ *   topk_idx [R, k] device int32, gates [R, k] device fp32. */
+moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void *W_gate,
+                              const void *W_up, const void *W_down, const int *slot_of_expert,
+                              const int *topk_idx, const float *gates, int R, void *y,
+                              void *workspace, const moe_run_opts *opts, moe_stream_t stream);
+
+/* The whole layer over one verification block: router, selection (or natural
+ * routing), permute, grouped SwiGLU experts, combine. Arguments as in the calls
+ * above; `out` (may be NULL) receives intermediate results. */
+moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P, const void *x,
+                            const void *W_r, const void *W_gate, const void *W_up,
+                            const void *W_down, const int *slot_of_expert, const int *depth,
+                            int B, int N, const uint8_t *resident, void *y,
+                            const moe_tree_outputs *out, void *workspace,
+                            const moe_run_opts *opts, moe_stream_t stream);
+
+/* Reads and clears the kernel-side check word of a workspace. Waits for `stream`.
+ * *flags = 0 when no kernel reported a problem since the last call; bit 0 = an
+ * expert id outside [0, E) was skipped; bit 1 = a bounded device wait gave up. */
+moe_status moe_workspace_check(void *workspace, int *flags, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- offload ----
+ * Expert residency for offloaded layers ("AcceptMoE" news article, section 03:
+ * 48 expert slots per layer on the GPU, the other experts in CPU memory and
+ * uploaded on demand). The table lives in host memory; each layer has `slots`
+ * device slots and an LRU order over them. */
+typedef struct moe_residency moe_residency;
+
+moe_status moe_residency_create(int n_layers, int E, int slots, moe_residency **table);
+moe_status moe_residency_destroy(moe_residency *table);
+
+/* Host copy of one layer's state: slot_of_expert [E] (-1 = not resident) and
+ * resident [E] (0/1); either may be NULL. */
+moe_status moe_residency_query(const moe_residency *table, int layer, int *slot_of_expert,
+                               uint8_t *resident);
+
+/* Makes the `n_needed` experts of `needed` (host) resident in `layer`: experts
+ * already in a slot are hits and move to the front of the LRU order; each miss
+ * takes a free slot or evicts the least recently used slot not needed now. Writes
+ * the uploads to perform to up_expert/up_slot (host, room for n_needed) and their
+ * number to *n_up; *hits may be NULL. MOE_ERR_NOSLOT if n_needed > slots (split the
+ * set and call once per part). Host only; enqueues nothing. */
+moe_status moe_residency_plan(moe_residency *table, int layer, const int *needed, int n_needed,
+                              int *up_expert, int *up_slot, int *n_up, int *hits);
+
+/* Writes the layer's slot map and resident mask to device arrays (int32 [E] and
+ * uint8 [E]; either may be NULL) with a kernel on `stream`. */
+moe_status moe_residency_publish(const moe_residency *table, int layer, int *slot_of_expert,
+                                 uint8_t *resident, moe_stream_t stream);
+
+/* Copies whole experts host -> device slot: for each i, expert up_expert[i]'s
+ * W_gate, W_up, W_down from the host stores (pinned, [E, f, d], [E, f, d], [E, d, f])
+ * into slot up_slot[i] of the device pools ([S, ...]) with one cudaMemcpyAsync per
+ * matrix on `side`, then records `done` (may be NULL) on `side`. Arrays are host. */
+moe_status moe_expert_upload(const moe_layer_desc *L, const void *host_gate, const void *host_up,
+                             const void *host_down, void *slot_gate, void *slot_up,
+                             void *slot_down, const int *up_expert, const int *up_slot, int n,
+                             moe_stream_t side, moe_event_t done);
+
+/* Host poll of cudaEventQuery(ev) for at most timeout_s seconds. MOE_ERR_TIMEOUT if
+ * the event has not completed by then. */
+moe_status moe_event_wait(moe_event_t ev, double timeout_s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOETREE_H */

@@ -112,10 +112,49 @@ static void softmax_row(const float *l, int E, double *p) {
     for (int e = 0; e < E; ++e) p[e] /= s;
 }
 
-/* Order used by the fill and by pruning: a before b when D_a > D_b (descending), or
- * equal demand and lower id. */
+/* Fill order: a before b when D_a > D_b, or equal demand and lower id. */
 static int before_desc(const double *D, int a, int b) {
     return D[a] > D[b] || (D[a] == D[b] && a < b);
+}
+
+/* Pruning order: a before b when D_a < D_b, or equal demand and lower id. */
+static int before_asc(const double *D, int a, int b) {
+    return D[a] < D[b] || (D[a] == D[b] && a < b);
+}
+
+/* exp(H) within this relative distance of an integer counts as that integer. */
+#define SNAP 1e-5
+
+/* The demand / effective-rank steps in fp32, the precision of the device kernel:
+ * softmax row p = exp(l - max) / sum (sum in ascending expert order), D_e += c * p_e
+ * in ascending node order, sum D and H = -sum q ln q in ascending expert order.
+ * D is returned widened to fp64 (exactly), r = exp(H). */
+static float demand_f32(const float *logits, const int *depth, int N, int E, const double *c,
+                        int n_c, double *D) {
+    float *Df = (float *)calloc((size_t)E, sizeof(float));
+    float *ex = (float *)malloc(sizeof(float) * (size_t)E);
+    for (int n = 0; n < N; ++n) {
+        const float *l = logits + (size_t)n * E;
+        int t = depth[n] < n_c ? depth[n] : n_c - 1;
+        float cf = (float)c[t], mx = l[0], s = 0.f;
+        for (int e = 1; e < E; ++e)
+            if (l[e] > mx) mx = l[e];
+        for (int e = 0; e < E; ++e) {
+            ex[e] = expf(l[e] - mx);
+            s += ex[e];
+        }
+        for (int e = 0; e < E; ++e) Df[e] += cf * (ex[e] / s);
+    }
+    float sum = 0.f, H = 0.f;
+    for (int e = 0; e < E; ++e) sum += Df[e];
+    for (int e = 0; e < E; ++e) {
+        float q = Df[e] / sum;
+        if (q > 0.f) H -= q * logf(q);
+    }
+    for (int e = 0; e < E; ++e) D[e] = (double)Df[e];
+    free(Df);
+    free(ex);
+    return expf(H);
 }
 
 /* Selection for one draft tree of N nodes (node 0 is the root).
@@ -125,7 +164,7 @@ static int before_desc(const double *D, int a, int b) {
  *  2. demand D_e = sum_n c(depth_n) * softmax(l_n)_e, nodes in ascending order;
  *     c(depth) beyond the table repeats the last entry.
  *  3. effective rank r = exp(H(D / sum D)), H = -sum q ln q over all E experts.
- *     m = max(k, ceil(r)) (a value within 1e-9 relative of an integer counts as that
+ *     m = max(k, ceil(r)) (a value within 1e-5 relative of an integer counts as that
  *     integer), capped at the pool size. FIXED_B takes m = max(k, fixed_B) instead.
  *  4. root anchor A = natural top-k of node 0 (when `anchor`); S = A plus the best
  *     m - |A| experts of pool \ A in (D desc, id asc) order. pool = U, or all experts.
@@ -139,11 +178,13 @@ static int before_desc(const double *D, int a, int b) {
  * margins[0] = smallest top-k gap (fp32 logits, natural), margins[1] = relative
  * distance of r to the nearest integer, margins[2] = relative demand gap at the
  * fill cut, margins[3] = relative demand gap at the prune cut, margins[4] =
- * smallest restricted top-k gap. Returns 0, or -1 on bad arguments. */
+ * smallest restricted top-k gap. prec = 0 runs steps 2-3 in fp64; prec = 1 runs them
+ * in fp32 (demand_f32), the precision the device decides in. Returns 0, or -1 on bad
+ * arguments. */
 ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int E, int k,
                                const double *c, int n_c, int mode, int pool_all, int anchor,
                                int prune, const unsigned char *resident, int budget,
-                               int min_set, int fixed_B, int *idx, double *gates,
+                               int min_set, int fixed_B, int prec, int *idx, double *gates,
                                unsigned char *eligible, int *info, double *D, double *margins) {
     if (N < 1 || E < 1 || E > 1024 || k < 1 || k > E || n_c < 1) return -1;
     int *nat = (int *)malloc(sizeof(int) * (size_t)N * k);
@@ -167,27 +208,31 @@ ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int
         memset(inS, 1, (size_t)E);
         info[2] = E;
     } else {
-        /* 2. commitment-weighted demand */
-        for (int e = 0; e < E; ++e) D[e] = 0.0;
-        for (int n = 0; n < N; ++n) {
-            int t = depth[n] < n_c ? depth[n] : n_c - 1;
-            softmax_row(logits + (size_t)n * E, E, p);
-            for (int e = 0; e < E; ++e) D[e] += c[t] * p[e];
-        }
-        /* 3. effective rank and set size */
+        /* 2. commitment-weighted demand, 3. effective rank and set size */
         int pool = pool_all ? E : U;
-        int m;
-        if (mode == ORC_ACCEPT) {
+        double r = 0.0;
+        if (prec == 1) {
+            r = demand_f32(logits, depth, N, E, c, n_c, D);
+        } else {
+            for (int e = 0; e < E; ++e) D[e] = 0.0;
+            for (int n = 0; n < N; ++n) {
+                int t = depth[n] < n_c ? depth[n] : n_c - 1;
+                softmax_row(logits + (size_t)n * E, E, p);
+                for (int e = 0; e < E; ++e) D[e] += c[t] * p[e];
+            }
             double sum = 0.0, H = 0.0;
             for (int e = 0; e < E; ++e) sum += D[e];
             for (int e = 0; e < E; ++e) {
                 double q = D[e] / sum;
                 if (q > 0.0) H -= q * log(q);
             }
-            double r = exp(H);
+            r = exp(H);
+        }
+        int m;
+        if (mode == ORC_ACCEPT) {
             double rn = nearbyint(r);
             margins[1] = fabs(r - rn) / r;
-            m = (fabs(r - rn) <= 1e-9 * r) ? (int)rn : (int)ceil(r);
+            m = (fabs(r - rn) <= SNAP * r) ? (int)rn : (int)ceil(r);
         } else {
             m = fixed_B;
         }
@@ -231,7 +276,7 @@ ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int
                 int worst = -1;
                 for (int e = 0; e < E; ++e) {
                     if (!inS[e] || inA[e] || resident[e]) continue;
-                    if (worst < 0 || before_desc(D, worst, e)) worst = e;
+                    if (worst < 0 || before_asc(D, e, worst)) worst = e;
                 }
                 if (worst < 0) break;
                 if (removed >= budget || size <= floor_) {

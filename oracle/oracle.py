@@ -46,7 +46,7 @@ def lib():
         _lib.oracle_router.restype = None
         _lib.oracle_topk.argtypes = [P, i, i, i, P]
         _lib.oracle_topk.restype = C.c_double
-        _lib.oracle_select_tree.argtypes = [P, P, i, i, i, P, i, i, i, i, i, P, i, i, i,
+        _lib.oracle_select_tree.argtypes = [P, P, i, i, i, P, i, i, i, i, i, P, i, i, i, i,
                                             P, P, P, P, P, P]
         _lib.oracle_select_tree.restype = i
         _lib.oracle_permute.argtypes = [P, i, i, i, P, P, P]
@@ -103,7 +103,10 @@ def topk(logits: np.ndarray, k: int):
 def select_tree(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float],
                 mode: int = ACCEPT, pool_all: bool = False, anchor: bool = True,
                 prune: bool = False, resident: Optional[np.ndarray] = None,
-                budget: int = 8, min_set: int = 16, fixed_B: int = 0) -> Dict:
+                budget: int = 8, min_set: int = 16, fixed_B: int = 0,
+                precision: str = "fp64") -> Dict:
+    """Selection for one tree. precision="fp32" takes the demand / effective-rank
+    decisions in fp32 like the device does; "fp64" is the reference definition."""
     l = np.ascontiguousarray(logits, dtype=np.float32)
     N, E = l.shape
     dep = np.ascontiguousarray(depth, dtype=np.int32)
@@ -117,7 +120,8 @@ def select_tree(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float
     margins = np.empty(5, dtype=np.float64)
     rc = lib().oracle_select_tree(_p(l), _p(dep), N, E, k, _p(cc), len(cc), mode,
                                   int(pool_all), int(anchor), int(prune), _p(res), budget,
-                                  min_set, fixed_B, _p(idx), _p(gates), _p(elig), _p(info),
+                                  min_set, fixed_B, 1 if precision == "fp32" else 0,
+                                  _p(idx), _p(gates), _p(elig), _p(info),
                                   _p(D), _p(margins))
     if rc != 0:
         raise ValueError("oracle_select_tree: bad arguments")
