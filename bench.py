@@ -1,0 +1,461 @@
+"""Benchmark: the MoE tree-verification layer (Qwen3-30B-A3B-shaped, resident).
+
+One step = one pass of the whole hot path over one verification block: router,
+natural top-k, AcceptMoE selection (demand, effective-rank size, root anchor,
+fill), restricted top-k, permute, grouped SwiGLU experts over the union, and the
+gated combine, through the C entry point moe_tree_forward. Each step verifies a
+different seeded EAGLE-3-shaped draft tree (65 nodes). Throughput is verification
+blocks per second; the grouped-expert kernel is also reported against the HBM
+roofline on its algorithmic bytes (union expert weights + token rows in/out).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own GPU (the layer has no cross-GPU exchange); the reported value is
+the blocks all ranks processed divided by the slowest rank's time.
+
+--impl reference times the CPU oracle instead (the checker, on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE verify layer tree-blocks/s; union expert-weight HBM GB/s vs ~8 TB/s"
+UNIT = "tree-blocks/s"
+TREES = 64            # distinct seeded trees cycled through by the steps
+SEED = 1000           # seed base of this workload
+
+
+def workload_config(shape, routing, router_std):
+    return {"workload": "qwen3-30b-a3b-moe-layer-resident-eagle3-tree",
+            "d": shape.d, "E": shape.E, "k": shape.k, "f": shape.f,
+            "tree_nodes": 65, "trees_per_block": 1, "draft": "eagle3 5 steps top-10 64 tokens",
+            "routing": routing, "router_std": router_std, "commitment": "1,.8,.55,.35,.2,.1",
+            "l2": "inputs larger than L2: each step streams ~0.7 GB of union expert weights "
+                  "(L2 is 126 MB)"}
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over the process group (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: int, world: int, slowest_s: float) -> float:
+    return units_per_rank * world / slowest_s
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [v.strip() for v in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# --------------------------------------------------------------- workload
+
+def make_trees(n_trees: int, shape, seed: int):
+    import torch
+    from expert_select_gb300 import workload as W
+    xs, deps = [], []
+    for i in range(n_trees):
+        t = W.eagle_tree(seed + i)
+        xs.append(W.hidden_states(seed + 10_000 + i, t.parent, shape.d, shape.torch_dtype))
+        deps.append(torch.from_numpy(t.depth.copy()))
+    return torch.stack(xs), torch.stack(deps)
+
+
+def oracle_block(x, wr, wg, wu, wd, depth, shape, routing, rows=None):
+    """The oracle on one tree (optionally only `rows` of its expert outputs)."""
+    from expert_select_gb300 import workload as W
+    from oracle import oracle as O
+    mode = O.ACCEPT if routing == "acceptmoe" else O.NATURAL
+    return O.forward(x, wr, wg, wu, wd, depth, shape.k, W.C_EAGLE, rows=rows, mode=mode,
+                     precision="fp32")
+
+
+def time_oracle(xs, deps, wr, wg, wu, wd, shape, routing, n_trees):
+    """Seconds per tree-block of the oracle on whole trees (all rows)."""
+    per = []
+    for i in range(n_trees):
+        t0 = time.perf_counter()
+        oracle_block(xs[i], wr, wg, wu, wd, deps[i].numpy(), shape, routing)
+        per.append(time.perf_counter() - t0)
+    return per
+
+
+class OracleSample:
+    """One bounded, scaled sample of the oracle's work on one tree: the router on
+    `rows` of its 65 rows, the whole selection (from the tree's fp32 logits, computed
+    by the oracle beforehand), and the expert layer on `assign` of its 65*k
+    assignments. The time is scaled to the whole tree:
+        t = t_router * 65/rows + t_select + t_experts * (65*k)/assign."""
+
+    def __init__(self, x, depth, wr, wg, wu, wd, shape, routing):
+        from oracle import oracle as O
+        self.O, self.x, self.depth, self.shape = O, x, depth, shape
+        self.wr, self.wg, self.wu, self.wd = wr, wg, wu, wd
+        self.mode = O.ACCEPT if routing == "acceptmoe" else O.NATURAL
+        self.l32 = O.router(x, wr).astype(np.float32)
+        sel = O.select_tree(self.l32, depth, shape.k, self._c(), mode=self.mode, precision="fp32")
+        self.idx = sel["idx"]
+
+    def _c(self):
+        from expert_select_gb300 import workload as W
+        return W.C_EAGLE
+
+    def run(self, rows: int, assign: int, rng) -> float:
+        O, x, N, k = self.O, self.x, self.x.shape[0], self.shape.k
+        rr = sorted(rng.choice(N, size=rows, replace=False).tolist())
+        t0 = time.perf_counter()
+        O.router(x[rr], self.wr)
+        t1 = time.perf_counter()
+        O.select_tree(self.l32, self.depth, k, self._c(), mode=self.mode, precision="fp32")
+        t2 = time.perf_counter()
+        picks = rng.choice(N * k, size=assign, replace=False)
+        xf = x.float().numpy().astype(np.float64)
+        t3 = time.perf_counter()
+        for a in picks:
+            O.expert_ffn(xf[a // k], int(self.idx[a // k, a % k]), self.wg, self.wu, self.wd)
+        t4 = time.perf_counter()
+        return (t1 - t0) * N / rows + (t2 - t1) + (t4 - t3) * (N * k) / assign
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    from expert_select_gb300 import build
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+
+    shape = W.QWEN3_30B_A3B
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    seed = SEED + 7919 * rank
+    xs_h, deps_h = make_trees(TREES, shape, seed)
+    wr_std = args.router_std
+    wr = W.router_weight(seed + 1, shape, std=wr_std, device=dev)
+    wg, wu, wd = W.expert_weights(seed + 2, shape, device=dev)
+    xs = xs_h.to(dev)
+    deps = deps_h.to(dev).int()
+    N = xs.shape[1]
+    ws = M.workspace(L, 1, N, device=dev)
+    y = torch.empty(N, shape.d, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+    routing_mode = {"acceptmoe": M.MOE_ROUTE_ACCEPT, "natural": M.MOE_ROUTE_NATURAL}
+
+    def loop(K, routing, counts=None, info=None, ev=None, e2e=None):
+        P = M.select_params(routing_mode[routing], W.C_EAGLE)
+        opts = M.run_opts(args.ffn_path)
+        for i in range(K):
+            j = i % TREES
+            if e2e is not None:
+                xin, din, yout, xh, dh, yh = e2e
+                xin.copy_(xh[j], non_blocking=True)
+                din.copy_(dh[j], non_blocking=True)
+                xx, dd = xin, din
+            else:
+                xx, dd = xs[j], deps[j]
+            out = None
+            if counts is not None:
+                out = M.tree_outputs(counts=counts[i], info=info[i])
+            if ev is not None:
+                opts = M.run_opts(args.ffn_path, ev[i][0], ev[i][1])
+            M.moe_tree_forward(L, P, xx, wr, wg, wu, wd, None, dd, 1, N, None,
+                               yout if e2e is not None else y, ws, out, opts)
+            if e2e is not None:
+                yh[j].copy_(yout, non_blocking=True)
+
+    def timed(K, routing, **kw):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        loop(K, routing, **kw)
+        b.record(s)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b) / 1e3, world)
+
+    K, Wm = args.steps, args.warmup
+    routing = args.routing
+    loop(Wm, routing)
+    counts = torch.zeros(K, shape.E, dtype=torch.int32, device=dev)
+    info = torch.zeros(K, 4, dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for a, b in ev:  # torch creates the CUDA event on first record
+        a.record(s)
+        b.record(s)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        sec = timed(K, routing, counts=counts, info=info, ev=ev)
+    clocks = clk.summary()
+    ffn_ms = [a.elapsed_time(b) for a, b in ev]
+    cn = counts.cpu().numpy()
+    inf = info.cpu().numpy()
+    union = (cn > 0).sum(axis=1)
+    value = whole_job_rate(K, world, sec)
+
+    # roofline of the grouped-expert stage on its algorithmic bytes
+    algo_bytes = union * shape.expert_bytes + 2 * N * shape.d * shape.elem_bytes
+    achieved = float(algo_bytes.sum() / (np.sum(ffn_ms) / 1e3)) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "ffn_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as fh:
+                pj = json.load(fh)
+            if pj.get("kernel_rev") == M.lib().moe_abi_version():
+                traffic = pj.get("bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    xh = xs_h.pin_memory()
+    dh = deps_h.int().pin_memory()
+    yh = torch.empty(TREES, N, shape.d, dtype=torch.bfloat16).pin_memory()
+    xin = torch.empty_like(xs[0])
+    din = torch.empty_like(deps[0])
+    yout = torch.empty_like(y)
+    loop(Wm, routing, e2e=(xin, din, yout, xh, dh, yh))
+    sec_e2e = timed(K, routing, e2e=(xin, din, yout, xh, dh, yh))
+    e2e = {"value": whole_job_rate(K, world, sec_e2e), "unit": UNIT,
+           "h2d_bytes_per_step": int(xin.numel() * xin.element_size() + din.numel() * 4),
+           "d2h_bytes_per_step": int(yout.numel() * yout.element_size())}
+
+    # natural routing on the same trees (the pages' Standard SD), for comparison
+    Kv = min(K, 2000)
+    loop(Wm, "natural" if routing != "natural" else "acceptmoe")
+    cnat = torch.zeros(Kv, shape.E, dtype=torch.int32, device=dev)
+    inat = torch.zeros(Kv, 4, dtype=torch.int32, device=dev)
+    other = "natural" if routing != "natural" else "acceptmoe"
+    sec_o = timed(Kv, other, counts=cnat, info=inat)
+    u_o = (cnat.cpu().numpy() > 0).sum(axis=1)
+
+    # router, select, permute, combine + the grouped-expert launches
+    launches_per_step = 4 + ffn_launches(M, L, args.ffn_path)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wg_h, wu_h, wd_h = wg.cpu(), wu.cpu(), wd.cpu()
+        per = time_oracle(xs_h, deps_h, wr.cpu(), wg_h, wu_h, wd_h, shape, routing,
+                          args.cpu_trees)
+        cpu = {"value": len(per) / sum(per), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{len(per)} whole trees of this workload (65 rows each), oracle "
+                         f"single-threaded on {cpu_model()}",
+               "seconds": round(sum(per), 2)}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": round(sec / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded EAGLE-3-shaped trees, N(0,0.02) weights)",
+        "config": dict(workload_config(shape, routing, wr_std), parallelism=f"replicas{world}"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "grouped SwiGLU experts", "peak_kind": peak_kind,
+                     "ffn_ms_mean": round(float(np.mean(ffn_ms)), 5),
+                     "algo_bytes_per_launch_mean": int(algo_bytes.mean())},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * K),
+        "clocks": clocks,
+        "union": {"mean": float(union.mean()), "min": int(union.min()), "max": int(union.max()),
+                  "natural_mean": float(inf[:, 0].mean()), "selected_mean": float(inf[:, 1].mean()),
+                  "m_mean": float(inf[:, 2].mean()),
+                  f"{other}_union_mean": float(u_o.mean()),
+                  f"{other}_value": round(whole_job_rate(Kv, world, sec_o), 2)},
+    }
+    print(json.dumps(line))
+
+
+def ffn_launches(M, L, path):
+    """Kernel launches of the grouped-expert stage per step (gate/up + down)."""
+    return 2
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    from expert_select_gb300 import workload as W
+    from oracle import oracle as O
+
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    O.build()
+    shape = W.QWEN3_30B_A3B
+    n_trees = 4
+    xs_h, deps_h = make_trees(n_trees, shape, SEED)
+    wr = W.router_weight(SEED + 1, shape, std=args.router_std)
+    wg, wu, wd = W.expert_weights(SEED + 2, shape)
+    samples = [OracleSample(xs_h[i], deps_h[i].numpy(), wr, wg, wu, wd, shape, args.routing)
+               for i in range(n_trees)]
+    # size each step's sample so the whole run is about 75 s of oracle work
+    budget = 75.0 / (args.steps + args.warmup)
+    rng = np.random.default_rng(0)
+    t_row = samples[0].run(1, 1, rng)  # warm-up and a cost probe
+    rows = 65 if budget > 0.25 else (8 if budget > 0.05 else 1)
+    assign = int(max(1, min(65 * shape.k, (budget - 0.001 * rows) / 0.012)))
+    per = []
+    for i in range(args.warmup + args.steps):
+        t = samples[i % n_trees].run(rows, assign, rng)
+        if i >= args.warmup:
+            per.append(t)
+    del t_row
+    sec = sum(per)
+    value = args.steps / sec
+    sample = (f"per step: one tree of this workload; router on {rows} of 65 rows, the whole "
+              f"selection, experts on {assign} of {65 * shape.k} assignments; each part's time "
+              f"scaled to the whole tree; oracle single-threaded on {cpu_model()}")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded EAGLE-3-shaped trees, N(0,0.02) weights)",
+        "config": dict(workload_config(shape, args.routing, args.router_std),
+                       parallelism="cpu-oracle"),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--routing", choices=["acceptmoe", "natural"], default="acceptmoe")
+    ap.add_argument("--router-std", type=float, default=0.02)
+    ap.add_argument("--ffn-path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
+    ap.add_argument("--cpu-trees", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

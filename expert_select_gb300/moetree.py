@@ -164,9 +164,18 @@ def moe_expert_permute(L, topk_idx, counts, offsets, perm, ws, stream=None):
         _ptr(ws), _stream(stream)))
 
 
+def _event(ev):
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        raise ValueError("torch.cuda.Event has no CUDA event yet: record it once first")
+    return C.c_void_p(ev.cuda_event)
+
+
 def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None) -> RunOpts:
-    return RunOpts(ffn_path, None if begin is None else C.c_void_p(begin.cuda_event),
-                   None if end is None else C.c_void_p(end.cuda_event))
+    """Options for moe_expert_forward / moe_tree_forward. `begin`/`end` are
+    torch.cuda.Event objects recorded around the grouped-expert kernel."""
+    return RunOpts(ffn_path, _event(begin), _event(end))
 
 
 def moe_expert_forward(L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, y, ws,
@@ -255,8 +264,8 @@ def moe_expert_upload(L, host_gate, host_up, host_down, slot_gate, slot_up, slot
         C.byref(L), _ptr(host_gate), _ptr(host_up), _ptr(host_down), _ptr(slot_gate),
         _ptr(slot_up), _ptr(slot_down), ue.ctypes.data_as(C.c_void_p),
         us.ctypes.data_as(C.c_void_p), len(ue), C.c_void_p(side_stream.cuda_stream),
-        None if done_event is None else C.c_void_p(done_event.cuda_event)))
+        _event(done_event)))
 
 
 def moe_event_wait(event, timeout_s: float) -> None:
-    _check("moe_event_wait", lib().moe_event_wait(C.c_void_p(event.cuda_event), float(timeout_s)))
+    _check("moe_event_wait", lib().moe_event_wait(_event(event), float(timeout_s)))
