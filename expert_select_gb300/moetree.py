@@ -32,7 +32,7 @@ EXPORTS = (
     "moe_tree_select", "moe_expert_permute", "moe_expert_forward", "moe_tree_forward",
     "moe_workspace_check", "moe_residency_create", "moe_residency_destroy",
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
-    "moe_event_wait",
+    "moe_event_wait", "moe_tree_forward_noalloc",
 )
 
 
@@ -89,6 +89,7 @@ def lib() -> C.CDLL:
             "moe_residency_publish": ([P, I, P, P, P], I),
             "moe_expert_upload": ([P, P, P, P, P, P, P, P, P, I, P, P], I),
             "moe_event_wait": ([P, C.c_double], I),
+            "moe_tree_forward_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -201,6 +202,18 @@ def moe_tree_forward(L, P, x, W_r, W_gate, W_up, W_down, slot_of_expert, depth, 
         _ptr(slot_of_expert), _ptr(depth), B, N, _ptr(resident), _ptr(y),
         None if out is None else C.byref(out), _ptr(ws),
         None if opts is None else C.byref(opts), _stream(stream)))
+
+
+def moe_tree_forward_noalloc(L, P, x, W_r, W_gate, W_up, W_down, slot_of_expert, depth, B, N,
+                             resident, y, out: Optional[TreeOutputs] = None,
+                             opts: Optional[RunOpts] = None, stream=None):
+    """moe_tree_forward with the library's built-in 16 MiB scratch instead of a
+    caller-allocated workspace (for callers that cannot allocate device memory)."""
+    return _check("moe_tree_forward_noalloc", lib().moe_tree_forward_noalloc(
+        C.byref(L), C.byref(P), _ptr(x), _ptr(W_r), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+        _ptr(slot_of_expert), _ptr(depth), B, N, _ptr(resident), _ptr(y),
+        None if out is None else C.byref(out), None if opts is None else C.byref(opts),
+        _stream(stream)))
 
 
 def moe_workspace_check(ws, stream=None) -> int:

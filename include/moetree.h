@@ -189,6 +189,32 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
                             const moe_tree_outputs *out, void *workspace,
                             const moe_run_opts *opts, moe_stream_t stream);
 
+/* moe_tree_forward without a `workspace` argument, for callers that cannot allocate
+ * device memory when they run the layer: an engine whose free HBM is already reserved
+ * for its KV cache, a plug-in that is handed only input/output device pointers, or a
+ * loop that must not let cudaMalloc/cudaFree synchronise the device. The pages have no
+ * counterpart to this entry point; it is a deployment convenience of this library.
+ *   - Scratch is one built-in 16 MiB device array (a file-scope __device__ buffer).
+ *     Every device that has loaded it keeps those 16 MiB until the process exits.
+ *     Requests whose moe_workspace_bytes(L, B, N) exceed 16 MiB return
+ *     MOE_ERR_UNSUPPORTED (one 65-node tree of the Qwen3-30B-A3B- or GPT-OSS-120B-shaped
+ *     layer needs about 8 MiB); nothing is enqueued then.
+ *   - The first call on a device looks up that array's device address (with that
+ *     device current); make that first call before any stream capture begins.
+ *   - All calls in the process share the one array, and it keeps the last call's
+ *     contents; what must start at zero is cleared by the call itself. Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads without
+ *     ordering) race on the array: order them on one stream.
+ *   - Calls no allocating routine. Other arguments, results and errors are those of
+ *     moe_tree_forward. */
+moe_status moe_tree_forward_noalloc(const moe_layer_desc *L, const moe_select_params *P,
+                                    const void *x, const void *W_r, const void *W_gate,
+                                    const void *W_up, const void *W_down,
+                                    const int *slot_of_expert, const int *depth, int B, int N,
+                                    const uint8_t *resident, void *y,
+                                    const moe_tree_outputs *out, const moe_run_opts *opts,
+                                    moe_stream_t stream);
+
 /* Reads and clears the kernel-side check word of a workspace. Waits for `stream`.
  * *flags = 0 when no kernel reported a problem since the last call; bit 0 = an
  * expert id outside [0, E) was skipped; bit 1 = a bounded device wait gave up. */
