@@ -385,8 +385,11 @@ def run_gpu(args):
 
 
 def ffn_launches(M, L, path):
-    """Kernel launches of the grouped-expert stage per step (gate/up + down)."""
-    return 2
+    """Kernel launches of the grouped-expert stage per step: CUDA cores = gate/up +
+    down; tensor cores = token-row gather + gate/up + down."""
+    tc = path == M.MOE_FFN_TCGEN05 or (path == M.MOE_FFN_AUTO and L.dtype == M.MOE_DTYPE_BF16
+                                       and L.d % 64 == 0 and L.f % 64 == 0)
+    return 3 if tc else 2
 
 
 # ------------------------------------------------------------ reference arm

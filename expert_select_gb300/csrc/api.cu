@@ -34,6 +34,7 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.perm = take(A * 4);
     w.pos = take(A * 4);
     w.active = take((E + 1) * 4);
+    w.rowtiles = take((size_t)(1 + 4 * max_rowtiles(L.E, (int)A)) * 4);
     w.xp = take(A * L.d * elem_size(L.dtype));
     w.h = take(A * L.f * 4);
     w.o = take(A * L.d * 4);
@@ -44,7 +45,8 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
 static bool desc_ok(const moe_layer_desc *L) {
     return L && L->k >= 1 && L->k <= kMaxK && L->E >= L->k && L->E <= kMaxE && L->d >= 8 &&
            L->d % 8 == 0 && L->d <= kMaxD && L->f >= 8 && L->f % 8 == 0 && L->f <= kMaxD &&
-           (L->dtype == MOE_DTYPE_F32 || L->dtype == MOE_DTYPE_BF16);
+           (L->dtype == MOE_DTYPE_F32 || L->dtype == MOE_DTYPE_BF16) && L->slots >= 0 &&
+           L->slots <= 65535;
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -86,7 +88,9 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
                               cudaStream_t s) {
     int *flags = at<int>(ws, w.flags);
     int *pos = at<int>(ws, w.pos), *active = at<int>(ws, w.active);
-    cudaError_t err = launch_permute(L, idx, R, counts, offsets, perm, pos, active, flags, s);
+    int *rowtiles = at<int>(ws, w.rowtiles);
+    cudaError_t err =
+        launch_permute(L, idx, R, counts, offsets, perm, pos, active, rowtiles, flags, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
 
     FfnArgs fa{};
@@ -99,12 +103,14 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
     fa.offsets = offsets;
     fa.perm = perm;
     fa.active = active;
+    fa.rowtiles = rowtiles;
     fa.R = R;
     fa.d = L.d;
     fa.f = L.f;
     fa.E = L.E;
     fa.k = L.k;
     fa.dtype = L.dtype;
+    fa.slots = L.slots > 0 ? L.slots : L.E;
     fa.flags = flags;
     fa.xp = at<void>(ws, w.xp);
     fa.h = at<void>(ws, w.h);
@@ -184,6 +190,7 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
     const Workspace w = workspace_layout(*L, 1, R);
     return cuda_status(launch_permute(*L, topk_idx, R, counts, offsets, perm,
                                       at<int>(workspace, w.pos), at<int>(workspace, w.active),
+                                      at<int>(workspace, w.rowtiles),
                                       at<int>(workspace, w.flags), (cudaStream_t)stream));
 }
 

@@ -30,6 +30,7 @@ struct Workspace {
     size_t perm;      // i32 [A]  permuted position -> assignment id
     size_t pos;       // i32 [A]  assignment id -> permuted position (-1 = skipped)
     size_t active;    // i32 [E + 1]  [0] = n_active, then active experts ascending
+    size_t rowtiles;  // i32 [1 + 4 * max_rowtiles]: count, then (expert, first token, tokens, 0)
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
     size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)
     size_t o;         // f32 [A, d]  expert outputs in permuted order
@@ -52,9 +53,13 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s);
 
+// Token rows per row tile of the tensor-core expert kernel (its largest MMA N).
+constexpr int kRowTile = 256;
+inline int max_rowtiles(int E, int A) { return E + (A + kRowTile - 1) / kRowTile + 1; }
+
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
-                           int *offsets, int *perm, int *pos, int *active, int *flags,
-                           cudaStream_t s);
+                           int *offsets, int *perm, int *pos, int *active, int *rowtiles,
+                           int *flags, cudaStream_t s);
 size_t permute_smem_bytes(int R, int E);
 
 struct FfnArgs {
@@ -62,8 +67,9 @@ struct FfnArgs {
     const void *Wg, *Wu; // [S, f, d]
     const void *Wd;      // [S, d, f]
     const int *slot;     // [E] or nullptr
-    const int *counts, *offsets, *perm, *active;
+    const int *counts, *offsets, *perm, *active, *rowtiles;
     int R, d, f, E, k, dtype;
+    int slots;           // expert slots in the weight pools
     int *flags;
     void *xp;            // gathered x (tensor-core path)
     void *h;             // activations

@@ -24,10 +24,10 @@ constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32
 constexpr int kTok = 8;                              // token rows per pass
 
 template <typename T>
-__device__ __forceinline__ const T *expert_base(const void *W, const int *slot, int e,
+__device__ __forceinline__ const T *expert_base(const void *W, const int *slot, int slots, int e,
                                                 size_t per_expert, int *flags, bool &ok) {
     const int s = slot ? slot[e] : e;
-    ok = s >= 0;
+    ok = s >= 0 && s < slots;
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(flags, FLAG_BAD_EXPERT);
         return nullptr;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads) ffn_gateup_simt(FfnArgs a) {
     const int cnt = a.counts[e];
     if (cnt == 0) return;
     bool ok;
-    const T *Wg = expert_base<T>(a.Wg, a.slot, e, (size_t)a.f * a.d, a.flags, ok);
+    const T *Wg = expert_base<T>(a.Wg, a.slot, a.slots, e, (size_t)a.f * a.d, a.flags, ok);
     if (!ok) return;
     const T *Wu = reinterpret_cast<const T *>(a.Wu) + (Wg - reinterpret_cast<const T *>(a.Wg));
     extern __shared__ float xs[];  // [kTok][d]
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) ffn_down_simt(FfnArgs a) {
     const int cnt = a.counts[e];
     if (cnt == 0) return;
     bool ok;
-    const T *Wd = expert_base<T>(a.Wd, a.slot, e, (size_t)a.f * a.d, a.flags, ok);
+    const T *Wd = expert_base<T>(a.Wd, a.slot, a.slots, e, (size_t)a.f * a.d, a.flags, ok);
     if (!ok) return;
     extern __shared__ float hs[];  // [kTok][f]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -1,7 +1,587 @@
-// Placeholder until the tcgen05 grouped-expert kernel lands.
+// Grouped SwiGLU experts on the 5th-generation tensor cores (tcgen05 + TMA + TMEM)
+// ("MoE and speculative decoding" blog, "grouped GEMM for active experts"):
+//   phase 1  h   = silu(X_e W_gate[e]^T) * (X_e W_up[e]^T)      (bf16 out)
+//   phase 2  O_e = h W_down[e]^T                                (fp32 out)
+// for every expert e with assignments, X_e its token rows in permuted order.
+//
+// A verification block routes only ~4-20 tokens to an expert, so the weights are
+// the large operand: each unit of work streams one 128-row weight tile through
+// shared memory once and multiplies it by all of the expert's tokens (up to 256).
+// The weight tile is the MMA's A operand (M = 128 rows: 64 W_gate rows stacked on
+// the same 64 W_up rows in phase 1, 128 W_down rows in phase 2), the token rows are
+// the B operand (N = tokens rounded up to 16), and the fp32 accumulator lives in
+// tensor memory. Both operands are K-major bf16 tiles of 64 elements (one 128-byte
+// swizzle atom) loaded by TMA with 128-byte swizzling, which is the layout the
+// tcgen05 shared-memory descriptors describe.
+//
+// One persistent CTA per SM (192 threads, warp-specialised):
+//   warp 0       TMA producer (one lane) filling a ring of `stages` buffers
+//   warp 1       TMEM allocator and MMA issuer (one lane)
+//   warps 2..5   epilogue: tcgen05.ld the accumulator (each warp may read the 32
+//                TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
+// Two 256-column accumulators alternate so the epilogue of one unit overlaps the
+// MMAs of the next. Units (row tile x weight tile) are dealt round-robin over CTAs.
+//
+// Every wait is bounded: after 2 s a wait gives up, sets the workspace check bit
+// FLAG_WAIT_TIMEOUT and makes the CTA stop; the CTA then waits (again bounded) for
+// its TMA loads and MMAs in flight, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
-bool ffn_tc_supported(const moe_layer_desc &) { return false; }
-cudaError_t launch_ffn_tc(const FfnArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 64;                     // K elements per stage: one 128-B swizzle atom
+constexpr int kM = 128;                     // MMA M: weight rows per unit
+constexpr int kAccCols = 256;               // TMEM columns per accumulator (max N)
+constexpr int kTmemCols = 2 * kAccCols;     // two accumulators
+constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
+constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
+constexpr int kCtlBytes = 256;
+
+struct Maps {
+    CUtensorMap a0;          // phase 1: W_gate [S][f][d], box 64x64x1; phase 2: W_down [S][d][f], box 64x128x1
+    CUtensorMap a1;          // phase 1: W_up, box 64x64x1
+    CUtensorMap b[kBoxes];   // token rows [A][K] (gathered x or h), box 64 x (16 << i)
+};
+
+struct Params {
+    int K;        // reduction length: d (phase 1) or f (phase 2)
+    int m_tiles;  // weight tiles per expert
+    int out_ld;   // row length of the output: f (phase 1) or d (phase 2)
+    int stages;
+    int box_cap;  // rows of the per-stage token buffer
+    int slots;    // expert slots in the weight pool
+    const int *rowtiles, *offsets, *slot;
+    int *flags;
+    __nv_bfloat16 *h;
+    float *o;
+};
+
+// ------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with parity `parity`. Gives up when *abort is set
+// (if abort != nullptr) or after kTimeoutNs; a timeout sets *abort and the check bit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *flags) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (abort && *abort) return false;
+            const unsigned long long t = now_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kTimeoutNs) {
+                if (abort) *abort = 1;
+                atomicOr(flags, FLAG_WAIT_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile with 128-byte swizzling:
+// rows of 128 B, 8-row groups 1024 B apart (stride byte offset), fixed field 0b001 at
+// bit 46, swizzle mode 2 (128 B) at bits 61-63. The leading byte offset is unused for
+// swizzled K-major tiles.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// N and M encoded as N/8 and M/16.
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier of the four epilogue warps (bar.sync is warp-aligned: reconverge first).
+__device__ __forceinline__ void epi_bar() {
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Which token-row box (16 << i rows) holds n tokens.
+__device__ __forceinline__ int box_of(int n) {
+    int i = 0;
+    while ((16 << i) < n && i < kBoxes - 1) ++i;
+    return i;
+}
+
+struct Unit {
+    int e, n0, ntok, slot, m;
+};
+
+__device__ __forceinline__ bool decode(const Params &p, int u, Unit &w) {
+    const int rt = u / p.m_tiles;
+    w.m = u - rt * p.m_tiles;
+    const int *t = p.rowtiles + 1 + 4 * rt;
+    w.e = t[0];
+    w.n0 = t[1];
+    w.ntok = t[2];
+    w.slot = p.slot ? p.slot[w.e] : w.e;
+    return w.slot >= 0 && w.slot < p.slots && w.ntok > 0;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int PHASE>
+__global__ void __launch_bounds__(kThreads, 1)
+ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int S = p.stages;
+    const uint32_t b_bytes = (uint32_t)p.box_cap * 128u;
+    const uint32_t sA = base, sB = base + (uint32_t)S * kABytes;
+    uint8_t *ctl = gbase + (size_t)S * (kABytes + b_bytes);
+    const uint32_t ctl_s = base + (uint32_t)S * (kABytes + b_bytes);
+    // control block: full[S], empty[S], tfull[2], tempty[2], done, tmem slot, abort, ok[2]
+    const uint32_t full = ctl_s, empty = ctl_s + 8 * S, tfull = ctl_s + 16 * S,
+                   tempty = tfull + 16, done = tempty + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 16 * S + 40);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctl + 16 * S + 44);
+    volatile int *epi_ok = reinterpret_cast<volatile int *>(ctl + 16 * S + 48);  // [2]
+    float *sg = reinterpret_cast<float *>(ctl + kCtlBytes);  // [64][kSgStride]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + 8 * a, 1);
+            mbar_init(tempty + 8 * a, 128);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&maps.a0);
+        if (PHASE == 1) prefetch_map(&maps.a1);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_units = p.rowtiles[0] * p.m_tiles;
+    const int kchunks = p.K / kBK;
+    constexpr int kRowsA = PHASE == 1 ? 64 : 128;
+
+    uint32_t issued = 0, last_par = 0;  // producer: stages with a load issued, parity of it
+    bool mma_issued = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+                Unit w;
+                if (!decode(p, u, w)) {
+                    atomicOr(p.flags, FLAG_BAD_EXPERT);
+                    continue;
+                }
+                const int bx = box_of((w.ntok + 15) & ~15);
+                const uint32_t bb = (uint32_t)(16 << bx) * 128u;
+                const int brow = p.offsets[w.e] + w.n0;
+                for (int kc = 0; kc < kchunks; ++kc) {
+                    if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.flags)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full + 8 * s;
+                    mbar_expect_tx(fb, kABytes + bb);
+                    const uint32_t a = sA + (uint32_t)s * kABytes;
+                    tma_load_3d(a, &maps.a0, kc * kBK, w.m * kRowsA, w.slot, fb, pol);
+                    if (PHASE == 1)
+                        tma_load_3d(a + kABytes / 2, &maps.a1, kc * kBK, w.m * kRowsA, w.slot, fb,
+                                    pol);
+                    tma_load_2d(sB + (uint32_t)s * b_bytes, &maps.b[bx], kc * kBK, brow, fb);
+                    issued |= 1u << s;
+                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0, it = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+                Unit w;
+                if (!decode(p, u, w)) continue;
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                ++it;
+                if (!mbar_wait(tempty + 8 * acc, aph ^ 1u, abort_flag, p.flags)) break;
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16((uint32_t)((w.ntok + 15) & ~15));
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
+                for (int kc = 0; kc < kchunks; ++kc) {
+                    if (!mbar_wait(full + 8 * s, ph, abort_flag, p.flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = sA + (uint32_t)s * kABytes, b = sB + (uint32_t)s * b_bytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        mma_bf16(d_tmem, sw128_desc(a + 32u * k), sw128_desc(b + 32u * k), idesc,
+                                 (kc | k) != 0);
+                    mma_issued = true;
+                    mma_commit(empty + 8 * s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(tfull + 8 * acc);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;          // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;   // accumulator row
+        int it = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            Unit w;
+            if (!decode(p, u, w)) continue;
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            ++it;
+            // one thread waits, the named barrier releases the others; the verdict slot
+            // alternates so the next unit's write cannot overtake a late reader
+            if (threadIdx.x == 64)
+                epi_ok[acc] = mbar_wait(tfull + 8 * acc, aph, abort_flag, p.flags);
+            epi_bar();
+            if (!epi_ok[acc]) break;  // uniform over the four warps
+            tc_fence_after();
+            const int N = (w.ntok + 15) & ~15;
+            const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
+            const size_t row0 = (size_t)p.offsets[w.e] + w.n0;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + (uint32_t)c0, v);
+                if (PHASE == 1) {
+                    if (q < 2) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float g = __uint_as_float(v[c]);
+                            sg[row * kSgStride + c] = g / (1.f + __expf(-g));
+                        }
+                    }
+                    epi_bar();
+                    if (q >= 2) {
+                        const int i = row - 64;
+                        __nv_bfloat16 *hp = p.h + row0 * p.out_ld + (size_t)w.m * 64 + i;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int tok = c0 + c;
+                            if (tok < w.ntok)
+                                hp[(size_t)tok * p.out_ld] =
+                                    __float2bfloat16_rn(sg[i * kSgStride + c] * __uint_as_float(v[c]));
+                        }
+                    }
+                    epi_bar();
+                } else {
+                    const int drow = w.m * kM + row;
+                    if (drow < p.out_ld) {
+                        float *op = p.o + row0 * p.out_ld + drow;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int tok = c0 + c;
+                            if (tok < w.ntok) op[(size_t)tok * p.out_ld] = __uint_as_float(v[c]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty + 8 * acc);
+        }
+    }
+
+    // ---- teardown: nothing may be in flight when the CTA frees TMEM and exits ----
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < S; ++s)
+            if (issued & (1u << s)) mbar_wait(full + 8 * s, (last_par >> s) & 1u, nullptr, p.flags);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+        mma_commit(done);
+        mbar_wait(done, 0, nullptr, p.flags);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+// Gathers the token rows of every assignment into permuted order: xp[p] = x[perm[p] / k].
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ perm,
+                   const int *__restrict__ offsets, int E, int k, int d,
+                   __nv_bfloat16 *__restrict__ xp) {
+    const int pidx = blockIdx.x;
+    if (pidx >= offsets[E]) return;
+    const int r = perm[pidx] / k;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pidx * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+            const uint64_t *row_strides, const uint32_t *box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = row_strides[i];
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd,
+              gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weight pool [S][rows][K] as a 3-D map with a 64 x box_rows x 1 box.
+bool encode_weights(CUtensorMap *m, const void *w, int S, int rows, int K, int box_rows) {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)S};
+    const uint64_t st[2] = {(uint64_t)K * 2, (uint64_t)rows * K * 2};
+    const uint32_t box[3] = {(uint32_t)kBK, (uint32_t)box_rows, 1};
+    return encode(m, w, 3, dims, st, box);
+}
+
+// Token rows [A][K] as 2-D maps with 64 x (16 << i) boxes.
+bool encode_rows(CUtensorMap *maps, const void *t, int A, int K) {
+    for (int i = 0; i < kBoxes; ++i) {
+        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)A};
+        const uint64_t st[1] = {(uint64_t)K * 2};
+        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(16 << i)};
+        if (!encode(&maps[i], t, 2, dims, st, box)) return false;
+    }
+    return true;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+size_t smem_bytes(int stages, int box_cap) {
+    return 1024 + (size_t)stages * (kABytes + (size_t)box_cap * 128) + kCtlBytes +
+           64 * kSgStride * sizeof(float);
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_layer_desc &L) {
+    if (L.dtype != MOE_DTYPE_BF16 || L.d % 64 != 0 || L.f % 64 != 0) return false;
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return false;
+    return major >= 10 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
+    const int A = a.R * a.k;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    // token-row buffer per stage: the box that holds min(256, R) rows (a row picks an
+    // expert at most once, so no expert has more than R tokens)
+    int box_cap = 16;
+    const int need = ((std::min(a.R, kRowTile) + 15) / 16) * 16;
+    while (box_cap < need) box_cap <<= 1;
+    const size_t budget = 227 * 1024;
+    int stages = 8;
+    while (stages > 2 && smem_bytes(stages, box_cap) > budget) --stages;
+    const size_t smem = smem_bytes(stages, box_cap);
+    const int S = a.slots;
+
+    Maps m1{}, m2{};
+    if (!encode_weights(&m1.a0, a.Wg, S, a.f, a.d, 64) ||
+        !encode_weights(&m1.a1, a.Wu, S, a.f, a.d, 64) || !encode_rows(m1.b, a.xp, A, a.d) ||
+        !encode_weights(&m2.a0, a.Wd, S, a.d, a.f, 128) || !encode_rows(m2.b, a.h, A, a.f))
+        return cudaErrorInvalidValue;
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(ffn_tc_kernel<1>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(
+                ffn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    gather_rows_kernel<<<A, 256, 0, s>>>((const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k,
+                                         a.d, (__nv_bfloat16 *)a.xp);
+    Params p{};
+    p.stages = stages;
+    p.box_cap = box_cap;
+    p.slots = S;
+    p.rowtiles = a.rowtiles;
+    p.offsets = a.offsets;
+    p.slot = a.slot;
+    p.flags = a.flags;
+    p.h = (__nv_bfloat16 *)a.h;
+    p.o = a.o;
+    p.K = a.d;
+    p.m_tiles = a.f / 64;
+    p.out_ld = a.f;
+    ffn_tc_kernel<1><<<nsm, kThreads, smem, s>>>(m1, p);
+    p.K = a.f;
+    p.m_tiles = (a.d + kM - 1) / kM;
+    p.out_ld = a.d;
+    ffn_tc_kernel<2><<<nsm, kThreads, smem, s>>>(m2, p);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -8,8 +8,8 @@
 // prefix; an assignment's position is then
 //   offsets[e] + prefix[block][e] + popc(mask[block][e] & lanes_below(row)).
 // Everything stays in shared memory: (R/32) x E x 8 bytes (133 KB at 4160 rows and
-// 128 experts). The same kernel also writes the active-expert list the grouped
-// expert kernels walk.
+// 128 experts). The same kernel also writes the active-expert list and the list of
+// row tiles (at most 256 tokens of one expert) that the grouped expert kernels walk.
 #include "common.cuh"
 
 namespace moe {
@@ -20,7 +20,7 @@ constexpr int kThreads = 1024;
 __global__ void __launch_bounds__(kThreads)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
-               int *__restrict__ active, int *__restrict__ flags) {
+               int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags) {
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
     uint32_t *mask = sm;                  // [nb][E]
@@ -58,6 +58,17 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         }
         off[E] = s;
         active[0] = na;
+        // row tiles of at most kRowTile tokens of one expert, for the tensor-core kernel
+        int nrt = 0;
+        for (int e = 0; e < E; ++e)
+            for (int n0 = 0; n0 < cnt[e]; n0 += kRowTile) {
+                int *t = rowtiles + 1 + 4 * nrt++;
+                t[0] = e;
+                t[1] = n0;
+                t[2] = min(kRowTile, cnt[e] - n0);
+                t[3] = 0;
+            }
+        rowtiles[0] = nrt;
     }
     __syncthreads();
     for (int e = tid; e <= E; e += kThreads) {
@@ -91,14 +102,14 @@ size_t permute_smem_bytes(int R, int E) {
 }
 
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
-                           int *offsets, int *perm, int *pos, int *active, int *flags,
-                           cudaStream_t s) {
+                           int *offsets, int *perm, int *pos, int *active, int *rowtiles,
+                           int *flags, cudaStream_t s) {
     const size_t smem = permute_smem_bytes(R, L.E);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     permute_kernel<<<1, kThreads, smem, s>>>(idx, R, L.k, L.E, counts, offsets, perm, pos, active,
-                                             flags);
+                                             rowtiles, flags);
     return cudaGetLastError();
 }
 

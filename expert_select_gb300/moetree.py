@@ -43,7 +43,8 @@ class MoeError(RuntimeError):
 
 
 class LayerDesc(C.Structure):
-    _fields_ = [("d", C.c_int), ("E", C.c_int), ("k", C.c_int), ("f", C.c_int), ("dtype", C.c_int)]
+    _fields_ = [("d", C.c_int), ("E", C.c_int), ("k", C.c_int), ("f", C.c_int), ("dtype", C.c_int),
+                ("slots", C.c_int)]
 
 
 class SelectParams(C.Structure):
@@ -118,9 +119,10 @@ def _stream(stream=None):
     return C.c_void_p(s.cuda_stream)
 
 
-def layer_desc(d: int, E: int, k: int, f: int, dtype) -> LayerDesc:
+def layer_desc(d: int, E: int, k: int, f: int, dtype, slots: int = 0) -> LayerDesc:
+    """slots: expert slots in the weight pools (0 = E, one slot per expert)."""
     code = MOE_DTYPE_BF16 if dtype in (torch.bfloat16, "bf16") else MOE_DTYPE_F32
-    return LayerDesc(d, E, k, f, code)
+    return LayerDesc(d, E, k, f, code, slots)
 
 
 def select_params(mode: int = MOE_ROUTE_ACCEPT, c: Sequence[float] = (1.0,), pool_all=False,

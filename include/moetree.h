@@ -65,11 +65,14 @@ typedef enum { MOE_ROUTE_NATURAL = 0, MOE_ROUTE_ACCEPT = 1, MOE_ROUTE_FIXED_B = 
 typedef enum { MOE_FFN_AUTO = 0, MOE_FFN_SIMT = 1, MOE_FFN_TCGEN05 = 2 } moe_ffn_path;
 
 /* One MoE layer: hidden size d, E routed experts, top-k, SwiGLU width f.
- * Limits: 1 <= k <= 16, k <= E <= 256, d and f multiples of 8 and at most 6144
- * (multiples of 64 for the tcgen05 expert kernel). */
+ * `slots` is the number of expert slots in the weight pools the expert entry points
+ * read (0 means E: one slot per expert). Limits: 1 <= k <= 16, k <= E <= 256, d and f
+ * multiples of 8 and at most 6144 (multiples of 64 for the tcgen05 expert kernel),
+ * 0 <= slots <= 65535. */
 typedef struct {
     int d, E, k, f;
     int dtype; /* moe_dtype */
+    int slots;
 } moe_layer_desc;
 
 #define MOE_MAX_DEPTHS 16
@@ -171,8 +174,10 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
  * assignment streams its weights from HBM once per launch (a token count above 256
  * re-streams them once per 256 tokens).
  *   x [R, d] device; y [R, d] device, layer dtype.
- *   W_gate, W_up [S, f, d] and W_down [S, d, f] device: a pool of S expert slots.
- *   slot_of_expert [E] device int32 maps expert -> slot, or NULL for slot = expert.
+ *   W_gate, W_up [S, f, d] and W_down [S, d, f] device: a pool of S = L->slots (or E)
+ *   expert slots.
+ *   slot_of_expert [E] device int32 maps expert -> slot, or NULL for slot = expert. An
+ *   expert routed to a slot outside [0, S) is skipped and flagged (moe_workspace_check).
  *   topk_idx [R, k] device int32, gates [R, k] device fp32. */
 moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void *W_gate,
                               const void *W_up, const void *W_down, const int *slot_of_expert,

@@ -243,12 +243,21 @@ def _weights(shape, seed, device=DEV, E=None):
     return W.expert_weights(seed, shape, device=device, n_experts=E)
 
 
+GPTOSS32 = W.LayerShape(d=2880, E=32, k=4, f=2880, dtype="bf16")
+SMALL_BF16 = W.LayerShape(d=256, E=16, k=2, f=128, dtype="bf16")
+
 EXPERT_CASES = [
     ("tiny-simt", W.TINY, 9, 0.0, M.MOE_FFN_SIMT, None),
     ("tiny-ragged", W.TINY, 23, 1.2, M.MOE_FFN_SIMT, None),
     ("qwen-simt", W.QWEN3_30B_A3B, 65, 1.0, M.MOE_FFN_SIMT, 24),
-    ("gptoss-simt", W.LayerShape(d=2880, E=32, k=4, f=2880, dtype="bf16"), 65, 0.7,
-     M.MOE_FFN_SIMT, 24),
+    ("gptoss-simt", GPTOSS32, 65, 0.7, M.MOE_FFN_SIMT, 24),
+    ("small-tc-1row", SMALL_BF16, 1, 0.0, M.MOE_FFN_TCGEN05, None),
+    ("small-tc", SMALL_BF16, 37, 1.0, M.MOE_FFN_TCGEN05, None),
+    ("qwen-tc", W.QWEN3_30B_A3B, 65, 1.0, M.MOE_FFN_TCGEN05, 24),
+    ("qwen-tc-skewed", W.QWEN3_30B_A3B, 65, 3.0, M.MOE_FFN_TCGEN05, 24),
+    ("qwen-tc-4160rows", W.QWEN3_30B_A3B, 4160, 0.8, M.MOE_FFN_TCGEN05, 16),
+    ("qwen-tc-600rows-hot", W.QWEN3_30B_A3B, 600, 2.0, M.MOE_FFN_TCGEN05, 16),
+    ("gptoss-tc", GPTOSS32, 65, 0.7, M.MOE_FFN_TCGEN05, 24),
 ]
 
 
@@ -271,6 +280,56 @@ def test_expert_forward(case):
     ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64),
                         rows=sample.tolist())
     _assert_close_rows(y.float().cpu().numpy()[sample], ref, shape)
+
+
+@pytest.mark.parametrize("shape,R,skew", [(SMALL_BF16, 65, 1.0), (W.QWEN3_30B_A3B, 65, 1.0),
+                                          (W.QWEN3_30B_A3B, 520, 2.0), (GPTOSS32, 33, 0.5)])
+def test_tcgen05_matches_simt(shape, R, skew):
+    """The tensor-core and CUDA-core expert kernels agree on the same inputs."""
+    L = _desc(shape)
+    wg, wu, wd = _weights(shape, 61)
+    x = W.hidden_states(62, np.arange(-1, R - 1, dtype=np.int32), shape.d, shape.torch_dtype)
+    ti = torch.from_numpy(W.random_assignments(63, R, shape.E, shape.k, skew)).to(DEV)
+    tg = torch.from_numpy(W.random_gates(64, R, shape.k)).to(DEV)
+    ys = []
+    for path in (M.MOE_FFN_SIMT, M.MOE_FFN_TCGEN05):
+        y = torch.empty(R, shape.d, dtype=shape.torch_dtype, device=DEV)
+        ws = M.workspace(L, 1, R)
+        M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, ti, tg, y, ws, M.run_opts(path))
+        _sync()
+        assert M.moe_workspace_check(ws) == 0
+        ys.append(y.float().cpu().numpy())
+    ref = ys[0].astype(np.float64)
+    assert np.abs(ys[1] - ref).max() <= 2e-2 * np.abs(ref).max()
+
+
+def test_tcgen05_slot_pool_larger_than_E():
+    """Experts addressed through a slot map into a pool of S > E slots (the offload
+    layout): same result as the plain [E] layout."""
+    shape = SMALL_BF16
+    S = 24
+    wg, wu, wd = _weights(shape, 71)
+    slot = np.random.default_rng(5).choice(S, shape.E, replace=False).astype(np.int32)
+    pg = torch.zeros(S, shape.f, shape.d, dtype=torch.bfloat16, device=DEV)
+    pu, pd = torch.zeros_like(pg), torch.zeros(S, shape.d, shape.f, dtype=torch.bfloat16,
+                                               device=DEV)
+    ts = torch.from_numpy(slot).long().to(DEV)
+    pg[ts], pu[ts], pd[ts] = wg, wu, wd
+    R = 40
+    x = W.hidden_states(72, np.arange(-1, R - 1, dtype=np.int32), shape.d, torch.bfloat16).to(DEV)
+    ti = torch.from_numpy(W.random_assignments(73, R, shape.E, shape.k)).to(DEV)
+    tg = torch.from_numpy(W.random_gates(74, R, shape.k)).to(DEV)
+    y0 = torch.empty(R, shape.d, dtype=torch.bfloat16, device=DEV)
+    y1 = torch.empty_like(y0)
+    L = _desc(shape)
+    Ls = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16", slots=S)
+    ws = M.workspace(L, 1, R)
+    M.moe_expert_forward(L, x, wg, wu, wd, None, ti, tg, y0, ws, M.run_opts(M.MOE_FFN_TCGEN05))
+    M.moe_expert_forward(Ls, x, pg, pu, pd, torch.from_numpy(slot).to(DEV), ti, tg, y1, ws,
+                         M.run_opts(M.MOE_FFN_TCGEN05))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    assert torch.equal(y0, y1)
 
 
 def test_expert_forward_slot_map():
@@ -308,6 +367,8 @@ FORWARD_CASES = [
     ("cfg1-acc", W.QWEN3_30B_A3B, 1, "eagle", 0.02, M.MOE_ROUTE_ACCEPT, 12),
     ("cfg1-acc-peaked", W.QWEN3_30B_A3B, 1, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 12),
     ("cfg4-b4-acc-peaked", W.QWEN3_30B_A3B, 4, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 12),
+    ("cfg4-b16-nat", W.QWEN3_30B_A3B, 16, "eagle", 0.02, M.MOE_ROUTE_NATURAL, 12),
+    ("gptoss-acc-peaked", W.GPT_OSS_120B, 1, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 8),
 ]
 
 
