@@ -49,26 +49,54 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         cnt[e] = run;
     }
     __syncthreads();
-    if (tid == 0) {
-        int s = 0, na = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = s;
-            s += cnt[e];
-            if (cnt[e] > 0) active[1 + na++] = e;
+    if (tid < 32) {
+        // warp 0: exclusive scans over experts (ascending) of the assignment counts, of
+        // the active flags and of the row-tile counts; lane owns experts [lane*per, +per)
+        const int per = (E + 31) / 32;
+        int c_tot = 0, a_tot = 0, t_tot = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = tid * per + i;
+            const int c = e < E ? cnt[e] : 0;
+            c_tot += c;
+            a_tot += c > 0;
+            t_tot += (c + kRowTile - 1) / kRowTile;
         }
-        off[E] = s;
-        active[0] = na;
-        // row tiles of at most kRowTile tokens of one expert, for the tensor-core kernel
-        int nrt = 0;
-        for (int e = 0; e < E; ++e)
-            for (int n0 = 0; n0 < cnt[e]; n0 += kRowTile) {
-                int *t = rowtiles + 1 + 4 * nrt++;
+        int c_ex = c_tot, a_ex = a_tot, t_ex = t_tot;  // inclusive scans across lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int c2 = __shfl_up_sync(0xffffffffu, c_ex, o);
+            const int a2 = __shfl_up_sync(0xffffffffu, a_ex, o);
+            const int t2 = __shfl_up_sync(0xffffffffu, t_ex, o);
+            if (tid >= o) {
+                c_ex += c2;
+                a_ex += a2;
+                t_ex += t2;
+            }
+        }
+        c_ex -= c_tot;
+        a_ex -= a_tot;
+        t_ex -= t_tot;
+        for (int i = 0; i < per; ++i) {
+            const int e = tid * per + i;
+            if (e >= E) break;
+            const int c = cnt[e];
+            off[e] = c_ex;
+            c_ex += c;
+            if (c > 0) active[1 + a_ex++] = e;
+            // row tiles of at most kRowTile tokens of one expert, for the tensor-core kernel
+            for (int n0 = 0; n0 < c; n0 += kRowTile) {
+                int *t = rowtiles + 1 + 4 * t_ex++;
                 t[0] = e;
                 t[1] = n0;
-                t[2] = min(kRowTile, cnt[e] - n0);
+                t[2] = min(kRowTile, c - n0);
                 t[3] = 0;
             }
-        rowtiles[0] = nrt;
+        }
+        if (tid == 31) {
+            off[E] = c_ex;
+            active[0] = a_ex;
+            rowtiles[0] = t_ex;
+        }
     }
     __syncthreads();
     for (int e = tid; e <= E; e += kThreads) {

@@ -1,69 +1,80 @@
 // Verifier-side expert selection for a block of draft trees ("AcceptMoE" news
 // article, section 02; AcceptMoE abstract, arXiv 2608.02989).
 //
-// One CTA per tree. Phase A: a warp per node takes the node's natural top-k (the
-// natural routing and the natural union U) and, unless routing is natural, its
-// softmax weighted by the commitment probability of the node's depth; the CTA
-// then adds those rows into the demand D in node order. Phase B (one CTA, O(E^2)
-// rank counting, E <= 256): set size from the effective rank exp(H(D / sum D)),
-// root anchor + fill in (D desc, id asc) order, residency-aware pruning in
-// (D asc, id asc) order. Phase C: a warp per node re-runs top-k inside the
-// eligible set and writes renormalised gates.
+// One CTA of 32 warps per tree; the tree's logits are staged in shared memory once
+// (when they fit) and every later pass reads them from there.
+//   Phase A  a warp per node: natural top-k (the natural routing and the natural
+//            union U), and the node's softmax maximum and normaliser.
+//   Demand   a thread per expert: D_e = sum_n c(depth_n) * exp(l_ne - max_n) / sum_n,
+//            nodes in ascending order.
+//   Phase B  set size from the effective rank exp(H(D / sum D)), root anchor + fill in
+//            (D desc, id asc) order, residency-aware pruning in (D asc, id asc) order
+//            (ranks by counting, E <= 256).
+//   Phase C  a warp per node: top-k restricted to the eligible set S, renormalised
+//            gates. A node whose natural top-k lies inside S keeps it (it is then the
+//            restricted top-k by definition).
+//
+// Top-k: each lane holds experts lane + 32 i; a round takes every lane's best
+// candidate as an order-preserving 32-bit key of its logit (-0 folded onto +0) and
+// finds the winner with two warp reductions (max key, then min expert id among the
+// lanes holding that key): descending logits, ties to the lower id, as exact as a
+// comparison of the fp32 values.
 //
 // Demand, entropy and gates are computed in fp32 (GB300's fp64 rate is a small
-// fraction of its fp32 rate): the softmax row sum in a warp tree, the demand per
+// fraction of its fp32 rate): the softmax normaliser in a warp tree, the demand per
 // expert in ascending node order, sum D and H in ascending expert order in one
 // thread, each product and sum rounded on its own (no FMA contraction).
 #include <math.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
-constexpr int kVPL = kMaxE / 32;  // logits held per lane
+constexpr int kVPL = kMaxE / 32;     // logits held per lane
+constexpr int kStageFloats = 16384;  // logits staged in shared memory up to 64 KB
+static_assert(kThreads >= kMaxE, "block-wide counts take one expert per thread");
 
 // Relative distance to an integer under which exp(H) counts as that integer.
 constexpr float kSnap = 1e-5f;
 
-struct Top {
-    int idx;    // valid in lanes j < k: the j-th choice
-    float val;
-};
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.f);  // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
-// Warp-wide top-k of v (lane holds experts lane + 32 i) among experts whose bit is set
-// in `allowed` (bit i of lane's mask). Descending value, ties to the lower id.
-// Lane j < k receives the j-th choice.
-__device__ __forceinline__ Top warp_topk(const float v[kVPL], unsigned allowed, int E, int k) {
+// Warp top-k of v (lane holds experts lane + 32 i) among the experts whose bit i is
+// set in `allowed`. Returns, in lane j < k, the expert id of the j-th choice (-1 if
+// fewer than k experts are allowed).
+__device__ __forceinline__ int warp_topk(const float v[kVPL], unsigned allowed, int E, int k) {
     const int lane = threadIdx.x & 31;
-    unsigned taken = 0;
-    Top mine{-1, -INFINITY};
+    uint32_t key[kVPL];
+#pragma unroll
+    for (int i = 0; i < kVPL; ++i)
+        key[i] = (lane + 32 * i < E && ((allowed >> i) & 1u)) ? order_key(v[i]) : 0u;
+    int mine = -1;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        uint32_t bk = 0;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kVPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && ((allowed >> i) & 1u) && !((taken >> i) & 1u)) {
-                if (v[i] > bv || (v[i] == bv && e < bi)) {
-                    bv = v[i];
-                    bi = e;
-                }
+        for (int i = 0; i < kVPL; ++i)
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = lane + 32 * i;
             }
-        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t w = __reduce_min_sync(0xffffffffu, (bk == m && m != 0u) ? (uint32_t)bi
+                                                                               : 0xffffffffu);
+        if (w != 0xffffffffu && (int)(w & 31u) == lane) {
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
+            for (int i = 0; i < kVPL; ++i)
+                if ((int)(w >> 5) == i) key[i] = 0u;
         }
-        if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) mine = Top{bi == 0x7fffffff ? -1 : bi, bv};
+        if (lane == j) mine = w == 0xffffffffu ? -1 : (int)w;
     }
     return mine;
 }
@@ -74,15 +85,38 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Gates: softmax over the k chosen logits (lane j holds choice j), written with idx.
-__device__ __forceinline__ void write_choice(const Top &t, int k, int *idx, float *gates) {
+// Loads the E logits of one node into v[] (lane holds experts lane + 32 i).
+__device__ __forceinline__ void load_row(const float *Ln, int E, float v[kVPL]) {
     const int lane = threadIdx.x & 31;
-    const float top = __shfl_sync(0xffffffffu, t.val, 0);
-    const float ex = lane < k ? expf(t.val - top) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kVPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? Ln[e] : -INFINITY;
+    }
+}
+
+// The logit of expert `idx` (idx < 0: -inf), fetched from the lane that holds it.
+__device__ __forceinline__ float chosen_value(const float v[kVPL], int idx) {
+    const int lane = threadIdx.x & 31;
+    float out = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kVPL; ++i) {
+        const float got = __shfl_sync(0xffffffffu, v[i], idx < 0 ? lane : (idx & 31));
+        if (idx >= 0 && (idx >> 5) == i) out = got;
+    }
+    return out;
+}
+
+// Gates: softmax over the k chosen logits (lane j holds choice j), written with idx.
+__device__ __forceinline__ void write_choice(int idx, float val, int k, int *out_idx,
+                                             float *out_gates) {
+    const int lane = threadIdx.x & 31;
+    const float top = __shfl_sync(0xffffffffu, val, 0);
+    const float ex = lane < k ? expf(val - top) : 0.f;
     const float s = warp_sum(ex);
     if (lane < k) {
-        idx[lane] = t.idx;
-        gates[lane] = ex / s;
+        out_idx[lane] = idx;
+        out_gates[lane] = ex / s;
     }
 }
 
@@ -91,110 +125,120 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
               int N, int E, int k, const uint8_t *__restrict__ resident, int *__restrict__ idx_out,
               float *__restrict__ gates_out, uint8_t *__restrict__ elig_out,
               int *__restrict__ info_out) {
+    extern __shared__ float dyn[];  // [N][E] staged logits (when they fit), mx, nz, cN, nat
     __shared__ float D[kMaxE];
-    __shared__ float wbuf[kWarps][kMaxE];
     __shared__ float term[kMaxE];
-    __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE], rem[kMaxE];
+    __shared__ float rk[kMaxE];  // rank keys
+    __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
     __shared__ int natRoot[kMaxK];
+    __shared__ float s_sumD;
     __shared__ int s_m, s_removed;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
-    const float *L = logits + (size_t)b * N * E;
+    const float *Lg = logits + (size_t)b * N * E;
     const int *dep = depth + (size_t)b * N;
     int *idxb = idx_out + (size_t)b * N * k;
     float *gb = gates_out + (size_t)b * N * k;
     const bool natural = a.mode == MOE_ROUTE_NATURAL;
+    const bool staged = N * E <= kStageFloats;
+    float *stage = dyn;
+    float *mx = dyn + (staged ? N * E : 0);  // [N] softmax maxima
+    float *nz = mx + N;                       // [N] softmax normalisers
+    float *cN = nz + N;                       // [N] commitment of each node
+    int *nat = reinterpret_cast<int *>(cN + N);  // [N][k] natural choices
 
+    if (staged) {
+        if ((reinterpret_cast<uintptr_t>(Lg) & 15u) == 0) {
+            const int n4 = (N * E) / 4;
+            const float4 *src = reinterpret_cast<const float4 *>(Lg);
+            float4 *dst = reinterpret_cast<float4 *>(stage);
+            for (int i = tid; i < n4; i += kThreads) dst[i] = __ldg(src + i);
+            for (int i = n4 * 4 + tid; i < N * E; i += kThreads) stage[i] = __ldg(Lg + i);
+        } else {
+            for (int i = tid; i < N * E; i += kThreads) stage[i] = __ldg(Lg + i);
+        }
+    }
     for (int e = tid; e < kMaxE; e += kThreads) {
-        D[e] = 0.f;
         inU[e] = 0;
         inSel[e] = 0;
+        inA[e] = 0;
+    }
+    __syncthreads();
+    const float *L = staged ? stage : Lg;
+
+    // ---- phase A: natural top-k, natural union, softmax max / normaliser ----
+    for (int n = warp; n < N; n += kWarps) {
+        float v[kVPL];
+        load_row(L + (size_t)n * E, E, v);
+        const int t = warp_topk(v, 0xffffffffu, E, k);
+        const float val = chosen_value(v, t);
+        if (lane < k && t >= 0) inU[t] = 1;
+        if (n == 0 && lane < k) natRoot[lane] = t;
+        if (lane < k) nat[n * k + lane] = t;
+        if (natural) {
+            write_choice(t, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+        } else {
+            const float m = __shfl_sync(0xffffffffu, val, 0);  // the top-1 logit
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < kVPL; ++i)
+                if (lane + 32 * i < E) s += expf(v[i] - m);
+            s = warp_sum(s);
+            if (lane == 0) {
+                const int dd = min(dep[n], a.n_c - 1);
+                mx[n] = m;
+                nz[n] = s;
+                cN[n] = a.c[dd < 0 ? 0 : dd];
+            }
+        }
     }
     __syncthreads();
 
-    // ---- phase A: natural top-k, natural union, demand rows ----
-    for (int base = 0; base < N; base += kWarps) {
-        const int n = base + warp;
-        if (n < N) {
-            float v[kVPL];
-#pragma unroll
-            for (int i = 0; i < kVPL; ++i) {
-                const int e = lane + 32 * i;
-                v[i] = e < E ? L[(size_t)n * E + e] : -INFINITY;
-            }
-            const Top t = warp_topk(v, 0xffffffffu, E, k);
-            if (lane < k && t.idx >= 0) inU[t.idx] = 1;
-            if (n == 0 && lane < k) natRoot[lane] = t.idx;
-            if (natural) {
-                write_choice(t, k, idxb + (size_t)n * k, gb + (size_t)n * k);
-            } else {
-                const float mx = __shfl_sync(0xffffffffu, t.val, 0);
-                float ex[kVPL], s = 0.f;
-#pragma unroll
-                for (int i = 0; i < kVPL; ++i) {
-                    const int e = lane + 32 * i;
-                    ex[i] = e < E ? expf(v[i] - mx) : 0.f;
-                    s += ex[i];
-                }
-                s = warp_sum(s);
-                const int dd = dep[n] < a.n_c ? dep[n] : a.n_c - 1;
-                const float c = a.c[dd < 0 ? 0 : dd];
-#pragma unroll
-                for (int i = 0; i < kVPL; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < E) wbuf[warp][e] = __fmul_rn(c, __fdiv_rn(ex[i], s));
-                }
-            }
-        }
-        __syncthreads();
-        if (!natural) {
-            for (int e = tid; e < E; e += kThreads) {
-                float acc = D[e];
-                for (int w = 0; w < kWarps && base + w < N; ++w) acc = __fadd_rn(acc, wbuf[w][e]);
-                D[e] = acc;
-            }
-        }
-        __syncthreads();
-    }
-
     if (natural) {
-        if (tid == 0) {
-            int u = 0;
-            for (int e = 0; e < E; ++e) u += inU[e];
-            if (info_out) {
-                info_out[b * MOE_INFO_FIELDS + 0] = u;
-                info_out[b * MOE_INFO_FIELDS + 1] = u;
-                info_out[b * MOE_INFO_FIELDS + 2] = E;
-                info_out[b * MOE_INFO_FIELDS + 3] = 0;
-            }
+        const int u = __syncthreads_count(tid < E && inU[tid]);
+        if (tid == 0 && info_out) {
+            info_out[b * MOE_INFO_FIELDS + 0] = u;
+            info_out[b * MOE_INFO_FIELDS + 1] = u;
+            info_out[b * MOE_INFO_FIELDS + 2] = E;
+            info_out[b * MOE_INFO_FIELDS + 3] = 0;
         }
         if (elig_out)
             for (int e = tid; e < E; e += kThreads) elig_out[(size_t)b * E + e] = 1;
         return;
     }
 
+    // ---- demand: a thread per expert, nodes in ascending order ----
+    for (int e = tid; e < E; e += kThreads) {
+        float acc = 0.f;
+#pragma unroll 4
+        for (int n = 0; n < N; ++n) {
+            const float ex = expf(L[(size_t)n * E + e] - mx[n]);
+            acc = __fadd_rn(acc, __fmul_rn(cN[n], __fdiv_rn(ex, nz[n])));
+        }
+        D[e] = acc;
+    }
+    __syncthreads();
+
     // ---- phase B: size, anchor + fill, prune ----
+    const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
     if (tid == 0) {
         float sum = 0.f;
+#pragma unroll 16
         for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
-        term[0] = sum;  // borrowed as a broadcast slot until the terms are written
+        s_sumD = sum;
     }
     __syncthreads();
-    const float sumD = term[0];
-    __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
-        const float q = __fdiv_rn(D[e], sumD);
+        const float q = __fdiv_rn(D[e], s_sumD);
         term[e] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
-        inA[e] = 0;
     }
     __syncthreads();
     if (tid == 0) {
-        int pool = 0;
-        for (int e = 0; e < E; ++e) pool += (a.pool_all || inU[e]) ? 1 : 0;
         int m;
         if (a.mode == MOE_ROUTE_ACCEPT) {
             float H = 0.f;
+#pragma unroll 16
             for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
             const float r = expf(H);
             const float rn = rintf(r);
@@ -209,51 +253,52 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
             for (int j = 0; j < k; ++j) inA[natRoot[j]] = 1;
     }
     __syncthreads();
-    int nA = 0;
-    if (a.anchor) nA = k;
+    const int nA = a.anchor ? k : 0;
     const int m = s_m;
+    // fill: candidates (pool minus anchor) ranked by (D desc, id asc); demand is >= 0,
+    // so -1 marks a non-candidate
+    for (int e = tid; e < E; e += kThreads)
+        rk[e] = (!inA[e] && (a.pool_all || inU[e])) ? D[e] : -1.f;
+    __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
         int in = inA[e];
-        const bool cand = !inA[e] && (a.pool_all || inU[e]);
-        if (cand) {
-            const float De = D[e];
+        const float De = rk[e];
+        if (De >= 0.f) {
             int rank = 0;
+#pragma unroll 8
             for (int q = 0; q < E; ++q) {
-                const bool cq = !inA[q] && (a.pool_all || inU[q]);
-                rank += (cq && (D[q] > De || (D[q] == De && q < e))) ? 1 : 0;
+                const float Dq = rk[q];
+                rank += (Dq > De || (Dq == De && q < e)) ? 1 : 0;
             }
             in = rank < m - nA;
         }
         inS[e] = in;
     }
     __syncthreads();
+    int removed = 0;
     if (a.prune && resident) {
-        for (int e = tid; e < E; e += kThreads) rem[e] = inS[e] && !inA[e] && !resident[e];
-        __syncthreads();
-        if (tid == 0) {
-            int nrem = 0;
-            for (int e = 0; e < E; ++e) nrem += rem[e];
-            const int fl = a.min_set > k ? a.min_set : k;
-            int can = m - fl;
-            if (can < 0) can = 0;
-            if (can > a.budget) can = a.budget;
-            if (can > nrem) can = nrem;
-            s_removed = can;
+        // removable members (non-resident, not anchor) ranked by (D asc, id asc); +inf
+        // marks the others
+        int is_rem = 0;
+        if (tid < E) {
+            is_rem = inS[tid] && !inA[tid] && !resident[tid];
+            rk[tid] = is_rem ? D[tid] : INFINITY;
         }
-        __syncthreads();
-        const int nr = s_removed;
-        for (int e = tid; e < E; e += kThreads) {
-            if (!rem[e]) continue;
-            const float De = D[e];
+        const int nrem = __syncthreads_count(is_rem);
+        const int fl = a.min_set > k ? a.min_set : k;
+        removed = min(min(max(m - fl, 0), a.budget), nrem);
+        if (is_rem) {
+            const float De = rk[tid];
             int rank = 0;
-            for (int q = 0; q < E; ++q)
-                rank += (rem[q] && (D[q] < De || (D[q] == De && q < e))) ? 1 : 0;
-            if (rank < nr) inS[e] = 0;
+#pragma unroll 8
+            for (int q = 0; q < E; ++q) {
+                const float Dq = rk[q];
+                rank += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
+            }
+            if (rank < removed) inS[tid] = 0;
         }
-    } else if (tid == 0) {
-        s_removed = 0;
+        __syncthreads();
     }
-    __syncthreads();
 
     // ---- phase C: restricted top-k and gates ----
     unsigned allowed = 0;
@@ -264,26 +309,21 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
     }
     for (int n = warp; n < N; n += kWarps) {
         float v[kVPL];
-#pragma unroll
-        for (int i = 0; i < kVPL; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = e < E ? L[(size_t)n * E + e] : -INFINITY;
-        }
-        const Top t = warp_topk(v, allowed, E, k);
-        if (lane < k && t.idx >= 0) inSel[t.idx] = 1;
-        write_choice(t, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+        load_row(L + (size_t)n * E, E, v);
+        const int nt = lane < k ? nat[n * k + lane] : -1;
+        const bool keep = __all_sync(0xffffffffu, lane >= k || (nt >= 0 && inS[nt]));
+        const int t = keep ? nt : warp_topk(v, allowed, E, k);
+        const float val = chosen_value(v, t);
+        if (lane < k && t >= 0) inSel[t] = 1;
+        write_choice(t, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
     }
-    __syncthreads();
+    const int u_nat = __syncthreads_count(tid < E && inU[tid]);
+    const int u_sel = __syncthreads_count(tid < E && inSel[tid]);
     if (tid == 0 && info_out) {
-        int u = 0, us = 0;
-        for (int e = 0; e < E; ++e) {
-            u += inU[e];
-            us += inSel[e];
-        }
-        info_out[b * MOE_INFO_FIELDS + 0] = u;
-        info_out[b * MOE_INFO_FIELDS + 1] = us;
+        info_out[b * MOE_INFO_FIELDS + 0] = u_nat;
+        info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
         info_out[b * MOE_INFO_FIELDS + 2] = m;
-        info_out[b * MOE_INFO_FIELDS + 3] = s_removed;
+        info_out[b * MOE_INFO_FIELDS + 3] = removed;
     }
     if (elig_out)
         for (int e = tid; e < E; e += kThreads) elig_out[(size_t)b * E + e] = (uint8_t)inS[e];
@@ -295,8 +335,17 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s) {
     if (B <= 0 || N <= 0) return cudaSuccess;
-    select_kernel<<<B, kThreads, 0, s>>>(a, logits, depth, N, L.E, L.k, resident, idx, gates, elig,
-                                         info);
+    const bool staged = N * L.E <= kStageFloats;
+    const size_t smem =
+        ((staged ? (size_t)N * L.E : 0) + 3 * (size_t)N + (size_t)N * L.k) * sizeof(float);
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    if (smem > 40 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(
+            select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    select_kernel<<<B, kThreads, smem, s>>>(a, logits, depth, N, L.E, L.k, resident, idx, gates,
+                                            elig, info);
     return cudaGetLastError();
 }
 
