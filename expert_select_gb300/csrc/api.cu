@@ -35,6 +35,7 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.pos = take(A * 4);
     w.active = take((E + 1) * 4);
     w.rowtiles = take((size_t)(1 + 4 * max_rowtiles(L.E, (int)A)) * 4);
+    w.sched = take((size_t)(1 + max_rowtiles(L.E, (int)A)) * 4);
     w.xp = take(A * L.d * elem_size(L.dtype));
     w.h = take(A * L.f * 4);
     w.o = take(A * L.d * 4);
@@ -112,6 +113,7 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
     fa.dtype = L.dtype;
     fa.slots = L.slots > 0 ? L.slots : L.E;
     fa.flags = flags;
+    fa.sched = at<int>(ws, w.sched);
     fa.xp = at<void>(ws, w.xp);
     fa.h = at<void>(ws, w.h);
     fa.o = at<float>(ws, w.o);

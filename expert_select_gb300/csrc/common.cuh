@@ -31,6 +31,7 @@ struct Workspace {
     size_t pos;       // i32 [A]  assignment id -> permuted position (-1 = skipped)
     size_t active;    // i32 [E + 1]  [0] = n_active, then active experts ascending
     size_t rowtiles;  // i32 [1 + 4 * max_rowtiles]: count, then (expert, first token, tokens, 0)
+    size_t sched;     // i32 [1 + max_rowtiles]: ticket counter, finished phase-1 units per row tile
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
     size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)
     size_t o;         // f32 [A, d]  expert outputs in permuted order
@@ -71,6 +72,7 @@ struct FfnArgs {
     int R, d, f, E, k, dtype;
     int slots;           // expert slots in the weight pools
     int *flags;
+    int *sched;          // tensor-core path: ticket + row-tile counters
     void *xp;            // gathered x (tensor-core path)
     void *h;             // activations
     float *o;            // expert outputs, permuted order

@@ -14,13 +14,23 @@
 // swizzle atom) loaded by TMA with 128-byte swizzling, which is the layout the
 // tcgen05 shared-memory descriptors describe.
 //
-// One persistent CTA per SM (192 threads, warp-specialised):
-//   warp 0       TMA producer (one lane) filling a ring of `stages` buffers
+// Both phases run in one persistent launch, one CTA per SM (192 threads,
+// warp-specialised):
+//   warp 0       TMA producer (one lane): takes unit tickets from a global counter
+//                (every phase-1 unit before any phase-2 unit), passes each ticket to
+//                the other roles through a small shared-memory queue, and fills a ring
+//                of `stages` buffers
 //   warp 1       TMEM allocator and MMA issuer (one lane)
 //   warps 2..5   epilogue: tcgen05.ld the accumulator (each warp may read the 32
 //                TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
 // Two 256-column accumulators alternate so the epilogue of one unit overlaps the
-// MMAs of the next. Units (row tile x weight tile) are dealt round-robin over CTAs.
+// MMAs of the next. A unit is one weight tile x one row tile (<= 256 tokens of one
+// expert). A phase-2 unit needs the whole h of its row tile: the epilogue that
+// finishes a phase-1 unit publishes it with a release increment of the row tile's
+// counter, and the producer of a phase-2 unit waits for the count with acquire loads
+// before its TMA reads h. Tickets are handed out in order, so every phase-1 unit is
+// owned by a running CTA before any CTA waits on one: no deadlock even when fewer
+// CTAs than SMs are resident.
 //
 // Every wait is bounded: after 2 s a wait gives up, sets the workspace check bit
 // FLAG_WAIT_TIMEOUT and makes the CTA stop; the CTA then waits (again bounded) for
@@ -45,23 +55,25 @@ constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
-constexpr int kCtlBytes = 256;
+constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 144 bytes)
 
 struct Maps {
-    CUtensorMap a0;          // phase 1: W_gate [S][f][d], box 64x64x1; phase 2: W_down [S][d][f], box 64x128x1
-    CUtensorMap a1;          // phase 1: W_up, box 64x64x1
-    CUtensorMap b[kBoxes];   // token rows [A][K] (gathered x or h), box 64 x (16 << i)
+    CUtensorMap wg;           // W_gate [S][f][d], box 64 x 64 x 1
+    CUtensorMap wu;           // W_up   [S][f][d], box 64 x 64 x 1
+    CUtensorMap wd;           // W_down [S][d][f], box 64 x 128 x 1
+    CUtensorMap bx[kBoxes];   // gathered token rows x [A][d], box 64 x (16 << i)
+    CUtensorMap bh[kBoxes];   // activations h [A][f], box 64 x (16 << i)
 };
 
 struct Params {
-    int K;        // reduction length: d (phase 1) or f (phase 2)
-    int m_tiles;  // weight tiles per expert
-    int out_ld;   // row length of the output: f (phase 1) or d (phase 2)
+    int d, f;
+    int mt1, mt2;  // weight tiles per expert: f / 64 (phase 1), ceil(d / 128) (phase 2)
     int stages;
-    int box_cap;  // rows of the per-stage token buffer
-    int slots;    // expert slots in the weight pool
+    int box_cap;   // rows of the per-stage token buffer
+    int slots;     // expert slots in the weight pool
     const int *rowtiles, *offsets, *slot;
     int *flags;
+    int *sched;    // [0] ticket counter, [1 + rt] finished phase-1 units of row tile rt
     __nv_bfloat16 *h;
     float *o;
 };
@@ -212,14 +224,29 @@ __device__ __forceinline__ int box_of(int n) {
     return i;
 }
 
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 struct Unit {
-    int e, n0, ntok, slot, m;
+    int phase, rt, m, e, n0, ntok, slot;
 };
 
-__device__ __forceinline__ bool decode(const Params &p, int u, Unit &w) {
-    const int rt = u / p.m_tiles;
-    w.m = u - rt * p.m_tiles;
-    const int *t = p.rowtiles + 1 + 4 * rt;
+// Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2.
+__device__ __forceinline__ bool decode(const Params &p, int U1, int u, Unit &w) {
+    if (u < U1) {
+        w.phase = 1;
+        w.rt = u / p.mt1;
+        w.m = u - w.rt * p.mt1;
+    } else {
+        const int v = u - U1;
+        w.phase = 2;
+        w.rt = v / p.mt2;
+        w.m = v - w.rt * p.mt2;
+    }
+    const int *t = p.rowtiles + 1 + 4 * w.rt;
     w.e = t[0];
     w.n0 = t[1];
     w.ntok = t[2];
@@ -227,9 +254,10 @@ __device__ __forceinline__ bool decode(const Params &p, int u, Unit &w) {
     return w.slot >= 0 && w.slot < p.slots && w.ntok > 0;
 }
 
+constexpr int kQ = 4;  // ticket queue depth
+
 // ------------------------------------------------------------------ kernel
 
-template <int PHASE>
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -241,12 +269,17 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     const uint32_t sA = base, sB = base + (uint32_t)S * kABytes;
     uint8_t *ctl = gbase + (size_t)S * (kABytes + b_bytes);
     const uint32_t ctl_s = base + (uint32_t)S * (kABytes + b_bytes);
-    // control block: full[S], empty[S], tfull[2], tempty[2], done, tmem slot, abort, ok[2]
+    // control block: full[S], empty[S], tfull[2], tempty[2], done, qfull[kQ], qempty[kQ],
+    // then tmem slot, abort, epilogue verdict[2], epilogue ticket[2], ticket queue[kQ]
     const uint32_t full = ctl_s, empty = ctl_s + 8 * S, tfull = ctl_s + 16 * S,
-                   tempty = tfull + 16, done = tempty + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 16 * S + 40);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctl + 16 * S + 44);
-    volatile int *epi_ok = reinterpret_cast<volatile int *>(ctl + 16 * S + 48);  // [2]
+                   tempty = tfull + 16, done = tempty + 16, qfull = done + 8,
+                   qempty = qfull + 8 * kQ;
+    int *ints = reinterpret_cast<int *>(ctl + 16 * S + 40 + 16 * kQ);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ints);
+    volatile int *abort_flag = ints + 1;
+    volatile int *epi_ok = ints + 2;    // [2]
+    volatile int *epi_u = ints + 4;     // [2]
+    volatile int *queue = ints + 6;     // [kQ]
     float *sg = reinterpret_cast<float *>(ctl + kCtlBytes);  // [64][kSgStride]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -260,12 +293,17 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             mbar_init(tempty + 8 * a, 128);
         }
         mbar_init(done, 1);
+        for (int q = 0; q < kQ; ++q) {
+            mbar_init(qfull + 8 * q, 1);
+            mbar_init(qempty + 8 * q, 2);  // the MMA lane and one epilogue thread
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        prefetch_map(&maps.a0);
-        if (PHASE == 1) prefetch_map(&maps.a1);
+        prefetch_map(&maps.wg);
+        prefetch_map(&maps.wu);
+        prefetch_map(&maps.wd);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -279,9 +317,8 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int n_units = p.rowtiles[0] * p.m_tiles;
-    const int kchunks = p.K / kBK;
-    constexpr int kRowsA = PHASE == 1 ? 64 : 128;
+    const int n_rt = p.rowtiles[0];
+    const int U1 = n_rt * p.mt1, U = U1 + n_rt * p.mt2;
 
     uint32_t issued = 0, last_par = 0;  // producer: stages with a load issued, parity of it
     bool mma_issued = false;
@@ -289,18 +326,48 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = evict_first_policy();
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, qs = 0;
+            uint32_t ph = 0, qph = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+            while (ok) {
+                int u = atomicAdd(p.sched, 1);
+                if (u >= U) u = -1;
+                if (!mbar_wait(qempty + 8 * qs, qph ^ 1u, abort_flag, p.flags)) break;
+                queue[qs] = u;
+                mbar_arrive(qfull + 8 * qs);
+                if (++qs == kQ) {
+                    qs = 0;
+                    qph ^= 1u;
+                }
+                if (u < 0) break;
                 Unit w;
-                if (!decode(p, u, w)) {
+                if (!decode(p, U1, u, w)) {
                     atomicOr(p.flags, FLAG_BAD_EXPERT);
                     continue;
                 }
-                const int bx = box_of((w.ntok + 15) & ~15);
-                const uint32_t bb = (uint32_t)(16 << bx) * 128u;
+                if (w.phase == 2) {  // wait until the row tile's h is complete
+                    const unsigned long long t0 = now_ns();
+                    while (ld_acquire(p.sched + 1 + w.rt) < p.mt1) {
+                        __nanosleep(64);
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (now_ns() - t0 > kTimeoutNs) {
+                            *abort_flag = 1;
+                            atomicOr(p.flags, FLAG_WAIT_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                const int bxi = box_of((w.ntok + 15) & ~15);
+                const uint32_t bb = (uint32_t)(16 << bxi) * 128u;
                 const int brow = p.offsets[w.e] + w.n0;
+                const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
+                const CUtensorMap *bmap = w.phase == 1 ? &maps.bx[bxi] : &maps.bh[bxi];
                 for (int kc = 0; kc < kchunks; ++kc) {
                     if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.flags)) {
                         ok = false;
@@ -309,11 +376,14 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     const uint32_t fb = full + 8 * s;
                     mbar_expect_tx(fb, kABytes + bb);
                     const uint32_t a = sA + (uint32_t)s * kABytes;
-                    tma_load_3d(a, &maps.a0, kc * kBK, w.m * kRowsA, w.slot, fb, pol);
-                    if (PHASE == 1)
-                        tma_load_3d(a + kABytes / 2, &maps.a1, kc * kBK, w.m * kRowsA, w.slot, fb,
+                    if (w.phase == 1) {
+                        tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
+                        tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, w.m * 64, w.slot, fb,
                                     pol);
-                    tma_load_2d(sB + (uint32_t)s * b_bytes, &maps.b[bx], kc * kBK, brow, fb);
+                    } else {
+                        tma_load_3d(a, &maps.wd, kc * kBK, w.m * kM, w.slot, fb, pol);
+                    }
+                    tma_load_2d(sB + (uint32_t)s * b_bytes, bmap, kc * kBK, brow, fb);
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -326,12 +396,20 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            int s = 0, it = 0;
-            uint32_t ph = 0;
+            int s = 0, it = 0, qs = 0;
+            uint32_t ph = 0, qph = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+            while (ok) {
+                if (!mbar_wait(qfull + 8 * qs, qph, abort_flag, p.flags)) break;
+                const int u = queue[qs];
+                mbar_arrive(qempty + 8 * qs);
+                if (++qs == kQ) {
+                    qs = 0;
+                    qph ^= 1u;
+                }
+                if (u < 0) break;
                 Unit w;
-                if (!decode(p, u, w)) continue;
+                if (!decode(p, U1, u, w)) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -339,6 +417,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16((uint32_t)((w.ntok + 15) & ~15));
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
+                const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
                 for (int kc = 0; kc < kchunks; ++kc) {
                     if (!mbar_wait(full + 8 * s, ph, abort_flag, p.flags)) {
                         ok = false;
@@ -364,15 +443,32 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     } else {
         const int q = warp & 3;          // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;   // accumulator row
-        int it = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        int it = 0, qs = 0, turn = 0;
+        uint32_t qph = 0;
+        for (;; turn ^= 1) {
+            // thread 64 takes the next ticket and the named barrier hands it to the
+            // others; the slots alternate so a fast thread cannot overwrite a value a
+            // slow one has yet to read
+            if (threadIdx.x == 64) {
+                int u = -1;
+                if (mbar_wait(qfull + 8 * qs, qph, abort_flag, p.flags)) {
+                    u = queue[qs];
+                    mbar_arrive(qempty + 8 * qs);
+                }
+                epi_u[turn] = u;
+            }
+            if (++qs == kQ) {
+                qs = 0;
+                qph ^= 1u;
+            }
+            epi_bar();
+            const int u = epi_u[turn];
+            if (u < 0) break;
             Unit w;
-            if (!decode(p, u, w)) continue;
+            if (!decode(p, U1, u, w)) continue;
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             ++it;
-            // one thread waits, the named barrier releases the others; the verdict slot
-            // alternates so the next unit's write cannot overtake a late reader
             if (threadIdx.x == 64)
                 epi_ok[acc] = mbar_wait(tfull + 8 * acc, aph, abort_flag, p.flags);
             epi_bar();
@@ -381,10 +477,10 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int N = (w.ntok + 15) & ~15;
             const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
             const size_t row0 = (size_t)p.offsets[w.e] + w.n0;
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(taddr + (uint32_t)c0, v);
-                if (PHASE == 1) {
+            if (w.phase == 1) {
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + (uint32_t)c0, v);
                     if (q < 2) {
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
@@ -395,24 +491,33 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     epi_bar();
                     if (q >= 2) {
                         const int i = row - 64;
-                        __nv_bfloat16 *hp = p.h + row0 * p.out_ld + (size_t)w.m * 64 + i;
+                        __nv_bfloat16 *hp = p.h + row0 * p.f + (size_t)w.m * 64 + i;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int tok = c0 + c;
                             if (tok < w.ntok)
-                                hp[(size_t)tok * p.out_ld] =
-                                    __float2bfloat16_rn(sg[i * kSgStride + c] * __uint_as_float(v[c]));
+                                hp[(size_t)tok * p.f] = __float2bfloat16_rn(
+                                    sg[i * kSgStride + c] * __uint_as_float(v[c]));
                         }
                     }
                     epi_bar();
-                } else {
-                    const int drow = w.m * kM + row;
-                    if (drow < p.out_ld) {
-                        float *op = p.o + row0 * p.out_ld + drow;
+                }
+                // every h store of this unit precedes the barrier above: publish them
+                if (threadIdx.x == 64) {
+                    __threadfence();
+                    atomicAdd(p.sched + 1 + w.rt, 1);
+                }
+            } else {
+                const int drow = w.m * kM + row;
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + (uint32_t)c0, v);
+                    if (drow < p.d) {
+                        float *op = p.o + row0 * p.d + drow;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int tok = c0 + c;
-                            if (tok < w.ntok) op[(size_t)tok * p.out_ld] = __uint_as_float(v[c]);
+                            if (tok < w.ntok) op[(size_t)tok * p.d] = __uint_as_float(v[c]);
                         }
                     }
                 }
@@ -443,10 +548,13 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
 }
 
 // Gathers the token rows of every assignment into permuted order: xp[p] = x[perm[p] / k].
+// Block 0 also zeroes the expert kernel's ticket counter and row-tile counters.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ perm,
                    const int *__restrict__ offsets, int E, int k, int d,
-                   __nv_bfloat16 *__restrict__ xp) {
+                   __nv_bfloat16 *__restrict__ xp, int *__restrict__ sched, int n_sched) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_sched; i += blockDim.x) sched[i] = 0;
     const int pidx = blockIdx.x;
     if (pidx >= offsets[E]) return;
     const int r = perm[pidx] / k;
@@ -544,26 +652,29 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const size_t smem = smem_bytes(stages, box_cap);
     const int S = a.slots;
 
-    Maps m1{}, m2{};
-    if (!encode_weights(&m1.a0, a.Wg, S, a.f, a.d, 64) ||
-        !encode_weights(&m1.a1, a.Wu, S, a.f, a.d, 64) || !encode_rows(m1.b, a.xp, A, a.d) ||
-        !encode_weights(&m2.a0, a.Wd, S, a.d, a.f, 128) || !encode_rows(m2.b, a.h, A, a.f))
+    Maps m{};
+    if (!encode_weights(&m.wg, a.Wg, S, a.f, a.d, 64) ||
+        !encode_weights(&m.wu, a.Wu, S, a.f, a.d, 64) ||
+        !encode_weights(&m.wd, a.Wd, S, a.d, a.f, kM) || !encode_rows(m.bx, a.xp, A, a.d) ||
+        !encode_rows(m.bh, a.h, A, a.f))
         return cudaErrorInvalidValue;
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(ffn_tc_kernel<1>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(
-                ffn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attr_err = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
+    const int n_sched = 1 + max_rowtiles(a.E, A);
     gather_rows_kernel<<<A, 256, 0, s>>>((const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k,
-                                         a.d, (__nv_bfloat16 *)a.xp);
+                                         a.d, (__nv_bfloat16 *)a.xp, a.sched, n_sched);
     Params p{};
+    p.d = a.d;
+    p.f = a.f;
+    p.mt1 = a.f / 64;
+    p.mt2 = (a.d + kM - 1) / kM;
     p.stages = stages;
     p.box_cap = box_cap;
     p.slots = S;
@@ -571,16 +682,10 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.offsets = a.offsets;
     p.slot = a.slot;
     p.flags = a.flags;
+    p.sched = a.sched;
     p.h = (__nv_bfloat16 *)a.h;
     p.o = a.o;
-    p.K = a.d;
-    p.m_tiles = a.f / 64;
-    p.out_ld = a.f;
-    ffn_tc_kernel<1><<<nsm, kThreads, smem, s>>>(m1, p);
-    p.K = a.f;
-    p.m_tiles = (a.d + kM - 1) / kM;
-    p.out_ld = a.d;
-    ffn_tc_kernel<2><<<nsm, kThreads, smem, s>>>(m2, p);
+    ffn_tc_kernel<<<nsm, kThreads, smem, s>>>(m, p);
     return cudaGetLastError();
 }
 
