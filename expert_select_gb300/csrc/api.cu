@@ -34,6 +34,9 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.perm = take(A * 4);
     w.pos = take(A * 4);
     w.active = take((E + 1) * 4);
+    w.slotmap = take(E * 4);
+    w.resident = take(E);
+    w.pass = take(E);
     w.rowtiles = take((size_t)(1 + 4 * max_rowtiles(L.E, (int)A)) * 4);
     w.sched = take((size_t)(1 + max_rowtiles(L.E, (int)A)) * 4);
     w.xp = take(A * L.d * elem_size(L.dtype));
@@ -43,23 +46,17 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     return w;
 }
 
-static bool desc_ok(const moe_layer_desc *L) {
+bool desc_ok(const moe_layer_desc *L) {
     return L && L->k >= 1 && L->k <= kMaxK && L->E >= L->k && L->E <= kMaxE && L->d >= 8 &&
            L->d % 8 == 0 && L->d <= kMaxD && L->f >= 8 && L->f % 8 == 0 && L->f <= kMaxD &&
            (L->dtype == MOE_DTYPE_F32 || L->dtype == MOE_DTYPE_BF16) && L->slots >= 0 &&
            L->slots <= 65535;
 }
 
-static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-template <typename T>
-static T *at(void *ws, size_t off) {
-    return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
-}
-
-static bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
+bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
     if (!P) return false;
     if (P->mode < MOE_ROUTE_NATURAL || P->mode > MOE_ROUTE_FIXED_B) return false;
     if (P->mode != MOE_ROUTE_NATURAL && (P->n_c < 1 || P->n_c > MOE_MAX_DEPTHS)) return false;
@@ -79,32 +76,31 @@ static bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
     return true;
 }
 
-static bool permute_fits(int R, int E) { return permute_smem_bytes(R, E) <= 227 * 1024; }
+bool permute_fits(int R, int E) { return permute_smem_bytes(R, E) <= 227 * 1024; }
 
-// permute -> experts -> combine, shared by moe_expert_forward and moe_tree_forward.
-static moe_status run_experts(const moe_layer_desc &L, const void *x, const void *Wg,
-                              const void *Wu, const void *Wd, const int *slot, const int *idx,
-                              const float *gates, int R, void *y, void *ws, const Workspace &w,
-                              int *counts, int *offsets, int *perm, const moe_run_opts *opts,
-                              cudaStream_t s) {
-    int *flags = at<int>(ws, w.flags);
-    int *pos = at<int>(ws, w.pos), *active = at<int>(ws, w.active);
-    int *rowtiles = at<int>(ws, w.rowtiles);
-    cudaError_t err =
-        launch_permute(L, idx, R, counts, offsets, perm, pos, active, rowtiles, flags, s);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
+moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
+                       const Workspace &w, int *counts, int *offsets, int *perm, cudaStream_t s) {
+    return cuda_status(launch_permute(L, idx, R, counts, offsets, perm, at<int>(ws, w.pos),
+                                      at<int>(ws, w.active), at<int>(ws, w.rowtiles),
+                                      at<int>(ws, w.flags), s));
+}
 
+moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const void *Wu,
+                   const void *Wd, const int *slot, const uint8_t *pass, int R, void *ws,
+                   const Workspace &w, const int *counts, const int *offsets, const int *perm,
+                   const moe_run_opts *opts, cudaStream_t s) {
     FfnArgs fa{};
     fa.x = x;
     fa.Wg = Wg;
     fa.Wu = Wu;
     fa.Wd = Wd;
     fa.slot = slot;
+    fa.pass = pass;
     fa.counts = counts;
     fa.offsets = offsets;
     fa.perm = perm;
-    fa.active = active;
-    fa.rowtiles = rowtiles;
+    fa.active = at<int>(ws, w.active);
+    fa.rowtiles = at<int>(ws, w.rowtiles);
     fa.R = R;
     fa.d = L.d;
     fa.f = L.f;
@@ -112,7 +108,7 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
     fa.k = L.k;
     fa.dtype = L.dtype;
     fa.slots = L.slots > 0 ? L.slots : L.E;
-    fa.flags = flags;
+    fa.flags = at<int>(ws, w.flags);
     fa.sched = at<int>(ws, w.sched);
     fa.xp = at<void>(ws, w.xp);
     fa.h = at<void>(ws, w.h);
@@ -124,11 +120,30 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
     const bool timed = opts && opts->ffn_begin && opts->ffn_end;
     if (timed && cudaEventRecord((cudaEvent_t)opts->ffn_begin, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    err = path == MOE_FFN_TCGEN05 ? launch_ffn_tc(fa, s) : launch_ffn_simt(fa, s);
+    const cudaError_t err = path == MOE_FFN_TCGEN05 ? launch_ffn_tc(fa, s) : launch_ffn_simt(fa, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (timed && cudaEventRecord((cudaEvent_t)opts->ffn_end, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    return cuda_status(launch_combine(L, fa.o, pos, gates, R, y, s));
+    return MOE_OK;
+}
+
+moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
+                       void *y, void *ws, const Workspace &w, cudaStream_t s) {
+    return cuda_status(launch_combine(L, at<float>(ws, w.o), at<int>(ws, w.pos), gates, residual,
+                                      R, y, s));
+}
+
+// permute -> experts -> combine, shared by moe_expert_forward and moe_tree_forward.
+static moe_status run_experts(const moe_layer_desc &L, const void *x, const void *Wg,
+                              const void *Wu, const void *Wd, const int *slot, const int *idx,
+                              const float *gates, int R, void *y, void *ws, const Workspace &w,
+                              int *counts, int *offsets, int *perm, const moe_run_opts *opts,
+                              cudaStream_t s) {
+    moe_status st = run_permute(L, idx, R, ws, w, counts, offsets, perm, s);
+    if (st != MOE_OK) return st;
+    st = run_ffn(L, x, Wg, Wu, Wd, slot, nullptr, R, ws, w, counts, offsets, perm, opts, s);
+    if (st != MOE_OK) return st;
+    return run_combine(L, (opts && opts->residual) ? x : nullptr, gates, R, y, ws, w, s);
 }
 
 }  // namespace moe

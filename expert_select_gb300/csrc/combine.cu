@@ -1,6 +1,7 @@
 // Unpermute + weighted combine ("MoE and speculative decoding" blog, pipeline step
 // "unpermute + weighted combine"): y[r] = sum_j gates[r, j] O[pos(r, j)], slots in
-// ascending j, fp32 accumulation, rounded once to the layer dtype.
+// ascending j, fp32 accumulation, rounded once to the layer dtype. With a residual
+// input the sum starts from it (y = x + MoE(x), as in a stack of layers).
 //
 // Also holds the small kernel that publishes a residency table to the device.
 #include "common.cuh"
@@ -27,13 +28,26 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *y, float4 v
 }
 
 template <typename TO>
+__device__ __forceinline__ float4 load4(const TO *p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+
+// `res` (may be null, may alias y) is added first: y = res + sum_j g_j O_j.
+template <typename TO>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
-               const float *__restrict__ gates, int d, int k, TO *__restrict__ y) {
+               const float *__restrict__ gates, const TO *res, int d, int k, TO *y) {
     const int r = blockIdx.x;
     const int c = (blockIdx.y * kThreads + threadIdx.x) * 4;
     if (c >= d) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = res ? load4<TO>(res + (size_t)r * d + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         const int p = pos[r * k + j];
         if (p < 0) continue;
@@ -62,14 +76,16 @@ __global__ void publish_kernel(PublishArgs p, int E, int *slot, uint8_t *res) {
 }  // namespace
 
 cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
-                           const float *gates, int R, void *y, cudaStream_t s) {
+                           const float *gates, const void *residual, int R, void *y,
+                           cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
     dim3 grid(R, (L.d / 4 + kThreads - 1) / kThreads);
     if (L.dtype == MOE_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(o, pos, gates, L.d, L.k,
-                                                                (__nv_bfloat16 *)y);
+        combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+            o, pos, gates, (const __nv_bfloat16 *)residual, L.d, L.k, (__nv_bfloat16 *)y);
     else
-        combine_kernel<float><<<grid, kThreads, 0, s>>>(o, pos, gates, L.d, L.k, (float *)y);
+        combine_kernel<float><<<grid, kThreads, 0, s>>>(o, pos, gates, (const float *)residual,
+                                                        L.d, L.k, (float *)y);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,9 @@ struct Workspace {
     size_t perm;      // i32 [A]  permuted position -> assignment id
     size_t pos;       // i32 [A]  assignment id -> permuted position (-1 = skipped)
     size_t active;    // i32 [E + 1]  [0] = n_active, then active experts ascending
+    size_t slotmap;   // i32 [E]  expert -> slot (offload)
+    size_t resident;  // u8  [E]  residency before this call's uploads (offload)
+    size_t pass;      // u8  [E]  experts computed by the current expert pass (offload)
     size_t rowtiles;  // i32 [1 + 4 * max_rowtiles]: count, then (expert, first token, tokens, 0)
     size_t sched;     // i32 [1 + max_rowtiles]: ticket counter, finished phase-1 units per row tile
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
@@ -68,6 +71,7 @@ struct FfnArgs {
     const void *Wg, *Wu; // [S, f, d]
     const void *Wd;      // [S, d, f]
     const int *slot;     // [E] or nullptr
+    const uint8_t *pass; // [E] or nullptr: experts with 0 are skipped (not an error)
     const int *counts, *offsets, *perm, *active, *rowtiles;
     int R, d, f, E, k, dtype;
     int slots;           // expert slots in the weight pools
@@ -82,10 +86,32 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s);
 bool ffn_tc_supported(const moe_layer_desc &L);
 
 cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
-                           const float *gates, int R, void *y, cudaStream_t s);
+                           const float *gates, const void *residual, int R, void *y,
+                           cudaStream_t s);
 
 cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,
                            uint8_t *res_dev, cudaStream_t s);
+
+// ---- host helpers shared by the entry points (api.cu, offload.cu) ----
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+inline T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(reinterpret_cast<char *>(ws) + off);
+}
+
+bool desc_ok(const moe_layer_desc *L);
+bool select_args(const moe_select_params *P, int k, SelectArgs *a);
+bool permute_fits(int R, int E);
+bool aligned16(const void *p);
+moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
+                       const Workspace &w, int *counts, int *offsets, int *perm, cudaStream_t s);
+moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const void *Wu,
+                   const void *Wd, const int *slot, const uint8_t *pass, int R, void *ws,
+                   const Workspace &w, const int *counts, const int *offsets, const int *perm,
+                   const moe_run_opts *opts, cudaStream_t s);
+moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
+                       void *y, void *ws, const Workspace &w, cudaStream_t s);
 
 // ---- device helpers ----
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -69,7 +69,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) ffn_gateup_simt(FfnArgs a) {
     const int e = blockIdx.x;
     const int cnt = a.counts[e];
-    if (cnt == 0) return;
+    if (cnt == 0 || (a.pass && !a.pass[e])) return;
     bool ok;
     const T *Wg = expert_base<T>(a.Wg, a.slot, a.slots, e, (size_t)a.f * a.d, a.flags, ok);
     if (!ok) return;
@@ -124,7 +124,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) ffn_down_simt(FfnArgs a) {
     const int e = blockIdx.x;
     const int cnt = a.counts[e];
-    if (cnt == 0) return;
+    if (cnt == 0 || (a.pass && !a.pass[e])) return;
     bool ok;
     const T *Wd = expert_base<T>(a.Wd, a.slot, a.slots, e, (size_t)a.f * a.d, a.flags, ok);
     if (!ok) return;

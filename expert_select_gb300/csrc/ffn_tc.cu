@@ -72,6 +72,7 @@ struct Params {
     int box_cap;   // rows of the per-stage token buffer
     int slots;     // expert slots in the weight pool
     const int *rowtiles, *offsets, *slot;
+    const uint8_t *pass;  // experts computed by this launch (null: all)
     int *flags;
     int *sched;    // [0] ticket counter, [1 + rt] finished phase-1 units of row tile rt
     __nv_bfloat16 *h;
@@ -235,7 +236,9 @@ struct Unit {
 };
 
 // Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2.
-__device__ __forceinline__ bool decode(const Params &p, int U1, int u, Unit &w) {
+// Returns 0 for a unit to compute, 1 for one outside this launch's expert pass, 2 for an
+// expert whose slot is outside the pool (skipped and flagged).
+__device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w) {
     if (u < U1) {
         w.phase = 1;
         w.rt = u / p.mt1;
@@ -250,8 +253,9 @@ __device__ __forceinline__ bool decode(const Params &p, int U1, int u, Unit &w) 
     w.e = t[0];
     w.n0 = t[1];
     w.ntok = t[2];
+    if (p.pass && !p.pass[w.e]) return 1;
     w.slot = p.slot ? p.slot[w.e] : w.e;
-    return w.slot >= 0 && w.slot < p.slots && w.ntok > 0;
+    return (w.slot >= 0 && w.slot < p.slots && w.ntok > 0) ? 0 : 2;
 }
 
 constexpr int kQ = 4;  // ticket queue depth
@@ -341,8 +345,9 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                if (!decode(p, U1, u, w)) {
-                    atomicOr(p.flags, FLAG_BAD_EXPERT);
+                const int dc = decode(p, U1, u, w);
+                if (dc != 0) {
+                    if (dc == 2) atomicOr(p.flags, FLAG_BAD_EXPERT);
                     continue;
                 }
                 if (w.phase == 2) {  // wait until the row tile's h is complete
@@ -409,7 +414,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                if (!decode(p, U1, u, w)) continue;
+                if (decode(p, U1, u, w) != 0) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -465,7 +470,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int u = epi_u[turn];
             if (u < 0) break;
             Unit w;
-            if (!decode(p, U1, u, w)) continue;
+            if (decode(p, U1, u, w) != 0) continue;
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             ++it;
@@ -681,6 +686,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.rowtiles = a.rowtiles;
     p.offsets = a.offsets;
     p.slot = a.slot;
+    p.pass = a.pass;
     p.flags = a.flags;
     p.sched = a.sched;
     p.h = (__nv_bfloat16 *)a.h;

@@ -132,7 +132,7 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
     __shared__ int natRoot[kMaxK];
     __shared__ float s_sumD;
-    __shared__ int s_m, s_removed;
+    __shared__ int s_m;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;

@@ -32,7 +32,7 @@ EXPORTS = (
     "moe_tree_select", "moe_expert_permute", "moe_expert_forward", "moe_tree_forward",
     "moe_workspace_check", "moe_residency_create", "moe_residency_destroy",
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
-    "moe_event_wait", "moe_tree_forward_noalloc",
+    "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward",
 )
 
 
@@ -58,8 +58,14 @@ class TreeOutputs(C.Structure):
                 ("logits", "topk_idx", "gates", "eligible", "info", "counts", "offsets", "perm")]
 
 
+class OffloadStats(C.Structure):
+    _fields_ = [("needed", C.c_int), ("hits", C.c_int), ("uploads", C.c_int),
+                ("passes", C.c_int), ("h2d_bytes", C.c_longlong)]
+
+
 class RunOpts(C.Structure):
-    _fields_ = [("ffn_path", C.c_int), ("ffn_begin", C.c_void_p), ("ffn_end", C.c_void_p)]
+    _fields_ = [("ffn_path", C.c_int), ("ffn_begin", C.c_void_p), ("ffn_end", C.c_void_p),
+                ("residual", C.c_int)]
 
 
 _lib = None
@@ -91,6 +97,8 @@ def lib() -> C.CDLL:
             "moe_expert_upload": ([P, P, P, P, P, P, P, P, P, I, P, P], I),
             "moe_event_wait": ([P, C.c_double], I),
             "moe_tree_forward_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P], I),
+            "moe_offload_forward": ([P, P, P, P, P, P, P, P, P, P, P, I, P, I, I, P, P, P, P, P,
+                                     P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -175,10 +183,10 @@ def _event(ev):
     return C.c_void_p(ev.cuda_event)
 
 
-def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None) -> RunOpts:
-    """Options for moe_expert_forward / moe_tree_forward. `begin`/`end` are
-    torch.cuda.Event objects recorded around the grouped-expert kernel."""
-    return RunOpts(ffn_path, _event(begin), _event(end))
+def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None, residual=False) -> RunOpts:
+    """Options for the forward entry points. `begin`/`end` are torch.cuda.Event
+    objects recorded around the grouped-expert kernel; `residual` returns x + MoE(x)."""
+    return RunOpts(ffn_path, _event(begin), _event(end), int(residual))
 
 
 def moe_expert_forward(L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, y, ws,
@@ -280,6 +288,21 @@ def moe_expert_upload(L, host_gate, host_up, host_down, slot_gate, slot_up, slot
         _ptr(slot_up), _ptr(slot_down), ue.ctypes.data_as(C.c_void_p),
         us.ctypes.data_as(C.c_void_p), len(ue), C.c_void_p(side_stream.cuda_stream),
         _event(done_event)))
+
+
+def moe_offload_forward(L, P, x, W_r, host_gate, host_up, host_down, slot_gate, slot_up,
+                        slot_down, table: "Residency", layer: int, depth, B, N, y, ws,
+                        out: Optional[TreeOutputs] = None, opts: Optional[RunOpts] = None,
+                        stream=None, side_stream=None) -> OffloadStats:
+    """The layer with offloaded experts; returns the call's OffloadStats."""
+    st = OffloadStats()
+    side = side_stream if side_stream is not None else torch.cuda.current_stream()
+    _check("moe_offload_forward", lib().moe_offload_forward(
+        C.byref(L), C.byref(P), _ptr(x), _ptr(W_r), _ptr(host_gate), _ptr(host_up),
+        _ptr(host_down), _ptr(slot_gate), _ptr(slot_up), _ptr(slot_down), table.h, layer,
+        _ptr(depth), B, N, _ptr(y), None if out is None else C.byref(out), C.byref(st), _ptr(ws),
+        None if opts is None else C.byref(opts), _stream(stream), C.c_void_p(side.cuda_stream)))
+    return st
 
 
 def moe_event_wait(event, timeout_s: float) -> None:

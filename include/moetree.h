@@ -117,11 +117,14 @@ typedef struct {
 
 /* Run options; pass NULL for defaults. If both events are non-NULL they are
  * recorded on the stream immediately before and after the grouped-expert kernel
- * (for timing the dominant kernel with CUDA events). */
+ * (for timing the dominant kernel with CUDA events). With `residual` set the layer
+ * returns y = x + MoE(x) instead of MoE(x), for a residual stack of layers; y may then
+ * be the same buffer as x. */
 typedef struct {
     int ffn_path; /* moe_ffn_path */
     moe_event_t ffn_begin;
     moe_event_t ffn_end;
+    int residual;
 } moe_run_opts;
 
 /* Text for a status code. Never NULL. */
@@ -262,6 +265,40 @@ moe_status moe_expert_upload(const moe_layer_desc *L, const void *host_gate, con
                              const void *host_down, void *slot_gate, void *slot_up,
                              void *slot_down, const int *up_expert, const int *up_slot, int n,
                              moe_stream_t side, moe_event_t done);
+
+/* Counters of one moe_offload_forward call. */
+typedef struct {
+    int needed;          /* experts with at least one assignment in the block */
+    int hits;            /* of those, already resident when the call began */
+    int uploads;         /* experts copied host -> device by the call */
+    int passes;          /* grouped-expert launches (resident experts, then upload chunks) */
+    long long h2d_bytes; /* bytes copied host -> device */
+} moe_offload_stats;
+
+/* The whole layer with offloaded experts ("AcceptMoE" news article, section 03: a fixed
+ * number of expert slots per layer on the GPU, the rest in CPU memory uploaded on
+ * demand; section 02 and the abstract: residency-aware pruning conditions eligibility
+ * on what is resident now). Router, selection (pruning, if P->prune, sees the residency
+ * as it was before this call), permute; then ONE host wait for the per-expert counts;
+ * the resident needed experts are computed at once while missing experts are copied on
+ * `side` (one cudaMemcpyAsync per matrix, least-recently-used slots replaced, in chunks
+ * when they do not fit next to the experts being computed); finally the gated combine.
+ *   L->slots        device slots of this layer (the table's `slots`).
+ *   host_gate/up/down  pinned host stores [E, f, d], [E, f, d], [E, d, f].
+ *   slot_gate/up/down  device pools [slots, f, d], [slots, f, d], [slots, d, f].
+ *   table, layer    the residency table and this layer's index in it; updated.
+ *   stats           host, optional.
+ * Other arguments as moe_tree_forward. Returns after enqueueing the last kernel; the
+ * call itself waits (bounded, 10 s -> MOE_ERR_TIMEOUT) only for the routing of this
+ * block. Uploads never overwrite a slot that an enqueued kernel may still read. */
+moe_status moe_offload_forward(const moe_layer_desc *L, const moe_select_params *P,
+                               const void *x, const void *W_r, const void *host_gate,
+                               const void *host_up, const void *host_down, void *slot_gate,
+                               void *slot_up, void *slot_down, moe_residency *table, int layer,
+                               const int *depth, int B, int N, void *y,
+                               const moe_tree_outputs *out, moe_offload_stats *stats,
+                               void *workspace, const moe_run_opts *opts, moe_stream_t stream,
+                               moe_stream_t side);
 
 /* Host poll of cudaEventQuery(ev) for at most timeout_s seconds. MOE_ERR_TIMEOUT if
  * the event has not completed by then. */

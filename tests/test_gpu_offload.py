@@ -1,0 +1,123 @@
+"""GPU tests of the offloaded layer (moe_offload_forward) and of the residual option.
+
+The offloaded layer computes every expert with the same kernels as the resident layer,
+only addressed through slots that uploads fill, in one or more passes; so its output
+must equal moe_tree_forward on the same inputs bit for bit, given the residency mask the
+table had before the call (pruning reads that mask). The counters must add up: every
+needed expert is either a hit or uploaded once, and the bytes copied are the uploaded
+experts' weights.
+"""
+import numpy as np
+import pytest
+import torch
+
+from expert_select_gb300 import moetree as M
+from expert_select_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from expert_select_gb300 import build
+    build.build()
+    M.lib()
+
+
+SHAPE_TC = W.LayerShape(d=256, E=32, k=4, f=128, dtype="bf16")
+SHAPE_SIMT = W.LayerShape(d=256, E=16, k=2, f=128, dtype="fp32")
+
+
+def _params(mode, prune):
+    if mode == "natural":
+        return M.select_params(M.MOE_ROUTE_NATURAL, W.C_EAGLE)
+    return M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=prune, reroute_budget=8,
+                           min_set=4)
+
+
+@pytest.mark.parametrize("shape,slots,mode,prune,router_std", [
+    (SHAPE_TC, 8, "natural", False, 0.02),
+    (SHAPE_TC, 8, "accept", False, 0.3),
+    (SHAPE_TC, 12, "accept", True, 0.3),
+    (SHAPE_TC, 30, "natural", False, 0.02),
+    (SHAPE_SIMT, 4, "accept", True, 0.3),
+])
+def test_offload_matches_resident_layer(shape, slots, mode, prune, router_std):
+    E, k = shape.E, shape.k
+    wg, wu, wd = W.expert_weights(5, shape, device=DEV)
+    hg, hu, hd = (w.cpu().pin_memory() for w in (wg, wu, wd))
+    pg = torch.zeros(slots, shape.f, shape.d, dtype=shape.torch_dtype, device=DEV)
+    pu = torch.zeros_like(pg)
+    pd = torch.zeros(slots, shape.d, shape.f, dtype=shape.torch_dtype, device=DEV)
+    wr = W.router_weight(6, shape, std=router_std, device=DEV)
+    L = M.layer_desc(shape.d, E, k, shape.f, shape.dtype)
+    Ls = M.layer_desc(shape.d, E, k, shape.f, shape.dtype, slots=slots)
+    P = _params(mode, prune)
+    table = M.Residency(n_layers=2, E=E, slots=slots)
+    side = torch.cuda.Stream()
+    expert_bytes = 3 * shape.d * shape.f * shape.elem_bytes
+    total_up = 0
+    for step in range(4):
+        t = W.eagle_tree(40 + step)
+        N = t.N
+        x = W.hidden_states(50 + step, t.parent, shape.d, shape.torch_dtype).to(DEV)
+        dep = torch.from_numpy(t.depth.copy()).to(DEV)
+        _, res_before = table.query(1)
+        res_dev = torch.from_numpy(res_before.copy()).to(DEV)
+        # the resident layer, pruning against the same residency
+        idx_ref = torch.empty(N, k, dtype=torch.int32, device=DEV)
+        cnt_ref = torch.empty(E, dtype=torch.int32, device=DEV)
+        y_ref = torch.empty(N, shape.d, dtype=shape.torch_dtype, device=DEV)
+        ws = M.workspace(L, 1, N)
+        M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dep, 1, N, res_dev, y_ref, ws,
+                           M.tree_outputs(topk_idx=idx_ref, counts=cnt_ref))
+        # the offloaded layer
+        idx = torch.empty_like(idx_ref)
+        y = torch.full_like(y_ref, float("nan"))
+        ws2 = M.workspace(Ls, 1, N)
+        st = M.moe_offload_forward(Ls, P, x, wr, hg, hu, hd, pg, pu, pd, table, 1, dep, 1, N,
+                                   y, ws2, M.tree_outputs(topk_idx=idx), side_stream=side)
+        torch.cuda.synchronize()
+        assert M.moe_workspace_check(ws2) == 0
+        assert torch.equal(idx, idx_ref)
+        assert torch.equal(y, y_ref), step
+        union = int((cnt_ref > 0).sum())
+        assert st.needed == union
+        assert st.hits + st.uploads == union
+        assert st.h2d_bytes == st.uploads * expert_bytes
+        if union > slots:
+            assert st.passes >= 2
+        total_up += st.uploads
+        slot_map, res_after = table.query(1)
+        needed = np.flatnonzero(cnt_ref.cpu().numpy())
+        # the last pass's experts are resident; at most `slots` experts are
+        assert int(res_after.sum()) <= slots
+        assert len(set(slot_map[slot_map >= 0].tolist())) == int(res_after.sum())
+        if union <= slots:
+            assert res_after[needed].all()
+    assert total_up > 0
+
+
+def test_residual_option_adds_the_input():
+    shape = W.QWEN3_30B_A3B
+    t = W.eagle_tree(3)
+    N = t.N
+    x = W.hidden_states(4, t.parent, shape.d, torch.bfloat16).to(DEV)
+    dep = torch.from_numpy(t.depth.copy()).to(DEV)
+    wr = W.router_weight(7, shape, std=0.1, device=DEV)
+    wg, wu, wd = W.expert_weights(8, shape, device=DEV)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    ws = M.workspace(L, 1, N)
+    y = torch.empty_like(x)
+    M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dep, 1, N, None, y, ws)
+    yr = x.clone()  # in place: y aliases x
+    M.moe_tree_forward(L, P, yr, wr, wg, wu, wd, None, dep, 1, N, None, yr, ws, None,
+                       M.run_opts(residual=True))
+    torch.cuda.synchronize()
+    ref = x.double() + y.double()
+    err = (yr.double() - ref).abs().max().item()
+    assert err <= 2e-2 * ref.abs().max().item()
