@@ -441,6 +441,291 @@ def run_reference(args):
     }))
 
 
+# ------------------------------------------------------- secondary workloads
+# Each prints one JSON line with the same contract keys as the headline line.
+
+def _setup_gpu():
+    import torch
+    from expert_select_gb300 import build
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    return world, rank, local, torch.device("cuda", local)
+
+
+def _timed(fn, dev, world):
+    """Runs fn() between synchronised CUDA events; max over ranks (seconds)."""
+    import torch
+    s = torch.cuda.current_stream(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    fn()
+    b.record(s)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return max_over_ranks(a.elapsed_time(b) / 1e3, world)
+
+
+def _line(metric, value, unit, world, K, Wm, sec, config, **extra):
+    d = {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K,
+         "warmup": Wm, "ms_per_step": round(sec / K * 1e3, 4), "higher_is_better": True,
+         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+         "data": "synthetic (seeded EAGLE-3-shaped trees, N(0,0.02) weights)", "config": config}
+    d.update(extra)
+    return json.dumps(d)
+
+
+def run_stack48(args):
+    """48 independent Qwen3-shaped layers resident in HBM (~58 GB of experts), one fresh
+    65-node tree per step through all layers with a residual chain x <- x + MoE_l(x)."""
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.QWEN3_30B_A3B
+    NL = args.layers or 48
+    seed = SEED + 2000 + 7919 * rank
+    xs_h, deps_h = make_trees(TREES, shape, seed)
+    xs, deps = xs_h.to(dev), deps_h.to(dev).int()
+    layers = []
+    for l in range(NL):
+        wr = W.router_weight(seed + 10 ** 6 * (l + 1), shape, std=args.router_std, device=dev)
+        wg, wu, wd = W.expert_weights(seed + 10 ** 6 * (l + 1) + 1, shape, device=dev)
+        layers.append((wr, wg, wu, wd))
+    N = xs.shape[1]
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    mode = M.MOE_ROUTE_ACCEPT if args.routing == "acceptmoe" else M.MOE_ROUTE_NATURAL
+    P = M.select_params(mode, W.C_EAGLE)
+    ws = M.workspace(L, 1, N, device=dev)
+    x = torch.empty_like(xs[0])
+    K, Wm = args.steps, args.warmup
+    counts = torch.zeros(K, NL, shape.E, dtype=torch.int32, device=dev)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(NL)] for _ in range(K)]
+    s = torch.cuda.current_stream(dev)
+    for row in ev:
+        for a, b in row:
+            a.record(s)
+            b.record(s)
+    torch.cuda.synchronize(dev)
+
+    def step(i, record):
+        x.copy_(xs[i % TREES])
+        for l, (wr, wg, wu, wd) in enumerate(layers):
+            out = M.tree_outputs(counts=counts[i, l]) if record else None
+            opts = M.run_opts(args.ffn_path, ev[i][l][0], ev[i][l][1], residual=True) if record \
+                else M.run_opts(args.ffn_path, residual=True)
+            M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, deps[i % TREES], 1, N, None, x,
+                               ws, out, opts)
+
+    for i in range(Wm):
+        step(i, False)
+    with ClockSampler(local) as clk:
+        sec = _timed(lambda: [step(i, True) for i in range(K)], dev, world)
+    ffn_s = sum(a.elapsed_time(b) for row in ev for a, b in row) / 1e3
+    union = (counts.cpu().numpy() > 0).sum(axis=2)  # [K, NL]
+    algo = float((union * shape.expert_bytes).sum() + K * NL * 2 * N * shape.d * 2)
+    peak, kind = measured_peaks()
+    if rank == 0:
+        print(_line("MoE verify, 48-layer stack: tree-blocks/s through all layers",
+                    whole_job_rate(K, world, sec), "tree-blocks/s", world, K, Wm, sec,
+                    {"workload": f"qwen3-30b-a3b-{NL}-layer-stack-resident", "layers": NL,
+                     "routing": args.routing, "router_std": args.router_std,
+                     "expert_bytes_resident_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1),
+                     "l2": "inputs larger than L2 (0.7 GB of union weights per layer)"},
+                    per_layer_blocks_per_s=round(whole_job_rate(K, world, sec) * NL, 1),
+                    roofline={"bound": "hbm", "achieved": round(algo / ffn_s / 1e9, 1),
+                              "peak": peak, "unit": "GB/s",
+                              "frac": round(algo / ffn_s / 1e9 / peak, 4), "peak_kind": kind,
+                              "kernel": "grouped SwiGLU experts"},
+                    union={"mean": float(union.mean()), "min": int(union.min()),
+                           "max": int(union.max())},
+                    clocks=clk.summary()))
+
+
+def _pinned_empty(shape, dtype):
+    """A host tensor of exactly this size, page-locked in place (cudaHostRegister)."""
+    import torch
+    t = torch.empty(shape, dtype=dtype)
+    rc = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 0)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed ({rc})")
+    return t
+
+
+def run_offload(args):
+    """GPT-OSS-120B-shaped layers with experts offloaded: `slots` expert slots per layer
+    on the GPU, every expert in pinned host memory, uploads on a side stream."""
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.GPT_OSS_120B
+    NL = args.layers or 8
+    slots = args.slots
+    seed = SEED + 3000 + 7919 * rank
+    xs_h, deps_h = make_trees(TREES, shape, seed)
+    xs, deps = xs_h.to(dev), deps_h.to(dev).int()
+    t0 = time.perf_counter()
+    layers = []
+    for l in range(NL):
+        wr = W.router_weight(seed + 10 ** 6 * (l + 1), shape, std=args.router_std, device=dev)
+        wg, wu, wd = W.expert_weights(seed + 10 ** 6 * (l + 1) + 1, shape, device=dev)
+        host = [_pinned_empty(w.shape, w.dtype) for w in (wg, wu, wd)]
+        for h, w in zip(host, (wg, wu, wd)):
+            h.copy_(w)
+        del wg, wu, wd
+        pools = [torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
+                 torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
+                 torch.empty(slots, shape.d, shape.f, dtype=torch.bfloat16, device=dev)]
+        layers.append((wr, host, pools))
+    torch.cuda.empty_cache()
+    setup_s = time.perf_counter() - t0
+    # host link bandwidth: one 1 GiB pinned -> device copy
+    hb = layers[0][1][0].view(-1)[: 1 << 29]
+    db = torch.empty_like(hb, device=dev)
+    db.copy_(hb)
+    torch.cuda.synchronize(dev)
+    link_s = _timed(lambda: db.copy_(hb, non_blocking=True), dev, 1)
+    link_gbs = hb.numel() * 2 / link_s / 1e9
+    del db
+    N = xs.shape[1]
+    Ls = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16", slots=slots)
+    ws = M.workspace(Ls, 1, N, device=dev)
+    x = torch.empty_like(xs[0])
+    side = torch.cuda.Stream(dev)
+    K, Wm = args.steps, args.warmup
+    results = {}
+    for name, mode, prune in (("natural", M.MOE_ROUTE_NATURAL, False),
+                              ("acceptmoe", M.MOE_ROUTE_ACCEPT, False),
+                              ("acceptmoe+prune", M.MOE_ROUTE_ACCEPT, True)):
+        P = M.select_params(mode, W.C_EAGLE, prune=prune, reroute_budget=8, min_set=16)
+        table = M.Residency(n_layers=NL, E=shape.E, slots=slots)
+        stats = []
+
+        def step(i, keep):
+            x.copy_(xs[i % TREES])
+            for l, (wr, host, pools) in enumerate(layers):
+                st = M.moe_offload_forward(Ls, P, x, wr, *host, *pools, table, l,
+                                           deps[i % TREES], 1, N, x, ws,
+                                           opts=M.run_opts(residual=True), side_stream=side)
+                if keep:
+                    stats.append((st.needed, st.hits, st.uploads, st.h2d_bytes, st.passes))
+
+        for i in range(Wm):
+            step(i, False)
+        sec = _timed(lambda: [step(i, True) for i in range(K)], dev, world)
+        a = np.array(stats, dtype=np.float64)
+        results[name] = {"tree_blocks_per_s": round(K / sec, 3),
+                         "ms_per_step": round(sec / K * 1e3, 3),
+                         "needed_per_layer": round(float(a[:, 0].mean()), 2),
+                         "hit_rate": round(float(a[:, 1].sum() / a[:, 0].sum()), 4),
+                         "uploads_per_layer": round(float(a[:, 2].mean()), 2),
+                         "h2d_gb_per_step": round(float(a[:, 3].sum()) / K / 1e9, 3),
+                         "passes_per_layer": round(float(a[:, 4].mean()), 2)}
+        table.close()
+    nat = results["natural"]
+    for name in ("acceptmoe", "acceptmoe+prune"):
+        r = results[name]
+        r["speedup_vs_natural"] = round(r["tree_blocks_per_s"] / nat["tree_blocks_per_s"], 3)
+        r["h2d_reduction_vs_natural"] = round(
+            1 - r["h2d_gb_per_step"] / max(nat["h2d_gb_per_step"], 1e-12), 4)
+        r["hit_rate_gain_pp"] = round(100 * (r["hit_rate"] - nat["hit_rate"]), 2)
+    main_r = results["acceptmoe+prune"]
+    if rank == 0:
+        print(_line("MoE verify with expert offload: tree-blocks/s through all layers",
+                    main_r["tree_blocks_per_s"] * world, "tree-blocks/s", world, K, Wm,
+                    K / main_r["tree_blocks_per_s"],
+                    {"workload": f"gpt-oss-120b-{NL}-layer-offload-{slots}-slots",
+                     "layers": NL, "slots": slots, "router_std": args.router_std,
+                     "routing": "acceptmoe + residency-aware pruning (budget 8, min 16)",
+                     "host_store_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1)},
+                    modes=results, h2d_link_gbs=round(link_gbs, 1), setup_s=round(setup_s, 1)))
+
+
+def run_batched(args):
+    """The Qwen3-shaped layer with B independent 65-node trees per verification block."""
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.QWEN3_30B_A3B
+    seed = SEED + 4000 + 7919 * rank
+    Bs = [int(b) for b in args.batches.split(",")]
+    n_trees = max(TREES, 2 * max(Bs))
+    xs_h, deps_h = make_trees(n_trees, shape, seed)
+    xs, deps = xs_h.to(dev), deps_h.to(dev).int()
+    wr = W.router_weight(seed + 1, shape, std=args.router_std, device=dev)
+    wg, wu, wd = W.expert_weights(seed + 2, shape, device=dev)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    N = xs.shape[1]
+    peak, kind = measured_peaks()
+    tflops_peak = 1934.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            tflops_peak = float(json.load(fh)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        pass
+    rows = []
+    K, Wm = args.steps, args.warmup
+    for B in Bs:
+        R = B * N
+        ws = M.workspace(L, B, N, device=dev)
+        y = torch.empty(R, shape.d, dtype=torch.bfloat16, device=dev)
+        nblk = n_trees // B
+        xb = [xs[j * B:(j + 1) * B].reshape(R, shape.d) for j in range(nblk)]
+        db = [deps[j * B:(j + 1) * B].reshape(R) for j in range(nblk)]
+        for routing, mode in (("natural", M.MOE_ROUTE_NATURAL), ("acceptmoe", M.MOE_ROUTE_ACCEPT)):
+            P = M.select_params(mode, W.C_EAGLE)
+            counts = torch.zeros(K, shape.E, dtype=torch.int32, device=dev)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            s = torch.cuda.current_stream(dev)
+            for a, b in ev:
+                a.record(s)
+                b.record(s)
+
+            def loop(n, rec):
+                for i in range(n):
+                    j = i % nblk
+                    M.moe_tree_forward(L, P, xb[j], wr, wg, wu, wd, None, db[j], B, N, None, y,
+                                       ws, M.tree_outputs(counts=counts[i]) if rec else None,
+                                       M.run_opts(args.ffn_path, ev[i][0], ev[i][1]) if rec
+                                       else None)
+
+            loop(Wm, False)
+            sec = _timed(lambda: loop(K, True), dev, world)
+            ffn_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+            c = counts.cpu().numpy()
+            union = (c > 0).sum(axis=1)
+            A = c.sum(axis=1)
+            algo = float((union * shape.expert_bytes).sum() + K * 2 * R * shape.d * 2)
+            flops = float((2.0 * A * 3 * shape.d * shape.f).sum())
+            rows.append({"B": B, "rows": R, "routing": routing,
+                         "blocks_per_s": round(whole_job_rate(K, world, sec), 2),
+                         "trees_per_s": round(whole_job_rate(K, world, sec) * B, 1),
+                         "ms_per_block": round(sec / K * 1e3, 4),
+                         "ffn_ms": round(ffn_s / K * 1e3, 4), "union": round(float(union.mean()), 2),
+                         "tokens_per_expert": round(float((A / np.maximum(union, 1)).mean()), 1),
+                         "ffn_gbs": round(algo / ffn_s / 1e9, 1),
+                         "ffn_hbm_frac": round(algo / ffn_s / 1e9 / peak, 4),
+                         "ffn_tflops": round(flops / ffn_s / 1e12, 1),
+                         "ffn_tensor_frac": round(flops / ffn_s / 1e12 / tflops_peak, 4)})
+    if rank == 0:
+        best = rows[-1]
+        print(_line("MoE verify layer, batched trees: tree-blocks/s", best["blocks_per_s"],
+                    "tree-blocks/s", world, K, Wm, 1.0 / best["blocks_per_s"] * K,
+                    {"workload": "qwen3-30b-a3b-moe-layer-batched-trees", "batches": Bs,
+                     "router_std": args.router_std,
+                     "l2": "inputs larger than L2 (>= 0.7 GB of union weights per block)"},
+                    sweep=rows, hbm_peak=peak, bf16_tflops_peak=tflops_peak))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,10 +737,21 @@ def main(argv=None):
     ap.add_argument("--ffn-path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--cpu-trees", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched"],
+                    default="layer", help="layer: the Qwen3-shaped layer (default line)")
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--slots", type=int, default=48)
+    ap.add_argument("--batches", default="1,4,16,64")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack48":
+        run_stack48(args)
+    elif args.workload == "offload":
+        run_offload(args)
+    elif args.workload == "batched":
+        run_batched(args)
     else:
         run_gpu(args)
 
