@@ -44,6 +44,7 @@ template <typename TO>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
                const float *__restrict__ gates, const TO *res, int d, int k, TO *y) {
+    pdl_wait();
     const int r = blockIdx.x;
     const int c = (blockIdx.y * kThreads + threadIdx.x) * 4;
     if (c >= d) return;
@@ -67,6 +68,7 @@ struct PublishArgs {
 };
 
 __global__ void publish_kernel(PublishArgs p, int E, int *slot, uint8_t *res) {
+    pdl_wait();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         if (slot) slot[e] = p.slot[e];
         if (res) res[e] = p.res[e];
@@ -81,12 +83,10 @@ cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *p
     if (R <= 0) return cudaSuccess;
     dim3 grid(R, (L.d / 4 + kThreads - 1) / kThreads);
     if (L.dtype == MOE_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
-            o, pos, gates, (const __nv_bfloat16 *)residual, L.d, L.k, (__nv_bfloat16 *)y);
-    else
-        combine_kernel<float><<<grid, kThreads, 0, s>>>(o, pos, gates, (const float *)residual,
-                                                        L.d, L.k, (float *)y);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s, o, pos,
+                          gates, (const __nv_bfloat16 *)residual, L.d, L.k, (__nv_bfloat16 *)y);
+    return launch_pdl(combine_kernel<float>, grid, dim3(kThreads), 0, s, o, pos, gates,
+                      (const float *)residual, L.d, L.k, (float *)y);
 }
 
 cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,
@@ -96,8 +96,7 @@ cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host,
         p.slot[e] = slot_host[e];
         p.res[e] = res_host[e];
     }
-    publish_kernel<<<1, 256, 0, s>>>(p, E, slot_dev, res_dev);
-    return cudaGetLastError();
+    return launch_pdl(publish_kernel, dim3(1), dim3(256), 0, s, p, E, slot_dev, res_dev);
 }
 
 }  // namespace moe

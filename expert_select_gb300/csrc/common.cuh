@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "moetree.h"
 
 namespace moe {
@@ -57,13 +59,17 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s);
 
-// Token rows per row tile of the tensor-core expert kernel (its largest MMA N).
-constexpr int kRowTile = 256;
-inline int max_rowtiles(int E, int A) { return E + (A + kRowTile - 1) / kRowTile + 1; }
+// Token rows per row tile of the tensor-core expert kernel (its MMA N is at most 256).
+// Small blocks use 64-row tiles: no expert then needs more than a 64-row token buffer
+// per pipeline stage, which leaves shared memory for more stages of weight bytes in
+// flight; an expert with more tokens than that takes a second row tile.
+constexpr int kMinRowTile = 64;
+inline int rowtile_size(int R) { return R <= 128 ? 64 : 256; }
+inline int max_rowtiles(int E, int A) { return E + (A + kMinRowTile - 1) / kMinRowTile + 1; }
 
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
-                           int *flags, cudaStream_t s);
+                           int *flags, cudaStream_t s);  // row tiles of rowtile_size(R)
 size_t permute_smem_bytes(int R, int E);
 
 struct FfnArgs {
@@ -112,6 +118,30 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
                    const moe_run_opts *opts, cudaStream_t s);
 moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
                        void *y, void *ws, const Workspace &w, cudaStream_t s);
+
+// ---- launches ----
+// Every kernel of the library is launched with programmatic stream serialization, so a
+// kernel may be scheduled while its predecessor in the stream drains, and every kernel
+// calls pdl_wait() before it touches memory: the wait returns once the predecessor grid
+// has completed and its writes are visible. (Because every kernel waits, completion stays
+// ordered along the whole chain.)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- device helpers ----
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -67,6 +67,7 @@ __device__ __forceinline__ float dot8(const float w[8], const float *x) {
 // h[p, i] = silu(Wg[i] . x_p) * (Wu[i] . x_p) for the expert's permuted rows p.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ffn_gateup_simt(FfnArgs a) {
+    pdl_wait();
     const int e = blockIdx.x;
     const int cnt = a.counts[e];
     if (cnt == 0 || (a.pass && !a.pass[e])) return;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads) ffn_gateup_simt(FfnArgs a) {
 // O[p, i] = Wd[i] . h_p for the expert's permuted rows p.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ffn_down_simt(FfnArgs a) {
+    pdl_wait();
     const int e = blockIdx.x;
     const int cnt = a.counts[e];
     if (cnt == 0 || (a.pass && !a.pass[e])) return;
@@ -173,8 +175,9 @@ cudaError_t launch_ffn_simt(const FfnArgs &a, cudaStream_t s) {
         err = cudaFuncSetAttribute(ffn_down_simt<__nv_bfloat16>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
         if (err != cudaSuccess) return err;
-        ffn_gateup_simt<__nv_bfloat16><<<g1, kThreads, smem_gu, s>>>(a);
-        ffn_down_simt<__nv_bfloat16><<<g2, kThreads, smem_dn, s>>>(a);
+        err = launch_pdl(ffn_gateup_simt<__nv_bfloat16>, g1, dim3(kThreads), smem_gu, s, a);
+        if (err != cudaSuccess) return err;
+        err = launch_pdl(ffn_down_simt<__nv_bfloat16>, g2, dim3(kThreads), smem_dn, s, a);
     } else {
         err = cudaFuncSetAttribute(ffn_gateup_simt<float>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
@@ -182,10 +185,11 @@ cudaError_t launch_ffn_simt(const FfnArgs &a, cudaStream_t s) {
         err = cudaFuncSetAttribute(ffn_down_simt<float>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
         if (err != cudaSuccess) return err;
-        ffn_gateup_simt<float><<<g1, kThreads, smem_gu, s>>>(a);
-        ffn_down_simt<float><<<g2, kThreads, smem_dn, s>>>(a);
+        err = launch_pdl(ffn_gateup_simt<float>, g1, dim3(kThreads), smem_gu, s, a);
+        if (err != cudaSuccess) return err;
+        err = launch_pdl(ffn_down_simt<float>, g2, dim3(kThreads), smem_dn, s, a);
     }
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moe

@@ -320,6 +320,9 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // everything above only touched this CTA's own resources: wait for the previous
+    // kernel before reading the routing tables it wrote
+    pdl_wait();
     const uint32_t tmem = *tmem_slot;
     const int n_rt = p.rowtiles[0];
     const int U1 = n_rt * p.mt1, U = U1 + n_rt * p.mt2;
@@ -558,6 +561,7 @@ __global__ void __launch_bounds__(256)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ perm,
                    const int *__restrict__ offsets, int E, int k, int d,
                    __nv_bfloat16 *__restrict__ xp, int *__restrict__ sched, int n_sched) {
+    pdl_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_sched; i += blockDim.x) sched[i] = 0;
     const int pidx = blockIdx.x;
@@ -646,13 +650,13 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const int A = a.R * a.k;
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorInvalidDevice;
-    // token-row buffer per stage: the box that holds min(256, R) rows (a row picks an
-    // expert at most once, so no expert has more than R tokens)
+    // token-row buffer per stage: the box that holds a full row tile, or R rows if fewer
+    // (a row picks an expert at most once, so no expert has more than R tokens)
     int box_cap = 16;
-    const int need = ((std::min(a.R, kRowTile) + 15) / 16) * 16;
+    const int need = ((std::min(a.R, rowtile_size(a.R)) + 15) / 16) * 16;
     while (box_cap < need) box_cap <<= 1;
     const size_t budget = 227 * 1024;
-    int stages = 8;
+    int stages = 12;
     while (stages > 2 && smem_bytes(stages, box_cap) > budget) --stages;
     const size_t smem = smem_bytes(stages, box_cap);
     const int S = a.slots;
@@ -673,8 +677,10 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     if (attr_err != cudaSuccess) return attr_err;
 
     const int n_sched = 1 + max_rowtiles(a.E, A);
-    gather_rows_kernel<<<A, 256, 0, s>>>((const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k,
-                                         a.d, (__nv_bfloat16 *)a.xp, a.sched, n_sched);
+    cudaError_t err = launch_pdl(gather_rows_kernel, dim3(A), dim3(256), 0, s,
+                                 (const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k, a.d,
+                                 (__nv_bfloat16 *)a.xp, a.sched, n_sched);
+    if (err != cudaSuccess) return err;
     Params p{};
     p.d = a.d;
     p.f = a.f;
@@ -691,8 +697,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.sched = a.sched;
     p.h = (__nv_bfloat16 *)a.h;
     p.o = a.o;
-    ffn_tc_kernel<<<nsm, kThreads, smem, s>>>(m, p);
-    return cudaGetLastError();
+    return launch_pdl(ffn_tc_kernel, dim3(nsm), dim3(kThreads), smem, s, m, p);
 }
 
 }  // namespace moe

@@ -9,7 +9,7 @@
 //   offsets[e] + prefix[block][e] + popc(mask[block][e] & lanes_below(row)).
 // Everything stays in shared memory: (R/32) x E x 8 bytes (133 KB at 4160 rows and
 // 128 experts). The same kernel also writes the active-expert list and the list of
-// row tiles (at most 256 tokens of one expert) that the grouped expert kernels walk.
+// row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels walk.
 #include "common.cuh"
 
 namespace moe {
@@ -20,7 +20,9 @@ constexpr int kThreads = 1024;
 __global__ void __launch_bounds__(kThreads)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
-               int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags) {
+               int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags,
+               int rt_size) {
+    pdl_wait();
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
     uint32_t *mask = sm;                  // [nb][E]
@@ -59,7 +61,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             const int c = e < E ? cnt[e] : 0;
             c_tot += c;
             a_tot += c > 0;
-            t_tot += (c + kRowTile - 1) / kRowTile;
+            t_tot += (c + rt_size - 1) / rt_size;
         }
         int c_ex = c_tot, a_ex = a_tot, t_ex = t_tot;  // inclusive scans across lanes
 #pragma unroll
@@ -83,12 +85,12 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             off[e] = c_ex;
             c_ex += c;
             if (c > 0) active[1 + a_ex++] = e;
-            // row tiles of at most kRowTile tokens of one expert, for the tensor-core kernel
-            for (int n0 = 0; n0 < c; n0 += kRowTile) {
+            // row tiles of at most rt_size tokens of one expert, for the tensor-core kernel
+            for (int n0 = 0; n0 < c; n0 += rt_size) {
                 int *t = rowtiles + 1 + 4 * t_ex++;
                 t[0] = e;
                 t[1] = n0;
-                t[2] = min(kRowTile, c - n0);
+                t[2] = min(rt_size, c - n0);
                 t[3] = 0;
             }
         }
@@ -136,9 +138,8 @@ cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *
     cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    permute_kernel<<<1, kThreads, smem, s>>>(idx, R, L.k, L.E, counts, offsets, perm, pos, active,
-                                             rowtiles, flags);
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
+                      offsets, perm, pos, active, rowtiles, flags, rowtile_size(R));
 }
 
 }  // namespace moe

@@ -23,6 +23,7 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 router_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, int d, int E,
               float *__restrict__ logits) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int e0 = blockIdx.y * kExp;
@@ -67,6 +68,7 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 router_splitd_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, int d, int E,
                      float *__restrict__ logits) {
+    pdl_wait();
     __shared__ float part[kWarps][32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -119,21 +121,19 @@ cudaError_t launch_router(const moe_layer_desc &L, const void *x, const void *Wr
     if (R <= kSplitRows) {
         dim3 g((R + kRows - 1) / kRows, (L.E + kExp - 1) / kExp);
         if (L.dtype == MOE_DTYPE_BF16)
-            router_splitd_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, s>>>(
-                (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E, logits);
-        else
-            router_splitd_kernel<float><<<g, kWarps * 32, 0, s>>>(
-                (const float *)x, (const float *)Wr, R, L.d, L.E, logits);
-        return cudaGetLastError();
+            return launch_pdl(router_splitd_kernel<__nv_bfloat16>, g, dim3(kWarps * 32), 0, s,
+                              (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E,
+                              logits);
+        return launch_pdl(router_splitd_kernel<float>, g, dim3(kWarps * 32), 0, s,
+                          (const float *)x, (const float *)Wr, R, L.d, L.E, logits);
     }
     dim3 grid((R + kWarps * kRows - 1) / (kWarps * kRows), (L.E + kExp - 1) / kExp);
     if (L.dtype == MOE_DTYPE_BF16)
-        router_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(
-            (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E, logits);
-    else
-        router_kernel<float><<<grid, kWarps * 32, 0, s>>>((const float *)x, (const float *)Wr,
-                                                          R, L.d, L.E, logits);
-    return cudaGetLastError();
+        return launch_pdl(router_kernel<__nv_bfloat16>, grid, dim3(kWarps * 32), 0, s,
+                          (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E,
+                          logits);
+    return launch_pdl(router_kernel<float>, grid, dim3(kWarps * 32), 0, s, (const float *)x,
+                      (const float *)Wr, R, L.d, L.E, logits);
 }
 
 }  // namespace moe

@@ -134,6 +134,7 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
     __shared__ float s_sumD;
     __shared__ int s_m;
 
+    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const float *Lg = logits + (size_t)b * N * E;
@@ -344,9 +345,8 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
             select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
-    select_kernel<<<B, kThreads, smem, s>>>(a, logits, depth, N, L.E, L.k, resident, idx, gates,
-                                            elig, info);
-    return cudaGetLastError();
+    return launch_pdl(select_kernel, dim3(B), dim3(kThreads), smem, s, a, logits, depth, N, L.E,
+                      L.k, resident, idx, gates, elig, info);
 }
 
 }  // namespace moe
