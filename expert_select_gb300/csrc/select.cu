@@ -5,8 +5,8 @@
 // (when they fit) and every later pass reads them from there.
 //   Phase A  a warp per node: natural top-k (the natural routing and the natural
 //            union U), and the node's softmax maximum and normaliser.
-//   Demand   a thread per expert: D_e = sum_n c(depth_n) * exp(l_ne - max_n) / sum_n,
-//            nodes in ascending order.
+//   Demand   every term c(depth_n) * exp(l_ne - max_n) / sum_n in parallel, then a
+//            thread per expert adds its terms in ascending node order.
 //   Phase B  set size from the effective rank exp(H(D / sum D)), root anchor + fill in
 //            (D desc, id asc) order, residency-aware pruning in (D asc, id asc) order
 //            (ranks by counting, E <= 256).
@@ -125,7 +125,7 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
               int N, int E, int k, const uint8_t *__restrict__ resident, int *__restrict__ idx_out,
               float *__restrict__ gates_out, uint8_t *__restrict__ elig_out,
               int *__restrict__ info_out) {
-    extern __shared__ float dyn[];  // [N][E] staged logits (when they fit), mx, nz, cN, nat
+    extern __shared__ float dyn[];  // staged logits, mx, nz, cN, nat, demand terms
     __shared__ float D[kMaxE];
     __shared__ float term[kMaxE];
     __shared__ float rk[kMaxE];  // rank keys
@@ -209,15 +209,31 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         return;
     }
 
-    // ---- demand: a thread per expert, nodes in ascending order ----
-    for (int e = tid; e < E; e += kThreads) {
-        float acc = 0.f;
-#pragma unroll 4
-        for (int n = 0; n < N; ++n) {
-            const float ex = expf(L[(size_t)n * E + e] - mx[n]);
-            acc = __fadd_rn(acc, __fmul_rn(cN[n], __fdiv_rn(ex, nz[n])));
+    // ---- demand: D_e = sum over nodes (ascending) of c_n * exp(l_ne - max_n) / sum_n ----
+    if (staged) {
+        // all N*E terms in parallel, then a thread per expert adds its column in order
+        float *wt = reinterpret_cast<float *>(nat + N * k);  // [N][E]
+        for (int i = tid; i < N * E; i += kThreads) {
+            const int n = i / E;
+            wt[i] = __fmul_rn(cN[n], __fdiv_rn(expf(L[i] - mx[n]), nz[n]));
         }
-        D[e] = acc;
+        __syncthreads();
+        for (int e = tid; e < E; e += kThreads) {
+            float acc = 0.f;
+#pragma unroll 8
+            for (int n = 0; n < N; ++n) acc = __fadd_rn(acc, wt[(size_t)n * E + e]);
+            D[e] = acc;
+        }
+    } else {
+        for (int e = tid; e < E; e += kThreads) {
+            float acc = 0.f;
+#pragma unroll 4
+            for (int n = 0; n < N; ++n) {
+                const float ex = expf(L[(size_t)n * E + e] - mx[n]);
+                acc = __fadd_rn(acc, __fmul_rn(cN[n], __fdiv_rn(ex, nz[n])));
+            }
+            D[e] = acc;
+        }
     }
     __syncthreads();
 
@@ -337,8 +353,9 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           float *gates, uint8_t *elig, int *info, cudaStream_t s) {
     if (B <= 0 || N <= 0) return cudaSuccess;
     const bool staged = N * L.E <= kStageFloats;
+    // staged: logits and demand terms [N][E] each; always: mx, nz, cN [N] and nat [N][k]
     const size_t smem =
-        ((staged ? (size_t)N * L.E : 0) + 3 * (size_t)N + (size_t)N * L.k) * sizeof(float);
+        ((staged ? 2 * (size_t)N * L.E : 0) + 3 * (size_t)N + (size_t)N * L.k) * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     if (smem > 40 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(
