@@ -1,8 +1,10 @@
 // Verifier-side expert selection for a block of draft trees ("AcceptMoE" news
 // article, section 02; AcceptMoE abstract, arXiv 2608.02989).
 //
-// One CTA of 32 warps per tree; the tree's logits are staged in shared memory once
-// (when they fit) and every later pass reads them from there.
+// Trees of up to 256 nodes run as one cluster of 8 CTAs per tree (see the cluster
+// variant below); larger trees run on one CTA of 32 warps per tree, described here. The
+// tree's logits are staged in shared memory once (when they fit) and every later pass
+// reads them from there.
 //   Phase A  a warp per node: natural top-k (the natural routing and the natural
 //            union U), and the node's softmax maximum and normaliser.
 //   Demand   every term c(depth_n) * exp(l_ne - max_n) / sum_n in parallel, then a
@@ -24,6 +26,7 @@
 // fraction of its fp32 rate): the softmax normaliser in a warp tree, the demand per
 // expert in ascending node order, sum D and H in ascending expert order in one
 // thread, each product and sum rounded on its own (no FMA contraction).
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include <algorithm>
@@ -346,12 +349,262 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         for (int e = tid; e < E; e += kThreads) elig_out[(size_t)b * E + e] = (uint8_t)inS[e];
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant: one cluster of kCC CTAs (kCW warps each) per tree, for trees of up to
+// kClusterMaxN nodes. Node n belongs to global warp g = n mod (kCC*kCW), i.e. CTA
+// g / kCW, warp g mod kCW, local slot (n / (kCC*kCW)) * kCW + warp. Each CTA takes its
+// nodes' natural top-k and softmax terms, adds the terms of its nodes per expert in node
+// order, and stores the partial demand and the natural choices into CTA 0's shared memory
+// (distributed shared memory). CTA 0 adds the partials in CTA order and runs the size /
+// anchor / fill / prune phase; every CTA then reads the eligible set back and re-routes
+// its own nodes. The demand is summed in a different order than in the one-CTA kernel
+// (partials per CTA), a difference at the level of fp32 rounding.
+namespace cg = cooperative_groups;
+constexpr int kCC = 8;                  // CTAs per tree
+constexpr int kCW = 8;                  // warps per CTA
+constexpr int kCThreads = kCW * 32;
+constexpr int kClusterMaxN = 256;
+static_assert(kCThreads >= kMaxE, "phase B takes one expert per thread");
+
+__global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(kCThreads)
+select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
+                      const int *__restrict__ depth, int N, int E, int k,
+                      const uint8_t *__restrict__ resident, int *__restrict__ idx_out,
+                      float *__restrict__ gates_out, uint8_t *__restrict__ elig_out,
+                      int *__restrict__ info_out) {
+    extern __shared__ float cdyn[];  // wt [slots][E], nat_all [N][k] (CTA 0), nat_loc [slots][k]
+    __shared__ float part[kCC][kMaxE];  // CTA 0: partial demand of every CTA
+    __shared__ float D[kMaxE], term[kMaxE], rk[kMaxE];
+    __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
+    __shared__ float s_sumD;
+    __shared__ int s_m;
+
+    // every CTA of the cluster must be running before any touches another's shared
+    // memory: arrive now, wait just before the first remote store
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    pdl_wait();
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x / kCC;
+    const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
+    float *wt = cdyn;
+    int *nat_all = reinterpret_cast<int *>(wt + (size_t)slots * E);
+    int *nat_loc = nat_all + (size_t)N * k;
+    int *nat0 = cl.map_shared_rank(nat_all, 0);
+    const float *Lg = logits + (size_t)b * N * E;
+    const int *dep = depth + (size_t)b * N;
+    int *idxb = idx_out + (size_t)b * N * k;
+    float *gb = gates_out + (size_t)b * N * k;
+    const bool natural = a.mode == MOE_ROUTE_NATURAL;
+
+    for (int e = tid; e < kMaxE; e += kCThreads) {
+        inU[e] = 0;
+        inSel[e] = 0;
+        inA[e] = 0;
+    }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+
+    // ---- phase A: this CTA's nodes ----
+    for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
+        const int slot = t * kCW + warp;
+        float v[kVPL];
+        load_row(Lg + (size_t)n * E, E, v);
+        const int c = warp_topk(v, 0xffffffffu, E, k);
+        const float val = chosen_value(v, c);
+        if (lane < k) {
+            nat_loc[slot * k + lane] = c;
+            nat0[n * k + lane] = c;
+        }
+        if (natural) {
+            write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+        } else {
+            const float m = __shfl_sync(0xffffffffu, val, 0);
+            float ex[kVPL], s = 0.f;
+#pragma unroll
+            for (int i = 0; i < kVPL; ++i) {
+                ex[i] = lane + 32 * i < E ? expf(v[i] - m) : 0.f;
+                s += ex[i];
+            }
+            s = warp_sum(s);
+            const int dd = min(dep[n], a.n_c - 1);
+            const float cn = a.c[dd < 0 ? 0 : dd];
+#pragma unroll
+            for (int i = 0; i < kVPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) wt[slot * E + e] = __fmul_rn(cn, __fdiv_rn(ex[i], s));
+            }
+        }
+    }
+    __syncthreads();
+    if (!natural && tid < E) {  // partial demand of this CTA's nodes, node order
+        float acc = 0.f;
+        for (int t = 0; t * kCC * kCW < N; ++t)
+            for (int w = 0; w < kCW; ++w) {
+                const int n = t * kCC * kCW + rank * kCW + w;
+                if (n < N) acc = __fadd_rn(acc, wt[(t * kCW + w) * E + tid]);
+            }
+        cl.map_shared_rank(&part[0][0], 0)[rank * kMaxE + tid] = acc;
+    }
+    cl.sync();
+
+    // ---- phase B on CTA 0 ----
+    if (rank == 0) {
+        for (int i = tid; i < N * k; i += kCThreads) inU[nat_all[i]] = 1;
+        __syncthreads();
+        if (natural) {
+            const int u = __syncthreads_count(tid < E && inU[tid]);
+            if (tid == 0 && info_out) {
+                info_out[b * MOE_INFO_FIELDS + 0] = u;
+                info_out[b * MOE_INFO_FIELDS + 1] = u;
+                info_out[b * MOE_INFO_FIELDS + 2] = E;
+                info_out[b * MOE_INFO_FIELDS + 3] = 0;
+            }
+            if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = 1;
+        } else {
+            if (tid < E) {
+                float acc = 0.f;
+                for (int r = 0; r < kCC; ++r) acc = __fadd_rn(acc, part[r][tid]);
+                D[tid] = acc;
+            }
+            const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
+            if (tid == 0) {
+                float sum = 0.f;
+#pragma unroll 16
+                for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
+                s_sumD = sum;
+            }
+            __syncthreads();
+            if (tid < E) {
+                const float q = __fdiv_rn(D[tid], s_sumD);
+                term[tid] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                int m;
+                if (a.mode == MOE_ROUTE_ACCEPT) {
+                    float H = 0.f;
+#pragma unroll 16
+                    for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
+                    const float r = expf(H);
+                    const float rn = rintf(r);
+                    m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
+                } else {
+                    m = a.fixed_B;
+                }
+                m = min(max(m, k), pool);
+                s_m = m;
+                if (a.anchor)
+                    for (int j = 0; j < k; ++j) inA[nat_all[j]] = 1;
+            }
+            __syncthreads();
+            const int nA = a.anchor ? k : 0;
+            const int m = s_m;
+            if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? D[tid] : -1.f;
+            __syncthreads();
+            if (tid < E) {
+                int in = inA[tid];
+                const float De = rk[tid];
+                if (De >= 0.f) {
+                    int rnk = 0;
+#pragma unroll 8
+                    for (int q = 0; q < E; ++q) {
+                        const float Dq = rk[q];
+                        rnk += (Dq > De || (Dq == De && q < tid)) ? 1 : 0;
+                    }
+                    in = rnk < m - nA;
+                }
+                inS[tid] = in;
+            }
+            __syncthreads();
+            int removed = 0;
+            if (a.prune && resident) {
+                int is_rem = 0;
+                if (tid < E) {
+                    is_rem = inS[tid] && !inA[tid] && !resident[tid];
+                    rk[tid] = is_rem ? D[tid] : INFINITY;
+                }
+                const int nrem = __syncthreads_count(is_rem);
+                const int fl = a.min_set > k ? a.min_set : k;
+                removed = min(min(max(m - fl, 0), a.budget), nrem);
+                if (is_rem) {
+                    const float De = rk[tid];
+                    int rnk = 0;
+#pragma unroll 8
+                    for (int q = 0; q < E; ++q) {
+                        const float Dq = rk[q];
+                        rnk += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
+                    }
+                    if (rnk < removed) inS[tid] = 0;
+                }
+                __syncthreads();
+            }
+            if (tid == 0 && info_out) {
+                info_out[b * MOE_INFO_FIELDS + 2] = m;
+                info_out[b * MOE_INFO_FIELDS + 3] = removed;
+            }
+            if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
+        }
+    }
+    if (natural) {
+        cl.sync();  // nobody exits while CTA 0 still reads what the others stored
+        return;
+    }
+    cl.sync();
+
+    // ---- phase C: this CTA's nodes, restricted to the eligible set ----
+    if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
+    __syncthreads();
+    unsigned allowed = 0;
+#pragma unroll
+    for (int i = 0; i < kVPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && inS[e]) allowed |= 1u << i;
+    }
+    for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
+        const int slot = t * kCW + warp;
+        float v[kVPL];
+        load_row(Lg + (size_t)n * E, E, v);
+        const int nt = lane < k ? nat_loc[slot * k + lane] : -1;
+        const bool keep = __all_sync(0xffffffffu, lane >= k || (nt >= 0 && inS[nt]));
+        const int c = keep ? nt : warp_topk(v, allowed, E, k);
+        const float val = chosen_value(v, c);
+        if (lane < k && c >= 0) inSel[c] = 1;
+        write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+    }
+    cl.sync();
+    if (rank == 0) {
+        int sel = 0;
+        if (tid < E)
+            for (int r = 0; r < kCC; ++r) sel |= cl.map_shared_rank(inSel, r)[tid];
+        const int u_sel = __syncthreads_count(sel);
+        const int u_nat = __syncthreads_count(tid < E && inU[tid]);
+        if (tid == 0 && info_out) {
+            info_out[b * MOE_INFO_FIELDS + 0] = u_nat;
+            info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
+        }
+    }
+    cl.sync();  // keep every CTA's shared memory alive until CTA 0 has read it
+}
+
 }  // namespace
 
 cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s) {
     if (B <= 0 || N <= 0) return cudaSuccess;
+    if (N <= kClusterMaxN) {
+        const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
+        const size_t smem =
+            ((size_t)slots * L.E + (size_t)N * L.k + (size_t)slots * L.k) * sizeof(float);
+        if (smem > 40 * 1024) {
+            cudaError_t err = cudaFuncSetAttribute(
+                select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err != cudaSuccess) return err;
+        }
+        return launch_pdl(select_cluster_kernel, dim3(B * kCC), dim3(kCThreads), smem, s, a,
+                          logits, depth, N, L.E, L.k, resident, idx, gates, elig, info);
+    }
     const bool staged = N * L.E <= kStageFloats;
     // staged: logits and demand terms [N][E] each; always: mx, nz, cN [N] and nat [N][k]
     const size_t smem =

@@ -159,6 +159,27 @@ def test_selection_bit_exact(case):
     assert exact >= max(1, B - 1)
 
 
+def test_selection_large_tree_single_cta_path():
+    """Trees of more than 256 nodes take the one-CTA selector; 300- and 1000-node random
+    trees, AcceptMoE and pruning, against the oracle."""
+    shape = W.LayerShape(d=64, E=64, k=4, f=64, dtype="fp32")
+    for N, seed in ((300, 1), (1000, 2)):
+        rng = np.random.default_rng(seed)
+        parent = np.array([-1] + [int(rng.integers(0, n)) for n in range(1, N)], np.int32)
+        depth = np.zeros(N, np.int32)
+        for n in range(1, N):
+            depth[n] = depth[parent[n]] + 1
+        logits = W.synthetic_logits(seed, parent, shape.E, 3.0)
+        res = W.residency_mask(seed, shape.E, 20)
+        P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=True, reroute_budget=8,
+                            min_set=6)
+        gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth[None], 1, N, res)
+        exact = _check_selection(shape, dict(mode=O.ACCEPT, prune=True, budget=8, min_set=6,
+                                             resident=res, c=W.C_EAGLE),
+                                 logits, depth[None], gidx, gg, ge, gi, N, 1)
+        assert exact == 1
+
+
 def test_selection_root_only_and_all_experts():
     # N = 1: the root alone; E = k: every expert is chosen by every node
     for shape, N in ((W.LayerShape(d=64, E=16, k=2, f=64, dtype="fp32"), 1),
