@@ -145,6 +145,28 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def kernel_sha(name="ffn_tc.cu"):
+    import hashlib
+    with open(os.path.join(ROOT, "expert_select_gb300", "csrc", name), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def measured_traffic(mean_union: float):
+    """DRAM bytes (read + write) per launch of the expert kernel, from the ncu capture
+    summarised in profiles/ (bytes per union expert x this run's mean union), or None
+    when that capture was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "ffn_tcgen05_qwen3_layer.md")
+    try:
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_union_expert:"):
+                f = line.split()
+                if f[3] == kernel_sha():
+                    return int(float(f[1]) * mean_union)
+    except (OSError, IndexError, ValueError):
+        pass
+    return None
+
+
 def cpu_model():
     try:
         out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
@@ -316,16 +338,7 @@ def run_gpu(args):
     algo_bytes = union * shape.expert_bytes + 2 * N * shape.d * shape.elem_bytes
     achieved = float(algo_bytes[::EV_EVERY].sum() / (np.sum(ffn_ms) / 1e3)) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "ffn_traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as fh:
-                pj = json.load(fh)
-            if pj.get("kernel_rev") == M.lib().moe_abi_version():
-                traffic = pj.get("bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = measured_traffic(float(union.mean()))
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     xh = xs_h.pin_memory()
@@ -371,6 +384,7 @@ def run_gpu(args):
         "data": "synthetic (seeded EAGLE-3-shaped trees, N(0,0.02) weights)",
         "config": dict(workload_config(shape, routing, wr_std), parallelism=f"replicas{world}"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "kernel_source_sha": kernel_sha(),
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "grouped SwiGLU experts", "peak_kind": peak_kind,
                      "ffn_ms_mean": round(float(np.mean(ffn_ms)), 5),
@@ -381,6 +395,7 @@ def run_gpu(args):
         "gpu_launches": int(launches_per_step * K),
         "clocks": clocks,
         "union": {"mean": float(union.mean()), "min": int(union.min()), "max": int(union.max()),
+                  "first_steps": union[:20].tolist(),
                   "natural_mean": float(inf[:, 0].mean()), "selected_mean": float(inf[:, 1].mean()),
                   "m_mean": float(inf[:, 2].mean()),
                   f"{other}_union_mean": float(u_o.mean()),

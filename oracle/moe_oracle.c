@@ -67,8 +67,9 @@ ORC_API void oracle_router(const void *x, const void *Wr, int dtype, int R, int 
 
 /* [LAYER] TopR: the k largest scores of one row, in descending order, ties to the
  * lower expert id. softmax is monotone, so top-k of the probabilities is top-k of
- * the logits. `allowed` (may be NULL) restricts the candidates. Returns the gap
- * between the k-th chosen score and the best score left out (+inf if none left). */
+ * the logits. `allowed` (may be NULL) restricts the candidates. Returns the smallest
+ * gap between consecutive scores among the k chosen and the best score left out (the
+ * order of the k is part of the result), +inf if there is no such pair. */
 static double topk_row(const float *l, int E, int k, const unsigned char *allowed, int *out) {
     unsigned char taken[1024];
     memset(taken, 0, (size_t)E);
@@ -86,8 +87,13 @@ static double topk_row(const float *l, int E, int k, const unsigned char *allowe
         if ((allowed && !allowed[e]) || taken[e]) continue;
         if (rest < 0 || l[e] > l[rest]) rest = e;
     }
-    if (rest < 0 || out[k - 1] < 0) return INFINITY;
-    return (double)l[out[k - 1]] - (double)l[rest];
+    double gap = INFINITY;
+    for (int j = 0; j + 1 < k; ++j)
+        if (out[j + 1] >= 0 && (double)l[out[j]] - (double)l[out[j + 1]] < gap)
+            gap = (double)l[out[j]] - (double)l[out[j + 1]];
+    if (rest >= 0 && out[k - 1] >= 0 && (double)l[out[k - 1]] - (double)l[rest] < gap)
+        gap = (double)l[out[k - 1]] - (double)l[rest];
+    return gap;
 }
 
 ORC_API double oracle_topk(const float *logits, int R, int E, int k, int *idx) {

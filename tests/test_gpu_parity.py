@@ -389,6 +389,7 @@ FORWARD_CASES = [
     ("cfg1-acc-peaked", W.QWEN3_30B_A3B, 1, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 12),
     ("cfg4-b4-acc-peaked", W.QWEN3_30B_A3B, 4, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 12),
     ("cfg4-b16-nat", W.QWEN3_30B_A3B, 16, "eagle", 0.02, M.MOE_ROUTE_NATURAL, 12),
+    ("cfg4-b64-acc-peaked", W.QWEN3_30B_A3B, 64, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 8),
     ("gptoss-acc-peaked", W.GPT_OSS_120B, 1, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, 8),
 ]
 
@@ -467,3 +468,44 @@ def test_tree_forward_is_deterministic():
     b = _run_forward(W.QWEN3_30B_A3B, 1, "eagle", 0.1, M.MOE_ROUTE_ACCEPT, seed=77)
     for k in a["got"]:
         np.testing.assert_array_equal(a["got"][k], b["got"][k])
+
+
+def test_residual_chain_of_layers_against_oracle():
+    """Three Qwen3-shaped layers in a residual chain, x <- x + MoE_l(x) with x stored in
+    bf16 between layers (the 48-layer stack's step). The oracle runs the chain itself from
+    the same seeded inputs, rounding each layer's x to bf16 as the stored dtype requires."""
+    shape = W.QWEN3_30B_A3B
+    t = W.eagle_tree(900)
+    N = t.N
+    x0 = W.hidden_states(901, t.parent, shape.d, torch.bfloat16)
+    L = _desc(shape)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    layers = [(W.router_weight(910 + l, shape, std=0.1, device=DEV),) + _weights(shape, 920 + l)
+              for l in range(3)]
+    x = x0.to(DEV).clone()
+    dep = torch.from_numpy(t.depth.copy()).to(DEV)
+    ws = M.workspace(L, 1, N)
+    idx = torch.empty(N, shape.k, dtype=torch.int32, device=DEV)
+    got_idx = []
+    for wr, wg, wu, wd in layers:
+        M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dep, 1, N, None, x, ws,
+                           M.tree_outputs(topk_idx=idx), M.run_opts(residual=True))
+        torch.cuda.synchronize()
+        got_idx.append(idx.cpu().numpy().copy())
+    xo = x0
+    for l, (wr, wg, wu, wd) in enumerate(layers):
+        ref = O.forward(xo, wr.cpu(), wg.cpu(), wu.cpu(), wd.cpu(), t.depth, shape.k, W.C_EAGLE,
+                        mode=O.ACCEPT, precision="fp32")
+        if l == 0:  # identical inputs: exact unless the oracle reports a tie
+            tied = ref["margin_topk"] < 1e-4 or ref["margin_restricted"] < 1e-4 or \
+                ref["margin_rank"] < TIE or ref["margin_fill"] < TIE
+            if not tied:
+                np.testing.assert_array_equal(got_idx[l], ref["idx"])
+        else:  # inputs differ by the bf16 rounding of the previous layer's output
+            same = sum(set(got_idx[l][r].tolist()) == set(ref["idx"][r].tolist())
+                       for r in range(N))
+            assert same >= 0.9 * N
+        xo = (xo.double() + torch.from_numpy(ref["y"])).to(torch.bfloat16)
+    ref_x = xo.double().numpy()
+    got = x.double().cpu().numpy()
+    assert np.abs(got - ref_x).max() <= 2e-2 * np.abs(ref_x).max()
