@@ -278,18 +278,12 @@ def run_gpu(args):
     s = torch.cuda.current_stream(dev)
     routing_mode = {"acceptmoe": M.MOE_ROUTE_ACCEPT, "natural": M.MOE_ROUTE_NATURAL}
 
-    def loop(K, routing, counts=None, info=None, ev=None, e2e=None):
+    def loop(K, routing, counts=None, info=None, ev=None):
         P = M.select_params(routing_mode[routing], W.C_EAGLE)
         opts = M.run_opts(args.ffn_path)
         for i in range(K):
             j = i % TREES
-            if e2e is not None:
-                xin, din, yout, xh, dh, yh = e2e
-                xin.copy_(xh[j], non_blocking=True)
-                din.copy_(dh[j], non_blocking=True)
-                xx, dd = xin, din
-            else:
-                xx, dd = xs[j], deps[j]
+            xx, dd = xs[j], deps[j]
             out = None
             if counts is not None:
                 out = M.tree_outputs(counts=counts[i], info=info[i])
@@ -298,10 +292,7 @@ def run_gpu(args):
                 # between two kernels stops the next one from launching early
                 opts = M.run_opts(args.ffn_path, *ev[i // EV_EVERY]) if i % EV_EVERY == 0 \
                     else M.run_opts(args.ffn_path)
-            M.moe_tree_forward(L, P, xx, wr, wg, wu, wd, None, dd, 1, N, None,
-                               yout if e2e is not None else y, ws, out, opts)
-            if e2e is not None:
-                yh[j].copy_(yout, non_blocking=True)
+            M.moe_tree_forward(L, P, xx, wr, wg, wu, wd, None, dd, 1, N, None, y, ws, out, opts)
 
     def timed(K, routing, **kw):
         barrier(world)
@@ -340,18 +331,54 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
     traffic = measured_traffic(float(union.mean()))
 
-    # end to end through the C ABI with host buffers (pinned), copies inside
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed
+    # region: a copy stream brings step i+1's inputs in while step i computes and takes
+    # step i's result out once it is done (double-buffered device inputs and outputs)
     xh = xs_h.pin_memory()
     dh = deps_h.int().pin_memory()
     yh = torch.empty(TREES, N, shape.d, dtype=torch.bfloat16).pin_memory()
-    xin = torch.empty_like(xs[0])
-    din = torch.empty_like(deps[0])
-    yout = torch.empty_like(y)
-    loop(Wm, routing, e2e=(xin, din, yout, xh, dh, yh))
-    sec_e2e = timed(K, routing, e2e=(xin, din, yout, xh, dh, yh))
+    xin = [torch.empty_like(xs[0]) for _ in range(2)]
+    din = [torch.empty_like(deps[0]) for _ in range(2)]
+    yout = [torch.empty_like(y) for _ in range(2)]
+    cs = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_loop(K):
+        P = M.select_params(routing_mode[routing], W.C_EAGLE)
+        with torch.cuda.stream(cs):
+            xin[0].copy_(xh[0], non_blocking=True)
+            din[0].copy_(dh[0], non_blocking=True)
+            ev_in[0].record(cs)
+        for i in range(K):
+            b, nb = i % 2, (i + 1) % 2
+            if i + 1 < K:
+                with torch.cuda.stream(cs):
+                    if i >= 1:
+                        cs.wait_event(ev_out[nb])  # step i-1 is done reading slot nb
+                    xin[nb].copy_(xh[(i + 1) % TREES], non_blocking=True)
+                    din[nb].copy_(dh[(i + 1) % TREES], non_blocking=True)
+                    ev_in[nb].record(cs)
+            s.wait_event(ev_in[b])
+            if i >= 2:
+                s.wait_event(ev_free[b])  # step i-2's result has left slot b
+            M.moe_tree_forward(L, P, xin[b], wr, wg, wu, wd, None, din[b], 1, N, None, yout[b],
+                               ws, None, M.run_opts(args.ffn_path))
+            ev_out[b].record(s)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_out[b])
+                yh[i % TREES].copy_(yout[b], non_blocking=True)
+                ev_free[b].record(cs)
+        s.wait_event(ev_free[(K - 1) % 2])
+
+    e2e_loop(Wm)
+    torch.cuda.synchronize(dev)
+    sec_e2e = _timed(lambda: e2e_loop(K), dev, world)
     e2e = {"value": whole_job_rate(K, world, sec_e2e), "unit": UNIT,
-           "h2d_bytes_per_step": int(xin.numel() * xin.element_size() + din.numel() * 4),
-           "d2h_bytes_per_step": int(yout.numel() * yout.element_size())}
+           "h2d_bytes_per_step": int(xin[0].numel() * xin[0].element_size() + din[0].numel() * 4),
+           "d2h_bytes_per_step": int(yout[0].numel() * yout[0].element_size()),
+           "pipelining": "copy stream: next step's inputs in, this step's output out"}
 
     # natural routing on the same trees (the pages' Standard SD), for comparison
     Kv = min(K, 2000)
@@ -746,6 +773,104 @@ def run_batched(args):
                     sweep=rows, hbm_peak=peak, bf16_tflops_peak=tflops_peak))
 
 
+def _layer_setup(args, seed_off):
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.QWEN3_30B_A3B
+    seed = SEED + seed_off + 7919 * rank
+    xs_h, deps_h = make_trees(TREES, shape, seed)
+    xs, deps = xs_h.to(dev), deps_h.to(dev).int()
+    wr = W.router_weight(seed + 1, shape, std=args.router_std, device=dev)
+    wg, wu, wd = W.expert_weights(seed + 2, shape, device=dev)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    return torch, M, W, world, rank, local, dev, shape, xs, deps, wr, wg, wu, wd, L
+
+
+def run_budget(args):
+    """Fixed-budget selection rules beside AcceptMoE on the Qwen3-shaped layer ("AcceptMoE"
+    news article, section 04): AcceptMoE-B (commitment-weighted demand, set size B) and the
+    MoE-Spec rule (uniform position weights, no anchor, set size B). Only the cost side is
+    measurable without trained models: union size and verify throughput."""
+    (torch, M, W, world, rank, local, dev, shape, xs, deps, wr, wg, wu, wd, L) = \
+        _layer_setup(args, 5000)
+    N = xs.shape[1]
+    ws = M.workspace(L, 1, N, device=dev)
+    y = torch.empty(N, shape.d, dtype=torch.bfloat16, device=dev)
+    K, Wm = args.steps, args.warmup
+    variants = [("natural", M.select_params(M.MOE_ROUTE_NATURAL, W.C_EAGLE)),
+                ("acceptmoe", M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE))]
+    for B in (16, 24, 32):
+        variants.append((f"acceptmoe-B{B}", M.select_params(M.MOE_ROUTE_FIXED_B, W.C_EAGLE,
+                                                           fixed_B=B)))
+        variants.append((f"moe-spec-B{B}", M.select_params(M.MOE_ROUTE_FIXED_B, [1.0],
+                                                           anchor=False, fixed_B=B)))
+    rows = []
+    for name, P in variants:
+        info = torch.zeros(K, 4, dtype=torch.int32, device=dev)
+
+        def loop(n, rec):
+            for i in range(n):
+                j = i % TREES
+                M.moe_tree_forward(L, P, xs[j], wr, wg, wu, wd, None, deps[j], 1, N, None, y,
+                                   ws, M.tree_outputs(info=info[i]) if rec else None)
+
+        loop(Wm, False)
+        sec = _timed(lambda: loop(K, True), dev, world)
+        inf = info.cpu().numpy()
+        rows.append({"rule": name, "blocks_per_s": round(whole_job_rate(K, world, sec), 1),
+                     "union": round(float(inf[:, 1].mean()), 2),
+                     "set_size": round(float(inf[:, 2].mean()), 2)})
+    if rank == 0:
+        acc = next(r for r in rows if r["rule"] == "acceptmoe")
+        print(_line("MoE verify layer tree-blocks/s under fixed-budget selection rules",
+                    acc["blocks_per_s"], "tree-blocks/s", world, K, Wm,
+                    K / acc["blocks_per_s"],
+                    {"workload": "qwen3-30b-a3b-moe-layer-resident-eagle3-tree",
+                     "router_std": args.router_std},
+                    rules=rows))
+
+
+def run_efficiency(args):
+    """Target efficiency eta(N) = T(1 row) / T(N rows) of the layer (MoESD notes, section
+    5.2), the N rows being the first N nodes of each tree (parents come first, so every
+    prefix is itself a tree), natural routing as in plain verification."""
+    (torch, M, W, world, rank, local, dev, shape, xs, deps, wr, wg, wu, wd, L) = \
+        _layer_setup(args, 6000)
+    K, Wm = args.steps, args.warmup
+    P = M.select_params(M.MOE_ROUTE_NATURAL, W.C_EAGLE)
+    rows = []
+    for n in (1, 2, 4, 8, 16, 33, 65):
+        ws = M.workspace(L, 1, n, device=dev)
+        y = torch.empty(n, shape.d, dtype=torch.bfloat16, device=dev)
+        xb = [xs[j, :n].contiguous() for j in range(TREES)]
+        db = [deps[j, :n].contiguous() for j in range(TREES)]
+        counts = torch.zeros(K, shape.E, dtype=torch.int32, device=dev)
+
+        def loop(m, rec):
+            for i in range(m):
+                j = i % TREES
+                M.moe_tree_forward(L, P, xb[j], wr, wg, wu, wd, None, db[j], 1, n, None, y, ws,
+                                   M.tree_outputs(counts=counts[i]) if rec else None)
+
+        loop(Wm, False)
+        sec = _timed(lambda: loop(K, True), dev, world)
+        union = (counts.cpu().numpy() > 0).sum(axis=1)
+        rows.append({"rows": n, "ms_per_block": round(sec / K * 1e3, 4),
+                     "union": round(float(union.mean()), 2)})
+    t1 = rows[0]["ms_per_block"]
+    for r in rows:
+        r["eta"] = round(t1 / r["ms_per_block"], 4)
+        r["expected_union_uniform"] = round(shape.E * (1 - ((shape.E - shape.k) / shape.E)
+                                                       ** r["rows"]), 2)
+    if rank == 0:
+        print(_line("MoE verify layer target efficiency T(1 row)/T(N rows)", rows[-1]["eta"],
+                    "ratio", world, K, Wm, rows[-1]["ms_per_block"] * K / 1e3,
+                    {"workload": "qwen3-30b-a3b-moe-layer-tree-prefixes",
+                     "router_std": args.router_std}, sweep=rows))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -757,7 +882,8 @@ def main(argv=None):
     ap.add_argument("--ffn-path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--cpu-trees", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched"],
+    ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched", "budget",
+                                           "efficiency"],
                     default="layer", help="layer: the Qwen3-shaped layer (default line)")
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--slots", type=int, default=48)
@@ -772,6 +898,10 @@ def main(argv=None):
         run_offload(args)
     elif args.workload == "batched":
         run_batched(args)
+    elif args.workload == "budget":
+        run_budget(args)
+    elif args.workload == "efficiency":
+        run_efficiency(args)
     else:
         run_gpu(args)
 
