@@ -114,9 +114,8 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
     fa.h = at<void>(ws, w.h);
     fa.o = at<float>(ws, w.o);
 
-    int path = opts ? opts->ffn_path : MOE_FFN_AUTO;
-    if (path == MOE_FFN_AUTO) path = ffn_tc_supported(L) ? MOE_FFN_TCGEN05 : MOE_FFN_SIMT;
-    if (path == MOE_FFN_TCGEN05 && !ffn_tc_supported(L)) return MOE_ERR_UNSUPPORTED;
+    const int path = resolve_ffn_path(L, opts);
+    if (path < 0) return MOE_ERR_UNSUPPORTED;
     const bool timed = opts && opts->ffn_begin && opts->ffn_end;
     if (timed && cudaEventRecord((cudaEvent_t)opts->ffn_begin, s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -125,6 +124,13 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
     if (timed && cudaEventRecord((cudaEvent_t)opts->ffn_end, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+int resolve_ffn_path(const moe_layer_desc &L, const moe_run_opts *opts) {
+    int path = opts ? opts->ffn_path : MOE_FFN_AUTO;
+    if (path == MOE_FFN_AUTO) path = ffn_tc_supported(L) ? MOE_FFN_TCGEN05 : MOE_FFN_SIMT;
+    if (path == MOE_FFN_TCGEN05 && !ffn_tc_supported(L)) return -1;
+    return path;
 }
 
 moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,

@@ -116,6 +116,7 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
                    const void *Wd, const int *slot, const uint8_t *pass, int R, void *ws,
                    const Workspace &w, const int *counts, const int *offsets, const int *perm,
                    const moe_run_opts *opts, cudaStream_t s);
+int resolve_ffn_path(const moe_layer_desc &L, const moe_run_opts *opts);  // -1: unsupported
 moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
                        void *y, void *ws, const Workspace &w, cudaStream_t s);
 

@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -372,8 +373,11 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                       const uint8_t *__restrict__ resident, int *__restrict__ idx_out,
                       float *__restrict__ gates_out, uint8_t *__restrict__ elig_out,
                       int *__restrict__ info_out) {
-    extern __shared__ float cdyn[];  // wt [slots][E], nat_all [N][k] (CTA 0), nat_loc [slots][k]
+    // wt [slots][E], lrow [slots][E] (this CTA's logit rows), nat_all [N][k] (CTA 0),
+    // nat_loc [slots][k]
+    extern __shared__ float cdyn[];
     __shared__ float part[kCC][kMaxE];  // CTA 0: partial demand of every CTA
+    __shared__ int selAll[kCC][kMaxE];  // CTA 0: experts chosen by every CTA's nodes
     __shared__ float D[kMaxE], term[kMaxE], rk[kMaxE];
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
     __shared__ float s_sumD;
@@ -389,7 +393,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     const int b = blockIdx.x / kCC;
     const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
     float *wt = cdyn;
-    int *nat_all = reinterpret_cast<int *>(wt + (size_t)slots * E);
+    float *lrow = wt + (size_t)slots * E;
+    int *nat_all = reinterpret_cast<int *>(lrow + (size_t)slots * E);
     int *nat_loc = nat_all + (size_t)N * k;
     int *nat0 = cl.map_shared_rank(nat_all, 0);
     const float *Lg = logits + (size_t)b * N * E;
@@ -410,6 +415,9 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         const int slot = t * kCW + warp;
         float v[kVPL];
         load_row(Lg + (size_t)n * E, E, v);
+#pragma unroll
+        for (int i = 0; i < kVPL; ++i)
+            if (lane + 32 * i < E) lrow[slot * E + lane + 32 * i] = v[i];
         const int c = warp_topk(v, 0xffffffffu, E, k);
         const float val = chosen_value(v, c);
         if (lane < k) {
@@ -546,10 +554,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
         }
     }
-    if (natural) {
-        cl.sync();  // nobody exits while CTA 0 still reads what the others stored
-        return;
-    }
+    // natural routing is complete: CTA 0 only reads its own shared memory from here on
+    if (natural) return;
     cl.sync();
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
@@ -564,7 +570,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
         const int slot = t * kCW + warp;
         float v[kVPL];
-        load_row(Lg + (size_t)n * E, E, v);
+        load_row(lrow + (size_t)slot * E, E, v);
         const int nt = lane < k ? nat_loc[slot * k + lane] : -1;
         const bool keep = __all_sync(0xffffffffu, lane >= k || (nt >= 0 && inS[nt]));
         const int c = keep ? nt : warp_topk(v, allowed, E, k);
@@ -572,11 +578,13 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         if (lane < k && c >= 0) inSel[c] = 1;
         write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
     }
-    cl.sync();
+    __syncthreads();
+    if (tid < E) cl.map_shared_rank(&selAll[0][0], 0)[rank * kMaxE + tid] = inSel[tid];
+    cl.sync();  // after this CTA 0 reads only its own shared memory
     if (rank == 0) {
         int sel = 0;
         if (tid < E)
-            for (int r = 0; r < kCC; ++r) sel |= cl.map_shared_rank(inSel, r)[tid];
+            for (int r = 0; r < kCC; ++r) sel |= selAll[r][tid];
         const int u_sel = __syncthreads_count(sel);
         const int u_nat = __syncthreads_count(tid < E && inU[tid]);
         if (tid == 0 && info_out) {
@@ -584,8 +592,22 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
         }
     }
-    cl.sync();  // keep every CTA's shared memory alive until CTA 0 has read it
 }
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` when it is above the largest
+// limit set so far (static + dynamic shared memory may not exceed 48 KB without it).
+template <typename K>
+cudaError_t allow_smem(K kernel, std::atomic<size_t> &set, size_t bytes) {
+    size_t cur = set.load();
+    if (bytes <= cur) return cudaSuccess;
+    const cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess)
+        while (cur < bytes && !set.compare_exchange_weak(cur, bytes)) {
+        }
+    return err;
+}
+std::atomic<size_t> cluster_smem_set{0}, single_smem_set{0};
 
 }  // namespace
 
@@ -596,12 +618,9 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
     if (N <= kClusterMaxN) {
         const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
         const size_t smem =
-            ((size_t)slots * L.E + (size_t)N * L.k + (size_t)slots * L.k) * sizeof(float);
-        if (smem > 40 * 1024) {
-            cudaError_t err = cudaFuncSetAttribute(
-                select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err != cudaSuccess) return err;
-        }
+            ((size_t)2 * slots * L.E + (size_t)N * L.k + (size_t)slots * L.k) * sizeof(float);
+        cudaError_t err = allow_smem(select_cluster_kernel, cluster_smem_set, smem);
+        if (err != cudaSuccess) return err;
         return launch_pdl(select_cluster_kernel, dim3(B * kCC), dim3(kCThreads), smem, s, a,
                           logits, depth, N, L.E, L.k, resident, idx, gates, elig, info);
     }
@@ -610,11 +629,8 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
     const size_t smem =
         ((staged ? 2 * (size_t)N * L.E : 0) + 3 * (size_t)N + (size_t)N * L.k) * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    if (smem > 40 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(
-            select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = allow_smem(select_kernel, single_smem_set, smem);
+    if (err != cudaSuccess) return err;
     return launch_pdl(select_kernel, dim3(B), dim3(kThreads), smem, s, a, logits, depth, N, L.E,
                       L.k, resident, idx, gates, elig, info);
 }
