@@ -95,6 +95,46 @@ def _depths(parent: np.ndarray) -> np.ndarray:
     return depth
 
 
+@dataclasses.dataclass
+class Candidates:
+    parent: np.ndarray   # int32 [C], parent[0] = -1, parents before children
+    depth: np.ndarray    # int32 [C]
+    logp: np.ndarray     # float32 [C], cumulative draft log-probability (root 0)
+
+    @property
+    def C(self) -> int:
+        return int(self.parent.shape[0])
+
+
+def eagle_candidates(seed: int, steps: int = 5, topk: int = 10, vocab: int = 32,
+                     alpha: float = 0.3) -> Candidates:
+    """Every node an EAGLE-3-shaped expansion generates (the pool a drafter selects the
+    verified tree from): `steps` steps, `topk` children per frontier node, the best
+    `topk` new nodes form the next frontier. Same draws as eagle_tree for the same seed.
+    Nodes in (depth, -logp) order, so parents come before children."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    par: List[int] = [-1]
+    dep: List[int] = [0]
+    lp: List[float] = [0.0]
+    frontier = [0]
+    for _ in range(steps):
+        new: List[int] = []
+        for p in frontier:
+            probs = np.sort(rng.dirichlet(np.full(vocab, alpha)))[::-1][:topk]
+            for q in probs:
+                par.append(p)
+                dep.append(dep[p] + 1)
+                lp.append(lp[p] + math.log(max(float(q), 1e-300)))
+                new.append(len(par) - 1)
+        new.sort(key=lambda i: (-lp[i], i))
+        frontier = new[:topk]
+    order = [0] + sorted(range(1, len(par)), key=lambda i: (dep[i], -lp[i], i))
+    remap = {old: new for new, old in enumerate(order)}
+    parent = np.array([-1] + [remap[par[i]] for i in order[1:]], dtype=np.int32)
+    return Candidates(parent=parent, depth=np.array([dep[i] for i in order], dtype=np.int32),
+                      logp=np.array([lp[i] for i in order], dtype=np.float32))
+
+
 def eagle_tree(seed: int, steps: int = 5, topk: int = 10, draft_tokens: int = 64,
                vocab: int = 32, alpha: float = 0.3) -> Tree:
     """An EAGLE-3-shaped draft tree: `steps` expansion steps, `topk` children per

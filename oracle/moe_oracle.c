@@ -18,6 +18,13 @@
  *            top-k is kept (root anchor); the set size follows the effective rank of
  *            the demand distribution; residency-aware pruning removes low-demand
  *            non-resident experts within a rerouting budget and a minimum set size.
+ *   [ECO]    "Fewer experts, faster decoding: cost-aware speculative decoding for MoE"
+ *            (EcoSpec, arXiv 2607.12696), abstract, section 1 and Fig. 2-3: before
+ *            verification, choose the candidate nodes greedily by acceptance likelihood
+ *            minus a weight times the number of new predicted experts, tracking the
+ *            experts the chosen nodes already cover in a buffer. The same scoring rule is
+ *            written out in the "MoE and speculative decoding" blog as
+ *            Score(v) = log P_q(v) - lambda * dC_expert(v).
  *   [ABS]    AcceptMoE abstract (arXiv 2608.02989): a verifier-side selector that
  *            combines target-router scores with offline commitment probabilities,
  *            sizes the eligible set per verification block, and constrains
@@ -384,4 +391,55 @@ ORC_API void oracle_moe_combine(const void *x, const void *Wg, const void *Wu, c
     }
     free(xr);
     free(o);
+}
+
+/* [ECO] cost-aware draft selection. Candidates 0..C-1, node 0 the root, parent[v] < v;
+ * logp[v] the cumulative draft log-probability; footprint[v*k .. v*k+k) the experts the
+ * node is predicted to use (distinct ids in [0, E)). S starts as {root} and the buffer B
+ * as its footprint; then, gamma - 1 times, among the candidates not in S whose parent is
+ * in S, take the one with the largest score logp[v] - lambda * |footprint(v) \ B|
+ * (computed in fp32: one product, one difference; ties to the lower index), and add it to
+ * S and its footprint to B. selected[] receives S in selection order (every parent before
+ * its children), *n_union = |B|. Returns the number selected (< gamma when the tree has
+ * fewer candidates). */
+ORC_API int oracle_draft_select(int C, int k, int E, const int *parent, const float *logp,
+                                const int *footprint, float lambda, int gamma, int *selected,
+                                int *n_union) {
+    unsigned char *inS = (unsigned char *)calloc((size_t)C, 1);
+    unsigned char *inB = (unsigned char *)calloc((size_t)E, 1);
+    int n = 0;
+    if (C < 1 || gamma < 1) {
+        *n_union = 0;
+        free(inS);
+        free(inB);
+        return 0;
+    }
+    inS[0] = 1;
+    selected[n++] = 0;
+    for (int j = 0; j < k; ++j) inB[footprint[j]] = 1;
+    while (n < gamma) {
+        int best = -1;
+        float best_sc = 0.f;
+        for (int v = 1; v < C; ++v) {
+            if (inS[v] || !inS[parent[v]]) continue;
+            int dc = 0;
+            for (int j = 0; j < k; ++j) dc += inB[footprint[(size_t)v * k + j]] ? 0 : 1;
+            const float pen = lambda * (float)dc;
+            const float sc = logp[v] - pen;
+            if (best < 0 || sc > best_sc) {
+                best = v;
+                best_sc = sc;
+            }
+        }
+        if (best < 0) break;
+        inS[best] = 1;
+        selected[n++] = best;
+        for (int j = 0; j < k; ++j) inB[footprint[(size_t)best * k + j]] = 1;
+    }
+    int u = 0;
+    for (int e = 0; e < E; ++e) u += inB[e];
+    *n_union = u;
+    free(inS);
+    free(inB);
+    return n;
 }

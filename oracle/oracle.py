@@ -55,6 +55,8 @@ def lib():
         _lib.oracle_expert_ffn.restype = None
         _lib.oracle_moe_combine.argtypes = [P, P, P, P, i, i, i, P, P, i, P, i, P]
         _lib.oracle_moe_combine.restype = None
+        _lib.oracle_draft_select.argtypes = [i, i, i, P, P, P, C.c_float, i, P, P]
+        _lib.oracle_draft_select.restype = i
     return _lib
 
 
@@ -202,3 +204,17 @@ def forward(x, Wr, Wg, Wu, Wd, depth: np.ndarray, k: int, c: Sequence[float],
     y = moe_combine(x, Wg, Wu, Wd, sel["idx"], sel["gates"], rows=rows)
     sel.update(logits=logits64, logits32=l32, counts=counts, offsets=offsets, perm=perm, y=y)
     return sel
+
+
+def draft_select(parent: np.ndarray, logp: np.ndarray, footprint: np.ndarray, E: int,
+                 lam: float, gamma: int):
+    """Cost-aware draft selection: (selected node ids in selection order, |union|)."""
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    lp = np.ascontiguousarray(logp, dtype=np.float32)
+    fp = np.ascontiguousarray(footprint, dtype=np.int32)
+    n_cand, k = fp.shape
+    sel = np.empty(max(gamma, 1), dtype=np.int32)
+    nu = np.zeros(1, dtype=np.int32)
+    n = lib().oracle_draft_select(n_cand, k, E, _p(par), _p(lp), _p(fp), float(lam), gamma,
+                                  _p(sel), _p(nu))
+    return sel[:n].copy(), int(nu[0])

@@ -337,3 +337,69 @@ def test_forward_composes_router_selection_and_experts():
     np.testing.assert_array_equal(out["idx"], sel["idx"])
     y = O.moe_combine(x, wg, wu, wd, sel["idx"], sel["gates"])
     np.testing.assert_array_equal(out["y"], y)
+
+
+# ------------------------------------------------- cost-aware draft selection
+
+def _footprints(seed, cand, E, k, scale=2.0):
+    logits = W.synthetic_logits(seed, cand.parent, E, scale)
+    fp, _ = O.topk(logits, k)
+    return fp
+
+
+def test_draft_select_without_cost_is_top_by_probability():
+    """lambda = 0 leaves only log P: cumulative log-probability falls along every edge,
+    so the greedy tree is the root plus the gamma - 1 most probable candidates, taken in
+    descending probability (the confidence-ordered tree)."""
+    cand = W.eagle_candidates(5)
+    fp = _footprints(5, cand, 64, 4)
+    sel, _ = O.draft_select(cand.parent, cand.logp, fp, 64, 0.0, 65)
+    order = sorted(range(1, cand.C), key=lambda v: (-float(cand.logp[v]), v))[:64]
+    assert sel.tolist() == [0] + order
+
+
+def test_draft_select_hand_example():
+    """root {0,1}; a (log P -0.5, {2,3}) and b (-0.7, {0,1}) under the root; c (-0.55, {2,3})
+    under a; d (-1.0, {1,5}) under b. gamma = 3.
+    lambda = 0: a (-0.5), then c (-0.55)  -> S = {root, a, c}, union {0,1,2,3}.
+    lambda = 0.2: b scores -0.7 > a's -0.5 - 0.4 = -0.9, so b; then a (-0.9) beats
+    d (-1.0 - 0.2 = -1.2) and is taken                  -> S = {root, b, a}, union {0,1,2,3}.
+    lambda = 0.6: b (-0.7); then a (-1.7) vs d (-1.6): d -> S = {root, b, d}, union {0,1,5}."""
+    parent = np.array([-1, 0, 0, 1, 2], np.int32)          # root, a, b, c, d
+    logp = np.array([0.0, -0.5, -0.7, -0.55, -1.0], np.float32)
+    fp = np.array([[0, 1], [2, 3], [0, 1], [2, 3], [1, 5]], np.int32)
+    s0, u0 = O.draft_select(parent, logp, fp, 8, 0.0, 3)
+    s1, u1 = O.draft_select(parent, logp, fp, 8, 0.2, 3)
+    s2, u2 = O.draft_select(parent, logp, fp, 8, 0.6, 3)
+    assert (s0.tolist(), u0) == ([0, 1, 3], 4)
+    assert (s1.tolist(), u1) == ([0, 2, 1], 4)
+    assert (s2.tolist(), u2) == ([0, 2, 4], 3)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_draft_select_invariants(seed):
+    """Ancestor-closed selection of gamma nodes, union = |union of the chosen footprints|,
+    and with a huge lambda every step takes a candidate adding the fewest new experts."""
+    E, k = 64, 4
+    cand = W.eagle_candidates(100 + seed)
+    fp = _footprints(seed, cand, E, k)
+    for lam in (0.0, 0.3, 1e6):
+        sel, u = O.draft_select(cand.parent, cand.logp, fp, E, lam, 65)
+        assert len(sel) == 65 and len(set(sel.tolist())) == 65 and sel[0] == 0
+        pos = {v: i for i, v in enumerate(sel.tolist())}
+        assert all(pos[int(cand.parent[v])] < pos[v] for v in sel[1:].tolist())
+        assert u == len(set(fp[sel].ravel().tolist()))
+        if lam == 1e6:
+            covered = set(fp[0].tolist())
+            chosen = {0}
+            for v in sel[1:].tolist():
+                elig = [c for c in range(1, cand.C) if c not in chosen and
+                        int(cand.parent[c]) in chosen]
+                new = lambda c: len(set(fp[c].tolist()) - covered)  # noqa: E731
+                assert new(v) == min(new(c) for c in elig)
+                chosen.add(v)
+                covered |= set(fp[v].tolist())
+    # a cost weight never enlarges the covered set relative to the confidence order here
+    s0, u0 = O.draft_select(cand.parent, cand.logp, fp, E, 0.0, 65)
+    s1, u1 = O.draft_select(cand.parent, cand.logp, fp, E, 1e6, 65)
+    assert u1 <= u0
