@@ -32,7 +32,7 @@ EXPORTS = (
     "moe_tree_select", "moe_expert_permute", "moe_expert_forward", "moe_tree_forward",
     "moe_workspace_check", "moe_residency_create", "moe_residency_destroy",
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
-    "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward",
+    "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward", "moe_draft_select",
 )
 
 
@@ -99,6 +99,7 @@ def lib() -> C.CDLL:
             "moe_tree_forward_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P], I),
             "moe_offload_forward": ([P, P, P, P, P, P, P, P, P, P, P, I, P, I, I, P, P, P, P, P,
                                      P, P], I),
+            "moe_draft_select": ([P, I, P, P, P, P, C.c_float, I, P, P, P, P, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -303,6 +304,15 @@ def moe_offload_forward(L, P, x, W_r, host_gate, host_up, host_down, slot_gate, 
         _ptr(depth), B, N, _ptr(y), None if out is None else C.byref(out), C.byref(st), _ptr(ws),
         None if opts is None else C.byref(opts), _stream(stream), C.c_void_p(side.cuda_stream)))
     return st
+
+
+def moe_draft_select(L, parent, depth, logp, footprint, lam: float, gamma: int, selected,
+                     sel_parent, sel_depth, x=None, x_sel=None, n_union=None, stream=None):
+    """Cost-aware choice of the draft tree to verify (see include/moetree.h)."""
+    return _check("moe_draft_select", lib().moe_draft_select(
+        C.byref(L), parent.shape[0], _ptr(parent), _ptr(depth), _ptr(logp), _ptr(footprint),
+        float(lam), gamma, _ptr(x), _ptr(selected), _ptr(sel_parent), _ptr(sel_depth),
+        _ptr(x_sel), _ptr(n_union), _stream(stream)))
 
 
 def moe_event_wait(event, timeout_s: float) -> None:

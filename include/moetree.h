@@ -223,6 +223,27 @@ moe_status moe_tree_forward_noalloc(const moe_layer_desc *L, const moe_select_pa
                                     const moe_tree_outputs *out, const moe_run_opts *opts,
                                     moe_stream_t stream);
 
+/* Cost-aware choice of the draft tree to verify ("Fewer experts, faster decoding:
+ * cost-aware speculative decoding for MoE" (EcoSpec, arXiv 2607.12696), section 1 and
+ * Fig. 2-3; Score(v) = log P_q(v) - lambda * dC_expert(v) in the "MoE and speculative
+ * decoding" blog). From C drafted candidates (node 0 the root, parent[v] < v) take
+ * gamma nodes: the root, then repeatedly the candidate whose parent is already taken with
+ * the largest logp[v] - lambda * (number of its predicted experts not yet covered), fp32,
+ * ties to the lower index; the covered set grows by each chosen node's footprint.
+ * Verification of the chosen tree is unchanged (plain moe_tree_forward).
+ *   parent, depth [C] int32, logp [C] fp32 (cumulative draft log-probability),
+ *   footprint [C, L->k] int32 predicted experts per candidate (e.g. the natural top-k of
+ *   the target router; ids outside [0, L->E) are ignored) -- all device.
+ *   selected [gamma]: candidate ids in selection order (parents first; -1 past the end
+ *   when fewer than gamma can be taken); sel_parent [gamma]: parent as a position in
+ *   `selected` (root -1); sel_depth [gamma]; x [C, d] / x_sel [gamma, d] (layer dtype,
+ *   both or neither): the chosen rows gathered in selection order; n_union (may be NULL):
+ *   covered experts. All device. C <= 8192, lambda >= 0. */
+moe_status moe_draft_select(const moe_layer_desc *L, int C, const int *parent, const int *depth,
+                            const float *logp, const int *footprint, float lambda, int gamma,
+                            const void *x, int *selected, int *sel_parent, int *sel_depth,
+                            void *x_sel, int *n_union, moe_stream_t stream);
+
 /* Reads and clears the kernel-side check word of a workspace. Waits for `stream`.
  * *flags = 0 when no kernel reported a problem since the last call; bit 0 = an
  * expert id outside [0, E) was skipped; bit 1 = a bounded device wait gave up. */

@@ -509,3 +509,87 @@ def test_residual_chain_of_layers_against_oracle():
     ref_x = xo.double().numpy()
     got = x.double().cpu().numpy()
     assert np.abs(got - ref_x).max() <= 2e-2 * np.abs(ref_x).max()
+
+
+# ------------------------------------------------- cost-aware draft selection
+
+def _sel_tree_from_oracle(cand, sel):
+    pos = {int(v): i for i, v in enumerate(sel)}
+    par = np.array([-1] + [pos[int(cand.parent[v])] for v in sel[1:]], np.int32)
+    return par, cand.depth[sel]
+
+
+@pytest.mark.parametrize("lam", [0.0, 0.2, 1.0])
+def test_draft_select_bit_exact(lam):
+    shape = W.QWEN3_30B_A3B
+    L = _desc(shape)
+    cand = W.eagle_candidates(77)
+    logits = W.synthetic_logits(78, cand.parent, shape.E, 2.0)
+    fp, _ = O.topk(logits, shape.k)
+    x = W.hidden_states(79, cand.parent, shape.d, torch.bfloat16)
+    gamma = 65
+    sel = torch.empty(gamma, dtype=torch.int32, device=DEV)
+    spar, sdep = torch.empty_like(sel), torch.empty_like(sel)
+    x_sel = torch.empty(gamma, shape.d, dtype=torch.bfloat16, device=DEV)
+    nu = torch.empty(1, dtype=torch.int32, device=DEV)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    M.moe_draft_select(L, td(cand.parent), td(cand.depth), td(cand.logp), td(fp), lam, gamma,
+                       sel, spar, sdep, x.to(DEV), x_sel, nu)
+    _sync()
+    ref_sel, ref_u = O.draft_select(cand.parent, cand.logp, fp, shape.E, lam, gamma)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    rp, rd = _sel_tree_from_oracle(cand, ref_sel)
+    np.testing.assert_array_equal(spar.cpu().numpy(), rp)
+    np.testing.assert_array_equal(sdep.cpu().numpy(), rd)
+    assert int(nu.item()) == ref_u
+    assert torch.equal(x_sel.cpu(), x[torch.from_numpy(ref_sel).long()])
+
+
+def test_draft_select_then_verify_against_oracle():
+    """The whole cost-aware pipeline on the device: router over every candidate, the
+    natural top-k as the predicted footprint, the selection, and verification of the
+    chosen tree (natural routing); the oracle runs the same steps from the same inputs."""
+    shape = W.QWEN3_30B_A3B
+    L = _desc(shape)
+    cand = W.eagle_candidates(81)
+    C = cand.C
+    x = W.hidden_states(82, cand.parent, shape.d, torch.bfloat16)
+    wr = W.router_weight(83, shape, std=0.1)
+    wg, wu, wd = _weights(shape, 84)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    logits = torch.empty(C, shape.E, device=DEV)
+    M.moe_router_logits(L, x.to(DEV), wr.to(DEV), logits)
+    fp = torch.empty(C, shape.k, dtype=torch.int32, device=DEV)
+    g = torch.empty(C, shape.k, device=DEV)
+    M.moe_tree_select(L, M.select_params(M.MOE_ROUTE_NATURAL, [1.0]), logits, td(cand.depth), 1,
+                      C, None, fp, g)
+    gamma, lam = 65, 0.3
+    sel = torch.empty(gamma, dtype=torch.int32, device=DEV)
+    spar, sdep = torch.empty_like(sel), torch.empty_like(sel)
+    x_sel = torch.empty(gamma, shape.d, dtype=torch.bfloat16, device=DEV)
+    M.moe_draft_select(L, td(cand.parent), td(cand.depth), td(cand.logp), fp, lam, gamma, sel,
+                       spar, sdep, x.to(DEV), x_sel)
+    y = torch.empty_like(x_sel)
+    ws = M.workspace(L, 1, gamma)
+    idx = torch.empty(gamma, shape.k, dtype=torch.int32, device=DEV)
+    M.moe_tree_forward(L, M.select_params(M.MOE_ROUTE_NATURAL, [1.0]), x_sel, wr.to(DEV), wg, wu,
+                       wd, None, sdep, 1, gamma, None, y, ws, M.tree_outputs(topk_idx=idx))
+    _sync()
+    l32 = O.router(x, wr).astype(np.float32)
+    rfp, _ = O.topk(l32, shape.k)
+    srt = -np.sort(-l32, axis=1)
+    boundary = srt[:, shape.k - 1] - srt[:, shape.k]  # k-th vs (k+1)-th logit
+    tied = boundary < 1e-5 * np.abs(srt[:, 0])
+    gfp = fp.cpu().numpy()
+    same = [set(gfp[r].tolist()) == set(rfp[r].tolist()) for r in range(C)]
+    assert all(same[r] for r in range(C) if not tied[r])
+    if not all(same):
+        pytest.skip("a footprint decided by an fp32 tie: both selections are valid")
+    ref_sel, _ = O.draft_select(cand.parent, cand.logp, rfp, shape.E, lam, gamma)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    xs = x[torch.from_numpy(ref_sel).long()]
+    rows = list(range(0, gamma, 6))
+    ref = O.forward(xs, wr, wg.cpu(), wu.cpu(), wd.cpu(), cand.depth[ref_sel], shape.k, [1.0],
+                    rows=rows, mode=O.NATURAL)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+    _assert_close_rows(y.float().cpu().numpy()[rows], ref["y"], shape)
