@@ -395,18 +395,37 @@ ORC_API void oracle_moe_combine(const void *x, const void *Wg, const void *Wu, c
 
 /* [ECO] cost-aware draft selection. Candidates 0..C-1, node 0 the root, parent[v] < v;
  * logp[v] the cumulative draft log-probability; footprint[v*k .. v*k+k) the experts the
- * node is predicted to use (distinct ids in [0, E)). S starts as {root} and the buffer B
- * as its footprint; then, gamma - 1 times, among the candidates not in S whose parent is
- * in S, take the one with the largest score logp[v] - lambda * |footprint(v) \ B|
- * (computed in fp32: one product, one difference; ties to the lower index), and add it to
- * S and its footprint to B. selected[] receives S in selection order (every parent before
- * its children), *n_union = |B|. Returns the number selected (< gamma when the tree has
- * fewer candidates). */
+ * node is predicted to use. The cost term is the size of a set difference, so an id
+ * listed twice in one footprint counts once, and ids outside [0, E) name no expert and
+ * are skipped. S starts as {root} and the buffer B as its footprint; then, gamma - 1
+ * times, among the candidates not in S whose parent is in S, take the one with the
+ * largest score logp[v] - lambda * |footprint(v) \ B| (computed in fp32: one product,
+ * one difference; ties to the lower index), and add it to S and its footprint to B.
+ * selected[] receives S in selection order (every parent before its children),
+ * *n_union = |B|. Returns the number selected (< gamma when the tree has fewer
+ * candidates). */
+static void add_footprint(const int *f, int k, int E, unsigned char *inB) {
+    for (int j = 0; j < k; ++j)
+        if (f[j] >= 0 && f[j] < E) inB[f[j]] = 1;
+}
+
+/* |f \ B| over the distinct valid ids of f */
+static int new_experts(const int *f, int k, int E, const unsigned char *inB) {
+    int dc = 0;
+    for (int j = 0; j < k; ++j) {
+        if (f[j] < 0 || f[j] >= E || inB[f[j]]) continue;
+        int seen = 0;
+        for (int i = 0; i < j; ++i) seen |= f[i] == f[j];
+        dc += !seen;
+    }
+    return dc;
+}
+
 ORC_API int oracle_draft_select(int C, int k, int E, const int *parent, const float *logp,
                                 const int *footprint, float lambda, int gamma, int *selected,
                                 int *n_union) {
-    unsigned char *inS = (unsigned char *)calloc((size_t)C, 1);
-    unsigned char *inB = (unsigned char *)calloc((size_t)E, 1);
+    unsigned char *inS = (unsigned char *)calloc((size_t)(C > 0 ? C : 1), 1);
+    unsigned char *inB = (unsigned char *)calloc((size_t)(E > 0 ? E : 1), 1);
     int n = 0;
     if (C < 1 || gamma < 1) {
         *n_union = 0;
@@ -416,14 +435,13 @@ ORC_API int oracle_draft_select(int C, int k, int E, const int *parent, const fl
     }
     inS[0] = 1;
     selected[n++] = 0;
-    for (int j = 0; j < k; ++j) inB[footprint[j]] = 1;
+    add_footprint(footprint, k, E, inB);
     while (n < gamma) {
         int best = -1;
         float best_sc = 0.f;
         for (int v = 1; v < C; ++v) {
-            if (inS[v] || !inS[parent[v]]) continue;
-            int dc = 0;
-            for (int j = 0; j < k; ++j) dc += inB[footprint[(size_t)v * k + j]] ? 0 : 1;
+            if (inS[v] || parent[v] < 0 || parent[v] >= C || !inS[parent[v]]) continue;
+            const int dc = new_experts(footprint + (size_t)v * k, k, E, inB);
             const float pen = lambda * (float)dc;
             const float sc = logp[v] - pen;
             if (best < 0 || sc > best_sc) {
@@ -434,7 +452,7 @@ ORC_API int oracle_draft_select(int C, int k, int E, const int *parent, const fl
         if (best < 0) break;
         inS[best] = 1;
         selected[n++] = best;
-        for (int j = 0; j < k; ++j) inB[footprint[(size_t)best * k + j]] = 1;
+        add_footprint(footprint + (size_t)best * k, k, E, inB);
     }
     int u = 0;
     for (int e = 0; e < E; ++e) u += inB[e];

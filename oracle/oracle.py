@@ -24,11 +24,12 @@ NATURAL, ACCEPT, FIXED_B = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with plain gcc (no fast-math, no vectorisation flags)."""
+    """Compile the oracle with plain gcc (no fast-math, no vectorisation flags, and no
+    fused multiply-add contraction, so that fp32 steps round the same on x86 and Arm)."""
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
         tmp = LIB + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fvisibility=hidden",
-                        "-o", tmp, SRC, "-lm"], check=True)
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                        "-fvisibility=hidden", "-o", tmp, SRC, "-lm"], check=True)
         os.replace(tmp, LIB)
     return LIB
 

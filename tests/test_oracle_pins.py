@@ -376,6 +376,20 @@ def test_draft_select_hand_example():
     assert (s2.tolist(), u2) == ([0, 2, 4], 3)
 
 
+def test_draft_select_cost_is_a_set_difference():
+    """The cost term counts experts, not footprint entries: with a footprint {2, 2} the
+    node adds one expert, and an id outside [0, E) adds none. Root {0}; a (-0.5, {2, 2})
+    and b (-0.45, {3, 4}) under the root; c (-0.6, {9, -1}) under the root, E = 8.
+    lambda = 0.1: a scores -0.6, b -0.65, c -0.6 (no valid new expert): a (lower index
+    than c on the tie) -> then c (-0.6) beats b (-0.65): S = {root, a, c}, union {0, 2}.
+    Counting entries instead would give a -0.7 and pick c first."""
+    parent = np.array([-1, 0, 0, 0], np.int32)
+    logp = np.array([0.0, -0.5, -0.45, -0.6], np.float32)
+    fp = np.array([[0, 0], [2, 2], [3, 4], [9, -1]], np.int32)
+    sel, u = O.draft_select(parent, logp, fp, 8, 0.1, 3)
+    assert (sel.tolist(), u) == ([0, 1, 3], 2)
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_draft_select_invariants(seed):
     """Ancestor-closed selection of gamma nodes, union = |union of the chosen footprints|,
