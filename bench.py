@@ -871,6 +871,80 @@ def run_efficiency(args):
                      "router_std": args.router_std}, sweep=rows))
 
 
+def run_ecospec(args):
+    """Cost-aware choice of the verified tree (EcoSpec stand-in) on the Qwen3-shaped layer:
+    per step, the router over all ~411 drafted candidates gives each candidate's predicted
+    footprint (its natural top-k), moe_draft_select picks 65 nodes with
+    log P - lambda * (new experts), and the chosen tree is verified with natural routing.
+    lambda = 0 is the confidence-ordered tree (the EAGLE-3 stand-in)."""
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.QWEN3_30B_A3B
+    seed = SEED + 7000 + 7919 * rank
+    n_pools = 16
+    pools = []
+    for i in range(n_pools):
+        c = W.eagle_candidates(seed + i)
+        x = W.hidden_states(seed + 100 + i, c.parent, shape.d, torch.bfloat16).to(dev)
+        td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        pools.append((c.C, td(c.parent), td(c.depth), td(c.logp), x))
+    wr = W.router_weight(seed + 1, shape, std=args.router_std, device=dev)
+    wg, wu, wd = W.expert_weights(seed + 2, shape, device=dev)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    gamma = 65
+    Cmax = max(p[0] for p in pools)
+    logits = torch.empty(Cmax, shape.E, device=dev)
+    fp = torch.empty(Cmax, shape.k, dtype=torch.int32, device=dev)
+    g = torch.empty(Cmax, shape.k, device=dev)
+    sel = torch.empty(gamma, dtype=torch.int32, device=dev)
+    spar, sdep = torch.empty_like(sel), torch.empty_like(sel)
+    x_sel = torch.empty(gamma, shape.d, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x_sel)
+    ws = M.workspace(L, 1, gamma, device=dev)
+    PN = M.select_params(M.MOE_ROUTE_NATURAL, [1.0])
+    K, Wm = args.steps, args.warmup
+    rows = []
+    for lam in (0.0, 0.1, 0.3, 1.0):
+        nu = torch.zeros(K, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(K, shape.E, dtype=torch.int32, device=dev)
+        sel_k = torch.zeros(K, gamma, dtype=torch.int32, device=dev)
+        cnt_v = torch.zeros(shape.E, dtype=torch.int32, device=dev)  # verify-only rounds
+
+        def step(i, verify_only=False):
+            C, par, dep, lp, x = pools[i % n_pools]
+            if not verify_only:
+                M.moe_router_logits(L, x, wr, logits[:C])
+                M.moe_tree_select(L, PN, logits[:C], dep, 1, C, None, fp[:C], g[:C])
+                M.moe_draft_select(L, par, dep, lp, fp[:C], lam, gamma, sel_k[i], spar, sdep,
+                                   x, x_sel, nu[i])
+            M.moe_tree_forward(L, PN, x_sel, wr, wg, wu, wd, None, sdep, 1, gamma, None, y, ws,
+                               M.tree_outputs(counts=cnt_v if verify_only else cnt[i]))
+
+        for i in range(Wm):
+            step(i)
+        sec = _timed(lambda: [step(i) for i in range(K)], dev, world)
+        sec_v = _timed(lambda: [step(i, True) for i in range(K)], dev, world)
+        mass = [float(pools[i % n_pools][3][sel_k[i].long()].sum()) for i in range(K)]
+        union = (cnt.cpu().numpy() > 0).sum(axis=1)
+        rows.append({"lambda": lam, "blocks_per_s": round(whole_job_rate(K, world, sec), 1),
+                     "verify_only_blocks_per_s": round(whole_job_rate(K, world, sec_v), 1),
+                     "verified_union": round(float(union.mean()), 2),
+                     "predicted_union": round(float(nu.float().mean().item()), 2),
+                     "sum_logp_selected": round(float(np.mean(mass)), 3)})
+    if rank == 0:
+        r0 = rows[0]
+        for r in rows:
+            r["union_vs_confidence"] = round(r["verified_union"] / r0["verified_union"], 4)
+        print(_line("MoE verify with cost-aware draft selection: tree-blocks/s incl. selection",
+                    rows[2]["blocks_per_s"], "tree-blocks/s", world, K, Wm,
+                    K / rows[2]["blocks_per_s"],
+                    {"workload": "qwen3-30b-a3b-layer-eagle3-candidates-ecospec",
+                     "candidates": "all nodes of a 5-step top-10 expansion", "gamma": gamma,
+                     "router_std": args.router_std}, sweep=rows))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -883,7 +957,7 @@ def main(argv=None):
     ap.add_argument("--cpu-trees", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched", "budget",
-                                           "efficiency"],
+                                           "efficiency", "ecospec"],
                     default="layer", help="layer: the Qwen3-shaped layer (default line)")
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--slots", type=int, default=48)
@@ -902,6 +976,8 @@ def main(argv=None):
         run_budget(args)
     elif args.workload == "efficiency":
         run_efficiency(args)
+    elif args.workload == "ecospec":
+        run_ecospec(args)
     else:
         run_gpu(args)
 

@@ -6,137 +6,173 @@
 // One CTA. S starts as {root}, the expert buffer B as the root's predicted footprint.
 // Each of the gamma - 1 steps scores every candidate whose parent is in S,
 // logp[v] - lambda * |footprint(v) \ B| (fp32: one product, one difference), takes the
-// best (ties to the lower index) with a block-wide argmax, and adds it to S and its
-// footprint to B (a bitmask of E <= 256 bits; footprint ids outside [0, E) are ignored,
-// and so are candidates whose parent index is outside [0, C)). The selection order is a
-// valid node order for the verified tree (parents first), so the kernel also writes that
-// tree's parent indices and depths and gathers its token rows for moe_tree_forward.
+// best (ties to the lower index), and adds it to S and its footprint to B.
+//
+// The steps are sequential, so the kernel is built for the latency of one step:
+//   - every footprint is turned once into a bit set of E <= 256 bits in shared memory;
+//     |footprint(v) \ B| is then a popcount of (footprint(v) & ~B) over E / 32 words
+//     (duplicate ids count once, ids outside [0, E) are ignored);
+//   - each thread owns up to kMaxCpt candidates and keeps their log-probability,
+//     parent and state (waiting / eligible / taken) in registers, and every thread keeps
+//     its own copy of B; nothing is written to shared memory inside a step except the
+//     per-warp best;
+//   - the best is an order-preserving 32-bit key of the score (max) and the lowest
+//     index among equal keys (min), two warp reductions per level; the per-warp results
+//     are double-buffered by step parity, so one barrier per step suffices: every warp
+//     then reduces the warp results itself and learns the winner.
+// The parent positions, depths, covered count and gathered rows are written after the
+// last step from the list of winners.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxCpt = 4;  // candidates per thread: C <= 1 + 4 * 1024
+constexpr int kMaxWords = kMaxE / 32;
+constexpr uint32_t kNone = 0u;
 
-__device__ __forceinline__ bool better(float s, int i, float bs, int bi) {
-    return bi < 0 || s > bs || (s == bs && i < bi);
+// Order-preserving key of a float score (larger score, larger key); 0 is "no candidate".
+// -0 is folded into +0 first, so equal scores give equal keys.
+__device__ __forceinline__ uint32_t score_key(float s) {
+    const uint32_t u = __float_as_uint(s + 0.f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kThreads)
+template <int CPT>
+__global__ void __launch_bounds__(kMaxThreads)
 draft_select_kernel(int C, int k, int E, const int *__restrict__ parent,
-                    const int *__restrict__ depth,
-                    const float *__restrict__ logp, const int *__restrict__ fp, float lambda,
-                    int gamma, int *__restrict__ selected, int *__restrict__ sel_parent,
+                    const int *__restrict__ depth, const float *__restrict__ logp,
+                    const int *__restrict__ fp, float lambda, int gamma,
+                    int *__restrict__ selected, int *__restrict__ sel_parent,
                     int *__restrict__ sel_depth, int *__restrict__ n_union,
                     const uint4 *__restrict__ x, uint4 *__restrict__ x_sel, int row_vec) {
     pdl_wait();
-    extern __shared__ int dsm[];
-    int *inS = dsm;      // [C]
-    int *pos = dsm + C;  // [C] position in the selection order, -1 if not selected
-    __shared__ uint32_t buf[kMaxE / 32];
-    __shared__ float wbs[kWarps];
-    __shared__ int wbi[kWarps];
-    __shared__ int s_best;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = (E + 31) >> 5;  // words of a bit set
+    extern __shared__ uint32_t dsm[];
+    uint32_t *fpm = dsm;                       // [C][nw] footprint bit sets
+    int *win = (int *)(dsm + (size_t)C * nw);  // [C] winners in selection order
+    int *pos = win + C;                        // [C] position of a winner
+    __shared__ uint32_t wkey[2][32];
+    __shared__ int widx[2][32];
+    const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = T >> 5;
 
-    for (int c = tid; c < C; c += kThreads) {
-        inS[c] = 0;
-        pos[c] = -1;
-    }
-    if (tid < kMaxE / 32) buf[tid] = 0u;
+    // footprint bit sets
+    for (int i = tid; i < C * nw; i += T) fpm[i] = 0u;
     __syncthreads();
-    if (tid == 0) {
-        inS[0] = 1;
-        pos[0] = 0;
-        selected[0] = 0;
-        sel_parent[0] = -1;
-        sel_depth[0] = depth[0];
-        for (int j = 0; j < k; ++j) {
-            const int e = fp[j];
-            if (e >= 0 && e < E) buf[e >> 5] |= 1u << (e & 31);
+    for (int i = tid; i < C * k; i += T) {
+        const int e = fp[i];
+        if (e >= 0 && e < E) atomicOr(&fpm[(size_t)(i / k) * nw + (e >> 5)], 1u << (e & 31));
+    }
+    // owned candidates: c = 1 + tid + s * T
+    float lp[CPT];
+    int par[CPT];
+    int st[CPT];  // 0 waiting for its parent, 1 eligible, 2 taken or not a candidate
+#pragma unroll
+    for (int s = 0; s < CPT; ++s) {
+        const int c = 1 + tid + s * T;
+        if (c < C) {
+            lp[s] = logp[c];
+            par[s] = parent[c];
+            st[s] = par[s] == 0 ? 1 : 0;
+        } else {
+            lp[s] = 0.f;
+            par[s] = -1;
+            st[s] = 2;
         }
     }
+    if (tid == 0) win[0] = 0;
     __syncthreads();
+    uint32_t B[kMaxWords];
+#pragma unroll
+    for (int q = 0; q < kMaxWords; ++q) B[q] = q < nw ? fpm[q] : 0u;
+
     int n = 1;
-    for (; n < gamma; ++n) {
-        float bs = 0.f;
-        int bi = -1;
-        for (int c = 1 + tid; c < C; c += kThreads) {
-            const int pc = parent[c];
-            if (inS[c] || pc < 0 || pc >= C || !inS[pc]) continue;
+    const int steps = min(gamma, C);
+    for (; n < steps; ++n) {
+        uint32_t key = kNone;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int s = 0; s < CPT; ++s) {
+            if (st[s] != 1) continue;
+            const int c = 1 + tid + s * T;
             int dc = 0;
-            for (int j = 0; j < k; ++j) {
-                const int e = fp[(size_t)c * k + j];
-                if (e >= 0 && e < E) dc += (buf[e >> 5] >> (e & 31)) & 1u ? 0 : 1;
-            }
-            const float sc = __fsub_rn(logp[c], __fmul_rn(lambda, (float)dc));
-            if (better(sc, c, bs, bi)) {
-                bs = sc;
+#pragma unroll
+            for (int q = 0; q < kMaxWords; ++q)
+                if (q < nw) dc += __popc(fpm[(size_t)c * nw + q] & ~B[q]);
+            const uint32_t kc = score_key(__fsub_rn(lp[s], __fmul_rn(lambda, (float)dc)));
+            if (kc > key) {  // owned candidates ascend with s: ties keep the lower index
+                key = kc;
                 bi = c;
             }
         }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (oi >= 0 && better(os, oi, bs, bi)) {
-                bs = os;
-                bi = oi;
-            }
-        }
+        uint32_t km = __reduce_max_sync(0xffffffffu, key);
+        int wi = (int)__reduce_min_sync(0xffffffffu, key == km ? (uint32_t)bi : 0x7fffffffu);
+        const int b = n & 1;
         if (lane == 0) {
-            wbs[warp] = bs;
-            wbi[warp] = bi;
+            wkey[b][warp] = km;
+            widx[b][warp] = wi;
         }
         __syncthreads();
-        if (warp == 0) {
-            bs = wbs[lane];
-            bi = wbi[lane];
+        key = lane < nwarps ? wkey[b][lane] : kNone;
+        bi = lane < nwarps ? widx[b][lane] : 0x7fffffff;
+        km = __reduce_max_sync(0xffffffffu, key);
+        if (km == kNone) break;  // no candidate left
+        const int w = (int)__reduce_min_sync(0xffffffffu, key == km ? (uint32_t)bi : 0x7fffffffu);
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (oi >= 0 && better(os, oi, bs, bi)) {
-                    bs = os;
-                    bi = oi;
-                }
-            }
-            if (lane == 0) {
-                s_best = bi;
-                if (bi >= 0) {
-                    inS[bi] = 1;
-                    pos[bi] = n;
-                    selected[n] = bi;
-                    sel_parent[n] = pos[parent[bi]];
-                    sel_depth[n] = depth[bi];
-                    for (int j = 0; j < k; ++j) {
-                        const int e = fp[(size_t)bi * k + j];
-                        if (e >= 0 && e < E) buf[e >> 5] |= 1u << (e & 31);
-                    }
-                }
-            }
+        for (int q = 0; q < kMaxWords; ++q)
+            if (q < nw) B[q] |= fpm[(size_t)w * nw + q];
+#pragma unroll
+        for (int s = 0; s < CPT; ++s) {
+            if (1 + tid + s * T == w) st[s] = 2;
+            else if (st[s] == 0 && par[s] == w) st[s] = 1;
         }
-        __syncthreads();
-        if (s_best < 0) break;
+        if (tid == 0) win[n] = w;
     }
-    for (int i = n + tid; i < gamma; i += kThreads) {  // fewer candidates than gamma
-        selected[i] = -1;
-        sel_parent[i] = -1;
-        sel_depth[i] = -1;
+    __syncthreads();
+    for (int i = tid; i < n; i += T) pos[win[i]] = i;
+    __syncthreads();
+    for (int i = tid; i < gamma; i += T) {
+        if (i < n) {
+            const int v = win[i];
+            selected[i] = v;
+            sel_parent[i] = i == 0 ? -1 : pos[parent[v]];
+            sel_depth[i] = depth[v];
+        } else {  // fewer candidates than gamma
+            selected[i] = -1;
+            sel_parent[i] = -1;
+            sel_depth[i] = -1;
+        }
     }
     if (tid == 0 && n_union) {
         int u = 0;
-        for (int w = 0; w < kMaxE / 32; ++w) u += __popc(buf[w]);
+#pragma unroll
+        for (int q = 0; q < kMaxWords; ++q) u += __popc(B[q]);
         *n_union = u;
     }
     if (x && x_sel) {
-        for (int i = warp; i < n; i += kWarps) {
-            const uint4 *src = x + (size_t)selected[i] * row_vec;
+        for (int i = warp; i < n; i += nwarps) {
+            const uint4 *src = x + (size_t)win[i] * row_vec;
             uint4 *dst = x_sel + (size_t)i * row_vec;
             for (int v = lane; v < row_vec; v += 32) dst[v] = __ldg(src + v);
         }
     }
+}
+
+template <int CPT>
+cudaError_t launch_draft(int T, size_t smem, cudaStream_t s, int C, int k, int E,
+                         const int *parent, const int *depth, const float *logp, const int *fp,
+                         float lambda, int gamma, int *selected, int *sel_parent, int *sel_depth,
+                         int *n_union, const void *x, void *x_sel, int row_vec) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            draft_select_kernel<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(draft_select_kernel<CPT>, dim3(1), dim3(T), smem, s, C, k, E, parent,
+                      depth, logp, fp, lambda, gamma, selected, sel_parent, sel_depth, n_union,
+                      (const uint4 *)x, (uint4 *)x_sel, row_vec);
 }
 
 }  // namespace
@@ -150,20 +186,28 @@ extern "C" moe_status moe_draft_select(const moe_layer_desc *L, int C, const int
                                        const void *x, int *selected, int *sel_parent,
                                        int *sel_depth, void *x_sel, int *n_union,
                                        moe_stream_t stream) {
-    if (!desc_ok(L) || C < 1 || C > 8192 || gamma < 1 || !parent || !depth || !logp ||
-        !footprint || !selected || !sel_parent || !sel_depth || !(lambda >= 0.f))
+    if (!desc_ok(L) || C < 1 || C > 1 + kMaxCpt * kMaxThreads || gamma < 1 || !parent ||
+        !depth || !logp || !footprint || !selected || !sel_parent || !sel_depth ||
+        !(lambda >= 0.f))
         return MOE_ERR_ARG;
     if ((x == nullptr) != (x_sel == nullptr)) return MOE_ERR_ARG;
     if (x && (!aligned16(x) || !aligned16(x_sel))) return MOE_ERR_ARG;
     const int row_vec = (int)((size_t)L->d * elem_size(L->dtype) / 16);
-    const size_t smem = (size_t)2 * C * sizeof(int);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(draft_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
-    return cuda_status(launch_pdl(draft_select_kernel, dim3(1), dim3(kThreads), smem,
-                                  (cudaStream_t)stream, C, L->k, L->E, parent, depth, logp,
-                                  footprint, lambda, gamma, selected, sel_parent, sel_depth,
-                                  n_union, (const uint4 *)x, (uint4 *)x_sel, row_vec));
+    const int nw = (L->E + 31) / 32;
+    const size_t smem = (size_t)C * (nw + 2) * sizeof(uint32_t);
+    const int cand = C > 1 ? C - 1 : 1;
+    const int cpt = (cand + kMaxThreads - 1) / kMaxThreads;
+    const int T = cpt == 1 ? ((cand + 31) / 32) * 32 : kMaxThreads;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    if (cpt == 1)
+        e = launch_draft<1>(T, smem, s, C, L->k, L->E, parent, depth, logp, footprint, lambda,
+                            gamma, selected, sel_parent, sel_depth, n_union, x, x_sel, row_vec);
+    else if (cpt == 2)
+        e = launch_draft<2>(T, smem, s, C, L->k, L->E, parent, depth, logp, footprint, lambda,
+                            gamma, selected, sel_parent, sel_depth, n_union, x, x_sel, row_vec);
+    else
+        e = launch_draft<4>(T, smem, s, C, L->k, L->E, parent, depth, logp, footprint, lambda,
+                            gamma, selected, sel_parent, sel_depth, n_union, x, x_sel, row_vec);
+    return cuda_status(e);
 }

@@ -233,12 +233,15 @@ moe_status moe_tree_forward_noalloc(const moe_layer_desc *L, const moe_select_pa
  * Verification of the chosen tree is unchanged (plain moe_tree_forward).
  *   parent, depth [C] int32, logp [C] fp32 (cumulative draft log-probability),
  *   footprint [C, L->k] int32 predicted experts per candidate (e.g. the natural top-k of
- *   the target router; ids outside [0, L->E) are ignored) -- all device.
+ *   the target router). The cost counts experts: an id listed twice counts once, ids
+ *   outside [0, L->E) are ignored, and a candidate whose parent is outside [0, C) is
+ *   never taken -- all device. logp must be finite.
  *   selected [gamma]: candidate ids in selection order (parents first; -1 past the end
  *   when fewer than gamma can be taken); sel_parent [gamma]: parent as a position in
  *   `selected` (root -1); sel_depth [gamma]; x [C, d] / x_sel [gamma, d] (layer dtype,
  *   both or neither): the chosen rows gathered in selection order; n_union (may be NULL):
- *   covered experts. All device. C <= 8192, lambda >= 0. */
+ *   covered experts. All device. 1 <= C <= 4097, gamma >= 1, lambda >= 0, else
+ *   MOE_ERR_ARG (nothing enqueued). One CTA; the gamma - 1 greedy steps are sequential. */
 moe_status moe_draft_select(const moe_layer_desc *L, int C, const int *parent, const int *depth,
                             const float *logp, const int *footprint, float lambda, int gamma,
                             const void *x, int *selected, int *sel_parent, int *sel_depth,

@@ -545,6 +545,59 @@ def test_draft_select_bit_exact(lam):
     assert torch.equal(x_sel.cpu(), x[torch.from_numpy(ref_sel).long()])
 
 
+@pytest.mark.parametrize("steps,topk,E,k,lam,junk", [
+    (9, 12, 256, 16, 0.05, False),   # C = 1165: two candidates per thread, 8-word bit sets
+    (8, 20, 128, 8, 0.3, False),     # C = 2821: four candidates per thread
+    (3, 6, 64, 4, 0.5, True),        # repeated and out-of-range footprint ids
+])
+def test_draft_select_large_and_junk_footprints(steps, topk, E, k, lam, junk):
+    cand = W.eagle_candidates(90 + steps, steps=steps, topk=topk)
+    C = cand.C
+    rng = np.random.default_rng(91 + steps)
+    if junk:
+        fp = rng.integers(-3, E + 3, size=(C, k)).astype(np.int32)
+        fp[:, 1] = fp[:, 0]  # every footprint lists one id twice
+    else:
+        fp = np.stack([rng.choice(E, size=k, replace=False) for _ in range(C)]).astype(np.int32)
+    L = M.layer_desc(256, E, k, 128, "bf16")
+    gamma = min(200, C)
+    sel = torch.empty(gamma, dtype=torch.int32, device=DEV)
+    spar, sdep = torch.empty_like(sel), torch.empty_like(sel)
+    nu = torch.empty(1, dtype=torch.int32, device=DEV)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    M.moe_draft_select(L, td(cand.parent), td(cand.depth), td(cand.logp), td(fp), lam, gamma,
+                       sel, spar, sdep, n_union=nu)
+    _sync()
+    ref_sel, ref_u = O.draft_select(cand.parent, cand.logp, fp, E, lam, gamma)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    rp, rd = _sel_tree_from_oracle(cand, ref_sel)
+    np.testing.assert_array_equal(spar.cpu().numpy(), rp)
+    np.testing.assert_array_equal(sdep.cpu().numpy(), rd)
+    assert int(nu.item()) == ref_u
+
+
+def test_draft_select_fewer_candidates_than_gamma():
+    parent = np.array([-1, 0, 0, 1, 7], np.int32)  # node 4's parent is out of range
+    depth = np.array([0, 1, 1, 2, 3], np.int32)
+    logp = np.array([0.0, -0.5, -0.7, -0.9, -0.1], np.float32)
+    fp = np.array([[0, 1], [2, 3], [0, 1], [2, 4], [5, 6]], np.int32)
+    L = M.layer_desc(256, 8, 2, 128, "bf16")
+    gamma = 8
+    sel = torch.full((gamma,), 99, dtype=torch.int32, device=DEV)
+    spar, sdep = torch.full_like(sel, 99), torch.full_like(sel, 99)
+    nu = torch.empty(1, dtype=torch.int32, device=DEV)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    M.moe_draft_select(L, td(parent), td(depth), td(logp), td(fp), 0.1, gamma, sel, spar, sdep,
+                       n_union=nu)
+    _sync()
+    ref_sel, ref_u = O.draft_select(parent, logp, fp, 8, 0.1, gamma)
+    assert ref_sel.tolist() == [0, 1, 2, 3]
+    assert sel.cpu().tolist() == [0, 1, 2, 3, -1, -1, -1, -1]
+    assert spar.cpu().tolist() == [-1, 0, 0, 1, -1, -1, -1, -1]
+    assert sdep.cpu().tolist() == [0, 1, 1, 2, -1, -1, -1, -1]
+    assert int(nu.item()) == ref_u == 5
+
+
 def test_draft_select_then_verify_against_oracle():
     """The whole cost-aware pipeline on the device: router over every candidate, the
     natural top-k as the predicted footprint, the selection, and verification of the
