@@ -1,8 +1,10 @@
 // Verifier-side expert selection for a block of draft trees ("AcceptMoE" news
 // article, section 02; AcceptMoE abstract, arXiv 2608.02989).
 //
-// Trees of up to 256 nodes run as one cluster of 8 CTAs per tree (see the cluster
-// variant below); larger trees run on one CTA of 32 warps per tree, described here. The
+// Natural routing needs none of the per-tree steps and has its own kernel (the last one
+// in this file). For AcceptMoE and fixed-size routing, trees of up to 256 nodes run as
+// one cluster of 8 CTAs per tree (see the cluster variant below); larger trees run on
+// one CTA of 32 warps per tree, described here. The
 // tree's logits are staged in shared memory once (when they fit) and every later pass
 // reads them from there.
 //   Phase A  a warp per node: natural top-k (the natural routing and the natural
@@ -145,7 +147,6 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
     const int *dep = depth + (size_t)b * N;
     int *idxb = idx_out + (size_t)b * N * k;
     float *gb = gates_out + (size_t)b * N * k;
-    const bool natural = a.mode == MOE_ROUTE_NATURAL;
     const bool staged = N * E <= kStageFloats;
     float *stage = dyn;
     float *mx = dyn + (staged ? N * E : 0);  // [N] softmax maxima
@@ -181,37 +182,20 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         if (lane < k && t >= 0) inU[t] = 1;
         if (n == 0 && lane < k) natRoot[lane] = t;
         if (lane < k) nat[n * k + lane] = t;
-        if (natural) {
-            write_choice(t, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
-        } else {
-            const float m = __shfl_sync(0xffffffffu, val, 0);  // the top-1 logit
-            float s = 0.f;
+        const float m = __shfl_sync(0xffffffffu, val, 0);  // the top-1 logit
+        float s = 0.f;
 #pragma unroll
-            for (int i = 0; i < kVPL; ++i)
-                if (lane + 32 * i < E) s += expf(v[i] - m);
-            s = warp_sum(s);
-            if (lane == 0) {
-                const int dd = min(dep[n], a.n_c - 1);
-                mx[n] = m;
-                nz[n] = s;
-                cN[n] = a.c[dd < 0 ? 0 : dd];
-            }
+        for (int i = 0; i < kVPL; ++i)
+            if (lane + 32 * i < E) s += expf(v[i] - m);
+        s = warp_sum(s);
+        if (lane == 0) {
+            const int dd = min(dep[n], a.n_c - 1);
+            mx[n] = m;
+            nz[n] = s;
+            cN[n] = a.c[dd < 0 ? 0 : dd];
         }
     }
     __syncthreads();
-
-    if (natural) {
-        const int u = __syncthreads_count(tid < E && inU[tid]);
-        if (tid == 0 && info_out) {
-            info_out[b * MOE_INFO_FIELDS + 0] = u;
-            info_out[b * MOE_INFO_FIELDS + 1] = u;
-            info_out[b * MOE_INFO_FIELDS + 2] = E;
-            info_out[b * MOE_INFO_FIELDS + 3] = 0;
-        }
-        if (elig_out)
-            for (int e = tid; e < E; e += kThreads) elig_out[(size_t)b * E + e] = 1;
-        return;
-    }
 
     // ---- demand: D_e = sum over nodes (ascending) of c_n * exp(l_ne - max_n) / sum_n ----
     if (staged) {
@@ -401,7 +385,6 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     const int *dep = depth + (size_t)b * N;
     int *idxb = idx_out + (size_t)b * N * k;
     float *gb = gates_out + (size_t)b * N * k;
-    const bool natural = a.mode == MOE_ROUTE_NATURAL;
 
     for (int e = tid; e < kMaxE; e += kCThreads) {
         inU[e] = 0;
@@ -424,28 +407,24 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             nat_loc[slot * k + lane] = c;
             nat0[n * k + lane] = c;
         }
-        if (natural) {
-            write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
-        } else {
-            const float m = __shfl_sync(0xffffffffu, val, 0);
-            float ex[kVPL], s = 0.f;
+        const float m = __shfl_sync(0xffffffffu, val, 0);
+        float ex[kVPL], s = 0.f;
 #pragma unroll
-            for (int i = 0; i < kVPL; ++i) {
-                ex[i] = lane + 32 * i < E ? expf(v[i] - m) : 0.f;
-                s += ex[i];
-            }
-            s = warp_sum(s);
-            const int dd = min(dep[n], a.n_c - 1);
-            const float cn = a.c[dd < 0 ? 0 : dd];
+        for (int i = 0; i < kVPL; ++i) {
+            ex[i] = lane + 32 * i < E ? expf(v[i] - m) : 0.f;
+            s += ex[i];
+        }
+        s = warp_sum(s);
+        const int dd = min(dep[n], a.n_c - 1);
+        const float cn = a.c[dd < 0 ? 0 : dd];
 #pragma unroll
-            for (int i = 0; i < kVPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E) wt[slot * E + e] = __fmul_rn(cn, __fdiv_rn(ex[i], s));
-            }
+        for (int i = 0; i < kVPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) wt[slot * E + e] = __fmul_rn(cn, __fdiv_rn(ex[i], s));
         }
     }
     __syncthreads();
-    if (!natural && tid < E) {  // partial demand of this CTA's nodes, node order
+    if (tid < E) {  // partial demand of this CTA's nodes, node order
         float acc = 0.f;
         for (int t = 0; t * kCC * kCW < N; ++t)
             for (int w = 0; w < kCW; ++w) {
@@ -460,102 +439,89 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     if (rank == 0) {
         for (int i = tid; i < N * k; i += kCThreads) inU[nat_all[i]] = 1;
         __syncthreads();
-        if (natural) {
-            const int u = __syncthreads_count(tid < E && inU[tid]);
-            if (tid == 0 && info_out) {
-                info_out[b * MOE_INFO_FIELDS + 0] = u;
-                info_out[b * MOE_INFO_FIELDS + 1] = u;
-                info_out[b * MOE_INFO_FIELDS + 2] = E;
-                info_out[b * MOE_INFO_FIELDS + 3] = 0;
-            }
-            if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = 1;
-        } else {
-            if (tid < E) {
-                float acc = 0.f;
-                for (int r = 0; r < kCC; ++r) acc = __fadd_rn(acc, part[r][tid]);
-                D[tid] = acc;
-            }
-            const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
-            if (tid == 0) {
-                float sum = 0.f;
-#pragma unroll 16
-                for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
-                s_sumD = sum;
-            }
-            __syncthreads();
-            if (tid < E) {
-                const float q = __fdiv_rn(D[tid], s_sumD);
-                term[tid] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
-            }
-            __syncthreads();
-            if (tid == 0) {
-                int m;
-                if (a.mode == MOE_ROUTE_ACCEPT) {
-                    float H = 0.f;
-#pragma unroll 16
-                    for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
-                    const float r = expf(H);
-                    const float rn = rintf(r);
-                    m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
-                } else {
-                    m = a.fixed_B;
-                }
-                m = min(max(m, k), pool);
-                s_m = m;
-                if (a.anchor)
-                    for (int j = 0; j < k; ++j) inA[nat_all[j]] = 1;
-            }
-            __syncthreads();
-            const int nA = a.anchor ? k : 0;
-            const int m = s_m;
-            if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? D[tid] : -1.f;
-            __syncthreads();
-            if (tid < E) {
-                int in = inA[tid];
-                const float De = rk[tid];
-                if (De >= 0.f) {
-                    int rnk = 0;
-#pragma unroll 8
-                    for (int q = 0; q < E; ++q) {
-                        const float Dq = rk[q];
-                        rnk += (Dq > De || (Dq == De && q < tid)) ? 1 : 0;
-                    }
-                    in = rnk < m - nA;
-                }
-                inS[tid] = in;
-            }
-            __syncthreads();
-            int removed = 0;
-            if (a.prune && resident) {
-                int is_rem = 0;
-                if (tid < E) {
-                    is_rem = inS[tid] && !inA[tid] && !resident[tid];
-                    rk[tid] = is_rem ? D[tid] : INFINITY;
-                }
-                const int nrem = __syncthreads_count(is_rem);
-                const int fl = a.min_set > k ? a.min_set : k;
-                removed = min(min(max(m - fl, 0), a.budget), nrem);
-                if (is_rem) {
-                    const float De = rk[tid];
-                    int rnk = 0;
-#pragma unroll 8
-                    for (int q = 0; q < E; ++q) {
-                        const float Dq = rk[q];
-                        rnk += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
-                    }
-                    if (rnk < removed) inS[tid] = 0;
-                }
-                __syncthreads();
-            }
-            if (tid == 0 && info_out) {
-                info_out[b * MOE_INFO_FIELDS + 2] = m;
-                info_out[b * MOE_INFO_FIELDS + 3] = removed;
-            }
-            if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
+        if (tid < E) {
+            float acc = 0.f;
+            for (int r = 0; r < kCC; ++r) acc = __fadd_rn(acc, part[r][tid]);
+            D[tid] = acc;
         }
+        const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
+        if (tid == 0) {
+            float sum = 0.f;
+#pragma unroll 16
+            for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
+            s_sumD = sum;
+        }
+        __syncthreads();
+        if (tid < E) {
+            const float q = __fdiv_rn(D[tid], s_sumD);
+            term[tid] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int m;
+            if (a.mode == MOE_ROUTE_ACCEPT) {
+                float H = 0.f;
+#pragma unroll 16
+                for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
+                const float r = expf(H);
+                const float rn = rintf(r);
+                m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
+            } else {
+                m = a.fixed_B;
+            }
+            m = min(max(m, k), pool);
+            s_m = m;
+            if (a.anchor)
+                for (int j = 0; j < k; ++j) inA[nat_all[j]] = 1;
+        }
+        __syncthreads();
+        const int nA = a.anchor ? k : 0;
+        const int m = s_m;
+        if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? D[tid] : -1.f;
+        __syncthreads();
+        if (tid < E) {
+            int in = inA[tid];
+            const float De = rk[tid];
+            if (De >= 0.f) {
+                int rnk = 0;
+#pragma unroll 8
+                for (int q = 0; q < E; ++q) {
+                    const float Dq = rk[q];
+                    rnk += (Dq > De || (Dq == De && q < tid)) ? 1 : 0;
+                }
+                in = rnk < m - nA;
+            }
+            inS[tid] = in;
+        }
+        __syncthreads();
+        int removed = 0;
+        if (a.prune && resident) {
+            int is_rem = 0;
+            if (tid < E) {
+                is_rem = inS[tid] && !inA[tid] && !resident[tid];
+                rk[tid] = is_rem ? D[tid] : INFINITY;
+            }
+            const int nrem = __syncthreads_count(is_rem);
+            const int fl = a.min_set > k ? a.min_set : k;
+            removed = min(min(max(m - fl, 0), a.budget), nrem);
+            if (is_rem) {
+                const float De = rk[tid];
+                int rnk = 0;
+#pragma unroll 8
+                for (int q = 0; q < E; ++q) {
+                    const float Dq = rk[q];
+                    rnk += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
+                }
+                if (rnk < removed) inS[tid] = 0;
+            }
+            __syncthreads();
+        }
+        if (tid == 0 && info_out) {
+            info_out[b * MOE_INFO_FIELDS + 2] = m;
+            info_out[b * MOE_INFO_FIELDS + 3] = removed;
+        }
+        if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
     }
-    // natural routing is complete: CTA 0 only reads its own shared memory from here on
-    if (natural) return;
     cl.sync();
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
@@ -611,10 +577,68 @@ std::atomic<size_t> cluster_smem_set{0}, single_smem_set{0};
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Natural routing (every expert eligible): each node's top-k and renormalised gates are
+// independent of the other nodes, so a tree of any size runs on one cluster of kNC CTAs
+// of kNW warps, a warp per node (node n on global warp n mod (kNC*kNW)). The only
+// per-tree quantity is the natural union |U|: each CTA marks its nodes' experts in a bit
+// set, ORs it into CTA 0's bit set through distributed shared memory, and CTA 0 counts
+// the bits after the cluster barrier.
+constexpr int kNC = 8;    // CTAs per tree
+constexpr int kNW = 16;   // warps per CTA
+constexpr int kNWords = kMaxE / 32;
+
+__global__ void __cluster_dims__(kNC, 1, 1) __launch_bounds__(kNW * 32)
+select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
+                      int *__restrict__ idx_out, float *__restrict__ gates_out,
+                      uint8_t *__restrict__ elig_out, int *__restrict__ info_out) {
+    __shared__ uint32_t mask[kNWords];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < kNWords) mask[tid] = 0u;
+    // CTA 0's bit set must be cleared before any CTA ORs into it: the arrive releases
+    // the clearing store, the wait before the first remote update acquires it
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    pdl_wait();
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int b = blockIdx.x / kNC;
+    const float *Lg = logits + (size_t)b * N * E;
+    int *idxb = idx_out + (size_t)b * N * k;
+    float *gb = gates_out + (size_t)b * N * k;
+    __syncthreads();  // the local bit set is clear
+    for (int n = rank * kNW + warp; n < N; n += kNC * kNW) {
+        float v[kVPL];
+        load_row(Lg + (size_t)n * E, E, v);
+        const int c = warp_topk(v, 0xffffffffu, E, k);
+        const float val = chosen_value(v, c);
+        write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+        if (lane < k && c >= 0) atomicOr(&mask[c >> 5], 1u << (c & 31));
+    }
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (tid < kNWords && mask[tid]) atomicOr(cl.map_shared_rank(&mask[tid], 0), mask[tid]);
+    cl.sync();
+    if (rank == 0) {
+        if (tid == 0 && info_out) {
+            int u = 0;
+            for (int w = 0; w < kNWords; ++w) u += __popc(mask[w]);
+            info_out[b * MOE_INFO_FIELDS + 0] = u;
+            info_out[b * MOE_INFO_FIELDS + 1] = u;
+            info_out[b * MOE_INFO_FIELDS + 2] = E;
+            info_out[b * MOE_INFO_FIELDS + 3] = 0;
+        }
+        if (elig_out)
+            for (int e = tid; e < E; e += kNW * 32) elig_out[(size_t)b * E + e] = 1;
+    }
+}
+
 cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s) {
     if (B <= 0 || N <= 0) return cudaSuccess;
+    if (a.mode == MOE_ROUTE_NATURAL)
+        return launch_pdl(select_natural_kernel, dim3(B * kNC), dim3(kNW * 32), 0, s, logits, N,
+                          L.E, L.k, idx, gates, elig, info);
     if (N <= kClusterMaxN) {
         const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
         const size_t smem =

@@ -180,6 +180,27 @@ def test_selection_large_tree_single_cta_path():
         assert exact == 1
 
 
+@pytest.mark.parametrize("B,N,E,k", [(1, 411, 128, 8), (3, 1000, 64, 4), (2, 3000, 256, 16),
+                                     (64, 65, 128, 8)])
+def test_selection_natural_any_tree_size(B, N, E, k):
+    """Natural routing runs one cluster per tree with a warp per node, for any N."""
+    shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
+    rng = np.random.default_rng(N + B)
+    parent = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        parent[b, 1:] = [int(rng.integers(0, n)) for n in range(1, N)]
+    depth = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(1, N):
+            depth[b, n] = depth[b, parent[b, n]] + 1
+    logits = W.synthetic_logits(N + 7 * B, parent, E, 3.0)
+    P = M.select_params(M.MOE_ROUTE_NATURAL, [1.0])
+    gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth, B, N)
+    exact = _check_selection(shape, dict(mode=O.NATURAL, c=[1.0]), logits, depth, gidx, gg, ge,
+                             gi, N, B)
+    assert exact == B
+
+
 def test_selection_root_only_and_all_experts():
     # N = 1: the root alone; E = k: every expert is chosen by every node
     for shape, N in ((W.LayerShape(d=64, E=16, k=2, f=64, dtype="fp32"), 1),
