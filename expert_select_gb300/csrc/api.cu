@@ -79,10 +79,11 @@ bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
 bool permute_fits(int R, int E) { return permute_smem_bytes(R, E) <= 227 * 1024; }
 
 moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
-                       const Workspace &w, int *counts, int *offsets, int *perm, cudaStream_t s) {
+                       const Workspace &w, int *counts, int *offsets, int *perm,
+                       bool after_router, cudaStream_t s) {
     return cuda_status(launch_permute(L, idx, R, counts, offsets, perm, at<int>(ws, w.pos),
                                       at<int>(ws, w.active), at<int>(ws, w.rowtiles),
-                                      at<int>(ws, w.flags), s));
+                                      at<int>(ws, w.flags), after_router, s));
 }
 
 moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const void *Wu,
@@ -144,8 +145,8 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
                               const void *Wu, const void *Wd, const int *slot, const int *idx,
                               const float *gates, int R, void *y, void *ws, const Workspace &w,
                               int *counts, int *offsets, int *perm, const moe_run_opts *opts,
-                              cudaStream_t s) {
-    moe_status st = run_permute(L, idx, R, ws, w, counts, offsets, perm, s);
+                              bool after_router, cudaStream_t s) {
+    moe_status st = run_permute(L, idx, R, ws, w, counts, offsets, perm, after_router, s);
     if (st != MOE_OK) return st;
     st = run_ffn(L, x, Wg, Wu, Wd, slot, nullptr, R, ws, w, counts, offsets, perm, opts, s);
     if (st != MOE_OK) return st;
@@ -190,7 +191,7 @@ moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void 
                              float *logits, moe_stream_t stream) {
     if (!desc_ok(L) || R < 0 || (R > 0 && (!x || !W_r || !logits))) return MOE_ERR_ARG;
     if (R > 0 && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ARG;
-    return cuda_status(launch_router(*L, x, W_r, R, logits, (cudaStream_t)stream));
+    return cuda_status(launch_router(*L, x, W_r, R, logits, nullptr, (cudaStream_t)stream));
 }
 
 moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
@@ -214,7 +215,7 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
     return cuda_status(launch_permute(*L, topk_idx, R, counts, offsets, perm,
                                       at<int>(workspace, w.pos), at<int>(workspace, w.active),
                                       at<int>(workspace, w.rowtiles),
-                                      at<int>(workspace, w.flags), (cudaStream_t)stream));
+                                      at<int>(workspace, w.flags), false, (cudaStream_t)stream));
 }
 
 moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void *W_gate,
@@ -231,7 +232,7 @@ moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void
     const Workspace w = workspace_layout(*L, 1, R);
     return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, R, y,
                        workspace, w, at<int>(workspace, w.counts), at<int>(workspace, w.offsets),
-                       at<int>(workspace, w.perm), opts, (cudaStream_t)stream);
+                       at<int>(workspace, w.perm), opts, false, (cudaStream_t)stream);
 }
 
 moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P, const void *x,
@@ -263,12 +264,14 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
     int *offsets = o.offsets ? o.offsets : at<int>(workspace, w.offsets);
     int *perm = o.perm ? o.perm : at<int>(workspace, w.perm);
 
-    if (launch_router(*L, x, W_r, R, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router(*L, x, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord, s) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, s) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, idx, gates, R, y, workspace,
-                       w, counts, offsets, perm, opts, s);
+                       w, counts, offsets, perm, opts, true, s);
 }
 
 moe_status moe_workspace_check(void *workspace, int *flags, moe_stream_t stream) {

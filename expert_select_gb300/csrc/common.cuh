@@ -14,6 +14,10 @@ namespace moe {
 
 // Bits of the kernel-side check word (first int of the workspace).
 enum : int { FLAG_BAD_EXPERT = 1, FLAG_WAIT_TIMEOUT = 2 };
+// Workspace flag words: [0] the check word moe_workspace_check reads; [kRouterCheckWord]
+// the router's, which runs before the permute kernel clears the words and is carried into
+// [0] by it.
+constexpr int kRouterCheckWord = 1;
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
@@ -49,7 +53,7 @@ inline size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_router(const moe_layer_desc &L, const void *x, const void *Wr, int R,
-                          float *logits, cudaStream_t s);
+                          float *logits, int *flags, cudaStream_t s);  // flags may be null
 
 struct SelectArgs {
     int mode, n_c, pool_all, anchor, prune, budget, min_set, fixed_B;
@@ -67,9 +71,11 @@ constexpr int kMinRowTile = 64;
 inline int rowtile_size(int R) { return R <= 128 ? 64 : 256; }
 inline int max_rowtiles(int E, int A) { return E + (A + kMinRowTile - 1) / kMinRowTile + 1; }
 
+// Row tiles of rowtile_size(R). The kernel starts the call's check word: the router's
+// word is carried into it when the router ran earlier in the same call (after_router).
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
-                           int *flags, cudaStream_t s);  // row tiles of rowtile_size(R)
+                           int *flags, bool after_router, cudaStream_t s);
 size_t permute_smem_bytes(int R, int E);
 
 struct FfnArgs {
@@ -111,7 +117,8 @@ bool select_args(const moe_select_params *P, int k, SelectArgs *a);
 bool permute_fits(int R, int E);
 bool aligned16(const void *p);
 moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
-                       const Workspace &w, int *counts, int *offsets, int *perm, cudaStream_t s);
+                       const Workspace &w, int *counts, int *offsets, int *perm,
+                       bool after_router, cudaStream_t s);
 moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const void *Wu,
                    const void *Wd, const int *slot, const uint8_t *pass, int R, void *ws,
                    const Workspace &w, const int *counts, const int *offsets, const int *perm,

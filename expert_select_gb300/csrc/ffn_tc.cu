@@ -35,16 +35,15 @@
 // Every wait is bounded: after 2 s a wait gives up, sets the workspace check bit
 // FLAG_WAIT_TIMEOUT and makes the CTA stop; the CTA then waits (again bounded) for
 // its TMA loads and MMAs in flight, frees its tensor memory and exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int kThreads = 192;
 constexpr int kBK = 64;                     // K elements per stage: one 128-B swizzle atom
@@ -53,7 +52,6 @@ constexpr int kAccCols = 256;               // TMEM columns per accumulator (max
 constexpr int kTmemCols = 2 * kAccCols;     // two accumulators
 constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
 constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 144 bytes)
 
@@ -78,139 +76,6 @@ struct Params {
     __nv_bfloat16 *h;
     float *o;
 };
-
-// ------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long now_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for the phase of `bar` with parity `parity`. Gives up when *abort is set
-// (if abort != nullptr) or after kTimeoutNs; a timeout sets *abort and the check bit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *flags) {
-    unsigned long long t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
-            if (abort && *abort) return false;
-            const unsigned long long t = now_ns();
-            if (t0 == 0) {
-                t0 = t;
-            } else if (t - t0 > kTimeoutNs) {
-                if (abort) *abort = 1;
-                atomicOr(flags, FLAG_WAIT_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major bf16 tile with 128-byte swizzling:
-// rows of 128 B, 8-row groups 1024 B apart (stride byte offset), fixed field 0b001 at
-// bit 46, swizzle mode 2 (128 B) at bits 61-63. The leading byte offset is unused for
-// swizzled K-major tiles.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major,
-// N and M encoded as N/8 and M/16.
-__device__ __forceinline__ uint32_t idesc_bf16(uint32_t N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 // Named barrier of the four epilogue warps (bar.sync is warp-aligned: reconverge first).
 __device__ __forceinline__ void epi_bar() {
@@ -423,7 +288,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 ++it;
                 if (!mbar_wait(tempty + 8 * acc, aph ^ 1u, abort_flag, p.flags)) break;
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16((uint32_t)((w.ntok + 15) & ~15));
+                const uint32_t idesc = idesc_bf16(kM, (uint32_t)((w.ntok + 15) & ~15));
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
                 const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
                 for (int kc = 0; kc < kchunks; ++kc) {
@@ -573,36 +438,6 @@ gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ 
 }
 
 // ------------------------------------------------------------------- host
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-            const uint64_t *row_strides, const uint32_t *box) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gd[3], gs[2];
-    cuuint32_t bx[3], es[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) {
-        gd[i] = dims[i];
-        bx[i] = box[i];
-    }
-    for (int i = 0; i < rank - 1; ++i) gs[i] = row_strides[i];
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd,
-              gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // Weight pool [S][rows][K] as a 3-D map with a 64 x box_rows x 1 box.
 bool encode_weights(CUtensorMap *m, const void *w, int S, int rows, int K, int box_rows) {

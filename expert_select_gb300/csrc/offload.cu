@@ -98,11 +98,13 @@ extern "C" moe_status moe_offload_forward(
     // 1. residency before uploads, routing, selection, permutation
     if (launch_publish(E, slot_host.data(), res_host.data(), slot_dev, res_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_router(*L, x, W_r, R, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router(*L, x, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord, s) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     if (launch_select(*L, a, logits, depth, B, N, a.prune ? res_dev : nullptr, idx, gates, elig,
                       info, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    moe_status st = run_permute(*L, idx, R, workspace, w, counts, offsets, perm, s);
+    moe_status st = run_permute(*L, idx, R, workspace, w, counts, offsets, perm, true, s);
     if (st != MOE_OK) return st;
 
     // 2. the needed set

@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(kThreads)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
                int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags,
-               int rt_size) {
+               int rt_size, int after_router) {
     pdl_wait();
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
@@ -33,7 +33,12 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     const int A = R * k;
 
     for (int i = tid; i < nb * E; i += kThreads) mask[i] = 0u;
-    if (tid < 64) flags[tid] = 0;  // check word + scheduler counters of this call
+    if (tid == 0) {  // a fresh check word for this call, keeping what the router reported
+        flags[0] = after_router ? flags[kRouterCheckWord] : 0;
+        flags[kRouterCheckWord] = 0;
+    } else if (tid < 64 && tid != kRouterCheckWord) {
+        flags[tid] = 0;
+    }
     __syncthreads();
     for (int a = tid; a < A; a += kThreads) {
         const int e = idx[a];
@@ -133,13 +138,14 @@ size_t permute_smem_bytes(int R, int E) {
 
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
-                           int *flags, cudaStream_t s) {
+                           int *flags, bool after_router, cudaStream_t s) {
     const size_t smem = permute_smem_bytes(R, L.E);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     return launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
-                      offsets, perm, pos, active, rowtiles, flags, rowtile_size(R));
+                      offsets, perm, pos, active, rowtiles, flags, rowtile_size(R),
+                      after_router ? 1 : 0);
 }
 
 }  // namespace moe

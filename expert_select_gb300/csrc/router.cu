@@ -10,10 +10,22 @@
 //     the 8 partial sums in shared memory (latency-bound regime);
 //   * large blocks: the 8 warps share their 8 experts and take consecutive row
 //     blocks, so a W_r slice is fetched from L2 once per CTA and served from L1.
+// From a few hundred rows on (bf16), the scores are a dense [R x d] x [d x E] product and
+// run on the tensor cores instead (router_tc_kernel below).
+#include <mutex>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
+
+// The router's check word starts every call at zero: the first thread of the grid
+// clears it before anything else (only the tensor-core kernel ever sets it, and only
+// after a wait of two seconds).
+__device__ __forceinline__ void clear_check_word(int *flags) {
+    if (flags && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *flags = 0;
+}
 
 constexpr int kRows = 4;     // rows per warp
 constexpr int kExp = 8;      // experts per warp
@@ -22,7 +34,8 @@ constexpr int kWarps = 8;    // warps per CTA (consecutive row blocks)
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 router_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, int d, int E,
-              float *__restrict__ logits) {
+              float *__restrict__ logits, int *flags) {
+    clear_check_word(flags);
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -67,7 +80,8 @@ router_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, int d, i
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 router_splitd_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, int d, int E,
-                     float *__restrict__ logits) {
+                     float *__restrict__ logits, int *flags) {
+    clear_check_word(flags);
     pdl_wait();
     __shared__ float part[kWarps][32];
     const int lane = threadIdx.x & 31;
@@ -110,30 +124,222 @@ router_splitd_kernel(const T *__restrict__ x, const T *__restrict__ Wr, int R, i
     }
 }
 
+// ------------------------------------------------------------------ tensor cores
+// One CTA per (32- or 64-row tile of x, 128 experts): the 128 router rows W_r[e0 .. e0+127]
+// are the MMA's A operand (M = 128; experts past E are zero-filled by TMA), the token
+// rows the B operand (N = 32 or 64), the fp32 accumulator [128 experts x N tokens] lives
+// in tensor memory. The hidden dimension streams through a ring of stages of 64 elements
+// (one 128-byte swizzle atom) loaded by TMA. Warp 0 loads, warp 1 allocates tensor memory
+// and issues the MMAs, then all four warps read the accumulator back (warp q owns experts
+// e0 + 32q .. +31, one per lane) and store the logits, a 128-byte row segment per token.
+// Every wait is bounded; a wait that gives up leaves NaN in the CTA's logits and sets
+// FLAG_WAIT_TIMEOUT in the router's check word `flags` when one is given.
+namespace rtc {
+
+using namespace tc;
+
+constexpr int kThreads = 128;
+constexpr int kStages = 8;
+constexpr int kBK = 64;
+constexpr int kM = 128;
+constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB of W_r per stage
+
+struct Maps {
+    CUtensorMap w;  // W_r [E][d], box 64 x 128
+    CUtensorMap x;  // x [R][d], box 64 x nt
+};
+
+__host__ __device__ constexpr size_t smem_bytes(int nt) {
+    return 1024 + (size_t)kStages * (kABytes + (size_t)nt * 128) + 256;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+router_tc_kernel(const __grid_constant__ Maps maps, int R, int E, int d, int nt,
+                 float *__restrict__ logits, int *flags) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t b_bytes = (uint32_t)nt * 128u;
+    const uint32_t sA = base, sB = base + kStages * kABytes;
+    const uint32_t ctl = sB + kStages * b_bytes;
+    // control block: full[kStages], empty[kStages], tfull, done, tmem slot, abort, ok
+    const uint32_t full = ctl, empty = ctl + 8 * kStages, tfull = ctl + 16 * kStages,
+                   done = tfull + 8;
+    uint8_t *ctl_p = smem_raw + (ctl - raw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl_p + 16 * kStages + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctl_p + 16 * kStages + 20);
+    volatile int *ok_flag = reinterpret_cast<volatile int *>(ctl_p + 16 * kStages + 24);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * nt, e0 = blockIdx.y * kM;
+    const int kc_n = d / kBK;
+    clear_check_word(flags);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        *ok_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&maps.w);
+        prefetch_map(&maps.x);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(nt)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();  // x is written by the previous kernel
+    const uint32_t tmem = *tmem_slot;
+
+    uint32_t issued = 0, last_par = 0;  // producer: stages with a load in flight, parity
+    bool mma_issued = false;
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kc = 0; kc < kc_n; ++kc) {
+                const int s = kc % kStages;
+                const uint32_t ph = (uint32_t)(kc / kStages) & 1u;
+                if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, flags)) break;
+                mbar_expect_tx(full + 8 * s, kABytes + b_bytes);
+                tma_load_2d(sA + s * kABytes, &maps.w, kc * kBK, e0, full + 8 * s);
+                tma_load_2d(sB + s * b_bytes, &maps.x, kc * kBK, r0, full + 8 * s);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kM, (uint32_t)nt);
+            bool ok = true;
+            for (int kc = 0; kc < kc_n; ++kc) {
+                const int s = kc % kStages;
+                if (!mbar_wait(full + 8 * s, (uint32_t)(kc / kStages) & 1u, abort_flag, flags)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = sA + s * kABytes, b = sB + s * b_bytes;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                    mma_bf16(tmem, sw128_desc(a + 32u * k), sw128_desc(b + 32u * k), idesc,
+                             (kc | k) != 0);
+                mma_issued = true;
+                mma_commit(empty + 8 * s);
+            }
+            if (ok) mma_commit(tfull);  // arrives once every MMA above has completed
+        }
+        __syncwarp();
+    }
+    if (threadIdx.x == 32) *ok_flag = mbar_wait(tfull, 0, abort_flag, flags) ? 1 : 0;
+    __syncthreads();
+    const bool ok = *ok_flag != 0;
+    if (!ok && threadIdx.x == 0 && flags) atomicOr(flags, FLAG_WAIT_TIMEOUT);
+    tc_fence_after();
+    const int e = e0 + warp * 32 + lane;
+    for (int c0 = 0; c0 < nt; c0 += 16) {
+        uint32_t v[16];
+        if (ok) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int r = r0 + c0 + c;
+            if (r < R && e < E) logits[(size_t)r * E + e] = ok ? __uint_as_float(v[c]) : NAN;
+        }
+    }
+    // teardown: nothing may be in flight when the CTA frees tensor memory and exits
+    if (!ok) {
+        if (warp == 0 && lane == 0)
+            for (int s = 0; s < kStages; ++s)
+                if (issued & (1u << s))
+                    mbar_wait(full + 8 * s, (last_par >> s) & 1u, nullptr, flags);
+        if (warp == 1 && lane == 0 && mma_issued) {
+            mma_commit(done);  // arrives once every MMA issued has completed
+            mbar_wait(done, 0, nullptr, flags);
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(nt)
+                     : "memory");
+}
+
+}  // namespace rtc
+
+// From this many rows on, bf16 scores go to the tensor cores.
+constexpr int kTcRows = 192;
+
 // Up to this many rows the split-hidden shape is used.
 constexpr int kSplitRows = 1024;
 
 }  // namespace
 
+bool router_tc_ok(const moe_layer_desc &L, int R) {
+    if (L.dtype != MOE_DTYPE_BF16 || L.d % 64 != 0 || R < kTcRows) return false;
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return false;
+    return major >= 10 && tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_router_tc(const moe_layer_desc &L, const void *x, const void *Wr, int R,
+                             float *logits, int *flags, cudaStream_t s) {
+    // 64-row tiles once 32-row tiles would fill more than one wave of 152 SMs
+    const int nt = (R + 31) / 32 > 152 ? 64 : 32;
+    rtc::Maps m{};
+    const uint64_t wd[2] = {(uint64_t)L.d, (uint64_t)L.E}, xd[2] = {(uint64_t)L.d, (uint64_t)R};
+    const uint64_t st[1] = {(uint64_t)L.d * 2};
+    const uint32_t wb[2] = {(uint32_t)rtc::kBK, (uint32_t)rtc::kM};
+    const uint32_t xb[2] = {(uint32_t)rtc::kBK, (uint32_t)nt};
+    if (!tc::encode(&m.w, Wr, 2, wd, st, wb) || !tc::encode(&m.x, x, 2, xd, st, xb))
+        return cudaErrorInvalidValue;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(rtc::router_tc_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)rtc::smem_bytes(64));
+    });
+    if (attr != cudaSuccess) return attr;
+    const dim3 grid((R + nt - 1) / nt, (L.E + rtc::kM - 1) / rtc::kM);
+    return launch_pdl(rtc::router_tc_kernel, grid, dim3(rtc::kThreads), rtc::smem_bytes(nt), s,
+                      m, R, L.E, L.d, nt, logits, flags);
+}
+
 cudaError_t launch_router(const moe_layer_desc &L, const void *x, const void *Wr, int R,
-                          float *logits, cudaStream_t s) {
+                          float *logits, int *flags, cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
+    if (router_tc_ok(L, R)) return launch_router_tc(L, x, Wr, R, logits, flags, s);
     if (R <= kSplitRows) {
         dim3 g((R + kRows - 1) / kRows, (L.E + kExp - 1) / kExp);
         if (L.dtype == MOE_DTYPE_BF16)
             return launch_pdl(router_splitd_kernel<__nv_bfloat16>, g, dim3(kWarps * 32), 0, s,
                               (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E,
-                              logits);
+                              logits, flags);
         return launch_pdl(router_splitd_kernel<float>, g, dim3(kWarps * 32), 0, s,
-                          (const float *)x, (const float *)Wr, R, L.d, L.E, logits);
+                          (const float *)x, (const float *)Wr, R, L.d, L.E, logits, flags);
     }
     dim3 grid((R + kWarps * kRows - 1) / (kWarps * kRows), (L.E + kExp - 1) / kExp);
     if (L.dtype == MOE_DTYPE_BF16)
         return launch_pdl(router_kernel<__nv_bfloat16>, grid, dim3(kWarps * 32), 0, s,
                           (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wr, R, L.d, L.E,
-                          logits);
+                          logits, flags);
     return launch_pdl(router_kernel<float>, grid, dim3(kWarps * 32), 0, s, (const float *)x,
-                      (const float *)Wr, R, L.d, L.E, logits);
+                      (const float *)Wr, R, L.d, L.E, logits, flags);
 }
 
 }  // namespace moe

@@ -97,9 +97,18 @@ def _check_selection(shape, kw, logits, depth, gidx, ggates, gelig, ginfo, N, B)
 
 # ------------------------------------------------------------------- router
 
+ROUTER_E256 = W.LayerShape(d=512, E=256, k=8, f=128, dtype="bf16")
+ROUTER_E64 = W.LayerShape(d=320, E=64, k=4, f=128, dtype="bf16")
+
+
+# R >= 192 (bf16) runs on the tensor cores: 32-row tiles, 64-row tiles past 152 x 32
+# rows, two 128-expert tiles for E = 256, zero-filled router rows for E = 64.
 @pytest.mark.parametrize("shape,R", [(W.TINY, 9), (W.TINY, 1), (W.QWEN3_30B_A3B, 65),
-                                     (W.QWEN3_30B_A3B, 37), (W.QWEN3_30B_A3B, 4160),
-                                     (W.GPT_OSS_120B, 65)])
+                                     (W.QWEN3_30B_A3B, 37), (W.QWEN3_30B_A3B, 191),
+                                     (W.QWEN3_30B_A3B, 192), (W.QWEN3_30B_A3B, 411),
+                                     (W.QWEN3_30B_A3B, 4160), (W.QWEN3_30B_A3B, 9797),
+                                     (W.GPT_OSS_120B, 65), (W.GPT_OSS_120B, 333),
+                                     (ROUTER_E256, 500), (ROUTER_E64, 200)])
 def test_router_logits(shape, R):
     chain = np.arange(-1, R - 1, dtype=np.int32)
     x = W.hidden_states(11 + R, chain, shape.d, shape.torch_dtype)
