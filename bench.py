@@ -145,10 +145,14 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_sha(name="ffn_tc.cu"):
+def kernel_sha(names=("ffn_tc.cu", "tc.cuh")):
+    """sha256 (16 hex digits) of the expert kernel's sources, concatenated in order."""
     import hashlib
-    with open(os.path.join(ROOT, "expert_select_gb300", "csrc", name), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "expert_select_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(mean_union: float):

@@ -14,15 +14,16 @@
 // swizzle atom) loaded by TMA with 128-byte swizzling, which is the layout the
 // tcgen05 shared-memory descriptors describe.
 //
-// Both phases run in one persistent launch, one CTA per SM (192 threads,
+// Both phases run in one persistent launch, one CTA per SM (320 threads,
 // warp-specialised):
 //   warp 0       TMA producer (one lane): takes unit tickets from a global counter
 //                (every phase-1 unit before any phase-2 unit), passes each ticket to
 //                the other roles through a small shared-memory queue, and fills a ring
 //                of `stages` buffers
 //   warp 1       TMEM allocator and MMA issuer (one lane)
-//   warps 2..5   epilogue: tcgen05.ld the accumulator (each warp may read the 32
-//                TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
+//   warps 2..9   epilogue, two teams of four (warps 2-5, 6-9) taking alternate
+//                16-column chunks of the accumulator: tcgen05.ld (each warp may read
+//                the 32 TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
 // Two 256-column accumulators alternate so the epilogue of one unit overlaps the
 // MMAs of the next. A unit is one weight tile x one row tile (<= 256 tokens of one
 // expert). A phase-2 unit needs the whole h of its row tile: the epilogue that
@@ -45,7 +46,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                // two teams of four, one warp per TMEM quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBK = 64;                     // K elements per stage: one 128-B swizzle atom
 constexpr int kM = 128;                     // MMA M: weight rows per unit
 constexpr int kAccCols = 256;               // TMEM columns per accumulator (max N)
@@ -53,6 +55,7 @@ constexpr int kTmemCols = 2 * kAccCols;     // two accumulators
 constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
+constexpr int kSgFloats = 64 * kSgStride;   // one buffer; two per team (double-buffered)
 constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 144 bytes)
 
 struct Maps {
@@ -77,10 +80,15 @@ struct Params {
     float *o;
 };
 
-// Named barrier of the four epilogue warps (bar.sync is warp-aligned: reconverge first).
+// Named barriers (bar.sync is warp-aligned: reconverge first): one per epilogue team of
+// four warps (ids 1, 2), and one over all eight epilogue warps (id 3).
+__device__ __forceinline__ void team_bar(int team) {
+    __syncwarp();
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + team) : "memory");
+}
 __device__ __forceinline__ void epi_bar() {
     __syncwarp();
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 3, %0;" ::"n"(32 * kEpiWarps) : "memory");
 }
 
 // Which token-row box (16 << i rows) holds n tokens.
@@ -149,7 +157,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     volatile int *epi_ok = ints + 2;    // [2]
     volatile int *epi_u = ints + 4;     // [2]
     volatile int *queue = ints + 6;     // [kQ]
-    float *sg = reinterpret_cast<float *>(ctl + kCtlBytes);  // [64][kSgStride]
+    float *sg_all = reinterpret_cast<float *>(ctl + kCtlBytes);  // [team][2][64][kSgStride]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -159,7 +167,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + 8 * a, 1);
-            mbar_init(tempty + 8 * a, 128);
+            mbar_init(tempty + 8 * a, 32 * kEpiWarps);
         }
         mbar_init(done, 1);
         for (int q = 0; q < kQ; ++q) {
@@ -314,8 +322,10 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;          // TMEM lane quadrant of this warp
-        const int row = q * 32 + lane;   // accumulator row
+        const int q = warp & 3;            // TMEM lane quadrant of this warp
+        const int team = (warp - 2) >> 2;  // epilogue team: warps 2-5 or 6-9
+        const int row = q * 32 + lane;     // accumulator row
+        float *sg = sg_all + team * 2 * kSgFloats;
         int it = 0, qs = 0, turn = 0;
         uint32_t qph = 0;
         for (;; turn ^= 1) {
@@ -345,23 +355,30 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (threadIdx.x == 64)
                 epi_ok[acc] = mbar_wait(tfull + 8 * acc, aph, abort_flag, p.flags);
             epi_bar();
-            if (!epi_ok[acc]) break;  // uniform over the four warps
+            if (!epi_ok[acc]) break;  // uniform over the eight warps
             tc_fence_after();
             const int N = (w.ntok + 15) & ~15;
             const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
             const size_t row0 = (size_t)p.offsets[w.e] + w.n0;
+            // the two teams take alternate 16-column chunks of the accumulator
             if (w.phase == 1) {
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                // within a team the gate warps (quadrants 0, 1) hand silu(gate) to the up
+                // warps (quadrants 2, 3) through a double-buffered exchange buffer: one
+                // team barrier per chunk (a buffer is rewritten two chunks later, after
+                // the up warps have passed the barrier in between)
+                int j = 0;
+                for (int c0 = team * 16; c0 < N; c0 += 32, ++j) {
+                    float *buf = sg + (j & 1) * kSgFloats;
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
                     if (q < 2) {
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const float g = __uint_as_float(v[c]);
-                            sg[row * kSgStride + c] = g / (1.f + __expf(-g));
+                            buf[row * kSgStride + c] = __fdividef(g, 1.f + __expf(-g));
                         }
                     }
-                    epi_bar();
+                    team_bar(team);
                     if (q >= 2) {
                         const int i = row - 64;
                         __nv_bfloat16 *hp = p.h + row0 * p.f + (size_t)w.m * 64 + i;
@@ -370,19 +387,19 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                             const int tok = c0 + c;
                             if (tok < w.ntok)
                                 hp[(size_t)tok * p.f] = __float2bfloat16_rn(
-                                    sg[i * kSgStride + c] * __uint_as_float(v[c]));
+                                    buf[i * kSgStride + c] * __uint_as_float(v[c]));
                         }
                     }
-                    epi_bar();
                 }
-                // every h store of this unit precedes the barrier above: publish them
+                // every h store of this unit precedes this barrier: publish them
+                epi_bar();
                 if (threadIdx.x == 64) {
                     __threadfence();
                     atomicAdd(p.sched + 1 + w.rt, 1);
                 }
             } else {
                 const int drow = w.m * kM + row;
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                for (int c0 = team * 16; c0 < N; c0 += 32) {
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
                     if (drow < p.d) {
@@ -467,7 +484,7 @@ int sm_count() {
 
 size_t smem_bytes(int stages, int box_cap) {
     return 1024 + (size_t)stages * (kABytes + (size_t)box_cap * 128) + kCtlBytes +
-           64 * kSgStride * sizeof(float);
+           2 * 2 * kSgFloats * sizeof(float);
 }
 
 }  // namespace
