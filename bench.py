@@ -394,7 +394,8 @@ def run_gpu(args):
     u_o = (cnat.cpu().numpy() > 0).sum(axis=1)
 
     # router, select, permute, combine + the grouped-expert launches
-    launches_per_step = 4 + ffn_launches(M, L, args.ffn_path)
+    # router, select, permute (a second, placing kernel past 2048 assignments), combine
+    launches_per_step = 3 + (2 if N * shape.k > 2048 else 1) + ffn_launches(M, L, args.ffn_path)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -33,6 +33,7 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.offsets = take((E + 1) * 4);
     w.perm = take(A * 4);
     w.pos = take(A * 4);
+    w.rbmask = take((size_t)2 * E * ((R + 31) / 32) * 4);
     w.active = take((E + 1) * 4);
     w.slotmap = take(E * 4);
     w.resident = take(E);
@@ -83,7 +84,8 @@ moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
                        bool after_router, cudaStream_t s) {
     return cuda_status(launch_permute(L, idx, R, counts, offsets, perm, at<int>(ws, w.pos),
                                       at<int>(ws, w.active), at<int>(ws, w.rowtiles),
-                                      at<int>(ws, w.flags), after_router, s));
+                                      at<int>(ws, w.flags), at<uint32_t>(ws, w.rbmask),
+                                      after_router, s));
 }
 
 moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const void *Wu,
@@ -215,7 +217,9 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
     return cuda_status(launch_permute(*L, topk_idx, R, counts, offsets, perm,
                                       at<int>(workspace, w.pos), at<int>(workspace, w.active),
                                       at<int>(workspace, w.rowtiles),
-                                      at<int>(workspace, w.flags), false, (cudaStream_t)stream));
+                                      at<int>(workspace, w.flags),
+                                      at<uint32_t>(workspace, w.rbmask), false,
+                                      (cudaStream_t)stream));
 }
 
 moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void *W_gate,

@@ -35,6 +35,7 @@ struct Workspace {
     size_t offsets;   // i32 [E + 1]
     size_t perm;      // i32 [A]  permuted position -> assignment id
     size_t pos;       // i32 [A]  assignment id -> permuted position (-1 = skipped)
+    size_t rbmask;    // u32 [2][E][ceil(R/32)]  row-block masks and prefixes of the permute
     size_t active;    // i32 [E + 1]  [0] = n_active, then active experts ascending
     size_t slotmap;   // i32 [E]  expert -> slot (offload)
     size_t resident;  // u8  [E]  residency before this call's uploads (offload)
@@ -75,7 +76,7 @@ inline int max_rowtiles(int E, int A) { return E + (A + kMinRowTile - 1) / kMinR
 // word is carried into it when the router ran earlier in the same call (after_router).
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
-                           int *flags, bool after_router, cudaStream_t s);
+                           int *flags, uint32_t *rbmask, bool after_router, cudaStream_t s);
 size_t permute_smem_bytes(int R, int E);
 
 struct FfnArgs {

@@ -6,10 +6,12 @@
 // order. One CTA builds, per block of 32 rows and per expert, the bitmask of rows
 // that chose the expert; a scan over row blocks gives each (block, expert) its
 // prefix; an assignment's position is then
-//   offsets[e] + prefix[block][e] + popc(mask[block][e] & lanes_below(row)).
-// Everything stays in shared memory: (R/32) x E x 8 bytes (133 KB at 4160 rows and
-// 128 experts). The same kernel also writes the active-expert list and the list of
-// row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels walk.
+//   offsets[e] + prefix[e][block] + popc(mask[e][block] & lanes_below(row)).
+// The masks and prefixes live in shared memory: (R/32) x E x 8 bytes (133 KB at 4160
+// rows and 128 experts). The same kernel also writes the active-expert list and the list
+// of row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels
+// walk. Past 2048 assignments it leaves the masks and prefixes in the workspace and a
+// second, many-CTA kernel places the assignments.
 #include "common.cuh"
 
 namespace moe {
@@ -17,16 +19,16 @@ namespace {
 
 constexpr int kThreads = 1024;
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
                int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags,
-               int rt_size, int after_router) {
+               uint32_t *__restrict__ gmask, int rt_size, int after_router) {
     pdl_wait();
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
-    uint32_t *mask = sm;                  // [nb][E]
-    uint32_t *pre = sm + (size_t)nb * E;  // [nb][E]
+    uint32_t *mask = sm;                  // [E][nb]
+    uint32_t *pre = sm + (size_t)nb * E;  // [E][nb]
     int *cnt = (int *)(pre + (size_t)nb * E);
     int *off = cnt + E;                   // [E + 1]
     const int tid = threadIdx.x;
@@ -40,20 +42,47 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         flags[tid] = 0;
     }
     __syncthreads();
-    for (int a = tid; a < A; a += kThreads) {
-        const int e = idx[a];
-        if (e < 0 || e >= E) continue;
-        const int r = a / k;
-        atomicOr(&mask[(r >> 5) * E + e], 1u << (r & 31));
+    // four loads in flight per thread before their atomics
+    for (int a0 = tid; a0 < A; a0 += 4 * kThreads) {
+        int ev[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ev[u] = a0 + u * kThreads < A ? idx[a0 + u * kThreads] : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = ev[u];
+            if (e < 0 || e >= E) continue;
+            const int r = (a0 + u * kThreads) / k;
+            atomicOr(&mask[e * nb + (r >> 5)], 1u << (r & 31));
+        }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        int run = 0;
-        for (int b = 0; b < nb; ++b) {
-            pre[b * E + e] = run;
-            run += __popc(mask[b * E + e]);
+    if (nb <= 8) {  // few row blocks: a thread per expert
+        for (int e = tid; e < E; e += kThreads) {
+            int run = 0;
+            for (int b = 0; b < nb; ++b) {
+                pre[e * nb + b] = run;
+                run += __popc(mask[e * nb + b]);
+            }
+            cnt[e] = run;
         }
-        cnt[e] = run;
+    } else {  // per expert, a warp scans the row blocks' counts (exclusive prefix over blocks)
+        const int lane = tid & 31;
+        for (int e = tid >> 5; e < E; e += kThreads / 32) {
+            int run = 0;
+            for (int b0 = 0; b0 < nb; b0 += 32) {
+                const int b = b0 + lane;
+                const int c = b < nb ? __popc(mask[e * nb + b]) : 0;
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                if (b < nb) pre[e * nb + b] = run + incl - c;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) cnt[e] = run;
+        }
     }
     __syncthreads();
     if (tid < 32) {
@@ -110,24 +139,62 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         offsets[e] = off[e];
         if (e < E) counts[e] = cnt[e];
     }
+    if (gmask) {  // large blocks: permute_scatter_kernel places the assignments
+        for (int i = tid; i < 2 * nb * E; i += kThreads) gmask[i] = sm[i];
+        return;
+    }
+    // a thread per assignment; a repeated expert keeps its first slot
     for (int a = tid; a < A; a += kThreads) {
         const int e = idx[a];
         const int r = a / k, j = a - r * k;
         bool ok = e >= 0 && e < E;
-        for (int q = 0; ok && q < j; ++q) ok = idx[r * k + q] != e;  // first slot wins
+        for (int q = 0; ok && q < j; ++q) ok = idx[r * k + q] != e;
         if (!ok) {
             pos[a] = -1;
             atomicOr(flags, FLAG_BAD_EXPERT);
             continue;
         }
         const int b = r >> 5;
-        const int p = off[e] + (int)pre[b * E + e] +
-                      __popc(mask[b * E + e] & ((1u << (r & 31)) - 1u));
+        const int p = off[e] + (int)pre[e * nb + b] +
+                      __popc(mask[e * nb + b] & ((1u << (r & 31)) - 1u));
         perm[p] = a;
         pos[a] = p;
     }
     for (int p = off[E] + tid; p < A; p += kThreads) perm[p] = -1;
 }
+
+// Places the assignments of a large block from the row-block masks and prefixes the
+// permute kernel left in `gmask` ([E][nb] masks, then [E][nb] prefixes): a thread per
+// assignment, spread over many CTAs (one CTA's stores would bound the whole step).
+__global__ void __launch_bounds__(256)
+permute_scatter_kernel(const int *__restrict__ idx, int R, int k, int E,
+                       const int *__restrict__ offsets, const uint32_t *__restrict__ gmask,
+                       int *__restrict__ perm, int *__restrict__ pos, int *__restrict__ flags) {
+    pdl_wait();
+    const int nb = (R + 31) >> 5;
+    const int A = R * k;
+    const int a = blockIdx.x * blockDim.x + threadIdx.x;
+    if (a >= A) return;
+    const int total = offsets[E];
+    if (a >= total) perm[a] = -1;  // positions past the placed assignments
+    const int e = idx[a];
+    const int r = a / k, j = a - r * k;
+    bool ok = e >= 0 && e < E;
+    for (int q = 0; ok && q < j; ++q) ok = idx[r * k + q] != e;  // first slot wins
+    if (!ok) {
+        pos[a] = -1;
+        atomicOr(flags, FLAG_BAD_EXPERT);
+        return;
+    }
+    const int b = r >> 5;
+    const int p = offsets[e] + (int)gmask[(size_t)nb * E + e * nb + b] +
+                  __popc(gmask[e * nb + b] & ((1u << (r & 31)) - 1u));
+    perm[p] = a;
+    pos[a] = p;
+}
+
+// Up to this many assignments one CTA also places them.
+constexpr int kOneCtaAssignments = 2048;
 
 }  // namespace
 
@@ -138,14 +205,19 @@ size_t permute_smem_bytes(int R, int E) {
 
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
-                           int *flags, bool after_router, cudaStream_t s) {
+                           int *flags, uint32_t *rbmask, bool after_router, cudaStream_t s) {
     const size_t smem = permute_smem_bytes(R, L.E);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
-                      offsets, perm, pos, active, rowtiles, flags, rowtile_size(R),
-                      after_router ? 1 : 0);
+    const int A = R * L.k;
+    uint32_t *gm = A > kOneCtaAssignments ? rbmask : nullptr;
+    err = launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
+                     offsets, perm, pos, active, rowtiles, flags, gm, rowtile_size(R),
+                     after_router ? 1 : 0);
+    if (err != cudaSuccess || !gm) return err;
+    return launch_pdl(permute_scatter_kernel, dim3((A + 255) / 256), dim3(256), 0, s, idx, R,
+                      L.k, L.E, (const int *)offsets, (const uint32_t *)gm, perm, pos, flags);
 }
 
 }  // namespace moe

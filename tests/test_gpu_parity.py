@@ -288,6 +288,45 @@ def test_permute_flags_bad_and_duplicate_ids():
     assert M.moe_workspace_check(ws) == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("R,k", [(1000, 4), (4160, 8), (700, 3)])
+def test_permute_large_blocks_with_bad_and_repeated_ids(R, k):
+    """Blocks past 2048 assignments place a row's choices from one thread; a repeated
+    expert keeps its first slot and ids outside [0, E) are dropped, as in small blocks.
+    Expected: the valid first-occurrence assignments sorted by (expert, row, slot)."""
+    E = 64
+    shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
+    L = _desc(shape)
+    idx = W.random_assignments(900 + R, R, E, k, 0.5)
+    rng = np.random.default_rng(R)
+    for r in rng.choice(R, 40, replace=False):
+        idx[r, k - 1] = idx[r, 0]            # a repeated expert
+    for r in rng.choice(R, 40, replace=False):
+        idx[r, int(rng.integers(0, k))] = int(rng.choice([-3, E, E + 7]))
+    keep = []
+    for r in range(R):
+        seen = set()
+        for j in range(k):
+            e = int(idx[r, j])
+            if 0 <= e < E and e not in seen:
+                keep.append((e, r, j))
+            seen.add(e)
+    keep.sort()
+    cnt = torch.empty(E, dtype=torch.int32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(R * k, dtype=torch.int32, device=DEV)
+    ws = M.workspace(L, 1, R)
+    M.moe_expert_permute(L, torch.from_numpy(idx).to(DEV), cnt, off, perm, ws)
+    _sync()
+    ref_perm = [r * k + j for _, r, j in keep]
+    got = perm.cpu().numpy()
+    assert got[:len(ref_perm)].tolist() == ref_perm
+    assert (got[len(ref_perm):] == -1).all()
+    ref_cnt = np.bincount([e for e, _, _ in keep], minlength=E)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+    np.testing.assert_array_equal(off.cpu().numpy(), np.concatenate([[0], np.cumsum(ref_cnt)]))
+    assert M.moe_workspace_check(ws) & 1
+
+
 # ------------------------------------------------------------- expert math
 
 def _weights(shape, seed, device=DEV, E=None):
