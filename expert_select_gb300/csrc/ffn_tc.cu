@@ -24,8 +24,10 @@
 //   warps 2..9   epilogue, two teams of four (warps 2-5, 6-9) taking alternate
 //                16-column chunks of the accumulator: tcgen05.ld (each warp may read
 //                the 32 TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
-// Two 256-column accumulators alternate so the epilogue of one unit overlaps the
-// MMAs of the next. A unit is one weight tile x one row tile (<= 256 tokens of one
+// At the start the epilogue warps copy the row-tile list (expert, first permuted row,
+// tokens, slot) into shared memory, so looking up a unit between two units costs no
+// global round trip. Two 256-column accumulators alternate so the epilogue of one unit
+// overlaps the MMAs of the next. A unit is one weight tile x one row tile (<= 256 tokens of one
 // expert). A phase-2 unit needs the whole h of its row tile: the epilogue that
 // finishes a phase-1 unit publishes it with a release increment of the row tile's
 // counter, and the producer of a phase-2 unit waits for the count with acquire loads
@@ -56,7 +58,7 @@ constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
 constexpr int kSgFloats = 64 * kSgStride;   // one buffer; two per team (double-buffered)
-constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 144 bytes)
+constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 152 bytes)
 
 struct Maps {
     CUtensorMap wg;           // W_gate [S][f][d], box 64 x 64 x 1
@@ -70,6 +72,7 @@ struct Params {
     int d, f;
     int mt1, mt2;  // weight tiles per expert: f / 64 (phase 1), ceil(d / 128) (phase 2)
     int stages;
+    int tbl_cap;   // row tiles described in the shared-memory table (the rest: global reads)
     int box_cap;   // rows of the per-stage token buffer
     int slots;     // expert slots in the weight pool
     const int *rowtiles, *offsets, *slot;
@@ -105,13 +108,30 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 }
 
 struct Unit {
-    int phase, rt, m, e, n0, ntok, slot;
+    int phase, rt, m, e, row0, ntok, slot;  // row0: the row tile's first permuted row
 };
 
-// Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2.
+// Row tile rt -> {expert, first permuted row, tokens, code}; code is the expert's slot, -1
+// for an expert outside this launch's expert pass, -2 for a slot outside the pool.
+__device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
+    const int *t = p.rowtiles + 1 + 4 * rt;
+    const int e = t[0], n0 = t[1], ntok = t[2];
+    int code;
+    if (p.pass && !p.pass[e]) {
+        code = -1;
+    } else {
+        const int sl = p.slot ? p.slot[e] : e;
+        code = (sl >= 0 && sl < p.slots && ntok > 0) ? sl : -2;
+    }
+    return make_int4(e, p.offsets[e] + n0, ntok, code);
+}
+
+// Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2. The
+// row tile's entry comes from the shared-memory table when it holds it (tbl != nullptr).
 // Returns 0 for a unit to compute, 1 for one outside this launch's expert pass, 2 for an
 // expert whose slot is outside the pool (skipped and flagged).
-__device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w) {
+__device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w,
+                                      const int4 *tbl) {
     if (u < U1) {
         w.phase = 1;
         w.rt = u / p.mt1;
@@ -122,13 +142,12 @@ __device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w) {
         w.rt = v / p.mt2;
         w.m = v - w.rt * p.mt2;
     }
-    const int *t = p.rowtiles + 1 + 4 * w.rt;
-    w.e = t[0];
-    w.n0 = t[1];
-    w.ntok = t[2];
-    if (p.pass && !p.pass[w.e]) return 1;
-    w.slot = p.slot ? p.slot[w.e] : w.e;
-    return (w.slot >= 0 && w.slot < p.slots && w.ntok > 0) ? 0 : 2;
+    const int4 t = (tbl && w.rt < p.tbl_cap) ? tbl[w.rt] : row_tile(p, w.rt);
+    w.e = t.x;
+    w.row0 = t.y;
+    w.ntok = t.z;
+    w.slot = t.w;
+    return t.w >= 0 ? 0 : (t.w == -1 ? 1 : 2);
 }
 
 constexpr int kQ = 4;  // ticket queue depth
@@ -157,7 +176,9 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     volatile int *epi_ok = ints + 2;    // [2]
     volatile int *epi_u = ints + 4;     // [2]
     volatile int *queue = ints + 6;     // [kQ]
+    const uint32_t tbl_bar = ctl_s + 16 * S + 144;  // the row-tile table is filled
     float *sg_all = reinterpret_cast<float *>(ctl + kCtlBytes);  // [team][2][64][kSgStride]
+    int4 *tbl = reinterpret_cast<int4 *>(sg_all + 2 * 2 * kSgFloats);  // [tbl_cap]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -170,6 +191,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             mbar_init(tempty + 8 * a, 32 * kEpiWarps);
         }
         mbar_init(done, 1);
+        mbar_init(tbl_bar, 32 * kEpiWarps);
         for (int q = 0; q < kQ; ++q) {
             mbar_init(qfull + 8 * q, 1);
             mbar_init(qempty + 8 * q, 2);  // the MMA lane and one epilogue thread
@@ -199,6 +221,13 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     const uint32_t tmem = *tmem_slot;
     const int n_rt = p.rowtiles[0];
     const int U1 = n_rt * p.mt1, U = U1 + n_rt * p.mt2;
+    // the epilogue warps copy the row-tile list into shared memory (expert, first row,
+    // tokens, slot), so that a unit's lookup costs no global round trips
+    if (warp >= 2) {
+        for (int rt = threadIdx.x - 64; rt < min(n_rt, p.tbl_cap); rt += 32 * kEpiWarps)
+            tbl[rt] = row_tile(p, rt);
+        mbar_arrive(tbl_bar);
+    }
 
     uint32_t issued = 0, last_par = 0;  // producer: stages with a load issued, parity of it
     bool mma_issued = false;
@@ -208,7 +237,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const uint64_t pol = evict_first_policy();
             int s = 0, qs = 0;
             uint32_t ph = 0, qph = 0;
-            bool ok = true;
+            bool ok = mbar_wait(tbl_bar, 0, abort_flag, p.flags);
             while (ok) {
                 int u = atomicAdd(p.sched, 1);
                 if (u >= U) u = -1;
@@ -221,7 +250,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                const int dc = decode(p, U1, u, w);
+                const int dc = decode(p, U1, u, w, tbl);
                 if (dc != 0) {
                     if (dc == 2) atomicOr(p.flags, FLAG_BAD_EXPERT);
                     continue;
@@ -246,7 +275,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 const int bxi = box_of((w.ntok + 15) & ~15);
                 const uint32_t bb = (uint32_t)(16 << bxi) * 128u;
-                const int brow = p.offsets[w.e] + w.n0;
+                const int brow = w.row0;
                 const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
                 const CUtensorMap *bmap = w.phase == 1 ? &maps.bx[bxi] : &maps.bh[bxi];
                 for (int kc = 0; kc < kchunks; ++kc) {
@@ -279,7 +308,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (lane == 0) {
             int s = 0, it = 0, qs = 0;
             uint32_t ph = 0, qph = 0;
-            bool ok = true;
+            bool ok = mbar_wait(tbl_bar, 0, abort_flag, p.flags);
             while (ok) {
                 if (!mbar_wait(qfull + 8 * qs, qph, abort_flag, p.flags)) break;
                 const int u = queue[qs];
@@ -290,7 +319,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                if (decode(p, U1, u, w) != 0) continue;
+                if (decode(p, U1, u, w, tbl) != 0) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -348,7 +377,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int u = epi_u[turn];
             if (u < 0) break;
             Unit w;
-            if (decode(p, U1, u, w) != 0) continue;
+            if (decode(p, U1, u, w, tbl) != 0) continue;
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             ++it;
@@ -359,7 +388,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             tc_fence_after();
             const int N = (w.ntok + 15) & ~15;
             const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
-            const size_t row0 = (size_t)p.offsets[w.e] + w.n0;
+            const size_t row0 = (size_t)w.row0;
             // the two teams take alternate 16-column chunks of the accumulator
             if (w.phase == 1) {
                 // within a team the gate warps (quadrants 0, 1) hand silu(gate) to the up
@@ -482,9 +511,9 @@ int sm_count() {
     return n;
 }
 
-size_t smem_bytes(int stages, int box_cap) {
+size_t smem_bytes(int stages, int box_cap, int tbl_cap) {
     return 1024 + (size_t)stages * (kABytes + (size_t)box_cap * 128) + kCtlBytes +
-           2 * 2 * kSgFloats * sizeof(float);
+           2 * 2 * kSgFloats * sizeof(float) + (size_t)tbl_cap * sizeof(int4);
 }
 
 }  // namespace
@@ -509,8 +538,12 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     while (box_cap < need) box_cap <<= 1;
     const size_t budget = 227 * 1024;
     int stages = 12;
-    while (stages > 2 && smem_bytes(stages, box_cap) > budget) --stages;
-    const size_t smem = smem_bytes(stages, box_cap);
+    while (stages > 2 && smem_bytes(stages, box_cap, 0) > budget) --stages;
+    // the row-tile table takes what the stages leave; row tiles past it are read from
+    // global memory
+    const int tbl_cap = (int)std::min<size_t>((size_t)max_rowtiles(a.E, A),
+                                              (budget - smem_bytes(stages, box_cap, 0)) / 16);
+    const size_t smem = smem_bytes(stages, box_cap, tbl_cap);
     const int S = a.slots;
 
     Maps m{};
@@ -539,6 +572,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.mt1 = a.f / 64;
     p.mt2 = (a.d + kM - 1) / kM;
     p.stages = stages;
+    p.tbl_cap = tbl_cap;
     p.box_cap = box_cap;
     p.slots = S;
     p.rowtiles = a.rowtiles;
