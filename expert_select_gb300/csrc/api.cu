@@ -283,7 +283,8 @@ moe_status moe_workspace_check(void *workspace, int *flags, moe_stream_t stream)
     cudaStream_t s = (cudaStream_t)stream;
     int v = 0;
     if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess || cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
+        cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess)
         return MOE_ERR_CUDA;
     *flags = v;
     return v ? MOE_ERR_DEVICE_CHECK : MOE_OK;

@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kThreads) ffn_down_simt(FfnArgs a) {
 cudaError_t launch_ffn_simt(const FfnArgs &a, cudaStream_t s) {
     const size_t smem_gu = (size_t)kTok * a.d * sizeof(float);
     const size_t smem_dn = (size_t)kTok * a.f * sizeof(float);
-    dim3 g1(a.E, (a.f + kRowsPerCta - 1) / kRowsPerCta), g2(a.E, (a.d + kRowsPerCta - 1) / kRowsPerCta);
+    dim3 g1(a.E, (a.f + kRowsPerCta - 1) / kRowsPerCta);
+    dim3 g2(a.E, (a.d + kRowsPerCta - 1) / kRowsPerCta);
     cudaError_t err;
     if (a.dtype == MOE_DTYPE_BF16) {
         err = cudaFuncSetAttribute(ffn_gateup_simt<__nv_bfloat16>,

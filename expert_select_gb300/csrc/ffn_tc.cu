@@ -27,13 +27,13 @@
 // At the start the epilogue warps copy the row-tile list (expert, first permuted row,
 // tokens, slot) into shared memory, so looking up a unit between two units costs no
 // global round trip. Two 256-column accumulators alternate so the epilogue of one unit
-// overlaps the MMAs of the next. A unit is one weight tile x one row tile (<= 256 tokens of one
-// expert). A phase-2 unit needs the whole h of its row tile: the epilogue that
-// finishes a phase-1 unit publishes it with a release increment of the row tile's
+// overlaps the MMAs of the next. A unit is one weight tile x one row tile (<= 256
+// tokens of one expert). A phase-2 unit needs the whole h of its row tile: the epilogue
+// that finishes a phase-1 unit publishes it with a release increment of the row tile's
 // counter, and the producer of a phase-2 unit waits for the count with acquire loads
 // before its TMA reads h. Tickets are handed out in order, so every phase-1 unit is
-// owned by a running CTA before any CTA waits on one: no deadlock even when fewer
-// CTAs than SMs are resident.
+// owned by a running CTA before any CTA waits on one: no deadlock even when fewer CTAs
+// than SMs are resident.
 //
 // Every wait is bounded: after 2 s a wait gives up, sets the workspace check bit
 // FLAG_WAIT_TIMEOUT and makes the CTA stop; the CTA then waits (again bounded) for
