@@ -14,6 +14,9 @@
  *     node inside the eligible set.
  *   - same article, section 03 and the abstract: expert offload with 48 expert
  *     slots per layer and host-to-device uploads of non-resident experts.
+ *   - "Fewer experts, faster decoding: cost-aware speculative decoding for MoE"
+ *     (EcoSpec), section 1 and Fig. 2-3, with the scoring rule of the blog above:
+ *     a cost-aware choice of which drafted nodes to verify (moe_draft_select).
  *
  * Conventions shared by every entry point:
  *   - All tensors are plain pointers, row-major, densely packed. "device" means
@@ -138,7 +141,9 @@ size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N);
 
 /* Router scores ("MoE and speculative decoding" blog, "starting from one MoE layer",
  * the W_r x inside E(x) = TopR(softmax(W_r x))): logits[r, e] = sum_i x[r, i] W_r[e, i],
- * fp32 accumulation, no bias.
+ * fp32 accumulation, no bias. From 192 rows on (bf16, d a multiple of 64, sm_100 or
+ * later) the product runs on the tensor cores; the accumulation order then differs
+ * from the CUDA-core kernel's at the level of fp32 rounding.
  *   x [R, d] and W_r [E, d] device, layer dtype; logits [R, E] device fp32. */
 moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void *W_r, int R,
                              float *logits, moe_stream_t stream);

@@ -190,7 +190,7 @@ def test_selection_large_tree_single_cta_path():
 
 
 @pytest.mark.parametrize("B,N,E,k", [(1, 411, 128, 8), (3, 1000, 64, 4), (2, 3000, 256, 16),
-                                     (64, 65, 128, 8)])
+                                     (64, 65, 128, 8), (1, 1, 40, 3), (5, 129, 40, 1)])
 def test_selection_natural_any_tree_size(B, N, E, k):
     """Natural routing runs one cluster per tree with a warp per node, for any N."""
     shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
@@ -253,7 +253,8 @@ def test_worked_examples_through_device():
 
 @pytest.mark.parametrize("R,E,k,skew", [(1, 16, 2, 0.0), (9, 16, 2, 0.0), (65, 128, 8, 0.0),
                                         (65, 128, 8, 1.5), (520, 128, 4, 1.0),
-                                        (4160, 128, 8, 0.8), (33, 256, 16, 0.5)])
+                                        (4160, 128, 8, 0.8), (33, 256, 16, 0.5),
+                                        (200, 256, 16, 0.7), (7000, 128, 8, 0.3)])
 def test_permute_bit_exact(R, E, k, skew):
     shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
     L = _desc(shape)
