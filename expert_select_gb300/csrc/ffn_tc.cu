@@ -55,7 +55,7 @@ constexpr int kM = 128;                     // MMA M: weight rows per unit
 constexpr int kAccCols = 256;               // TMEM columns per accumulator (max N)
 constexpr int kTmemCols = 2 * kAccCols;     // two accumulators
 constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
-constexpr int kBoxes = 5;                   // token-row boxes of 16, 32, 64, 128, 256 rows
+constexpr int kBoxes = 16;                  // token-row boxes of 16, 32, 48, ..., 256 rows
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
 constexpr int kSgFloats = 64 * kSgStride;   // one buffer; two per team (double-buffered)
 constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 152 bytes)
@@ -64,8 +64,8 @@ struct Maps {
     CUtensorMap wg;           // W_gate [S][f][d], box 64 x 64 x 1
     CUtensorMap wu;           // W_up   [S][f][d], box 64 x 64 x 1
     CUtensorMap wd;           // W_down [S][d][f], box 64 x 128 x 1
-    CUtensorMap bx[kBoxes];   // gathered token rows x [A][d], box 64 x (16 << i)
-    CUtensorMap bh[kBoxes];   // activations h [A][f], box 64 x (16 << i)
+    CUtensorMap bx[kBoxes];   // gathered token rows x [A][d], box 64 x 16 (i + 1)
+    CUtensorMap bh[kBoxes];   // activations h [A][f], box 64 x 16 (i + 1)
 };
 
 struct Params {
@@ -92,13 +92,6 @@ __device__ __forceinline__ void team_bar(int team) {
 __device__ __forceinline__ void epi_bar() {
     __syncwarp();
     asm volatile("bar.sync 3, %0;" ::"n"(32 * kEpiWarps) : "memory");
-}
-
-// Which token-row box (16 << i rows) holds n tokens.
-__device__ __forceinline__ int box_of(int n) {
-    int i = 0;
-    while ((16 << i) < n && i < kBoxes - 1) ++i;
-    return i;
 }
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -273,8 +266,9 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     if (!ok) break;
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
-                const int bxi = box_of((w.ntok + 15) & ~15);
-                const uint32_t bb = (uint32_t)(16 << bxi) * 128u;
+                // one box of exactly the row tile's tokens rounded up to 16 rows
+                const int bxi = ((w.ntok + 15) >> 4) - 1;
+                const uint32_t bb = (uint32_t)(bxi + 1) * 16u * 128u;
                 const int brow = w.row0;
                 const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
                 const CUtensorMap *bmap = w.phase == 1 ? &maps.bx[bxi] : &maps.bh[bxi];
@@ -493,12 +487,13 @@ bool encode_weights(CUtensorMap *m, const void *w, int S, int rows, int K, int b
     return encode(m, w, 3, dims, st, box);
 }
 
-// Token rows [A][K] as 2-D maps with 64 x (16 << i) boxes.
-bool encode_rows(CUtensorMap *maps, const void *t, int A, int K) {
-    for (int i = 0; i < kBoxes; ++i) {
+// Token rows [A][K] as 2-D maps with 64 x 16 (i + 1) boxes, for the row-tile heights up to
+// `cap` rows that a launch can meet.
+bool encode_rows(CUtensorMap *maps, const void *t, int A, int K, int cap) {
+    for (int i = 0; i < kBoxes && 16 * i < cap; ++i) {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)A};
         const uint64_t st[1] = {(uint64_t)K * 2};
-        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(16 << i)};
+        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(16 * (i + 1))};
         if (!encode(&maps[i], t, 2, dims, st, box)) return false;
     }
     return true;
@@ -531,11 +526,9 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const int A = a.R * a.k;
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorInvalidDevice;
-    // token-row buffer per stage: the box that holds a full row tile, or R rows if fewer
-    // (a row picks an expert at most once, so no expert has more than R tokens)
-    int box_cap = 16;
-    const int need = ((std::min(a.R, rowtile_size(a.R)) + 15) / 16) * 16;
-    while (box_cap < need) box_cap <<= 1;
+    // token-row buffer per stage: a full row tile, or R rows if fewer (a row picks an
+    // expert at most once, so no expert has more than R tokens), rounded up to 16
+    const int box_cap = ((std::min(a.R, rowtile_size(a.R)) + 15) / 16) * 16;
     const size_t budget = 227 * 1024;
     int stages = 12;
     while (stages > 2 && smem_bytes(stages, box_cap, 0) > budget) --stages;
@@ -549,8 +542,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     Maps m{};
     if (!encode_weights(&m.wg, a.Wg, S, a.f, a.d, 64) ||
         !encode_weights(&m.wu, a.Wu, S, a.f, a.d, 64) ||
-        !encode_weights(&m.wd, a.Wd, S, a.d, a.f, kM) || !encode_rows(m.bx, a.xp, A, a.d) ||
-        !encode_rows(m.bh, a.h, A, a.f))
+        !encode_weights(&m.wd, a.Wd, S, a.d, a.f, kM) ||
+        !encode_rows(m.bx, a.xp, A, a.d, box_cap) || !encode_rows(m.bh, a.h, A, a.f, box_cap))
         return cudaErrorInvalidValue;
 
     static std::once_flag attr_once;
