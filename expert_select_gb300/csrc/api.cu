@@ -38,7 +38,7 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.slotmap = take(E * 4);
     w.resident = take(E);
     w.pass = take(E);
-    w.rowtiles = take((size_t)(1 + 4 * max_rowtiles(L.E, (int)A)) * 4);
+    w.rowtiles = take((size_t)(kRowTileHeader + 4 * max_rowtiles(L.E, (int)A)) * 4);
     w.sched = take((size_t)(1 + max_rowtiles(L.E, (int)A)) * 4);
     w.xp = take(A * L.d * elem_size(L.dtype));
     w.h = take(A * L.f * 4);

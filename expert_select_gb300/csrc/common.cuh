@@ -40,7 +40,8 @@ struct Workspace {
     size_t slotmap;   // i32 [E]  expert -> slot (offload)
     size_t resident;  // u8  [E]  residency before this call's uploads (offload)
     size_t pass;      // u8  [E]  experts computed by the current expert pass (offload)
-    size_t rowtiles;  // i32 [1 + 4 * max_rowtiles]: count, then (expert, first token, tokens, 0)
+    size_t rowtiles;  // i32 [4 + 4 * max_rowtiles]: count, tile height, 0, 0, then
+                      // (expert, first token, tokens, 0) per tile
     size_t sched;     // i32 [1 + max_rowtiles]: ticket counter, finished phase-1 units per row tile
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
     size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)
@@ -64,16 +65,18 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, cudaStream_t s);
 
-// Token rows per row tile of the tensor-core expert kernel (its MMA N is at most 256).
-// Small blocks use 64-row tiles: no expert then needs more than a 64-row token buffer
-// per pipeline stage, which leaves shared memory for more stages of weight bytes in
-// flight; an expert with more tokens than that takes a second row tile.
-constexpr int kMinRowTile = 64;
-inline int rowtile_size(int R) { return R <= 128 ? 64 : 256; }
-inline int max_rowtiles(int E, int A) { return E + (A + kMinRowTile - 1) / kMinRowTile + 1; }
+// Row tiles of the tensor-core expert kernel: at most kMaxRowTile tokens of one expert
+// (its MMA N is at most 256). The permute kernel picks the height as the largest expert's
+// token count rounded up to 16, capped at kMaxRowTile, so an expert takes one tile unless
+// it has more tokens than that (at most E + A / kMaxRowTile tiles), and the expert kernel
+// sizes its per-stage token buffer to the height: small blocks leave shared memory for
+// more stages of weight bytes in flight.
+constexpr int kMaxRowTile = 256;
+constexpr int kRowTileHeader = 4;  // count, height, two unused ints
+inline int max_rowtiles(int E, int A) { return E + (A + kMaxRowTile - 1) / kMaxRowTile + 1; }
 
-// Row tiles of rowtile_size(R). The kernel starts the call's check word: the router's
-// word is carried into it when the router ran earlier in the same call (after_router).
+// The kernel starts the call's check word: the router's word is carried into it when the
+// router ran earlier in the same call (after_router).
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
                            int *flags, uint32_t *rbmask, bool after_router, cudaStream_t s);

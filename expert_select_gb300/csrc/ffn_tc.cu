@@ -58,7 +58,8 @@ constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 16;                  // token-row boxes of 16, 32, 48, ..., 256 rows
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
 constexpr int kSgFloats = 64 * kSgStride;   // one buffer; two per team (double-buffered)
-constexpr int kCtlBytes = 512;               // barriers and slots (16 * stages + 152 bytes)
+constexpr int kMaxStages = 12;              // pipeline stages at most
+constexpr int kCtlBytes = 512;              // barriers and slots (16 * kMaxStages + 152 bytes)
 
 struct Maps {
     CUtensorMap wg;           // W_gate [S][f][d], box 64 x 64 x 1
@@ -71,9 +72,8 @@ struct Maps {
 struct Params {
     int d, f;
     int mt1, mt2;  // weight tiles per expert: f / 64 (phase 1), ceil(d / 128) (phase 2)
-    int stages;
+    int smem;      // dynamic shared memory of the launch (bytes)
     int tbl_cap;   // row tiles described in the shared-memory table (the rest: global reads)
-    int box_cap;   // rows of the per-stage token buffer
     int slots;     // expert slots in the weight pool
     const int *rowtiles, *offsets, *slot;
     const uint8_t *pass;  // experts computed by this launch (null: all)
@@ -107,7 +107,7 @@ struct Unit {
 // Row tile rt -> {expert, first permuted row, tokens, code}; code is the expert's slot, -1
 // for an expert outside this launch's expert pass, -2 for a slot outside the pool.
 __device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
-    const int *t = p.rowtiles + 1 + 4 * rt;
+    const int *t = p.rowtiles + kRowTileHeader + 4 * rt;
     const int e = t[0], n0 = t[1], ntok = t[2];
     int code;
     if (p.pass && !p.pass[e]) {
@@ -153,29 +153,29 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const int S = p.stages;
-    const uint32_t b_bytes = (uint32_t)p.box_cap * 128u;
-    const uint32_t sA = base, sB = base + (uint32_t)S * kABytes;
-    uint8_t *ctl = gbase + (size_t)S * (kABytes + b_bytes);
-    const uint32_t ctl_s = base + (uint32_t)S * (kABytes + b_bytes);
-    // control block: full[S], empty[S], tfull[2], tempty[2], done, qfull[kQ], qempty[kQ],
-    // then tmem slot, abort, epilogue verdict[2], epilogue ticket[2], ticket queue[kQ]
-    const uint32_t full = ctl_s, empty = ctl_s + 8 * S, tfull = ctl_s + 16 * S,
+    // layout: control block, exchange buffers, row-tile table, then the ring of stages
+    // (sized after the previous kernel has finished, from the row-tile height)
+    uint8_t *ctl = gbase;
+    const uint32_t ctl_s = base;
+    // control block: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], done,
+    // qfull[kQ], qempty[kQ], then tmem slot, abort, epilogue verdict[2], epilogue
+    // ticket[2], ticket queue[kQ], then the table barrier
+    const uint32_t full = ctl_s, empty = ctl_s + 8 * kMaxStages, tfull = ctl_s + 16 * kMaxStages,
                    tempty = tfull + 16, done = tempty + 16, qfull = done + 8,
                    qempty = qfull + 8 * kQ;
-    int *ints = reinterpret_cast<int *>(ctl + 16 * S + 40 + 16 * kQ);
+    int *ints = reinterpret_cast<int *>(ctl + 16 * kMaxStages + 40 + 16 * kQ);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ints);
     volatile int *abort_flag = ints + 1;
     volatile int *epi_ok = ints + 2;    // [2]
     volatile int *epi_u = ints + 4;     // [2]
     volatile int *queue = ints + 6;     // [kQ]
-    const uint32_t tbl_bar = ctl_s + 16 * S + 144;  // the row-tile table is filled
+    const uint32_t tbl_bar = ctl_s + 16 * kMaxStages + 144;  // the row-tile table is filled
     float *sg_all = reinterpret_cast<float *>(ctl + kCtlBytes);  // [team][2][64][kSgStride]
     int4 *tbl = reinterpret_cast<int4 *>(sg_all + 2 * 2 * kSgFloats);  // [tbl_cap]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
         }
@@ -213,6 +213,14 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     pdl_wait();
     const uint32_t tmem = *tmem_slot;
     const int n_rt = p.rowtiles[0];
+    // the ring: as many stages as fit of 16 KB weights + a token buffer of the row-tile
+    // height (every row tile of this launch has at most that many tokens)
+    const uint32_t b_bytes = (uint32_t)p.rowtiles[1] * 128u;
+    const uint32_t ring = (base + kCtlBytes + 2 * 2 * kSgFloats * 4 +
+                           (uint32_t)p.tbl_cap * 16u + 1023u) & ~1023u;
+    const int S = max(1, min(kMaxStages, (int)((raw + (uint32_t)p.smem - ring) /
+                                               (kABytes + b_bytes))));
+    const uint32_t sA = ring, sB = ring + (uint32_t)S * kABytes;
     const int U1 = n_rt * p.mt1, U = U1 + n_rt * p.mt2;
     // the epilogue warps copy the row-tile list into shared memory (expert, first row,
     // tokens, slot), so that a unit's lookup costs no global round trips
@@ -506,10 +514,10 @@ int sm_count() {
     return n;
 }
 
-size_t smem_bytes(int stages, int box_cap, int tbl_cap) {
-    return 1024 + (size_t)stages * (kABytes + (size_t)box_cap * 128) + kCtlBytes +
-           2 * 2 * kSgFloats * sizeof(float) + (size_t)tbl_cap * sizeof(int4);
-}
+// Shared memory besides the ring and the table: alignment slack, control block,
+// exchange buffers.
+constexpr size_t kFixedSmem = 1024 + kCtlBytes + 2 * 2 * kSgFloats * sizeof(float);
+constexpr size_t kSmemBudget = 227 * 1024;
 
 }  // namespace
 
@@ -526,17 +534,16 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const int A = a.R * a.k;
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorInvalidDevice;
-    // token-row buffer per stage: a full row tile, or R rows if fewer (a row picks an
-    // expert at most once, so no expert has more than R tokens), rounded up to 16
-    const int box_cap = ((std::min(a.R, rowtile_size(a.R)) + 15) / 16) * 16;
-    const size_t budget = 227 * 1024;
-    int stages = 12;
-    while (stages > 2 && smem_bytes(stages, box_cap, 0) > budget) --stages;
-    // the row-tile table takes what the stages leave; row tiles past it are read from
-    // global memory
+    // the tallest row tile a launch can meet: kMaxRowTile tokens, or R if fewer (a row
+    // picks an expert at most once), rounded up to 16; the kernel sizes its stages from
+    // the height the permute kernel chose
+    const int box_cap = ((std::min(a.R, kMaxRowTile) + 15) / 16) * 16;
+    // the row-tile table takes what two stages of the tallest tiles leave; row tiles past
+    // it are read from global memory
+    const size_t two_stages = 2 * (kABytes + (size_t)box_cap * 128);
     const int tbl_cap = (int)std::min<size_t>((size_t)max_rowtiles(a.E, A),
-                                              (budget - smem_bytes(stages, box_cap, 0)) / 16);
-    const size_t smem = smem_bytes(stages, box_cap, tbl_cap);
+                                              (kSmemBudget - kFixedSmem - two_stages) / 16);
+    const size_t smem = kSmemBudget;
     const int S = a.slots;
 
     Maps m{};
@@ -550,7 +557,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        227 * 1024);
+                                        (int)kSmemBudget);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -564,9 +571,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.f = a.f;
     p.mt1 = a.f / 64;
     p.mt2 = (a.d + kM - 1) / kM;
-    p.stages = stages;
+    p.smem = (int)smem;
     p.tbl_cap = tbl_cap;
-    p.box_cap = box_cap;
     p.slots = S;
     p.rowtiles = a.rowtiles;
     p.offsets = a.offsets;

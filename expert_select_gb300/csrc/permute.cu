@@ -10,7 +10,8 @@
 // The masks and prefixes live in shared memory: (R/32) x E x 8 bytes (133 KB at 4160
 // rows and 128 experts). The same kernel also writes the active-expert list and the list
 // of row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels
-// walk. Past 2048 assignments it leaves the masks and prefixes in the workspace and a
+// walk; the tile height is the largest expert's token count rounded up to 16, at most
+// 256. Past 2048 assignments it leaves the masks and prefixes in the workspace and a
 // second, many-CTA kernel places the assignments.
 #include "common.cuh"
 
@@ -23,7 +24,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
                int *__restrict__ active, int *__restrict__ rowtiles, int *__restrict__ flags,
-               uint32_t *__restrict__ gmask, int rt_size, int after_router) {
+               uint32_t *__restrict__ gmask, int after_router) {
     pdl_wait();
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
@@ -89,6 +90,15 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         // warp 0: exclusive scans over experts (ascending) of the assignment counts, of
         // the active flags and of the row-tile counts; lane owns experts [lane*per, +per)
         const int per = (E + 31) / 32;
+        // row-tile height: the largest expert's tokens rounded up to 16 (every expert in
+        // one tile), at most kMaxRowTile (larger experts split into tiles of that many)
+        int cmax = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = tid * per + i;
+            if (e < E) cmax = max(cmax, cnt[e]);
+        }
+        cmax = __reduce_max_sync(0xffffffffu, cmax);
+        const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
         int c_tot = 0, a_tot = 0, t_tot = 0;
         for (int i = 0; i < per; ++i) {
             const int e = tid * per + i;
@@ -121,7 +131,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             if (c > 0) active[1 + a_ex++] = e;
             // row tiles of at most rt_size tokens of one expert, for the tensor-core kernel
             for (int n0 = 0; n0 < c; n0 += rt_size) {
-                int *t = rowtiles + 1 + 4 * t_ex++;
+                int *t = rowtiles + kRowTileHeader + 4 * t_ex++;
                 t[0] = e;
                 t[1] = n0;
                 t[2] = min(rt_size, c - n0);
@@ -132,6 +142,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             off[E] = c_ex;
             active[0] = a_ex;
             rowtiles[0] = t_ex;
+            rowtiles[1] = rt_size;
         }
     }
     __syncthreads();
@@ -213,8 +224,7 @@ cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *
     const int A = R * L.k;
     uint32_t *gm = A > kOneCtaAssignments ? rbmask : nullptr;
     err = launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
-                     offsets, perm, pos, active, rowtiles, flags, gm, rowtile_size(R),
-                     after_router ? 1 : 0);
+                     offsets, perm, pos, active, rowtiles, flags, gm, after_router ? 1 : 0);
     if (err != cudaSuccess || !gm) return err;
     return launch_pdl(permute_scatter_kernel, dim3((A + 255) / 256), dim3(256), 0, s, idx, R,
                       L.k, L.E, (const int *)offsets, (const uint32_t *)gm, perm, pos, flags);
