@@ -41,7 +41,7 @@ struct Workspace {
     size_t resident;  // u8  [E]  residency before this call's uploads (offload)
     size_t pass;      // u8  [E]  experts computed by the current expert pass (offload)
     size_t rowtiles;  // i32 [4 + 4 * max_rowtiles]: count, tile height, 0, 0, then
-                      // (expert, first token, tokens, 0) per tile
+                      // (expert, first permuted row, tokens, 0) per tile
     size_t sched;     // i32 [1 + max_rowtiles]: ticket counter, finished phase-1 units per row tile
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
     size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)

@@ -75,7 +75,7 @@ struct Params {
     int smem;      // dynamic shared memory of the launch (bytes)
     int tbl_cap;   // row tiles described in the shared-memory table (the rest: global reads)
     int slots;     // expert slots in the weight pool
-    const int *rowtiles, *offsets, *slot;
+    const int *rowtiles, *slot;
     const uint8_t *pass;  // experts computed by this launch (null: all)
     int *flags;
     int *sched;    // [0] ticket counter, [1 + rt] finished phase-1 units of row tile rt
@@ -108,7 +108,7 @@ struct Unit {
 // for an expert outside this launch's expert pass, -2 for a slot outside the pool.
 __device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
     const int *t = p.rowtiles + kRowTileHeader + 4 * rt;
-    const int e = t[0], n0 = t[1], ntok = t[2];
+    const int e = t[0], row0 = t[1], ntok = t[2];
     int code;
     if (p.pass && !p.pass[e]) {
         code = -1;
@@ -116,7 +116,7 @@ __device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
         const int sl = p.slot ? p.slot[e] : e;
         code = (sl >= 0 && sl < p.slots && ntok > 0) ? sl : -2;
     }
-    return make_int4(e, p.offsets[e] + n0, ntok, code);
+    return make_int4(e, row0, ntok, code);
 }
 
 // Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2. The
@@ -575,7 +575,6 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.tbl_cap = tbl_cap;
     p.slots = S;
     p.rowtiles = a.rowtiles;
-    p.offsets = a.offsets;
     p.slot = a.slot;
     p.pass = a.pass;
     p.flags = a.flags;

@@ -133,7 +133,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             for (int n0 = 0; n0 < c; n0 += rt_size) {
                 int *t = rowtiles + kRowTileHeader + 4 * t_ex++;
                 t[0] = e;
-                t[1] = n0;
+                t[1] = off[e] + n0;  // first permuted row of the tile
                 t[2] = min(rt_size, c - n0);
                 t[3] = 0;
             }
