@@ -18,10 +18,11 @@
 //            gates. A node whose natural top-k lies inside S keeps it (it is then the
 //            restricted top-k by definition).
 //
-// Top-k: each lane holds experts lane + 32 i as order-preserving 32-bit keys of their
-// logits (-0 folded onto +0); every lane sorts its own, then butterfly rounds merge the
-// lanes' sorted lists (warp_topk below): descending logits, ties to the lower id, as
-// exact as a comparison of the fp32 values.
+// Top-k: each lane holds experts lane + 32 i; a round takes every lane's best
+// candidate as an order-preserving 32-bit key of its logit (-0 folded onto +0) and
+// finds the winner with two warp reductions (max key, then min expert id among the
+// lanes holding that key): descending logits, ties to the lower id, as exact as a
+// comparison of the fp32 values.
 //
 // Demand, entropy and gates are computed in fp32 (GB300's fp64 rate is a small
 // fraction of its fp32 rate): the softmax normaliser in a warp tree, the demand per
@@ -52,103 +53,12 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// (key desc, id asc): the order of the top-k (larger logit first, ties to the lower id).
-__device__ __forceinline__ bool before(uint32_t ka, int ia, uint32_t kb, int ib) {
-    return ka > kb || (ka == kb && ia < ib);
-}
-
-// Compare-exchange: put the earlier of (i, j) at i.
-template <int LS>
-__device__ __forceinline__ void cex(uint32_t (&key)[LS], int (&id)[LS], int i, int j) {
-    if (before(key[j], id[j], key[i], id[i])) {
-        const uint32_t tk = key[i];
-        const int ti = id[i];
-        key[i] = key[j];
-        id[i] = id[j];
-        key[j] = tk;
-        id[j] = ti;
-    }
-}
-
-// Sorts a bitonic list of LS entries into (key desc, id asc) order.
-template <int LS>
-__device__ __forceinline__ void bitonic_merge(uint32_t (&key)[LS], int (&id)[LS]) {
-#pragma unroll
-    for (int half = LS / 2; half >= 1; half >>= 1)
-#pragma unroll
-        for (int i = 0; i < LS; ++i)
-            if ((i & half) == 0) cex<LS>(key, id, i, i + half);
-}
-
-// Sorts LS entries into (key desc, id asc) order (bitonic sorting network).
-template <int LS>
-__device__ __forceinline__ void bitonic_sort(uint32_t (&key)[LS], int (&id)[LS]) {
-#pragma unroll
-    for (int size = 2; size <= LS; size <<= 1)
-#pragma unroll
-        for (int stride = size / 2; stride >= 1; stride >>= 1)
-#pragma unroll
-            for (int i = 0; i < LS; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    if ((i & size) == 0) cex<LS>(key, id, i, j);  // this run in order
-                    else cex<LS>(key, id, j, i);                 // this run reversed
-                }
-            }
-}
-
-// Warp top-k (k <= LS) of v (lane holds experts lane + 32 i) among the experts whose bit
-// i is set in `allowed`: every lane sorts its own candidates, then five butterfly rounds
-// each merge two lanes' sorted lists and keep the best LS (the best LS of two sorted lists
-// are the element-wise better of one list and the other reversed, a bitonic list). Every
-// lane ends with the warp's best LS; lane j < k returns the id of the j-th (-1 if fewer
-// than k experts are allowed). The order is (logit desc, id asc) on order-preserving keys,
-// exactly the order of a comparison of the fp32 values.
-template <int LS>
-__device__ __forceinline__ int warp_topk_ls(const float v[kVPL], unsigned allowed, int E, int k) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[LS];
-    int id[LS];
-#pragma unroll
-    for (int i = 0; i < LS; ++i) {
-        if (i < kVPL) {
-            const int e = lane + 32 * i;
-            key[i] = (e < E && ((allowed >> i) & 1u)) ? order_key(v[i]) : 0u;
-            id[i] = e;
-        } else {
-            key[i] = 0u;
-            id[i] = 0x7fff;
-        }
-    }
-    bitonic_sort<LS>(key, id);
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        uint32_t ok[LS];
-        int oi[LS];
-#pragma unroll
-        for (int i = 0; i < LS; ++i) {
-            ok[i] = __shfl_xor_sync(0xffffffffu, key[LS - 1 - i], off);
-            oi[i] = __shfl_xor_sync(0xffffffffu, id[LS - 1 - i], off);
-        }
-#pragma unroll
-        for (int i = 0; i < LS; ++i)
-            if (before(ok[i], oi[i], key[i], id[i])) {
-                key[i] = ok[i];
-                id[i] = oi[i];
-            }
-        bitonic_merge<LS>(key, id);
-    }
-    int mine = -1;
-#pragma unroll
-    for (int i = 0; i < LS; ++i)
-        if (i == lane && i < k && key[i] != 0u) mine = id[i];
-    return mine;
-}
-
-// Warp top-k by k rounds: every lane offers its best remaining candidate, two warp
-// reductions (max key, then the lowest id holding it) pick the round's winner.
-__device__ __forceinline__ int warp_topk_rounds(const float v[kVPL], unsigned allowed, int E,
-                                                int k) {
+// Warp top-k of v (lane holds experts lane + 32 i) among the experts whose bit i is
+// set in `allowed`, in k rounds: every lane offers its best remaining candidate, two warp
+// reductions (max key, then the lowest id holding it) pick the round's winner. Returns,
+// in lane j < k, the expert id of the j-th choice (-1 if fewer than k experts are
+// allowed).
+__device__ __forceinline__ int warp_topk(const float v[kVPL], unsigned allowed, int E, int k) {
     const int lane = threadIdx.x & 31;
     uint32_t key[kVPL];
 #pragma unroll
@@ -177,18 +87,6 @@ __device__ __forceinline__ int warp_topk_rounds(const float v[kVPL], unsigned al
     return mine;
 }
 
-// Warp top-k of v (lane holds experts lane + 32 i) among the experts whose bit i is
-// set in `allowed`. Returns, in lane j < k, the expert id of the j-th choice (-1 if
-// fewer than k experts are allowed). Both methods give the same, exact order; which is
-// faster depends on the kernel around it (measured): the merge in the natural-routing
-// kernel, the rounds in the AcceptMoE kernels.
-__device__ __forceinline__ int warp_topk(const float v[kVPL], unsigned allowed, int E, int k) {
-    return warp_topk_rounds(v, allowed, E, k);
-}
-__device__ __forceinline__ int warp_topk_merge(const float v[kVPL], unsigned allowed, int E,
-                                               int k) {
-    return k <= 8 ? warp_topk_ls<8>(v, allowed, E, k) : warp_topk_rounds(v, allowed, E, k);
-}
 
 // c(depth) of the commitment table (the last entry repeats past the table). The table is
 // a kernel parameter: selecting the entry with unrolled compares keeps it in the
@@ -724,7 +622,7 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
     for (int n = rank * kNW + warp; n < N; n += kNC * kNW) {
         float v[kVPL];
         load_row(Lg + (size_t)n * E, E, v);
-        const int c = warp_topk_merge(v, 0xffffffffu, E, k);
+        const int c = warp_topk(v, 0xffffffffu, E, k);
         const float val = chosen_value(v, c);
         write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
         if (lane < k && c >= 0) atomicOr(&mask[c >> 5], 1u << (c & 31));
