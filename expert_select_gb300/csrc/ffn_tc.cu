@@ -468,21 +468,38 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                      : "memory");
 }
 
-// Gathers the token rows of every assignment into permuted order: xp[p] = x[perm[p] / k].
-// Block 0 also zeroes the expert kernel's ticket counter and row-tile counters.
-__global__ void __launch_bounds__(256)
+// Gathers the token rows of every assignment into permuted order: xp[p] = x[perm[p] / k],
+// a warp per row (16-byte loads, all of a lane's loads issued before its stores), rows
+// strided over the grid. Block 0 also zeroes the expert kernel's ticket counter and
+// row-tile counters.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ perm,
                    const int *__restrict__ offsets, int E, int k, int d,
                    __nv_bfloat16 *__restrict__ xp, int *__restrict__ sched, int n_sched) {
     pdl_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_sched; i += blockDim.x) sched[i] = 0;
-    const int pidx = blockIdx.x;
-    if (pidx >= offsets[E]) return;
-    const int r = perm[pidx] / k;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r * d);
-    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pidx * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+    const int lane = threadIdx.x & 31;
+    const int n = offsets[E];
+    const int vec = d / 8;  // 16-byte pieces of a row
+    for (int p = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); p < n;
+         p += gridDim.x * kGatherWarps) {
+        const int r = perm[p] / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r * d);
+        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)p * d);
+        int i = lane;
+        for (; i + 96 < vec; i += 128) {  // four pieces in flight per lane
+            const uint4 a0 = __ldg(src + i), a1 = __ldg(src + i + 32), a2 = __ldg(src + i + 64),
+                        a3 = __ldg(src + i + 96);
+            dst[i] = a0;
+            dst[i + 32] = a1;
+            dst[i + 64] = a2;
+            dst[i + 96] = a3;
+        }
+        for (; i < vec; i += 32) dst[i] = __ldg(src + i);
+    }
 }
 
 // ------------------------------------------------------------------- host
@@ -562,7 +579,10 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     if (attr_err != cudaSuccess) return attr_err;
 
     const int n_sched = 1 + max_rowtiles(a.E, A);
-    cudaError_t err = launch_pdl(gather_rows_kernel, dim3(A), dim3(256), 0, s,
+    const int gather_ctas =
+        std::max(1, std::min((A + kGatherWarps - 1) / kGatherWarps, 16 * nsm));
+    cudaError_t err = launch_pdl(gather_rows_kernel, dim3(gather_ctas), dim3(kGatherWarps * 32),
+                                 0, s,
                                  (const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k, a.d,
                                  (__nv_bfloat16 *)a.xp, a.sched, n_sched);
     if (err != cudaSuccess) return err;
