@@ -159,6 +159,22 @@ static moe_status run_experts(const moe_layer_desc &L, const void *x, const void
 
 using namespace moe;
 
+// Every argument check of moe_tree_forward except the workspace's.
+moe_status moe::tree_forward_check(const moe_layer_desc *L, const moe_select_params *P,
+                                   const void *x, const void *W_r, const void *W_gate,
+                                   const void *W_up, const void *W_down, const int *depth,
+                                   int B, int N, const uint8_t *resident, const void *y) {
+    SelectArgs a;
+    if (!desc_ok(L) || !select_args(P, L->k, &a) || B < 1 || N < 1) return MOE_ERR_ARG;
+    if (!x || !W_r || !W_gate || !W_up || !W_down || !depth || !y) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(W_r) || !aligned16(W_gate) || !aligned16(W_up) ||
+        !aligned16(W_down) || !aligned16(y))
+        return MOE_ERR_ARG;
+    if (a.prune && !resident) return MOE_ERR_ARG;
+    if ((long long)B * N > (1 << 30) || !permute_fits(B * N, L->E)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
 struct moe_residency {
     int n_layers = 0, E = 0, slots = 0;
     std::vector<int> slot_of;     // [layer][E], -1 = not resident
@@ -245,16 +261,13 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
                             int B, int N, const uint8_t *resident, void *y,
                             const moe_tree_outputs *out, void *workspace,
                             const moe_run_opts *opts, moe_stream_t stream) {
+    const moe_status st =
+        tree_forward_check(L, P, x, W_r, W_gate, W_up, W_down, depth, B, N, resident, y);
+    if (st != MOE_OK) return st;
+    if (!workspace || ((uintptr_t)workspace & 255u)) return MOE_ERR_ARG;
     SelectArgs a;
-    if (!desc_ok(L) || !select_args(P, L->k, &a) || B < 1 || N < 1) return MOE_ERR_ARG;
-    if (!x || !W_r || !W_gate || !W_up || !W_down || !depth || !y || !workspace)
-        return MOE_ERR_ARG;
-    if (!aligned16(x) || !aligned16(W_r) || !aligned16(W_gate) || !aligned16(W_up) ||
-        !aligned16(W_down) || !aligned16(y) || ((uintptr_t)workspace & 255u))
-        return MOE_ERR_ARG;
-    if (a.prune && !resident) return MOE_ERR_ARG;
+    select_args(P, L->k, &a);
     const int R = B * N;
-    if (!permute_fits(R, L->E)) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     const Workspace w = workspace_layout(*L, B, N);
     moe_tree_outputs o{};

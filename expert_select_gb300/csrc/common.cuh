@@ -120,6 +120,11 @@ bool desc_ok(const moe_layer_desc *L);
 bool select_args(const moe_select_params *P, int k, SelectArgs *a);
 bool permute_fits(int R, int E);
 bool aligned16(const void *p);
+// The argument checks of moe_tree_forward other than those of the workspace.
+moe_status tree_forward_check(const moe_layer_desc *L, const moe_select_params *P,
+                              const void *x, const void *W_r, const void *W_gate,
+                              const void *W_up, const void *W_down, const int *depth, int B,
+                              int N, const uint8_t *resident, const void *y);
 moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
                        const Workspace &w, int *counts, int *offsets, int *perm,
                        bool after_router, cudaStream_t s);

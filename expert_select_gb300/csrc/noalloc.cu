@@ -35,6 +35,10 @@ extern "C" moe_status moe_tree_forward_noalloc(
     const void *W_gate, const void *W_up, const void *W_down, const int *slot_of_expert,
     const int *depth, int B, int N, const uint8_t *resident, void *y,
     const moe_tree_outputs *out, const moe_run_opts *opts, moe_stream_t stream) {
+    // bad arguments are reported as such before any CUDA call
+    const moe_status st = moe::tree_forward_check(L, P, x, W_r, W_gate, W_up, W_down, depth, B,
+                                                  N, resident, y);
+    if (st != MOE_OK) return st;
     const size_t need = moe_workspace_bytes(L, B, N);
     if (need == 0) return MOE_ERR_ARG;
     if (need > kScratchBytes) return MOE_ERR_UNSUPPORTED;

@@ -81,6 +81,35 @@ def test_bad_arguments_rejected_before_any_launch():
     assert lib.moe_event_wait(nul, 1.0) == M.MOE_ERR_ARG
 
 
+def test_draft_select_and_other_entry_points_reject_bad_arguments():
+    import ctypes as C
+    lib = M.lib()
+    L = M.layer_desc(2048, 128, 8, 768, "bf16")
+    f = C.c_void_p(0x100000)  # 16-byte aligned, never dereferenced: argument checks fail first
+    nul = None
+
+    def draft(Cn, lam, gamma, x=nul, xs=nul, parent=f):
+        return lib.moe_draft_select(C.byref(L), Cn, parent, f, f, f, lam, gamma, x, f, f, f, xs,
+                                    nul, nul)
+    assert draft(4098, 0.1, 65) == M.MOE_ERR_ARG           # more candidates than supported
+    assert draft(0, 0.1, 65) == M.MOE_ERR_ARG              # no candidates
+    assert draft(411, -0.1, 65) == M.MOE_ERR_ARG           # negative cost weight
+    assert draft(411, float("nan"), 65) == M.MOE_ERR_ARG   # NaN cost weight
+    assert draft(411, 0.1, 0) == M.MOE_ERR_ARG             # nothing to select
+    assert draft(411, 0.1, 65, x=f) == M.MOE_ERR_ARG       # x without x_sel
+    assert draft(411, 0.1, 65, parent=nul) == M.MOE_ERR_ARG
+    odd = C.c_void_p(0x100004)
+    assert draft(411, 0.1, 65, x=odd, xs=f) == M.MOE_ERR_ARG  # rows not 16-byte aligned
+    assert lib.moe_expert_permute(C.byref(L), f, 0, f, f, f, f, nul) == M.MOE_ERR_ARG
+    assert lib.moe_tree_forward_noalloc(C.byref(L), nul, nul, nul, nul, nul, nul, nul, nul, 1, 65,
+                                        nul, nul, nul, nul, nul) == M.MOE_ERR_ARG
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, [1.0])
+    Ls = M.layer_desc(2048, 128, 8, 768, "bf16", slots=48)
+    # no residency table
+    assert lib.moe_offload_forward(C.byref(Ls), C.byref(P), f, f, f, f, f, f, f, f, nul, 0, f,
+                                   1, 65, f, nul, nul, f, nul, nul, nul) == M.MOE_ERR_ARG
+
+
 class _LruModel:
     """Independent model of the slot policy: hits refresh, misses take a free slot
     (lowest index) or evict the least recently used slot not needed now."""
