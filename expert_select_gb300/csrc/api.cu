@@ -221,7 +221,7 @@ moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
     if (B * N > 0 && (!logits || !depth || !topk_idx || !gates)) return MOE_ERR_ARG;
     if (a.prune && !resident) return MOE_ERR_ARG;
     return cuda_status(launch_select(*L, a, logits, depth, B, N, resident, topk_idx, gates,
-                                     eligible, info, (cudaStream_t)stream));
+                                     eligible, info, WeightPrefetch{}, (cudaStream_t)stream));
 }
 
 moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int R, int *counts,
@@ -284,7 +284,8 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
     if (launch_router(*L, x, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord, s) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, s) !=
+    const WeightPrefetch pf = weight_prefetch(*L, B, W_gate, W_up, W_down, slot_of_expert);
+    if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, pf, s) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, idx, gates, R, y, workspace,

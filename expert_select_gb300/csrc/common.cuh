@@ -61,9 +61,28 @@ struct SelectArgs {
     int mode, n_c, pool_all, anchor, prune, budget, min_set, fixed_B;
     float c[MOE_MAX_DEPTHS];
 };
+// L2 prefetch of expert weights during routing (AcceptMoE and fixed-size selection). The
+// root's natural top-k is the anchor that AcceptMoE keeps in every eligible set, and with
+// it the root's own routing, so those experts are in the block's union whatever the
+// selection decides. Extra CTAs of the selection launch take tree 0's root top-k from the
+// logits and ask L2 for the three weight matrices of each of those experts: the expert
+// kernel then finds part of them in L2, read from HBM while the routing kernels left it
+// idle.
+struct WeightPrefetch {
+    const char *wg, *wu, *wd;   // W_gate, W_up, W_down slot pools
+    const int *slot_of_expert;  // null: slot = expert id
+    int slots;                  // slots in each pool
+    int ctas;                   // extra CTAs doing the prefetch (a multiple of 8); 0 = none
+    unsigned long long bytes;   // bytes of one slot of one matrix (a multiple of 16)
+};
+// The prefetch for a layer's weight pools, sized for a launch of B trees (ctas = 0 when
+// the weights cannot be prefetched or the SMs are taken by the selection itself).
+WeightPrefetch weight_prefetch(const moe_layer_desc &L, int B, const void *W_gate,
+                               const void *W_up, const void *W_down, const int *slot_of_expert);
 cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
-                          float *gates, uint8_t *elig, int *info, cudaStream_t s);
+                          float *gates, uint8_t *elig, int *info, const WeightPrefetch &pf,
+                          cudaStream_t s);
 
 // Row tiles of the tensor-core expert kernel: at most kMaxRowTile tokens of one expert
 // (its MMA N is at most 256). The permute kernel picks the height as the largest expert's
