@@ -11,7 +11,8 @@
 // rows and 128 experts). The same kernel also writes the active-expert list and the list
 // of row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels
 // walk; the tile height is the largest expert's token count rounded up to 16, at most
-// 256. Past 2048 assignments it leaves the masks and prefixes in the workspace and a
+// 256. Up to 2048 assignments it keeps the expert ids in shared memory and places the
+// assignments itself; past that it leaves the masks and prefixes in the workspace and a
 // second, many-CTA kernel places the assignments.
 #include "common.cuh"
 
@@ -32,6 +33,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     uint32_t *pre = sm + (size_t)nb * E;  // [E][nb]
     int *cnt = (int *)(pre + (size_t)nb * E);
     int *off = cnt + E;                   // [E + 1]
+    int *sidx = off + E + 1;              // [A] the expert ids, when this CTA places them
     const int tid = threadIdx.x;
     const int A = R * k;
 
@@ -51,6 +53,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int e = ev[u];
+            if (!gmask && a0 + u * kThreads < A) sidx[a0 + u * kThreads] = e;
             if (e < 0 || e >= E) continue;
             const int r = (a0 + u * kThreads) / k;
             atomicOr(&mask[e * nb + (r >> 5)], 1u << (r & 31));
@@ -156,10 +159,12 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     }
     // a thread per assignment; a repeated expert keeps its first slot
     for (int a = tid; a < A; a += kThreads) {
-        const int e = idx[a];
+        const int e = sidx[a];
         const int r = a / k, j = a - r * k;
         bool ok = e >= 0 && e < E;
-        for (int q = 0; ok && q < j; ++q) ok = idx[r * k + q] != e;
+#pragma unroll
+        for (int q = 0; q < kMaxK; ++q)
+            if (q < j && sidx[r * k + q] == e) ok = false;
         if (!ok) {
             pos[a] = -1;
             atomicOr(flags, FLAG_BAD_EXPERT);
@@ -191,7 +196,9 @@ permute_scatter_kernel(const int *__restrict__ idx, int R, int k, int E,
     const int e = idx[a];
     const int r = a / k, j = a - r * k;
     bool ok = e >= 0 && e < E;
-    for (int q = 0; ok && q < j; ++q) ok = idx[r * k + q] != e;  // first slot wins
+#pragma unroll
+    for (int q = 0; q < kMaxK; ++q)  // first slot wins; the loads are independent
+        if (q < j && idx[r * k + q] == e) ok = false;
     if (!ok) {
         pos[a] = -1;
         atomicOr(flags, FLAG_BAD_EXPERT);
@@ -217,12 +224,14 @@ size_t permute_smem_bytes(int R, int E) {
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
                            int *flags, uint32_t *rbmask, bool after_router, cudaStream_t s) {
-    const size_t smem = permute_smem_bytes(R, L.E);
+    const int A = R * L.k;
+    uint32_t *gm = A > kOneCtaAssignments ? rbmask : nullptr;
+    // + the staged expert ids when this CTA places the assignments (A <= 2048, so R <= 2048
+    // and the masks take at most 64 row blocks: the total stays far below the limit)
+    const size_t smem = permute_smem_bytes(R, L.E) + (gm ? 0 : (size_t)A * 4);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    const int A = R * L.k;
-    uint32_t *gm = A > kOneCtaAssignments ? rbmask : nullptr;
     err = launch_pdl(permute_kernel, dim3(1), dim3(kThreads), smem, s, idx, R, L.k, L.E, counts,
                      offsets, perm, pos, active, rowtiles, flags, gm, after_router ? 1 : 0);
     if (err != cudaSuccess || !gm) return err;

@@ -56,23 +56,24 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Warp top-k of v (lane holds experts lane + 32 i) among the experts whose bit i is
+// Warp top-k of v (lane holds experts lane + 32 i, i < VPL) among the experts whose bit i is
 // set in `allowed`, in k rounds: every lane offers its best remaining candidate, two warp
 // reductions (max key, then the lowest id holding it) pick the round's winner. Returns,
 // in lane j < k, the expert id of the j-th choice (-1 if fewer than k experts are
 // allowed).
-__device__ __forceinline__ int warp_topk(const float v[kVPL], unsigned allowed, int E, int k) {
+template <int VPL>
+__device__ __forceinline__ int warp_topk(const float (&v)[VPL], unsigned allowed, int E, int k) {
     const int lane = threadIdx.x & 31;
-    uint32_t key[kVPL];
+    uint32_t key[VPL];
 #pragma unroll
-    for (int i = 0; i < kVPL; ++i)
+    for (int i = 0; i < VPL; ++i)
         key[i] = (lane + 32 * i < E && ((allowed >> i) & 1u)) ? order_key(v[i]) : 0u;
     int mine = -1;
     for (int j = 0; j < k; ++j) {
         uint32_t bk = 0;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kVPL; ++i)
+        for (int i = 0; i < VPL; ++i)
             if (key[i] > bk) {
                 bk = key[i];
                 bi = lane + 32 * i;
@@ -82,7 +83,7 @@ __device__ __forceinline__ int warp_topk(const float v[kVPL], unsigned allowed, 
                                                                                : 0xffffffffu);
         if (w != 0xffffffffu && (int)(w & 31u) == lane) {
 #pragma unroll
-            for (int i = 0; i < kVPL; ++i)
+            for (int i = 0; i < VPL; ++i)
                 if ((int)(w >> 5) == i) key[i] = 0u;
         }
         if (lane == j) mine = w == 0xffffffffu ? -1 : (int)w;
@@ -110,21 +111,23 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Loads the E logits of one node into v[] (lane holds experts lane + 32 i).
-__device__ __forceinline__ void load_row(const float *Ln, int E, float v[kVPL]) {
+template <int VPL>
+__device__ __forceinline__ void load_row(const float *Ln, int E, float (&v)[VPL]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < kVPL; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         v[i] = e < E ? Ln[e] : -INFINITY;
     }
 }
 
 // The logit of expert `idx` (idx < 0: -inf), fetched from the lane that holds it.
-__device__ __forceinline__ float chosen_value(const float v[kVPL], int idx) {
+template <int VPL>
+__device__ __forceinline__ float chosen_value(const float (&v)[VPL], int idx) {
     const int lane = threadIdx.x & 31;
     float out = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kVPL; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const float got = __shfl_sync(0xffffffffu, v[i], idx < 0 ? lane : (idx & 31));
         if (idx >= 0 && (idx >> 5) == i) out = got;
     }
@@ -404,16 +407,52 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
 // nodes' natural top-k and softmax terms, adds the terms of its nodes per expert in node
 // order, and stores the partial demand and the natural choices into CTA 0's shared memory
 // (distributed shared memory). CTA 0 adds the partials in CTA order and runs the size /
-// anchor / fill / prune phase; every CTA then reads the eligible set back and re-routes
-// its own nodes. The demand is summed in a different order than in the one-CTA kernel
-// (partials per CTA), a difference at the level of fp32 rounding.
+// anchor / fill / prune phase, with sum D and H as block reductions and the ranks counted
+// by two or four threads per expert; meanwhile the other CTAs write their nodes' natural
+// routing, which stands for every node whose natural top-k lies in the eligible set. Every
+// CTA then reads the eligible set back and re-routes the nodes that need it. The demand
+// and its entropy are summed in a different order than in the one-CTA kernel (partials
+// per CTA, tree reductions), a difference at the level of fp32 rounding.
 namespace cg = cooperative_groups;
 constexpr int kCC = 8;                  // CTAs per tree
 constexpr int kCW = 16;                 // warps per CTA
 constexpr int kCThreads = kCW * 32;
 constexpr int kClusterMaxN = 256;
-static_assert(kCThreads >= kMaxE, "phase B takes one expert per thread");
+static_assert(kCThreads >= 2 * kMaxE, "phase B takes at least two threads per expert");
 
+// Rank of expert e under the order of the keys rk (desc: larger first, else smaller
+// first; equal keys: lower id first), i.e. the number of experts before it. `per`
+// consecutive threads (a power of two dividing 32) share e: each counts one slice of the
+// experts and the slices are added with shuffles.
+__device__ __forceinline__ int rank_of(const float *rk, int e, int E, int per, int part,
+                                       bool desc) {
+    const float me = rk[e];
+    const int len = (E + per - 1) / per;
+    const int q0 = part * len, q1 = min(E, q0 + len);
+    int r = 0;
+#pragma unroll 8
+    for (int q = q0; q < q1; ++q) {
+        const float o = rk[q];
+        r += ((desc ? o > me : o < me) || (o == me && q < e)) ? 1 : 0;
+    }
+    for (int off = 1; off < per; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+// Sum of v over the block's threads, identical in every thread: a butterfly per warp,
+// then the warps' sums in warp order (red holds one float per warp; the call ends with
+// a barrier, and `red` may be reused after the next barrier).
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) s = __fadd_rn(s, red[w]);
+    return s;
+}
+
+template <int VPL>
 __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(kCThreads, 1)
 select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                       const int *__restrict__ depth, int N, int E, int k,
@@ -426,14 +465,14 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         return;
     }
     // wt [slots][E], lrow [slots][E] (this CTA's logit rows), nat_all [N][k] (CTA 0),
-    // nat_loc [slots][k]
+    // nat_loc [slots][k], nat_val [slots][k] (their logits)
     extern __shared__ float cdyn[];
     __shared__ float part[kCC][kMaxE];  // CTA 0: partial demand of every CTA
     __shared__ int selAll[kCC][kMaxE];  // CTA 0: experts chosen by every CTA's nodes
-    __shared__ float D[kMaxE], term[kMaxE], rk[kMaxE];
+    __shared__ float D[kMaxE], rk[kMaxE];
+    __shared__ float red[2][kCW];
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
-    __shared__ float s_sumD;
-    __shared__ int s_m;
+    __shared__ int s_m, s_removed;
 
     // every CTA of the cluster must be running before any touches another's shared
     // memory: arrive now, wait just before the first remote store
@@ -448,6 +487,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     float *lrow = wt + (size_t)slots * E;
     int *nat_all = reinterpret_cast<int *>(lrow + (size_t)slots * E);
     int *nat_loc = nat_all + (size_t)N * k;
+    float *nat_val = reinterpret_cast<float *>(nat_loc + (size_t)slots * k);
     int *nat0 = cl.map_shared_rank(nat_all, 0);
     const float *Lg = logits + (size_t)b * N * E;
     const int *dep = depth + (size_t)b * N;
@@ -464,28 +504,30 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     // ---- phase A: this CTA's nodes ----
     for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
         const int slot = t * kCW + warp;
-        float v[kVPL];
+        const int dn = dep[n];  // in flight with the logits
+        float v[VPL];
         load_row(Lg + (size_t)n * E, E, v);
 #pragma unroll
-        for (int i = 0; i < kVPL; ++i)
+        for (int i = 0; i < VPL; ++i)
             if (lane + 32 * i < E) lrow[slot * E + lane + 32 * i] = v[i];
         const int c = warp_topk(v, 0xffffffffu, E, k);
         const float val = chosen_value(v, c);
         if (lane < k) {
             nat_loc[slot * k + lane] = c;
+            nat_val[slot * k + lane] = val;
             nat0[n * k + lane] = c;
         }
         const float m = __shfl_sync(0xffffffffu, val, 0);
-        float ex[kVPL], s = 0.f;
+        float ex[VPL], s = 0.f;
 #pragma unroll
-        for (int i = 0; i < kVPL; ++i) {
+        for (int i = 0; i < VPL; ++i) {
             ex[i] = lane + 32 * i < E ? expf(v[i] - m) : 0.f;
             s += ex[i];
         }
         s = warp_sum(s);
-        const float cn = commitment(a, dep[n]);
+        const float cn = commitment(a, dn);
 #pragma unroll
-        for (int i = 0; i < kVPL; ++i) {
+        for (int i = 0; i < VPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E) wt[slot * E + e] = __fmul_rn(cn, __fdiv_rn(ex[i], s));
         }
@@ -493,120 +535,120 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     __syncthreads();
     if (tid < E) {  // partial demand of this CTA's nodes, node order
         float acc = 0.f;
-        for (int t = 0; t * kCC * kCW < N; ++t)
-            for (int w = 0; w < kCW; ++w) {
-                const int n = t * kCC * kCW + rank * kCW + w;
-                if (n < N) acc = __fadd_rn(acc, wt[(t * kCW + w) * E + tid]);
+        for (int t = 0; t * kCC * kCW < N; ++t) {
+            const int cnt = min(kCW, max(0, N - t * kCC * kCW - rank * kCW));
+            const float *w0 = wt + (size_t)t * kCW * E + tid;
+            if (cnt == kCW) {
+#pragma unroll
+                for (int w = 0; w < kCW; ++w) acc = __fadd_rn(acc, w0[(size_t)w * E]);
+            } else {
+                for (int w = 0; w < cnt; ++w) acc = __fadd_rn(acc, w0[(size_t)w * E]);
             }
+        }
         cl.map_shared_rank(&part[0][0], 0)[rank * kMaxE + tid] = acc;
     }
     cl.sync();
 
-    // ---- phase B on CTA 0 ----
+    // ---- phase B on CTA 0; the other CTAs write their nodes' natural routing, which
+    // stands unless phase C re-routes the node ----
     if (rank == 0) {
         for (int i = tid; i < N * k; i += kCThreads) inU[nat_all[i]] = 1;
-        __syncthreads();
+        float De = 0.f;
         if (tid < E) {
-            float acc = 0.f;
-            for (int r = 0; r < kCC; ++r) acc = __fadd_rn(acc, part[r][tid]);
-            D[tid] = acc;
+            for (int r = 0; r < kCC; ++r) De = __fadd_rn(De, part[r][tid]);
+            D[tid] = De;
         }
+        // sum D and H = -sum q ln q, each a block reduction (every thread gets the value)
+        const float sumD = block_sum(De, red[0]);
         const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
-        if (tid == 0) {
-            float sum = 0.f;
-#pragma unroll 16
-            for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
-            s_sumD = sum;
-        }
-        __syncthreads();
+        float term = 0.f;
         if (tid < E) {
-            const float q = __fdiv_rn(D[tid], s_sumD);
-            term[tid] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
+            const float q = __fdiv_rn(De, sumD);
+            term = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
         }
-        __syncthreads();
-        if (tid == 0) {
-            int m;
-            if (a.mode == MOE_ROUTE_ACCEPT) {
-                float H = 0.f;
-#pragma unroll 16
-                for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
-                const float r = expf(H);
-                const float rn = rintf(r);
-                m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
-            } else {
-                m = a.fixed_B;
-            }
-            m = min(max(m, k), pool);
-            s_m = m;
-            if (a.anchor)
-                for (int j = 0; j < k; ++j) inA[nat_all[j]] = 1;
+        const float H = -block_sum(term, red[1]);
+        int m;
+        if (a.mode == MOE_ROUTE_ACCEPT) {
+            const float r = expf(H);
+            const float rn = rintf(r);
+            m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
+        } else {
+            m = a.fixed_B;
         }
+        m = min(max(m, k), pool);
+        if (a.anchor && tid < k) inA[nat_all[tid]] = 1;
         __syncthreads();
         const int nA = a.anchor ? k : 0;
-        const int m = s_m;
         if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? D[tid] : -1.f;
         __syncthreads();
-        if (tid < E) {
-            int in = inA[tid];
-            const float De = rk[tid];
-            if (De >= 0.f) {
-                int rnk = 0;
-#pragma unroll 8
-                for (int q = 0; q < E; ++q) {
-                    const float Dq = rk[q];
-                    rnk += (Dq > De || (Dq == De && q < tid)) ? 1 : 0;
-                }
-                in = rnk < m - nA;
-            }
-            inS[tid] = in;
+        // fill: candidates (pool minus anchor) ranked by (D desc, id asc); demand is >= 0,
+        // so -1 marks a non-candidate. `per` threads share an expert.
+        const int per = E <= kCThreads / 4 ? 4 : 2;
+        const int e = tid / per, pe = tid % per;
+        int in = 0;
+        {
+            const int rnk = rank_of(rk, min(e, E - 1), E, per, pe, true);  // every thread
+            if (e < E) in = inA[e] || (rk[e] >= 0.f && rnk < m - nA);
         }
-        __syncthreads();
+        __syncthreads();  // rk is read above and rewritten below
+        if (e < E && pe == 0) inS[e] = in;
         int removed = 0;
         if (a.prune && resident) {
             int is_rem = 0;
-            if (tid < E) {
-                is_rem = inS[tid] && !inA[tid] && !resident[tid];
-                rk[tid] = is_rem ? D[tid] : INFINITY;
+            if (e < E) {
+                is_rem = in && !inA[e] && !resident[e];
+                if (pe == 0) rk[e] = is_rem ? D[e] : INFINITY;
             }
-            const int nrem = __syncthreads_count(is_rem);
+            const int nrem = __syncthreads_count(is_rem && pe == 0);
             const int fl = a.min_set > k ? a.min_set : k;
             removed = min(min(max(m - fl, 0), a.budget), nrem);
-            if (is_rem) {
-                const float De = rk[tid];
-                int rnk = 0;
-#pragma unroll 8
-                for (int q = 0; q < E; ++q) {
-                    const float Dq = rk[q];
-                    rnk += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
-                }
-                if (rnk < removed) inS[tid] = 0;
-            }
-            __syncthreads();
+            const int rnk = rank_of(rk, min(e, E - 1), E, per, pe, false);  // every thread
+            if (is_rem && pe == 0 && rnk < removed) inS[e] = 0;
         }
-        if (tid == 0 && info_out) {
-            info_out[b * MOE_INFO_FIELDS + 2] = m;
-            info_out[b * MOE_INFO_FIELDS + 3] = removed;
+        if (tid == 0) {
+            s_m = m;
+            s_removed = removed;
         }
-        if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
+    } else {
+        for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
+            const int slot = t * kCW + warp;
+            write_choice(lane < k ? nat_loc[slot * k + lane] : -1,
+                         lane < k ? nat_val[slot * k + lane] : -INFINITY, k,
+                         idxb + (size_t)n * k, gb + (size_t)n * k);
+        }
     }
     cl.sync();
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
     if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
+    if (rank == 0) {  // the set's size and the block's eligibility mask
+        if (tid == 0 && info_out) {
+            info_out[b * MOE_INFO_FIELDS + 2] = s_m;
+            info_out[b * MOE_INFO_FIELDS + 3] = s_removed;
+        }
+        if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
+    }
     __syncthreads();
     unsigned allowed = 0;
 #pragma unroll
-    for (int i = 0; i < kVPL; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         if (e < E && inS[e]) allowed |= 1u << i;
     }
     for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
         const int slot = t * kCW + warp;
-        float v[kVPL];
-        load_row(lrow + (size_t)slot * E, E, v);
         const int nt = lane < k ? nat_loc[slot * k + lane] : -1;
         const bool keep = __all_sync(0xffffffffu, lane >= k || (nt >= 0 && inS[nt]));
-        const int c = keep ? nt : warp_topk(v, allowed, E, k);
+        if (keep) {  // the natural routing stands (CTAs other than 0 wrote it already)
+            if (lane < k && nt >= 0) inSel[nt] = 1;
+            if (rank == 0)
+                write_choice(nt, lane < k ? nat_val[slot * k + lane] : -INFINITY, k,
+                             idxb + (size_t)n * k, gb + (size_t)n * k);
+            continue;
+        }
+        float v[VPL];
+        load_row(lrow + (size_t)slot * E, E, v);
+        const int c = warp_topk(v, allowed, E, k);
         const float val = chosen_value(v, c);
         if (lane < k && c >= 0) inSel[c] = 1;
         write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
@@ -640,7 +682,7 @@ cudaError_t allow_smem(K kernel, std::atomic<size_t> &set, size_t bytes) {
         }
     return err;
 }
-std::atomic<size_t> cluster_smem_set{0}, single_smem_set{0};
+std::atomic<size_t> cluster4_smem_set{0}, cluster8_smem_set{0}, single_smem_set{0};
 
 }  // namespace
 
@@ -747,6 +789,24 @@ WeightPrefetch sized(WeightPrefetch pf, int used, int avail, int per_slot) {
     return pf;
 }
 
+// One 8-CTA cluster per tree (+ the prefetch CTAs), VPL logits per lane (E <= 32 VPL).
+template <int VPL>
+cudaError_t launch_cluster(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
+                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
+                           float *gates, uint8_t *elig, int *info, WeightPrefetch pf,
+                           std::atomic<size_t> &smem_set, cudaStream_t s) {
+    const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
+    // wt and lrow [slots][E]; nat_all [N][k]; nat_loc and nat_val [slots][k]
+    const size_t smem =
+        ((size_t)2 * slots * L.E + (size_t)N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
+    cudaError_t err = allow_smem(select_cluster_kernel<VPL>, smem_set, smem);
+    if (err != cudaSuccess) return err;
+    if (pf.ctas > 0)
+        pf = sized(pf, B, active_clusters(select_cluster_kernel<VPL>, kCThreads, smem), 8);
+    return launch_pdl(select_cluster_kernel<VPL>, dim3(B * kCC + pf.ctas), dim3(kCThreads), smem,
+                      s, a, logits, depth, N, L.E, L.k, resident, idx, gates, elig, info, pf);
+}
+
 }  // namespace
 
 WeightPrefetch weight_prefetch(const moe_layer_desc &L, int B, const void *W_gate,
@@ -777,17 +837,11 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
     if (a.mode == MOE_ROUTE_NATURAL)
         return launch_pdl(select_natural_kernel, dim3(B * kNC), dim3(kNW * 32), 0, s, logits, N,
                           L.E, L.k, idx, gates, elig, info);
-    if (N <= kClusterMaxN) {
-        const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
-        const size_t smem =
-            ((size_t)2 * slots * L.E + (size_t)N * L.k + (size_t)slots * L.k) * sizeof(float);
-        cudaError_t err = allow_smem(select_cluster_kernel, cluster_smem_set, smem);
-        if (err != cudaSuccess) return err;
-        if (pf.ctas > 0)
-            pf = sized(pf, B, active_clusters(select_cluster_kernel, kCThreads, smem), 8);
-        return launch_pdl(select_cluster_kernel, dim3(B * kCC + pf.ctas), dim3(kCThreads), smem,
-                          s, a, logits, depth, N, L.E, L.k, resident, idx, gates, elig, info, pf);
-    }
+    if (N <= kClusterMaxN)
+        return L.E <= 128 ? launch_cluster<4>(L, a, logits, depth, B, N, resident, idx, gates,
+                                               elig, info, pf, cluster4_smem_set, s)
+                          : launch_cluster<8>(L, a, logits, depth, B, N, resident, idx, gates,
+                                               elig, info, pf, cluster8_smem_set, s);
     const bool staged = N * L.E <= kStageFloats;
     // staged: logits and demand terms [N][E] each; always: mx, nz, cN [N] and nat [N][k]
     const size_t smem =
