@@ -37,6 +37,10 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     const int tid = threadIdx.x;
     const int A = R * k;
 
+    // the first four expert ids of each thread are in flight while the masks are cleared
+    int ev0[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ev0[u] = tid + u * kThreads < A ? idx[tid + u * kThreads] : -1;
     for (int i = tid; i < nb * E; i += kThreads) mask[i] = 0u;
     if (tid == 0) {  // a fresh check word for this call, keeping what the router reported
         flags[0] = after_router ? flags[kRouterCheckWord] : 0;
@@ -49,7 +53,8 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     for (int a0 = tid; a0 < A; a0 += 4 * kThreads) {
         int ev[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ev[u] = a0 + u * kThreads < A ? idx[a0 + u * kThreads] : -1;
+        for (int u = 0; u < 4; ++u)
+            ev[u] = a0 == tid ? ev0[u] : (a0 + u * kThreads < A ? idx[a0 + u * kThreads] : -1);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int e = ev[u];
@@ -89,63 +94,69 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         }
     }
     __syncthreads();
-    if (tid < 32) {
-        // warp 0: exclusive scans over experts (ascending) of the assignment counts, of
-        // the active flags and of the row-tile counts; lane owns experts [lane*per, +per)
-        const int per = (E + 31) / 32;
+    {
+        // exclusive scans over experts (ascending) of the assignment counts, of the active
+        // flags and of the row-tile counts: a thread per expert, scans within each warp,
+        // then the totals of the lower warps
+        __shared__ int wred[4][kMaxE / 32];
+        const int lane = tid & 31, warp = tid >> 5;
+        const int nw = (E + 31) >> 5;
+        const int c = tid < E ? cnt[tid] : 0;
+        if (warp < nw) {
+            const int wm = __reduce_max_sync(0xffffffffu, c);
+            if (lane == 0) wred[3][warp] = wm;
+        }
+        __syncthreads();
         // row-tile height: the largest expert's tokens rounded up to 16 (every expert in
         // one tile), at most kMaxRowTile (larger experts split into tiles of that many)
         int cmax = 0;
-        for (int i = 0; i < per; ++i) {
-            const int e = tid * per + i;
-            if (e < E) cmax = max(cmax, cnt[e]);
-        }
-        cmax = __reduce_max_sync(0xffffffffu, cmax);
+        for (int w = 0; w < nw; ++w) cmax = max(cmax, wred[3][w]);
         const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
-        int c_tot = 0, a_tot = 0, t_tot = 0;
-        for (int i = 0; i < per; ++i) {
-            const int e = tid * per + i;
-            const int c = e < E ? cnt[e] : 0;
-            c_tot += c;
-            a_tot += c > 0;
-            t_tot += (c + rt_size - 1) / rt_size;
-        }
-        int c_ex = c_tot, a_ex = a_tot, t_ex = t_tot;  // inclusive scans across lanes
+        const int a = c > 0, nt = (c + rt_size - 1) / rt_size;
+        int ci = c, ai = a, ti = nt;  // inclusive scans within the warp
+        if (warp < nw) {
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int c2 = __shfl_up_sync(0xffffffffu, c_ex, o);
-            const int a2 = __shfl_up_sync(0xffffffffu, a_ex, o);
-            const int t2 = __shfl_up_sync(0xffffffffu, t_ex, o);
-            if (tid >= o) {
-                c_ex += c2;
-                a_ex += a2;
-                t_ex += t2;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int c2 = __shfl_up_sync(0xffffffffu, ci, o);
+                const int a2 = __shfl_up_sync(0xffffffffu, ai, o);
+                const int t2 = __shfl_up_sync(0xffffffffu, ti, o);
+                if (lane >= o) {
+                    ci += c2;
+                    ai += a2;
+                    ti += t2;
+                }
+            }
+            if (lane == 31) {
+                wred[0][warp] = ci;
+                wred[1][warp] = ai;
+                wred[2][warp] = ti;
             }
         }
-        c_ex -= c_tot;
-        a_ex -= a_tot;
-        t_ex -= t_tot;
-        for (int i = 0; i < per; ++i) {
-            const int e = tid * per + i;
-            if (e >= E) break;
-            const int c = cnt[e];
-            off[e] = c_ex;
-            c_ex += c;
-            if (c > 0) active[1 + a_ex++] = e;
+        __syncthreads();
+        if (tid < E) {
+            for (int w = 0; w < warp; ++w) {
+                ci += wred[0][w];
+                ai += wred[1][w];
+                ti += wred[2][w];
+            }
+            const int c_ex = ci - c, a_ex = ai - a;
+            int t_ex = ti - nt;
+            off[tid] = c_ex;
+            if (a) active[1 + a_ex] = tid;
             // row tiles of at most rt_size tokens of one expert, for the tensor-core kernel
             for (int n0 = 0; n0 < c; n0 += rt_size) {
                 int *t = rowtiles + kRowTileHeader + 4 * t_ex++;
-                t[0] = e;
-                t[1] = off[e] + n0;  // first permuted row of the tile
+                t[0] = tid;
+                t[1] = c_ex + n0;  // first permuted row of the tile
                 t[2] = min(rt_size, c - n0);
                 t[3] = 0;
             }
-        }
-        if (tid == 31) {
-            off[E] = c_ex;
-            active[0] = a_ex;
-            rowtiles[0] = t_ex;
-            rowtiles[1] = rt_size;
+            if (tid == E - 1) {
+                off[E] = ci;
+                active[0] = ai;
+                rowtiles[0] = ti;
+                rowtiles[1] = rt_size;
+            }
         }
     }
     __syncthreads();
