@@ -437,11 +437,10 @@ def run_gpu(args):
 
 
 def ffn_launches(M, L, path):
-    """Kernel launches of the grouped-expert stage per step: CUDA cores = gate/up +
-    down; tensor cores = token-row gather + gate/up + down."""
-    tc = path == M.MOE_FFN_TCGEN05 or (path == M.MOE_FFN_AUTO and L.dtype == M.MOE_DTYPE_BF16
-                                       and L.d % 64 == 0 and L.f % 64 == 0)
-    return 3 if tc else 2
+    """Kernel launches of the grouped-expert stage per step: two on either path (CUDA
+    cores: gate/up, then down; tensor cores: the token-row gather, then one persistent
+    launch for gate/up and down)."""
+    return 2
 
 
 # ------------------------------------------------------------ reference arm
