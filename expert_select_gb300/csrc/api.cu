@@ -142,13 +142,15 @@ moe_status run_combine(const moe_layer_desc &L, const void *residual, const floa
                                       R, y, s));
 }
 
-// permute -> experts -> combine, shared by moe_expert_forward and moe_tree_forward.
+// permute (unless the selection did it) -> experts -> combine, shared by
+// moe_expert_forward and moe_tree_forward.
 static moe_status run_experts(const moe_layer_desc &L, const void *x, const void *Wg,
                               const void *Wu, const void *Wd, const int *slot, const int *idx,
                               const float *gates, int R, void *y, void *ws, const Workspace &w,
                               int *counts, int *offsets, int *perm, const moe_run_opts *opts,
-                              bool after_router, cudaStream_t s) {
-    moe_status st = run_permute(L, idx, R, ws, w, counts, offsets, perm, after_router, s);
+                              bool after_router, bool permuted, cudaStream_t s) {
+    moe_status st = MOE_OK;
+    if (!permuted) st = run_permute(L, idx, R, ws, w, counts, offsets, perm, after_router, s);
     if (st != MOE_OK) return st;
     st = run_ffn(L, x, Wg, Wu, Wd, slot, nullptr, R, ws, w, counts, offsets, perm, opts, s);
     if (st != MOE_OK) return st;
@@ -221,7 +223,8 @@ moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
     if (B * N > 0 && (!logits || !depth || !topk_idx || !gates)) return MOE_ERR_ARG;
     if (a.prune && !resident) return MOE_ERR_ARG;
     return cuda_status(launch_select(*L, a, logits, depth, B, N, resident, topk_idx, gates,
-                                     eligible, info, WeightPrefetch{}, (cudaStream_t)stream));
+                                     eligible, info, WeightPrefetch{}, PermuteOut{}, nullptr,
+                                     (cudaStream_t)stream));
 }
 
 moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int R, int *counts,
@@ -252,7 +255,7 @@ moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void
     const Workspace w = workspace_layout(*L, 1, R);
     return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, R, y,
                        workspace, w, at<int>(workspace, w.counts), at<int>(workspace, w.offsets),
-                       at<int>(workspace, w.perm), opts, false, (cudaStream_t)stream);
+                       at<int>(workspace, w.perm), opts, false, false, (cudaStream_t)stream);
 }
 
 moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P, const void *x,
@@ -285,11 +288,15 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
         cudaSuccess)
         return MOE_ERR_CUDA;
     const WeightPrefetch pf = weight_prefetch(*L, B, W_gate, W_up, W_down, slot_of_expert);
-    if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, pf, s) !=
-        cudaSuccess)
+    const PermuteOut po{counts, offsets, perm, at<int>(workspace, w.pos),
+                        at<int>(workspace, w.active), at<int>(workspace, w.rowtiles),
+                        at<int>(workspace, w.flags), 1};
+    bool permuted = false;
+    if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, pf, po,
+                      &permuted, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, idx, gates, R, y, workspace,
-                       w, counts, offsets, perm, opts, true, s);
+                       w, counts, offsets, perm, opts, true, permuted, s);
 }
 
 moe_status moe_workspace_check(void *workspace, int *flags, moe_stream_t stream) {

@@ -79,10 +79,17 @@ struct WeightPrefetch {
 // the weights cannot be prefetched or the SMs are taken by the selection itself).
 WeightPrefetch weight_prefetch(const moe_layer_desc &L, int B, const void *W_gate,
                                const void *W_up, const void *W_down, const int *slot_of_expert);
+// The arrays of the permute step (see launch_permute), for a selection launch that also
+// performs it: one tree per block on the cluster path. counts == nullptr: it does not.
+struct PermuteOut {
+    int *counts, *offsets, *perm, *pos, *active, *rowtiles, *flags;
+    int after_router;
+};
+// *permuted (may be null) tells whether the launch also performed the permute step.
 cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, const WeightPrefetch &pf,
-                          cudaStream_t s);
+                          const PermuteOut &po, bool *permuted, cudaStream_t s);
 
 // Row tiles of the tensor-core expert kernel: at most kMaxRowTile tokens of one expert
 // (its MMA N is at most 256). The permute kernel picks the height as the largest expert's

@@ -102,7 +102,7 @@ extern "C" moe_status moe_offload_forward(
         cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_select(*L, a, logits, depth, B, N, a.prune ? res_dev : nullptr, idx, gates, elig,
-                      info, WeightPrefetch{}, s) != cudaSuccess)
+                      info, WeightPrefetch{}, PermuteOut{}, nullptr, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     moe_status st = run_permute(*L, idx, R, workspace, w, counts, offsets, perm, true, s);
     if (st != MOE_OK) return st;

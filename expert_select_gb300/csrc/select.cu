@@ -452,20 +452,119 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return s;
 }
 
+// The permute step for a block of one tree, on CTA 0 of the selection cluster ("MoE and
+// speculative decoding" blog, pipeline step "permute / group by expert"), with the same
+// results as the permute kernel: a stable counting sort of the assignments (n, j) by
+// (expert, node, slot). rmask[e] holds the nodes that chose e (a node chooses an expert
+// at most once, so within an expert the order is node order) and fin_all[n][j] the choices.
+// Writes counts, offsets, the active-expert list, the row tiles (height: the largest
+// expert's count rounded up to 16, at most kMaxRowTile), perm and pos, and starts the
+// call's check word (keeping what the router reported).
+__device__ void permute_tree(const PermuteOut &po, const int *fin_all,
+                             const uint32_t (*rmask)[kClusterMaxN / 32], int *soff,
+                             int (*wsc)[kCW], int N, int E, int k) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nbw = (N + 31) >> 5;
+    const int A = N * k;
+    if (tid == 0) {
+        po.flags[0] = po.after_router ? po.flags[kRouterCheckWord] : 0;
+        po.flags[kRouterCheckWord] = 0;
+    } else if (tid < 64 && tid != kRouterCheckWord) {
+        po.flags[tid] = 0;
+    }
+    int c = 0;
+    if (tid < E)
+        for (int q = 0; q < nbw; ++q) c += __popc(rmask[tid][q]);
+    const int nw = (E + 31) >> 5;
+    if (warp < nw) {
+        const int wm = __reduce_max_sync(0xffffffffu, c);
+        if (lane == 0) wsc[3][warp] = wm;
+    }
+    __syncthreads();
+    int cmax = 0;
+    for (int w = 0; w < nw; ++w) cmax = max(cmax, wsc[3][w]);
+    const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
+    const int act = c > 0, nt = (c + rt_size - 1) / rt_size;
+    int ci = c, ai = act, ti = nt;  // inclusive scans within the warp
+    if (warp < nw) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int c2 = __shfl_up_sync(0xffffffffu, ci, o);
+            const int a2 = __shfl_up_sync(0xffffffffu, ai, o);
+            const int t2 = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) {
+                ci += c2;
+                ai += a2;
+                ti += t2;
+            }
+        }
+        if (lane == 31) {
+            wsc[0][warp] = ci;
+            wsc[1][warp] = ai;
+            wsc[2][warp] = ti;
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        for (int w = 0; w < warp; ++w) {
+            ci += wsc[0][w];
+            ai += wsc[1][w];
+            ti += wsc[2][w];
+        }
+        const int c_ex = ci - c;
+        int t_ex = ti - nt;
+        soff[tid] = c_ex;
+        po.counts[tid] = c;
+        po.offsets[tid] = c_ex;
+        if (act) po.active[1 + ai - act] = tid;
+        for (int n0 = 0; n0 < c; n0 += rt_size) {
+            int *t = po.rowtiles + kRowTileHeader + 4 * t_ex++;
+            t[0] = tid;
+            t[1] = c_ex + n0;  // first permuted row of the tile
+            t[2] = min(rt_size, c - n0);
+            t[3] = 0;
+        }
+        if (tid == E - 1) {
+            soff[E] = ci;
+            po.offsets[E] = ci;
+            po.active[0] = ai;
+            po.rowtiles[0] = ti;
+            po.rowtiles[1] = rt_size;
+        }
+    }
+    __syncthreads();
+    for (int a = tid; a < A; a += kCThreads) {
+        const int e = fin_all[a];
+        if (e < 0 || e >= E) {  // cannot happen for a selection of k distinct experts
+            po.pos[a] = -1;
+            atomicOr(po.flags, FLAG_BAD_EXPERT);
+            continue;
+        }
+        const int n = a / k, q1 = n >> 5;
+        int pre = __popc(rmask[e][q1] & ((1u << (n & 31)) - 1u));
+        for (int q = 0; q < q1; ++q) pre += __popc(rmask[e][q]);
+        const int p = soff[e] + pre;
+        po.perm[p] = a;
+        po.pos[a] = p;
+    }
+    for (int p = soff[E] + tid; p < A; p += kCThreads) po.perm[p] = -1;
+}
+
 template <int VPL>
 __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(kCThreads, 1)
 select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                       const int *__restrict__ depth, int N, int E, int k,
                       const uint8_t *__restrict__ resident, int *__restrict__ idx_out,
                       float *__restrict__ gates_out, uint8_t *__restrict__ elig_out,
-                      int *__restrict__ info_out, WeightPrefetch pf) {
+                      int *__restrict__ info_out, WeightPrefetch pf, PermuteOut po) {
     // the last pf.ctas CTAs (whole clusters of their own) only prefetch
     if ((int)blockIdx.x >= (int)gridDim.x - pf.ctas) {
         prefetch_root_experts(pf, logits, E, k, (int)blockIdx.x - ((int)gridDim.x - pf.ctas));
         return;
     }
     // wt [slots][E], lrow [slots][E] (this CTA's logit rows), nat_all [N][k] (CTA 0),
-    // nat_loc [slots][k], nat_val [slots][k] (their logits)
+    // nat_loc [slots][k], nat_val [slots][k] (their logits), fin_all [N][k] (CTA 0: the
+    // final choices, for the permute step)
     extern __shared__ float cdyn[];
     __shared__ float part[kCC][kMaxE];  // CTA 0: partial demand of every CTA
     __shared__ int selAll[kCC][kMaxE];  // CTA 0: experts chosen by every CTA's nodes
@@ -473,6 +572,10 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     __shared__ float red[2][kCW];
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
     __shared__ int s_m, s_removed;
+    // CTA 0, permute step: bit n of rmask[e][n / 32] = node n chose e; offsets per expert
+    __shared__ uint32_t rmask[kMaxE][kClusterMaxN / 32];
+    __shared__ int soff[kMaxE + 1];
+    __shared__ int wsc[4][kCW];
 
     // every CTA of the cluster must be running before any touches another's shared
     // memory: arrive now, wait just before the first remote store
@@ -488,7 +591,9 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     int *nat_all = reinterpret_cast<int *>(lrow + (size_t)slots * E);
     int *nat_loc = nat_all + (size_t)N * k;
     float *nat_val = reinterpret_cast<float *>(nat_loc + (size_t)slots * k);
+    int *fin_all = reinterpret_cast<int *>(nat_val + (size_t)slots * k);
     int *nat0 = cl.map_shared_rank(nat_all, 0);
+    const bool fuse = po.counts != nullptr;
     const float *Lg = logits + (size_t)b * N * E;
     const int *dep = depth + (size_t)b * N;
     int *idxb = idx_out + (size_t)b * N * k;
@@ -499,6 +604,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         inSel[e] = 0;
         inA[e] = 0;
     }
+    if (fuse)
+        for (int i = tid; i < kMaxE * (kClusterMaxN / 32); i += kCThreads) (&rmask[0][0])[i] = 0u;
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
     // ---- phase A: this CTA's nodes ----
@@ -635,23 +742,30 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         const int e = lane + 32 * i;
         if (e < E && inS[e]) allowed |= 1u << i;
     }
+    int *fin0 = cl.map_shared_rank(fin_all, 0);
+    uint32_t *rm0 = cl.map_shared_rank(&rmask[0][0], 0);
     for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
         const int slot = t * kCW + warp;
         const int nt = lane < k ? nat_loc[slot * k + lane] : -1;
         const bool keep = __all_sync(0xffffffffu, lane >= k || (nt >= 0 && inS[nt]));
+        int c = nt;
         if (keep) {  // the natural routing stands (CTAs other than 0 wrote it already)
-            if (lane < k && nt >= 0) inSel[nt] = 1;
             if (rank == 0)
                 write_choice(nt, lane < k ? nat_val[slot * k + lane] : -INFINITY, k,
                              idxb + (size_t)n * k, gb + (size_t)n * k);
-            continue;
+        } else {
+            float v[VPL];
+            load_row(lrow + (size_t)slot * E, E, v);
+            c = warp_topk(v, allowed, E, k);
+            write_choice(c, chosen_value(v, c), k, idxb + (size_t)n * k, gb + (size_t)n * k);
         }
-        float v[VPL];
-        load_row(lrow + (size_t)slot * E, E, v);
-        const int c = warp_topk(v, allowed, E, k);
-        const float val = chosen_value(v, c);
-        if (lane < k && c >= 0) inSel[c] = 1;
-        write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
+        if (lane < k) {
+            if (c >= 0) inSel[c] = 1;
+            if (fuse) {  // into CTA 0's shared memory, for the permute step
+                fin0[n * k + lane] = c;
+                if (c >= 0) atomicOr(rm0 + c * (kClusterMaxN / 32) + (n >> 5), 1u << (n & 31));
+            }
+        }
     }
     __syncthreads();
     if (tid < E) cl.map_shared_rank(&selAll[0][0], 0)[rank * kMaxE + tid] = inSel[tid];
@@ -666,6 +780,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             info_out[b * MOE_INFO_FIELDS + 0] = u_nat;
             info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
         }
+        if (fuse) permute_tree(po, fin_all, rmask, soff, wsc, N, E, k);
     }
 }
 
@@ -794,17 +909,17 @@ template <int VPL>
 cudaError_t launch_cluster(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                            const int *depth, int B, int N, const uint8_t *resident, int *idx,
                            float *gates, uint8_t *elig, int *info, WeightPrefetch pf,
-                           std::atomic<size_t> &smem_set, cudaStream_t s) {
+                           PermuteOut po, std::atomic<size_t> &smem_set, cudaStream_t s) {
     const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
-    // wt and lrow [slots][E]; nat_all [N][k]; nat_loc and nat_val [slots][k]
+    // wt and lrow [slots][E]; nat_all and fin_all [N][k]; nat_loc and nat_val [slots][k]
     const size_t smem =
-        ((size_t)2 * slots * L.E + (size_t)N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
+        ((size_t)2 * slots * L.E + (size_t)2 * N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
     cudaError_t err = allow_smem(select_cluster_kernel<VPL>, smem_set, smem);
     if (err != cudaSuccess) return err;
     if (pf.ctas > 0)
         pf = sized(pf, B, active_clusters(select_cluster_kernel<VPL>, kCThreads, smem), 8);
     return launch_pdl(select_cluster_kernel<VPL>, dim3(B * kCC + pf.ctas), dim3(kCThreads), smem,
-                      s, a, logits, depth, N, L.E, L.k, resident, idx, gates, elig, info, pf);
+                      s, a, logits, depth, N, L.E, L.k, resident, idx, gates, elig, info, pf, po);
 }
 
 }  // namespace
@@ -828,7 +943,8 @@ WeightPrefetch weight_prefetch(const moe_layer_desc &L, int B, const void *W_gat
 cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                           const int *depth, int B, int N, const uint8_t *resident, int *idx,
                           float *gates, uint8_t *elig, int *info, const WeightPrefetch &pf_in,
-                          cudaStream_t s) {
+                          const PermuteOut &po_in, bool *permuted, cudaStream_t s) {
+    if (permuted) *permuted = false;
     if (B <= 0 || N <= 0) return cudaSuccess;
     WeightPrefetch pf = pf_in;
     // Natural routing: no prefetch. Its selection is short (a few microseconds), so the
@@ -837,11 +953,17 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
     if (a.mode == MOE_ROUTE_NATURAL)
         return launch_pdl(select_natural_kernel, dim3(B * kNC), dim3(kNW * 32), 0, s, logits, N,
                           L.E, L.k, idx, gates, elig, info);
-    if (N <= kClusterMaxN)
-        return L.E <= 128 ? launch_cluster<4>(L, a, logits, depth, B, N, resident, idx, gates,
-                                               elig, info, pf, cluster4_smem_set, s)
-                          : launch_cluster<8>(L, a, logits, depth, B, N, resident, idx, gates,
-                                               elig, info, pf, cluster8_smem_set, s);
+    if (N <= kClusterMaxN) {
+        // a block of one tree: the cluster also performs the permute step
+        const PermuteOut po = (B == 1 && po_in.counts) ? po_in : PermuteOut{};
+        const cudaError_t err =
+            L.E <= 128 ? launch_cluster<4>(L, a, logits, depth, B, N, resident, idx, gates, elig,
+                                           info, pf, po, cluster4_smem_set, s)
+                       : launch_cluster<8>(L, a, logits, depth, B, N, resident, idx, gates, elig,
+                                           info, pf, po, cluster8_smem_set, s);
+        if (err == cudaSuccess && permuted) *permuted = po.counts != nullptr;
+        return err;
+    }
     const bool staged = N * L.E <= kStageFloats;
     // staged: logits and demand terms [N][E] each; always: mx, nz, cN [N] and nat [N][k]
     const size_t smem =
