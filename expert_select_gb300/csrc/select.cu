@@ -812,15 +812,25 @@ constexpr int kNC = 8;    // CTAs per tree
 constexpr int kNW = 16;   // warps per CTA
 constexpr int kNWords = kMaxE / 32;
 
-__global__ void __cluster_dims__(kNC, 1, 1) __launch_bounds__(kNW * 32)
+__global__ void __cluster_dims__(kNC, 1, 1) __launch_bounds__(kNW * 32, 1)
 select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
                       int *__restrict__ idx_out, float *__restrict__ gates_out,
-                      uint8_t *__restrict__ elig_out, int *__restrict__ info_out) {
+                      uint8_t *__restrict__ elig_out, int *__restrict__ info_out,
+                      PermuteOut po) {
+    static_assert(kNW == kCW, "the permute step assumes the selection kernels' block size");
+    extern __shared__ int nfin[];  // CTA 0, permute step: the choices [N][k]
     __shared__ uint32_t mask[kNWords];
+    // CTA 0, permute step: bit n of rmask[e][n / 32] = node n chose e; offsets per expert
+    __shared__ uint32_t rmask[kMaxE][kClusterMaxN / 32];
+    __shared__ int soff[kMaxE + 1];
+    __shared__ int wsc[4][kCW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool fuse = po.counts != nullptr;
     if (tid < kNWords) mask[tid] = 0u;
-    // CTA 0's bit set must be cleared before any CTA ORs into it: the arrive releases
-    // the clearing store, the wait before the first remote update acquires it
+    if (fuse)
+        for (int i = tid; i < kMaxE * (kClusterMaxN / 32); i += kNW * 32) (&rmask[0][0])[i] = 0u;
+    // CTA 0's bit sets must be cleared before any CTA ORs into them: the arrive releases
+    // the clearing stores, the wait before the first remote update acquires them
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     pdl_wait();
     cg::cluster_group cl = cg::this_cluster();
@@ -829,7 +839,10 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
     const float *Lg = logits + (size_t)b * N * E;
     int *idxb = idx_out + (size_t)b * N * k;
     float *gb = gates_out + (size_t)b * N * k;
+    int *fin0 = cl.map_shared_rank(nfin, 0);
+    uint32_t *rm0 = cl.map_shared_rank(&rmask[0][0], 0);
     __syncthreads();  // the local bit set is clear
+    if (fuse) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     for (int n = rank * kNW + warp; n < N; n += kNC * kNW) {
         float v[kVPL];
         load_row(Lg + (size_t)n * E, E, v);
@@ -837,9 +850,13 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
         const float val = chosen_value(v, c);
         write_choice(c, val, k, idxb + (size_t)n * k, gb + (size_t)n * k);
         if (lane < k && c >= 0) atomicOr(&mask[c >> 5], 1u << (c & 31));
+        if (fuse && lane < k) {  // into CTA 0's shared memory, for the permute step
+            fin0[n * k + lane] = c;
+            if (c >= 0) atomicOr(rm0 + c * (kClusterMaxN / 32) + (n >> 5), 1u << (n & 31));
+        }
     }
     __syncthreads();
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (!fuse) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (tid < kNWords && mask[tid]) atomicOr(cl.map_shared_rank(&mask[tid], 0), mask[tid]);
     cl.sync();
     if (rank == 0) {
@@ -853,6 +870,7 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
         }
         if (elig_out)
             for (int e = tid; e < E; e += kNW * 32) elig_out[(size_t)b * E + e] = 1;
+        if (fuse) permute_tree(po, nfin, rmask, soff, wsc, N, E, k);
     }
 }
 
@@ -950,9 +968,17 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
     // Natural routing: no prefetch. Its selection is short (a few microseconds), so the
     // prefetch CTAs would outlast it and delay the chain; measured on GB300 the layer was
     // 1% slower with them.
-    if (a.mode == MOE_ROUTE_NATURAL)
-        return launch_pdl(select_natural_kernel, dim3(B * kNC), dim3(kNW * 32), 0, s, logits, N,
-                          L.E, L.k, idx, gates, elig, info);
+    if (a.mode == MOE_ROUTE_NATURAL) {
+        // a block of one tree of up to kClusterMaxN nodes: the cluster also permutes
+        const PermuteOut po =
+            (B == 1 && N <= kClusterMaxN && po_in.counts) ? po_in : PermuteOut{};
+        const size_t smem = po.counts ? (size_t)N * L.k * sizeof(int) : 0;
+        const cudaError_t err = launch_pdl(select_natural_kernel, dim3(B * kNC), dim3(kNW * 32),
+                                           smem, s, logits, N, L.E, L.k, idx, gates, elig, info,
+                                           po);
+        if (err == cudaSuccess && permuted) *permuted = po.counts != nullptr;
+        return err;
+    }
     if (N <= kClusterMaxN) {
         // a block of one tree: the cluster also performs the permute step
         const PermuteOut po = (B == 1 && po_in.counts) ? po_in : PermuteOut{};
