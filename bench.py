@@ -393,9 +393,11 @@ def run_gpu(args):
     sec_o = timed(Kv, other, counts=cnat, info=inat)
     u_o = (cnat.cpu().numpy() > 0).sum(axis=1)
 
-    # router, select, permute, combine + the grouped-expert launches
-    # router, select, permute (a second, placing kernel past 2048 assignments), combine
-    launches_per_step = 3 + (2 if N * shape.k > 2048 else 1) + ffn_launches(M, L, args.ffn_path)
+    # router, select, combine + the grouped-expert launches; the permute step runs inside
+    # the selection launch for a block of one tree of up to 256 nodes, else in its own
+    # kernel (and a second, placing kernel past 2048 assignments)
+    permute_launches = 0 if N <= 256 else (2 if N * shape.k > 2048 else 1)
+    launches_per_step = 3 + permute_launches + ffn_launches(M, L, args.ffn_path)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -459,15 +459,15 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // at most once, so within an expert the order is node order) and fin_all[n][j] the choices.
 // Writes counts, offsets, the active-expert list, the row tiles (height: the largest
 // expert's count rounded up to 16, at most kMaxRowTile), perm and pos, and starts the
-// call's check word (keeping what the router reported).
+// call's check word (keeping router_word, the router's, read by thread 0 long before).
 __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
                              const uint32_t (*rmask)[kClusterMaxN / 32], int *soff,
-                             int (*wsc)[kCW], int N, int E, int k) {
+                             int (*wsc)[kCW], int N, int E, int k, int router_word) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nbw = (N + 31) >> 5;
     const int A = N * k;
     if (tid == 0) {
-        po.flags[0] = po.after_router ? po.flags[kRouterCheckWord] : 0;
+        po.flags[0] = po.after_router ? router_word : 0;
         po.flags[kRouterCheckWord] = 0;
     } else if (tid < 64 && tid != kRouterCheckWord) {
         po.flags[tid] = 0;
@@ -594,6 +594,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     int *fin_all = reinterpret_cast<int *>(nat_val + (size_t)slots * k);
     int *nat0 = cl.map_shared_rank(nat_all, 0);
     const bool fuse = po.counts != nullptr;
+    // the router's check word, used at the very end (its load latency is hidden)
+    const int router_word = (fuse && rank == 0 && tid == 0) ? po.flags[kRouterCheckWord] : 0;
     const float *Lg = logits + (size_t)b * N * E;
     const int *dep = depth + (size_t)b * N;
     int *idxb = idx_out + (size_t)b * N * k;
@@ -768,19 +770,23 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         }
     }
     __syncthreads();
-    if (tid < E) cl.map_shared_rank(&selAll[0][0], 0)[rank * kMaxE + tid] = inSel[tid];
+    if (!fuse && tid < E) cl.map_shared_rank(&selAll[0][0], 0)[rank * kMaxE + tid] = inSel[tid];
     cl.sync();  // after this CTA 0 reads only its own shared memory
     if (rank == 0) {
         int sel = 0;
-        if (tid < E)
-            for (int r = 0; r < kCC; ++r) sel |= selAll[r][tid];
+        if (tid < E) {
+            if (fuse)  // the node masks of the permute step hold the union too
+                for (int q = 0; q < kClusterMaxN / 32; ++q) sel |= rmask[tid][q] != 0u;
+            else
+                for (int r = 0; r < kCC; ++r) sel |= selAll[r][tid];
+        }
         const int u_sel = __syncthreads_count(sel);
         const int u_nat = __syncthreads_count(tid < E && inU[tid]);
         if (tid == 0 && info_out) {
             info_out[b * MOE_INFO_FIELDS + 0] = u_nat;
             info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
         }
-        if (fuse) permute_tree(po, fin_all, rmask, soff, wsc, N, E, k);
+        if (fuse) permute_tree(po, fin_all, rmask, soff, wsc, N, E, k, router_word);
     }
 }
 
@@ -841,6 +847,8 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
     float *gb = gates_out + (size_t)b * N * k;
     int *fin0 = cl.map_shared_rank(nfin, 0);
     uint32_t *rm0 = cl.map_shared_rank(&rmask[0][0], 0);
+    // the router's check word, used at the very end (its load latency is hidden)
+    const int router_word = (fuse && rank == 0 && tid == 0) ? po.flags[kRouterCheckWord] : 0;
     __syncthreads();  // the local bit set is clear
     if (fuse) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     for (int n = rank * kNW + warp; n < N; n += kNC * kNW) {
@@ -870,7 +878,7 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
         }
         if (elig_out)
             for (int e = tid; e < E; e += kNW * 32) elig_out[(size_t)b * E + e] = 1;
-        if (fuse) permute_tree(po, nfin, rmask, soff, wsc, N, E, k);
+        if (fuse) permute_tree(po, nfin, rmask, soff, wsc, N, E, k, router_word);
     }
 }
 
