@@ -716,3 +716,58 @@ def test_draft_select_then_verify_against_oracle():
                     rows=rows, mode=O.NATURAL)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
     _assert_close_rows(y.float().cpu().numpy()[rows], ref["y"], shape)
+
+
+E256_BF16 = W.LayerShape(d=256, E=256, k=8, f=128, dtype="bf16")
+
+
+@pytest.mark.parametrize("shape,draft_tokens,mode", [
+    (E256_BF16, 64, M.MOE_ROUTE_ACCEPT),           # one tree: selection cluster permutes, 8 logits/lane
+    (E256_BF16, 64, M.MOE_ROUTE_NATURAL),          # one tree: natural cluster permutes
+    (W.QWEN3_30B_A3B, 299, M.MOE_ROUTE_ACCEPT),    # 300 nodes: one-CTA selection + permute kernel
+    (W.QWEN3_30B_A3B, 299, M.MOE_ROUTE_NATURAL),   # 300 nodes: permute kernel
+], ids=["e256-acc", "e256-nat", "n300-acc", "n300-nat"])
+def test_tree_forward_permute_outputs(shape, draft_tokens, mode):
+    """The layer's permute outputs, whichever kernel produced them (the selection launch for
+    a block of one tree of up to 256 nodes, else the permute kernel), equal the oracle's
+    counting sort of the layer's own expert choices, and the standalone permute kernel's;
+    the layer output matches the oracle on sampled rows."""
+    t = W.eagle_tree(4242, draft_tokens=draft_tokens)
+    N = t.N
+    x = W.hidden_states(4243, t.parent, shape.d, shape.torch_dtype)
+    wr = W.router_weight(4244, shape, std=0.1)
+    wg, wu, wd = _weights(shape, 4245)
+    L = _desc(shape)
+    P = M.select_params(mode, W.C_EAGLE)
+    idx = torch.empty(N, shape.k, dtype=torch.int32, device=DEV)
+    counts = torch.empty(shape.E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(shape.E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(N * shape.k, dtype=torch.int32, device=DEV)
+    y = torch.empty(N, shape.d, dtype=shape.torch_dtype, device=DEV)
+    ws = M.workspace(L, 1, N)
+    dp = torch.from_numpy(t.depth.copy()).to(DEV)
+    M.moe_tree_forward(L, P, x.to(DEV), wr.to(DEV), wg, wu, wd, None, dp, 1, N, None, y, ws,
+                       M.tree_outputs(topk_idx=idx, counts=counts, offsets=offsets, perm=perm))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    got_idx = idx.cpu().numpy()
+    rc, ro, rp = O.permute(got_idx, shape.E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(perm.cpu().numpy(), rp)
+    # the standalone permute kernel on the same choices
+    c2, o2, p2 = torch.empty_like(counts), torch.empty_like(offsets), torch.empty_like(perm)
+    ws2 = M.workspace(L, 1, N)
+    M.moe_expert_permute(L, idx, c2, o2, p2, ws2)
+    _sync()
+    np.testing.assert_array_equal(c2.cpu().numpy(), counts.cpu().numpy())
+    np.testing.assert_array_equal(o2.cpu().numpy(), offsets.cpu().numpy())
+    np.testing.assert_array_equal(p2.cpu().numpy(), perm.cpu().numpy())
+    # the layer output on sampled rows, against the oracle's combine of the same choices
+    rows = sorted(np.random.default_rng(5).choice(N, 6, replace=False).tolist())
+    gates = torch.empty(N, shape.k, device=DEV)
+    M.moe_tree_forward(L, P, x.to(DEV), wr.to(DEV), wg, wu, wd, None, dp, 1, N, None, y, ws,
+                       M.tree_outputs(gates=gates))
+    _sync()
+    yr = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got_idx, gates.cpu().numpy(), rows=rows)
+    _assert_close_rows(y.float().cpu().numpy()[rows], yr, shape)
