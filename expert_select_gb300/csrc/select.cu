@@ -420,6 +420,17 @@ constexpr int kCThreads = kCW * 32;
 constexpr int kClusterMaxN = 256;
 static_assert(kCThreads >= 2 * kMaxE, "phase B takes at least two threads per expert");
 
+// Cluster barrier whose arrival releases this thread's earlier writes to the cluster only
+// when `release` (uniform over the CTA); the wait always acquires. A CTA whose writes no
+// other CTA reads next need not wait for them (global stores in flight) before arriving.
+__device__ __forceinline__ void cluster_barrier(bool release) {
+    if (release)
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    else
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Rank of expert e under the order of the keys rk (desc: larger first, else smaller
 // first; equal keys: lower id first), i.e. the number of experts before it. `per`
 // consecutive threads (a power of two dividing 32) share e: each counts one slice of the
@@ -726,7 +737,9 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                          idxb + (size_t)n * k, gb + (size_t)n * k);
         }
     }
-    cl.sync();
+    // only CTA 0's writes (the eligible set) must be visible past this barrier: the other
+    // CTAs arrive without waiting for their global stores
+    cluster_barrier(rank == 0);
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
     if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
@@ -771,7 +784,10 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     }
     __syncthreads();
     if (!fuse && tid < E) cl.map_shared_rank(&selAll[0][0], 0)[rank * kMaxE + tid] = inSel[tid];
-    cl.sync();  // after this CTA 0 reads only its own shared memory
+    // the other CTAs' writes into CTA 0's shared memory must be visible to CTA 0 past this
+    // barrier; CTA 0 arrives without waiting for its global stores. After it CTA 0 reads
+    // only its own shared memory.
+    cluster_barrier(rank != 0);
     if (rank == 0) {
         int sel = 0;
         if (tid < E) {
