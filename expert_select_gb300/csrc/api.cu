@@ -102,6 +102,7 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
     fa.counts = counts;
     fa.offsets = offsets;
     fa.perm = perm;
+    fa.pos = at<int>(ws, w.pos);
     fa.active = at<int>(ws, w.active);
     fa.rowtiles = at<int>(ws, w.rowtiles);
     fa.R = R;

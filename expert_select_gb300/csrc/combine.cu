@@ -39,7 +39,8 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
 
-// `res` (may be null, may alias y) is added first: y = res + sum_j g_j O_j.
+// `res` (may be null, may alias y) is added first: y = res + sum_j g_j O_j, over the slots
+// in ascending j. A thread per 4 columns of a row.
 template <typename TO>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
@@ -62,6 +63,59 @@ combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
     store4<TO>(y + (size_t)r * d + c, acc);
 }
 
+// The same for small blocks, where the kernel is bound by load latency: every slot's
+// position and gate are loaded first, then every slot's output piece (up to KMAX slots in
+// flight per thread), and the sum runs over the slots in ascending j as above. Large
+// blocks keep the kernel above: its fewer registers let more threads stream.
+template <typename TO, int KMAX>
+__global__ void __launch_bounds__(kThreads)
+combine_small_kernel(const float *__restrict__ o, const int *__restrict__ pos,
+                     const float *__restrict__ gates, const TO *res, int d, int k, TO *y) {
+    pdl_wait();
+    const int r = blockIdx.x;
+    const int c = (blockIdx.y * kThreads + threadIdx.x) * 4;
+    if (c >= d) return;
+    int p[KMAX];
+    float g[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        p[j] = j < k ? pos[r * k + j] : -1;
+        g[j] = j < k ? gates[r * k + j] : 0.f;
+    }
+    float4 acc = res ? load4<TO>(res + (size_t)r * d + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+        if (p[j] >= 0) v[j] = __ldg(reinterpret_cast<const float4 *>(o + (size_t)p[j] * d + c));
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (p[j] < 0) continue;
+        acc.x = fmaf(g[j], v[j].x, acc.x);
+        acc.y = fmaf(g[j], v[j].y, acc.y);
+        acc.z = fmaf(g[j], v[j].z, acc.z);
+        acc.w = fmaf(g[j], v[j].w, acc.w);
+    }
+    store4<TO>(y + (size_t)r * d + c, acc);
+}
+
+// Assignments up to which the combine takes the small-block kernel.
+constexpr int kSmallCombine = 2048;
+
+template <typename TO>
+cudaError_t launch_combine_t(const float *o, const int *pos, const float *gates,
+                             const TO *res, int R, int d, int k, TO *y, cudaStream_t s) {
+    const dim3 grid(R, (d / 4 + kThreads - 1) / kThreads);
+    if (R * k <= kSmallCombine) {
+        if (k <= 8)
+            return launch_pdl(combine_small_kernel<TO, 8>, grid, dim3(kThreads), 0, s, o, pos,
+                              gates, res, d, k, y);
+        return launch_pdl(combine_small_kernel<TO, kMaxK>, grid, dim3(kThreads), 0, s, o, pos,
+                          gates, res, d, k, y);
+    }
+    return launch_pdl(combine_kernel<TO>, grid, dim3(kThreads), 0, s, o, pos, gates, res, d, k,
+                      y);
+}
+
 struct PublishArgs {
     int slot[kMaxE];
     uint8_t res[kMaxE];
@@ -81,12 +135,10 @@ cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *p
                            const float *gates, const void *residual, int R, void *y,
                            cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    dim3 grid(R, (L.d / 4 + kThreads - 1) / kThreads);
     if (L.dtype == MOE_DTYPE_BF16)
-        return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s, o, pos,
-                          gates, (const __nv_bfloat16 *)residual, L.d, L.k, (__nv_bfloat16 *)y);
-    return launch_pdl(combine_kernel<float>, grid, dim3(kThreads), 0, s, o, pos, gates,
-                      (const float *)residual, L.d, L.k, (float *)y);
+        return launch_combine_t(o, pos, gates, (const __nv_bfloat16 *)residual, R, L.d, L.k,
+                                (__nv_bfloat16 *)y, s);
+    return launch_combine_t(o, pos, gates, (const float *)residual, R, L.d, L.k, (float *)y, s);
 }
 
 cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,

@@ -115,6 +115,7 @@ struct FfnArgs {
     const int *slot;     // [E] or nullptr
     const uint8_t *pass; // [E] or nullptr: experts with 0 are skipped (not an error)
     const int *counts, *offsets, *perm, *active, *rowtiles;
+    const int *pos;      // [R*k] permuted position of each assignment (-1: skipped)
     int R, d, f, E, k, dtype;
     int slots;           // expert slots in the weight pools
     int *flags;

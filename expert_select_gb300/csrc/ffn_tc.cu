@@ -468,37 +468,37 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                      : "memory");
 }
 
-// Gathers the token rows of every assignment into permuted order: xp[p] = x[perm[p] / k],
-// a warp per row (16-byte loads, all of a lane's loads issued before its stores), rows
-// strided over the grid. Block 0 also zeroes the expert kernel's ticket counter and
-// row-tile counters.
+// Gathers the token rows of every assignment into permuted order: xp[pos[a]] = x[a / k]
+// for assignment a (row a / k, slot a % k), a warp per assignment, strided over the grid.
+// The source row needs no lookup, so the row's loads (all of a lane's pieces of a chunk of
+// 256 16-byte pieces at once) and the destination's lookup are in flight together. Block 0
+// also zeroes the expert kernel's ticket counter and row-tile counters.
 constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
-gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ perm,
-                   const int *__restrict__ offsets, int E, int k, int d,
-                   __nv_bfloat16 *__restrict__ xp, int *__restrict__ sched, int n_sched) {
+gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int *__restrict__ pos, int A,
+                   int k, int d, __nv_bfloat16 *__restrict__ xp, int *__restrict__ sched,
+                   int n_sched) {
     pdl_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_sched; i += blockDim.x) sched[i] = 0;
     const int lane = threadIdx.x & 31;
-    const int n = offsets[E];
     const int vec = d / 8;  // 16-byte pieces of a row
-    for (int p = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); p < n;
-         p += gridDim.x * kGatherWarps) {
-        const int r = perm[p] / k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r * d);
-        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)p * d);
-        int i = lane;
-        for (; i + 96 < vec; i += 128) {  // four pieces in flight per lane
-            const uint4 a0 = __ldg(src + i), a1 = __ldg(src + i + 32), a2 = __ldg(src + i + 64),
-                        a3 = __ldg(src + i + 96);
-            dst[i] = a0;
-            dst[i + 32] = a1;
-            dst[i + 64] = a2;
-            dst[i + 96] = a3;
+    for (int a = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); a < A;
+         a += gridDim.x * kGatherWarps) {
+        const int p = pos[a];  // -1: a skipped (bad or repeated) expert id
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * d);
+        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)max(p, 0) * d);
+        for (int i0 = 0; i0 < vec; i0 += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (i0 + lane + 32 * j < vec) v[j] = __ldg(src + i0 + lane + 32 * j);
+            if (p < 0) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (i0 + lane + 32 * j < vec) dst[i0 + lane + 32 * j] = v[j];
         }
-        for (; i < vec; i += 32) dst[i] = __ldg(src + i);
     }
 }
 
@@ -582,8 +582,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const int gather_ctas =
         std::max(1, std::min((A + kGatherWarps - 1) / kGatherWarps, 16 * nsm));
     cudaError_t err = launch_pdl(gather_rows_kernel, dim3(gather_ctas), dim3(kGatherWarps * 32),
-                                 0, s,
-                                 (const __nv_bfloat16 *)a.x, a.perm, a.offsets, a.E, a.k, a.d,
+                                 0, s, (const __nv_bfloat16 *)a.x, a.pos, A, a.k, a.d,
                                  (__nv_bfloat16 *)a.xp, a.sched, n_sched);
     if (err != cudaSuccess) return err;
     Params p{};
