@@ -433,16 +433,15 @@ __device__ __forceinline__ void cluster_barrier(bool release) {
 
 // Rank of expert e under the order of the keys rk (desc: larger first, else smaller
 // first; equal keys: lower id first), i.e. the number of experts before it. `per`
-// consecutive threads (a power of two dividing 32) share e: each counts one slice of the
-// experts and the slices are added with shuffles.
+// consecutive threads (a power of two dividing 32) share e: thread `part` counts the
+// experts q = part (mod per), so that at each step a warp reads `per` consecutive words
+// (distinct banks), and the counts are added with shuffles.
 __device__ __forceinline__ int rank_of(const float *rk, int e, int E, int per, int part,
                                        bool desc) {
     const float me = rk[e];
-    const int len = (E + per - 1) / per;
-    const int q0 = part * len, q1 = min(E, q0 + len);
     int r = 0;
 #pragma unroll 8
-    for (int q = q0; q < q1; ++q) {
+    for (int q = part; q < E; q += per) {
         const float o = rk[q];
         r += ((desc ? o > me : o < me) || (o == me && q < e)) ? 1 : 0;
     }
