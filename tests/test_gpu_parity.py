@@ -771,3 +771,24 @@ def test_tree_forward_permute_outputs(shape, draft_tokens, mode):
     _sync()
     yr = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got_idx, gates.cpu().numpy(), rows=rows)
     _assert_close_rows(y.float().cpu().numpy()[rows], yr, shape)
+
+
+@pytest.mark.parametrize("E,k", [(128, 8), (256, 8), (64, 4), (100, 16)])
+def test_topk_with_exact_ties(E, k):
+    """Logits drawn from three values, so nearly every top-k round has tied candidates in
+    several lanes: the choices are the natural top-k with ties to the lower expert id, both
+    in the natural-routing kernel and in the selection cluster (fixed size E over all
+    experts, so every expert is eligible and the restricted top-k is the natural one)."""
+    shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
+    N = 65
+    rng = np.random.default_rng(E + k)
+    logits = rng.integers(0, 3, size=(N, E)).astype(np.float32)
+    logits[7] = 1.0  # a row of all-equal logits: the k lowest ids
+    ref, _ = O.topk(logits, k)
+    np.testing.assert_array_equal(ref[7], np.arange(k))
+    depth = np.minimum(np.arange(N), 5).astype(np.int32)
+    for mode, kw in ((M.MOE_ROUTE_NATURAL, {}),
+                     (M.MOE_ROUTE_FIXED_B, dict(fixed_B=E, pool_all=True))):
+        P = M.select_params(mode, W.C_EAGLE, **kw)
+        gidx, _, _, _ = _select_gpu(shape, P, logits, depth, 1, N)
+        np.testing.assert_array_equal(gidx, ref)
