@@ -27,7 +27,13 @@
 // Demand, entropy and gates are computed in fp32 (GB300's fp64 rate is a small
 // fraction of its fp32 rate): the softmax normaliser in a warp tree, the demand per
 // expert in ascending node order, sum D and H in ascending expert order in one
-// thread, each product and sum rounded on its own (no FMA contraction).
+// thread (the cluster variant: block reductions), each product and sum rounded on its
+// own (no FMA contraction).
+//
+// Two more jobs ride on the selection launches of the whole layer (moe_tree_forward):
+// for a block of one tree of up to 256 nodes the cluster (AcceptMoE or natural) also
+// performs the permute step (permute_tree), and the AcceptMoE / fixed-size launches carry
+// extra CTAs that prefetch the root's experts into L2 (prefetch_root_experts).
 #include <cooperative_groups.h>
 #include <math.h>
 
