@@ -960,7 +960,7 @@ def main(argv=None):
     ap.add_argument("--routing", choices=["acceptmoe", "natural"], default="acceptmoe")
     ap.add_argument("--router-std", type=float, default=0.02)
     ap.add_argument("--ffn-path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
-    ap.add_argument("--cpu-trees", type=int, default=2)
+    ap.add_argument("--cpu-trees", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched", "budget",
                                            "efficiency", "ecospec"],
