@@ -200,8 +200,7 @@ def oracle_block(x, wr, wg, wu, wd, depth, shape, routing, rows=None):
     from expert_select_gb300 import workload as W
     from oracle import oracle as O
     mode = O.ACCEPT if routing == "acceptmoe" else O.NATURAL
-    return O.forward(x, wr, wg, wu, wd, depth, shape.k, W.C_EAGLE, rows=rows, mode=mode,
-                     precision="fp32")
+    return O.forward(x, wr, wg, wu, wd, depth, shape.k, W.C_EAGLE, rows=rows, mode=mode)
 
 
 def time_oracle(xs, deps, wr, wg, wu, wd, shape, routing, n_trees):
@@ -227,7 +226,7 @@ class OracleSample:
         self.wr, self.wg, self.wu, self.wd = wr, wg, wu, wd
         self.mode = O.ACCEPT if routing == "acceptmoe" else O.NATURAL
         self.l32 = O.router(x, wr).astype(np.float32)
-        sel = O.select_tree(self.l32, depth, shape.k, self._c(), mode=self.mode, precision="fp32")
+        sel = O.select_tree(self.l32, depth, shape.k, self._c(), mode=self.mode)
         self.idx = sel["idx"]
 
     def _c(self):
@@ -240,7 +239,7 @@ class OracleSample:
         t0 = time.perf_counter()
         O.router(x[rr], self.wr)
         t1 = time.perf_counter()
-        O.select_tree(self.l32, self.depth, k, self._c(), mode=self.mode, precision="fp32")
+        O.select_tree(self.l32, self.depth, k, self._c(), mode=self.mode)
         t2 = time.perf_counter()
         picks = rng.choice(N * k, size=assign, replace=False)
         xf = x.float().numpy().astype(np.float64)

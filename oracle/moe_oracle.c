@@ -135,39 +135,64 @@ static int before_asc(const double *D, int a, int b) {
     return D[a] < D[b] || (D[a] == D[b] && a < b);
 }
 
-/* exp(H) within this relative distance of an integer counts as that integer. */
-#define SNAP 1e-5
+/* exp(H) within this relative distance of an integer counts as that integer: the
+ * effective rank of a demand that is exactly uniform over j experts is exactly j, but
+ * evaluating it rounds to j(1 +- a few 1e-16); 1e-9 lies far above that fp64 noise and
+ * far below any distance a real tree's demand produces. */
+#define SNAP 1e-9
 
-/* The demand / effective-rank steps in fp32, the precision of the device kernel:
- * softmax row p = exp(l - max) / sum (sum in ascending expert order), D_e += c * p_e
- * in ascending node order, sum D and H = -sum q ln q in ascending expert order.
- * D is returned widened to fp64 (exactly), r = exp(H). */
-static float demand_f32(const float *logits, const int *depth, int N, int E, const double *c,
-                        int n_c, double *D) {
-    float *Df = (float *)calloc((size_t)E, sizeof(float));
-    float *ex = (float *)malloc(sizeof(float) * (size_t)E);
-    for (int n = 0; n < N; ++n) {
-        const float *l = logits + (size_t)n * E;
-        int t = depth[n] < n_c ? depth[n] : n_c - 1;
-        float cf = (float)c[t], mx = l[0], s = 0.f;
-        for (int e = 1; e < E; ++e)
-            if (l[e] > mx) mx = l[e];
-        for (int e = 0; e < E; ++e) {
-            ex[e] = expf(l[e] - mx);
-            s += ex[e];
-        }
-        for (int e = 0; e < E; ++e) Df[e] += cf * (ex[e] / s);
+/* The set size the effective rank r asks for: the integer n when r is within SNAP*r of
+ * it, else ceil(r); then floored at k and capped at the pool size. */
+static int size_from_rank(double r, int k, int pool) {
+    const double rn = nearbyint(r);
+    int m = (fabs(r - rn) <= SNAP * r) ? (int)rn : (int)ceil(r);
+    if (m < k) m = k;
+    if (m > pool) m = pool;
+    return m;
+}
+
+/* Relative distance of r to the nearest value where size_from_rank changes. Below an
+ * integer n the size is n all the way up to the integer; it becomes n + 1 once r is more
+ * than SNAP*r above n, i.e. at b_n = n / (1 - SNAP). A b_n counts only where the floor
+ * and the cap leave n and n + 1 distinct. +inf if no b_n is within one unit of r. */
+static double rank_margin(double r, int k, int pool) {
+    double best = INFINITY;
+    const double nf = floor(r);
+    for (double n = nf - 1.0; n <= nf + 1.0; n += 1.0) {
+        if (n < 1.0) continue;
+        const int lo = n < k ? k : (n > pool ? pool : (int)n);
+        const int hi = n + 1.0 < k ? k : (n + 1.0 > pool ? pool : (int)n + 1);
+        if (lo == hi) continue;
+        const double b = n / (1.0 - SNAP);
+        const double g = fabs(r - b) / r;
+        if (g < best) best = g;
     }
-    float sum = 0.f, H = 0.f;
-    for (int e = 0; e < E; ++e) sum += Df[e];
-    for (int e = 0; e < E; ++e) {
-        float q = Df[e] / sum;
-        if (q > 0.f) H -= q * logf(q);
+    return best;
+}
+
+/* Step 6 for one node: its k best logits inside the eligible set (`allowed`; NULL = all
+ * experts), in descending order, ties to the lower id, and the gates: the softmax over the
+ * k chosen logits (fp64, from the fp32 logits). Returns topk_row's gap. */
+static double route_row(const float *l, int E, int k, const unsigned char *allowed, int *o,
+                        double *g) {
+    const double gap = topk_row(l, E, k, allowed, o);
+    const double mx = l[o[0]];
+    double s = 0.0;
+    for (int j = 0; j < k; ++j) {
+        g[j] = exp((double)l[o[j]] - mx);
+        s += g[j];
     }
-    for (int e = 0; e < E; ++e) D[e] = (double)Df[e];
-    free(Df);
-    free(ex);
-    return expf(H);
+    for (int j = 0; j < k; ++j) g[j] /= s;
+    return gap;
+}
+
+/* [ABS] re-routing inside an eligible set, on its own: route_row for R rows with one
+ * eligibility mask (allowed [E], nonzero = eligible; it must hold at least k experts). */
+ORC_API void oracle_restricted_route(const float *logits, int R, int E, int k,
+                                     const unsigned char *allowed, int *idx, double *gates) {
+    for (int n = 0; n < R; ++n)
+        route_row(logits + (size_t)n * E, E, k, allowed, idx + (size_t)n * k,
+                  gates + (size_t)n * k);
 }
 
 /* Selection for one draft tree of N nodes (node 0 is the root).
@@ -177,7 +202,7 @@ static float demand_f32(const float *logits, const int *depth, int N, int E, con
  *  2. demand D_e = sum_n c(depth_n) * softmax(l_n)_e, nodes in ascending order;
  *     c(depth) beyond the table repeats the last entry.
  *  3. effective rank r = exp(H(D / sum D)), H = -sum q ln q over all E experts.
- *     m = max(k, ceil(r)) (a value within 1e-5 relative of an integer counts as that
+ *     m = max(k, ceil(r)) (a value within 1e-9 relative of an integer counts as that
  *     integer), capped at the pool size. FIXED_B takes m = max(k, fixed_B) instead.
  *  4. root anchor A = natural top-k of node 0 (when `anchor`); S = A plus the best
  *     m - |A| experts of pool \ A in (D desc, id asc) order. pool = U, or all experts.
@@ -187,23 +212,27 @@ static float demand_f32(const float *logits, const int *depth, int N, int E, con
  *  6. restricted top-k: each node takes its k best logits inside S, gates are the
  *     softmax over the k chosen logits. NATURAL: S = all experts.
  *
+ * Steps 2-3 run in fp64 (softmax, demand, entropy, exp).
+ *
  * info[0..3] = |U|, |union of restricted choices|, |S| after step 4 (m), removed.
  * margins[0] = smallest top-k gap (fp32 logits, natural), margins[1] = relative
- * distance of r to the nearest integer, margins[2] = relative demand gap at the
- * fill cut, margins[3] = relative demand gap at the prune cut, margins[4] =
- * smallest restricted top-k gap. prec = 0 runs steps 2-3 in fp64; prec = 1 runs them
- * in fp32 (demand_f32), the precision the device decides in. Returns 0, or -1 on bad
- * arguments. */
+ * distance of r to the nearest value where the size rule changes m (rank_margin),
+ * margins[2] = relative demand gap at the fill cut, margins[3] = relative demand gap
+ * at the prune cut, margins[4] = smallest restricted top-k gap; +inf where a decision
+ * does not depend on the demand. *r_out = r (NaN outside ACCEPT mode). Returns 0, or -1
+ * on bad arguments. */
 ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int E, int k,
                                const double *c, int n_c, int mode, int pool_all, int anchor,
                                int prune, const unsigned char *resident, int budget,
-                               int min_set, int fixed_B, int prec, int *idx, double *gates,
-                               unsigned char *eligible, int *info, double *D, double *margins) {
+                               int min_set, int fixed_B, int *idx, double *gates,
+                               unsigned char *eligible, int *info, double *D, double *margins,
+                               double *r_out) {
     if (N < 1 || E < 1 || E > 1024 || k < 1 || k > E || n_c < 1) return -1;
     int *nat = (int *)malloc(sizeof(int) * (size_t)N * k);
     double *p = (double *)malloc(sizeof(double) * (size_t)E);
     unsigned char inU[1024], inS[1024], inA[1024];
     for (int m = 0; m < 5; ++m) margins[m] = INFINITY;
+    *r_out = NAN;
 
     /* 1. natural top-k and union */
     memset(inU, 0, (size_t)E);
@@ -223,34 +252,29 @@ ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int
     } else {
         /* 2. commitment-weighted demand, 3. effective rank and set size */
         int pool = pool_all ? E : U;
-        double r = 0.0;
-        if (prec == 1) {
-            r = demand_f32(logits, depth, N, E, c, n_c, D);
-        } else {
-            for (int e = 0; e < E; ++e) D[e] = 0.0;
-            for (int n = 0; n < N; ++n) {
-                int t = depth[n] < n_c ? depth[n] : n_c - 1;
-                softmax_row(logits + (size_t)n * E, E, p);
-                for (int e = 0; e < E; ++e) D[e] += c[t] * p[e];
-            }
+        for (int e = 0; e < E; ++e) D[e] = 0.0;
+        for (int n = 0; n < N; ++n) {
+            int t = depth[n] < n_c ? depth[n] : n_c - 1;
+            softmax_row(logits + (size_t)n * E, E, p);
+            for (int e = 0; e < E; ++e) D[e] += c[t] * p[e];
+        }
+        int m;
+        if (mode == ORC_ACCEPT) {
             double sum = 0.0, H = 0.0;
             for (int e = 0; e < E; ++e) sum += D[e];
             for (int e = 0; e < E; ++e) {
                 double q = D[e] / sum;
                 if (q > 0.0) H -= q * log(q);
             }
-            r = exp(H);
-        }
-        int m;
-        if (mode == ORC_ACCEPT) {
-            double rn = nearbyint(r);
-            margins[1] = fabs(r - rn) / r;
-            m = (fabs(r - rn) <= SNAP * r) ? (int)rn : (int)ceil(r);
+            const double r = exp(H);
+            *r_out = r;
+            m = size_from_rank(r, k, pool);
+            margins[1] = rank_margin(r, k, pool);
         } else {
             m = fixed_B;
+            if (m < k) m = k;
+            if (m > pool) m = pool;
         }
-        if (m < k) m = k;
-        if (m > pool) m = pool;
         /* 4. anchor + fill */
         memset(inA, 0, (size_t)E);
         memset(inS, 0, (size_t)E);
@@ -308,16 +332,9 @@ ORC_API int oracle_select_tree(const float *logits, const int *depth, int N, int
     /* 6. restricted top-k and renormalised gates */
     memset(inU, 0, (size_t)E);
     for (int n = 0; n < N; ++n) {
-        const float *l = logits + (size_t)n * E;
         int *o = idx + (size_t)n * k;
-        double g = topk_row(l, E, k, inS, o);
+        double g = route_row(logits + (size_t)n * E, E, k, inS, o, gates + (size_t)n * k);
         if (g < margins[4]) margins[4] = g;
-        double mx = l[o[0]], s = 0.0;
-        for (int j = 0; j < k; ++j) {
-            gates[(size_t)n * k + j] = exp((double)l[o[j]] - mx);
-            s += gates[(size_t)n * k + j];
-        }
-        for (int j = 0; j < k; ++j) gates[(size_t)n * k + j] /= s;
         for (int j = 0; j < k; ++j) inU[o[j]] = 1;
     }
     int Us = 0;

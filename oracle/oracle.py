@@ -47,9 +47,11 @@ def lib():
         _lib.oracle_router.restype = None
         _lib.oracle_topk.argtypes = [P, i, i, i, P]
         _lib.oracle_topk.restype = C.c_double
-        _lib.oracle_select_tree.argtypes = [P, P, i, i, i, P, i, i, i, i, i, P, i, i, i, i,
-                                            P, P, P, P, P, P]
+        _lib.oracle_select_tree.argtypes = [P, P, i, i, i, P, i, i, i, i, i, P, i, i, i,
+                                            P, P, P, P, P, P, P]
         _lib.oracle_select_tree.restype = i
+        _lib.oracle_restricted_route.argtypes = [P, i, i, i, P, P, P]
+        _lib.oracle_restricted_route.restype = None
         _lib.oracle_permute.argtypes = [P, i, i, i, P, P, P]
         _lib.oracle_permute.restype = None
         _lib.oracle_expert_ffn.argtypes = [P, i, P, P, P, i, i, i, P]
@@ -106,10 +108,10 @@ def topk(logits: np.ndarray, k: int):
 def select_tree(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float],
                 mode: int = ACCEPT, pool_all: bool = False, anchor: bool = True,
                 prune: bool = False, resident: Optional[np.ndarray] = None,
-                budget: int = 8, min_set: int = 16, fixed_B: int = 0,
-                precision: str = "fp64") -> Dict:
-    """Selection for one tree. precision="fp32" takes the demand / effective-rank
-    decisions in fp32 like the device does; "fp64" is the reference definition."""
+                budget: int = 8, min_set: int = 16, fixed_B: int = 0) -> Dict:
+    """Selection for one tree (demand, entropy and effective rank in fp64). Besides the
+    choices it returns the demand D, the effective rank r (NaN outside ACCEPT) and the
+    decision margins (see oracle_select_tree)."""
     l = np.ascontiguousarray(logits, dtype=np.float32)
     N, E = l.shape
     dep = np.ascontiguousarray(depth, dtype=np.int32)
@@ -121,15 +123,15 @@ def select_tree(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[float
     info = np.empty(4, dtype=np.int32)
     D = np.zeros(E, dtype=np.float64)
     margins = np.empty(5, dtype=np.float64)
+    r = np.empty(1, dtype=np.float64)
     rc = lib().oracle_select_tree(_p(l), _p(dep), N, E, k, _p(cc), len(cc), mode,
                                   int(pool_all), int(anchor), int(prune), _p(res), budget,
-                                  min_set, fixed_B, 1 if precision == "fp32" else 0,
-                                  _p(idx), _p(gates), _p(elig), _p(info),
-                                  _p(D), _p(margins))
+                                  min_set, fixed_B, _p(idx), _p(gates), _p(elig), _p(info),
+                                  _p(D), _p(margins), _p(r))
     if rc != 0:
         raise ValueError("oracle_select_tree: bad arguments")
     return dict(idx=idx, gates=gates, eligible=elig, union_nat=int(info[0]),
-                union_sel=int(info[1]), m=int(info[2]), pruned=int(info[3]), D=D,
+                union_sel=int(info[1]), m=int(info[2]), pruned=int(info[3]), D=D, r=float(r[0]),
                 margin_topk=margins[0], margin_rank=margins[1], margin_fill=margins[2],
                 margin_prune=margins[3], margin_restricted=margins[4])
 
@@ -148,7 +150,23 @@ def select_block(logits: np.ndarray, depth: np.ndarray, k: int, c: Sequence[floa
     for key in ("margin_topk", "margin_rank", "margin_fill", "margin_prune", "margin_restricted"):
         res[key] = min(o[key] for o in outs)
     res["D"] = np.stack([o["D"] for o in outs])
+    res["r"] = np.array([o["r"] for o in outs])
+    res["trees"] = outs
     return res
+
+
+def restricted_route(logits: np.ndarray, allowed: np.ndarray, k: int):
+    """Each row's top-k among the experts with allowed[e] != 0 and its renormalised
+    gates (the re-routing step on its own): (idx [R, k] int32, gates [R, k] fp64)."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    R, E = l.shape
+    al = np.ascontiguousarray(np.asarray(allowed) != 0, dtype=np.uint8)
+    if al.shape != (E,) or int(al.sum()) < k:
+        raise ValueError("restricted_route: the mask needs E entries and at least k experts")
+    idx = np.empty((R, k), dtype=np.int32)
+    gates = np.empty((R, k), dtype=np.float64)
+    lib().oracle_restricted_route(_p(l), R, E, k, _p(al), _p(idx), _p(gates))
+    return idx, gates
 
 
 def permute(idx: np.ndarray, E: int):

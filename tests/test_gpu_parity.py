@@ -79,7 +79,7 @@ def _check_selection(shape, kw, logits, depth, gidx, ggates, gelig, ginfo, N, B)
     exact = 0
     for b in range(B):
         sl = slice(b * N, (b + 1) * N)
-        o = O.select_tree(logits[sl], depth[b], shape.k, kw["c"], precision="fp32",
+        o = O.select_tree(logits[sl], depth[b], shape.k, kw["c"],
                           **{k: v for k, v in kw.items() if k != "c"})
         if _oracle_tree_ambiguous(o):
             S = set(np.flatnonzero(gelig[b]).tolist())
@@ -219,7 +219,7 @@ def test_selection_root_only_and_all_experts():
         logits = W.synthetic_logits(5, parent, shape.E, 2.0)
         P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_TINY)
         gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth, 1, N)
-        o = O.select_tree(logits, depth[0], shape.k, W.C_TINY, precision="fp32")
+        o = O.select_tree(logits, depth[0], shape.k, W.C_TINY)
         np.testing.assert_array_equal(gidx, o["idx"])
         np.testing.assert_array_equal(ge[0], o["eligible"])
 
@@ -504,7 +504,7 @@ def test_tree_forward_against_oracle(case):
     sample = list(range(R)) if rows is None else \
         sorted(np.random.default_rng(3).choice(R, rows, replace=False).tolist())
     ref = O.forward(run["x"], run["wr"], run["wg"].cpu(), run["wu"].cpu(), run["wd"].cpu(),
-                    run["depth"], shape.k, run["c"], rows=sample, mode=omode, precision="fp32")
+                    run["depth"], shape.k, run["c"], rows=sample, mode=omode)
     scale = np.abs(ref["logits"]).max(axis=1, keepdims=True)
     assert (np.abs(got["logits"] - ref["logits"]) <= 1e-4 * scale).all()
     # decisions: exact unless the oracle's own margin says the inputs are tied at fp32
@@ -565,7 +565,7 @@ def test_residual_chain_of_layers_against_oracle():
     xo = x0
     for l, (wr, wg, wu, wd) in enumerate(layers):
         ref = O.forward(xo, wr.cpu(), wg.cpu(), wu.cpu(), wd.cpu(), t.depth, shape.k, W.C_EAGLE,
-                        mode=O.ACCEPT, precision="fp32")
+                        mode=O.ACCEPT)
         if l == 0:  # identical inputs: exact unless the oracle reports a tie
             tied = ref["margin_topk"] < 1e-4 or ref["margin_restricted"] < 1e-4 or \
                 ref["margin_rank"] < TIE or ref["margin_fill"] < TIE

@@ -144,14 +144,187 @@ def test_demand_one_hot_closed_form_and_depth_table():
 
 @pytest.mark.parametrize("j", [1, 3, 8, 13])
 def test_uniform_demand_effective_rank_is_j(j):
-    """D uniform over j experts has entropy ln j, so exp(H) = j and m = max(k, j)."""
+    """D uniform over j experts has entropy ln j, so exp(H) = j and m = max(k, j). An
+    integer effective rank sits 1e-9 (the snap distance) below the point where the size
+    would become j + 1, so its decision margin is 1e-9, not 0 (for j < k the floor at k
+    makes that point irrelevant)."""
     E, k = 16, 2
     l = np.full((5, E), -1000.0, dtype=np.float32)
     l[:, :j] = 0.0
     sel = O.select_tree(l, np.array([0, 1, 1, 2, 2]), k, [1.0, 0.6, 0.3], mode=O.ACCEPT,
                         pool_all=True)
     assert sel["m"] == max(k, j)
-    assert sel["margin_rank"] < 1e-12
+    assert sel["r"] == pytest.approx(j, rel=1e-14)
+    if j >= k:
+        assert sel["margin_rank"] == pytest.approx(1e-9, rel=1e-4)
+    else:
+        assert sel["margin_rank"] > 0.5
+
+
+# ------------------------------------------- the size rule and the decision margins
+
+SNAP = 1e-9  # the set-size reading: exp(H) within 1e-9 (relative) of an integer is it
+
+
+def _size_rule(r, k, pool):
+    """The reading of the pages' self-sizing taken here, as a rule on a number:
+    m = n if |r - n| <= 1e-9 r for the nearest integer n, else ceil(r); floor k, cap pool."""
+    n = round(r)
+    m = n if abs(r - n) <= SNAP * r else math.ceil(r)
+    return min(max(m, k), pool)
+
+
+def _flip_distance(r, k, pool):
+    """Brute force: the smallest relative change of r that changes _size_rule, found by a
+    geometric scan then bisection on each side (inf when none below 1/r)."""
+    m0 = _size_rule(r, k, pool)
+    best = math.inf
+    for sgn in (1.0, -1.0):
+        lo, hi = 0.0, None
+        eps = 1e-16
+        while eps < 1.0 / r:
+            if _size_rule(r * (1 + sgn * eps), k, pool) != m0:
+                hi = eps
+                break
+            lo, eps = eps, eps * 1.25
+        if hi is None:
+            continue
+        for _ in range(200):
+            mid = 0.5 * (lo + hi)
+            if _size_rule(r * (1 + sgn * mid), k, pool) != m0:
+                hi = mid
+            else:
+                lo = mid
+        best = min(best, hi)
+    return best
+
+
+def _two_level_demand(a, w):
+    """One-hot routing that makes the demand exactly (1, ..., 1 [a times], w): nodes
+    0..a-1 at depth 0 each routed to their own expert, node a at depth 1 (c = w) routed
+    to expert a; k = 1."""
+    E = a + 3
+    hot = list(range(a + 1))
+    depth = np.array([0] * a + [1], np.int32)
+    return _one_hot_logits(hot, E), depth, [1.0, w]
+
+
+@pytest.mark.parametrize("a,w,m_expect", [(5, 1e-13, 5), (5, 1e-6, 6), (12, 1e-12, 12),
+                                          (12, 1e-5, 13), (3, 1.0, 4), (7, 0.25, 8)])
+def test_effective_rank_closed_form_and_snap(a, w, m_expect):
+    """D = (1 x a, w): q = (1/T x a, w/T) with T = a + w, so exp(H) = T * w^(-w/T), which
+    lies just above a for small w. A distance to a below 1e-9 relative snaps to m = a
+    (w = 1e-13: r - a ~ 3e-12); beyond it m = ceil(r) = a + 1 (w = 1e-6: r - a ~ 1.5e-5)."""
+    l, depth, c = _two_level_demand(a, w)
+    sel = O.select_tree(l, depth, 1, c, mode=O.ACCEPT, pool_all=True)
+    T = a + w
+    assert sel["r"] == pytest.approx(T * w ** (-w / T), rel=1e-13)
+    assert sel["m"] == m_expect == _size_rule(sel["r"], 1, l.shape[1])
+
+
+@pytest.mark.parametrize("a,w,k", [(5, 1e-13, 1), (5, 1e-6, 1), (12, 3e-11, 1), (3, 1.0, 1),
+                                   (6, 0.4, 9), (6, 0.4, 2)])
+def test_rank_margin_is_distance_to_the_size_flip(a, w, k):
+    """margin_rank = the relative change of exp(H) that would change the set size, found
+    here by bisection on the size rule itself (k = 9 floors every nearby size: +inf)."""
+    l, depth, c = _two_level_demand(a, w)
+    sel = O.select_tree(l, depth, k, c, mode=O.ACCEPT, pool_all=True)
+    ref = _flip_distance(sel["r"], k, l.shape[1])
+    if math.isinf(ref):
+        assert sel["margin_rank"] > 1.0 / sel["r"] or math.isinf(sel["margin_rank"])
+    else:
+        assert sel["margin_rank"] == pytest.approx(ref, rel=1e-6, abs=1e-15)
+
+
+def _fill_prune_brute(sel_noprune, l, k, anchor=True, pool_all=False, res=None, budget=0,
+                      min_set=0):
+    """Fill and prune cut gaps by sorting: the candidates (pool minus anchor) in
+    (D desc, id asc) order, the first m - |anchor| taken; the removable members in
+    (D asc, id asc) order, the first `removed` dropped."""
+    D = sel_noprune["D"]
+    nat, _ = O.topk(l, k)
+    A = set(nat[0].tolist()) if anchor else set()
+    pool = set(range(l.shape[1])) if pool_all else set(nat.ravel().tolist())
+    cand = sorted(pool - A, key=lambda e: (-D[e], e))
+    F = sel_noprune["m"] - len(A)
+    fill = (D[cand[F - 1]] - D[cand[F]]) / D[cand[F - 1]] if 0 < F < len(cand) else math.inf
+    prune = math.inf
+    if res is not None:
+        S = set(np.flatnonzero(sel_noprune["eligible"]).tolist())
+        rem = sorted([e for e in S - A if not res[e]], key=lambda e: (D[e], e))
+        r = min(budget, max(0, sel_noprune["m"] - max(min_set, k)), len(rem))
+        if 0 < r < len(rem):
+            prune = (D[rem[r]] - D[rem[r - 1]]) / D[rem[r]]
+    return fill, prune
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fill_and_prune_margins_by_sorting(seed):
+    """margin_fill and margin_prune equal the relative demand gaps at the two cut points,
+    recomputed by sorting the demand (catches a gap taken at the wrong rank or with the
+    wrong sign)."""
+    E, k = 32, 2
+    t = W.eagle_tree(40 + seed)
+    l = W.synthetic_logits(50 + seed, t.parent, E, 2.0 + 0.2 * seed)
+    res = W.residency_mask(seed, E, 10)
+    budget, min_set = 1 + seed % 4, 3 + seed % 5
+    base = O.select_tree(l, t.depth, k, W.C_EAGLE, mode=O.ACCEPT)
+    sel = O.select_tree(l, t.depth, k, W.C_EAGLE, mode=O.ACCEPT, prune=True, resident=res,
+                        budget=budget, min_set=min_set)
+    fill, prune = _fill_prune_brute(base, l, k, res=res, budget=budget, min_set=min_set)
+    for got, ref in ((sel["margin_fill"], fill), (sel["margin_prune"], prune)):
+        if math.isinf(ref):
+            assert math.isinf(got)
+        else:
+            assert got == pytest.approx(ref, rel=1e-12)
+    assert sel["margin_fill"] > 0 and sel["margin_prune"] > 0
+
+
+def test_hand_built_fill_and_prune_cuts():
+    """Demand (one-hot routing, c = 1 at every depth) = (4, 3, 2.5, 2, 1, 0.5) on experts
+    0..5, k = 1, anchor = expert 0 (the root's), FIXED_B m = 4: the fill takes experts 1, 2,
+    3 and leaves 4: gap (2 - 1) / 2 = 0.5. Pruning with experts 1, 3 non-resident, budget 1,
+    min_set 2: removes expert 3 (the lowest removable), next is 1: gap (3 - 2) / 3."""
+    E = 8
+    counts = {0: 8, 1: 6, 2: 5, 3: 4, 4: 2, 5: 1}  # half-units: D = count / 2
+    hot = [e for e, n in counts.items() for _ in range(n)]
+    depth = np.zeros(len(hot), np.int32)
+    l = _one_hot_logits(hot, E)
+    c = [0.5]
+    sel = O.select_tree(l, depth, 1, c, mode=O.FIXED_B, fixed_B=4)
+    np.testing.assert_array_equal(sel["D"][:6], [4, 3, 2.5, 2, 1, 0.5])
+    assert np.flatnonzero(sel["eligible"]).tolist() == [0, 1, 2, 3]
+    assert sel["margin_fill"] == pytest.approx(0.5, rel=1e-15)
+    assert math.isinf(sel["margin_prune"]) and math.isnan(sel["r"])
+    res = np.array([1, 0, 1, 0, 1, 1, 1, 1], np.uint8)
+    sel = O.select_tree(l, depth, 1, c, mode=O.FIXED_B, fixed_B=4, prune=True, resident=res,
+                        budget=1, min_set=2)
+    assert np.flatnonzero(sel["eligible"]).tolist() == [0, 1, 2] and sel["pruned"] == 1
+    assert sel["margin_prune"] == pytest.approx(1.0 / 3.0, rel=1e-15)
+
+
+def test_restricted_route_brute_force_and_identity():
+    """The re-routing step on its own: with every expert allowed it is the natural top-k
+    with softmax gates over the chosen logits; with a mask it is the unique best k-subset
+    of the allowed experts (brute force), in descending order."""
+    rng = np.random.Generator(np.random.PCG64(21))
+    l = rng.standard_normal((7, 12)).astype(np.float32)
+    idx, gates = O.restricted_route(l, np.ones(12), 3)
+    nat, _ = O.topk(l, 3)
+    np.testing.assert_array_equal(idx, nat)
+    for r in range(7):
+        np.testing.assert_allclose(gates[r], sp_softmax(l[r, idx[r]].astype(np.float64)),
+                                   rtol=1e-13)
+    allowed = np.zeros(12)
+    allowed[[1, 4, 5, 8, 10]] = 1
+    idx, _ = O.restricted_route(l, allowed, 3)
+    for r in range(7):
+        best = max(itertools.combinations([1, 4, 5, 8, 10], 3),
+                   key=lambda T: sum(float(l[r, e]) for e in T))
+        assert set(idx[r].tolist()) == set(best)
+        assert all(l[r, idx[r][i]] >= l[r, idx[r][i + 1]] for i in range(2))
+    with pytest.raises(ValueError):
+        O.restricted_route(l, np.eye(12)[0], 3)
 
 
 def test_root_only_commitment_gives_root_softmax():
