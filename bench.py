@@ -312,7 +312,7 @@ def run_gpu(args):
     routing = args.routing
     loop(Wm, routing)
     counts = torch.zeros(K, shape.E, dtype=torch.int32, device=dev)
-    info = torch.zeros(K, 4, dtype=torch.int32, device=dev)
+    info = torch.zeros(K, M.MOE_INFO_FIELDS, dtype=torch.int32, device=dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range((K + EV_EVERY - 1) // EV_EVERY)]
     for a, b in ev:  # torch creates the CUDA event on first record
@@ -387,7 +387,7 @@ def run_gpu(args):
     Kv = min(K, 2000)
     loop(Wm, "natural" if routing != "natural" else "acceptmoe")
     cnat = torch.zeros(Kv, shape.E, dtype=torch.int32, device=dev)
-    inat = torch.zeros(Kv, 4, dtype=torch.int32, device=dev)
+    inat = torch.zeros(Kv, M.MOE_INFO_FIELDS, dtype=torch.int32, device=dev)
     other = "natural" if routing != "natural" else "acceptmoe"
     sec_o = timed(Kv, other, counts=cnat, info=inat)
     u_o = (cnat.cpu().numpy() > 0).sum(axis=1)
@@ -813,7 +813,7 @@ def run_budget(args):
                                                            anchor=False, fixed_B=B)))
     rows = []
     for name, P in variants:
-        info = torch.zeros(K, 4, dtype=torch.int32, device=dev)
+        info = torch.zeros(K, M.MOE_INFO_FIELDS, dtype=torch.int32, device=dev)
 
         def loop(n, rec):
             for i in range(n):

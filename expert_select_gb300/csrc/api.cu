@@ -71,8 +71,10 @@ bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
     a->budget = P->reroute_budget;
     a->min_set = P->min_set;
     a->fixed_B = P->fixed_B;
-    for (int t = 0; t < MOE_MAX_DEPTHS; ++t)
-        a->c[t] = (P->mode != MOE_ROUTE_NATURAL && t < P->n_c) ? (float)P->c_by_depth[t] : 0.f;
+    for (int t = 0; t < MOE_MAX_DEPTHS; ++t) {
+        a->c64[t] = (P->mode != MOE_ROUTE_NATURAL && t < P->n_c) ? P->c_by_depth[t] : 0.0;
+        a->c[t] = (float)a->c64[t];
+    }
     (void)k;
     return true;
 }
@@ -201,7 +203,7 @@ const char *moe_status_str(int status) {
     }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 200; }
 
 size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N) {
     if (!desc_ok(L) || B < 1 || N < 1) return 0;
@@ -226,6 +228,69 @@ moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
     return cuda_status(launch_select(*L, a, logits, depth, B, N, resident, topk_idx, gates,
                                      eligible, info, WeightPrefetch{}, PermuteOut{}, nullptr,
                                      (cudaStream_t)stream));
+}
+
+moe_status moe_tree_route(const moe_layer_desc *L, const moe_select_params *P, const void *x,
+                          const void *W_r, const int *depth, int B, int N,
+                          const uint8_t *resident, float *logits, int *topk_idx, float *gates,
+                          uint8_t *eligible, int *info, moe_stream_t stream) {
+    SelectArgs a;
+    if (!desc_ok(L) || !select_args(P, L->k, &a) || B < 0 || N < 0) return MOE_ERR_ARG;
+    if (B * N > 0 && (!x || !W_r || !logits || !depth || !topk_idx || !gates))
+        return MOE_ERR_ARG;
+    if (B * N > 0 && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ARG;
+    if (a.prune && !resident) return MOE_ERR_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_router(*L, x, W_r, B * N, logits, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_select(*L, a, logits, depth, B, N, resident, topk_idx, gates,
+                                     eligible, info, WeightPrefetch{}, PermuteOut{}, nullptr, s));
+}
+
+moe_status moe_tree_block_stats(const moe_layer_desc *L, int B, int N, const int *info,
+                                const int *counts, const void *workspace, moe_tree_stats *stats,
+                                moe_stream_t stream) {
+    if (!desc_ok(L) || B < 1 || N < 1 || !stats) return MOE_ERR_ARG;
+    if ((!info || !counts) && !workspace) return MOE_ERR_ARG;
+    const Workspace w = workspace_layout(*L, B, N);
+    void *ws = const_cast<void *>(workspace);
+    const int *inf = info ? info : at<int>(ws, w.info);
+    const int *cnt = counts ? counts : at<int>(ws, w.counts);
+    cudaStream_t s = (cudaStream_t)stream;
+    int c[kMaxE];
+    if (cudaMemcpyAsync(c, cnt, sizeof(int) * L->E, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    double sums[4] = {0, 0, 0, 0};
+    int exact = 0;
+    constexpr int kChunk = 128;  // trees per copy: the host buffer stays on the stack
+    int buf[kChunk * MOE_INFO_FIELDS];
+    for (int b0 = 0; b0 < B; b0 += kChunk) {
+        const int nb = std::min(kChunk, B - b0);
+        if (cudaMemcpyAsync(buf, inf + (size_t)b0 * MOE_INFO_FIELDS,
+                            sizeof(int) * nb * MOE_INFO_FIELDS, cudaMemcpyDeviceToHost,
+                            s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        for (int b = 0; b < nb; ++b) {
+            for (int f = 0; f < 4; ++f) sums[f] += buf[b * MOE_INFO_FIELDS + f];
+            exact += buf[b * MOE_INFO_FIELDS + 4] != 0;
+        }
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    moe_tree_stats st{};
+    st.trees = B;
+    for (int e = 0; e < L->E; ++e) {
+        st.assignments += c[e];
+        st.union_experts += c[e] > 0;
+        st.max_per_expert = std::max(st.max_per_expert, c[e]);
+    }
+    st.reuse = st.assignments > 0 ? 1.0 - (double)st.union_experts / st.assignments : 0.0;
+    st.union_nat_mean = sums[0] / B;
+    st.union_sel_mean = sums[1] / B;
+    st.m_mean = sums[2] / B;
+    st.pruned_mean = sums[3] / B;
+    st.exact_trees = exact;
+    *stats = st;
+    return MOE_OK;
 }
 
 moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int R, int *counts,

@@ -59,7 +59,8 @@ cudaError_t launch_router(const moe_layer_desc &L, const void *x, const void *Wr
 
 struct SelectArgs {
     int mode, n_c, pool_all, anchor, prune, budget, min_set, fixed_B;
-    float c[MOE_MAX_DEPTHS];
+    float c[MOE_MAX_DEPTHS];     // the commitment table rounded to fp32 (the fast pass)
+    double c64[MOE_MAX_DEPTHS];  // as given (the exact pass)
 };
 // L2 prefetch of expert weights during routing (AcceptMoE and fixed-size selection). The
 // root's natural top-k is the anchor that AcceptMoE keeps in every eligible set, and with

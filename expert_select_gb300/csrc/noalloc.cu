@@ -28,6 +28,21 @@ constexpr int kMaxDevices = 64;
 void *g_scratch_dev[kMaxDevices];
 std::mutex g_scratch_mu;
 
+// The built-in scratch's device address on the current device (set up on first use).
+moe_status scratch_address(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_dev[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_scratch_dev[dev] = p;
+    }
+    *out = g_scratch_dev[dev];
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" moe_status moe_tree_forward_noalloc(
@@ -42,21 +57,20 @@ extern "C" moe_status moe_tree_forward_noalloc(
     const size_t need = moe_workspace_bytes(L, B, N);
     if (need == 0) return MOE_ERR_ARG;
     if (need > kScratchBytes) return MOE_ERR_UNSUPPORTED;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     void *ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (!g_scratch_dev[dev]) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-            g_scratch_dev[dev] = p;
-        }
-        ws = g_scratch_dev[dev];
-    }
+    const moe_status sa = scratch_address(&ws);
+    if (sa != MOE_OK) return sa;
     // The check word and scheduler counters that must start at zero are cleared by
     // the first kernel that uses them (the permute kernel), as for any workspace.
     return moe_tree_forward(L, P, x, W_r, W_gate, W_up, W_down, slot_of_expert, depth, B, N,
                             resident, y, out, ws, opts, stream);
+}
+
+extern "C" moe_status moe_noalloc_check(int *flags, moe_stream_t stream) {
+    if (!flags) return MOE_ERR_ARG;
+    void *ws = nullptr;
+    const moe_status sa = scratch_address(&ws);
+    if (sa != MOE_OK) return sa;
+    // the check word is the first int of the workspace layout, as in any workspace
+    return moe_workspace_check(ws, flags, stream);
 }

@@ -24,11 +24,15 @@
 // lanes holding that key): descending logits, ties to the lower id, as exact as a
 // comparison of the fp32 values.
 //
-// Demand, entropy and gates are computed in fp32 (GB300's fp64 rate is a small
-// fraction of its fp32 rate): the softmax normaliser in a warp tree, the demand per
-// expert in ascending node order, sum D and H in ascending expert order in one
-// thread (the cluster variant: block reductions), each product and sum rounded on its
-// own (no FMA contraction).
+// Precision of the decisions. The demand, its entropy and the effective rank are defined in
+// fp64 (softmax of each node's logits, D_e summed over the nodes, H and exp(H)). A first
+// pass computes them in fp32, every operation rounded on its own, and bounds its own
+// rounding error (see phase_b): when every decision that depends on them (the set size
+// from exp(H), the fill cut, the prune cut) is farther from its decision point than that
+// bound, the fp32 pass has decided exactly as the fp64 definition does. Otherwise the
+// tree's demand is recomputed in fp64 and phase B runs again in fp64 (GB300's fp64 rate is
+// a small fraction of its fp32 rate, so that pass is kept for the trees that need it).
+// info[4] reports which trees took it.
 //
 // Two more jobs ride on the selection launches of the whole layer (moe_tree_forward):
 // for a block of one tree of up to 256 nodes the cluster (AcceptMoE or natural) also
@@ -54,8 +58,14 @@ constexpr int kVPL = kMaxE / 32;     // logits held per lane
 constexpr int kStageFloats = 16384;  // logits staged in shared memory up to 64 KB
 static_assert(kThreads >= kMaxE, "block-wide counts take one expert per thread");
 
-// Relative distance to an integer under which exp(H) counts as that integer.
-constexpr float kSnap = 1e-5f;
+// Relative distance to an integer under which exp(H) counts as that integer: an effective
+// rank that is mathematically an integer (demand uniform over j experts) still counts as
+// j after fp64 rounding.
+constexpr double kSnap = 1e-9;
+constexpr float kU = 5.9604645e-8f;  // 2^-24, the unit roundoff of fp32
+// Logit ranges above this make exp() underflow in fp32 (and the relative error bound
+// meaningless): such trees always take the fp64 pass.
+constexpr float kMaxRange = 80.f;
 
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t u = __float_as_uint(v + 0.f);  // -0 -> +0
@@ -110,10 +120,212 @@ __device__ __forceinline__ float commitment(const SelectArgs &a, int depth) {
     return c;
 }
 
+__device__ __forceinline__ double commitment64(const SelectArgs &a, int depth) {
+    const int dd = max(0, min(depth, a.n_c - 1));
+    double c = a.c64[0];
+#pragma unroll
+    for (int i = 1; i < MOE_MAX_DEPTHS; ++i)
+        if (i == dd) c = a.c64[i];
+    return c;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
+}
+
+__device__ __forceinline__ double warp_sum64(double v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// The logit range of a node (its largest minus its smallest logit), >= 0; lanes hold
+// experts lane + 32 i (entries past E are -inf and ignored); `top` is the largest.
+template <int VPL>
+__device__ __forceinline__ float node_range(const float (&v)[VPL], int E, float top) {
+    const int lane = threadIdx.x & 31;
+    float lo = INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (lane + 32 * i < E) lo = fminf(lo, v[i]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    return fmaxf(top - lo, 0.f);
+}
+
+// fp32 / fp64 arithmetic of phase B, every operation rounded on its own.
+template <typename T> struct Num;
+template <> struct Num<float> {
+    __device__ static float add(float a, float b) { return __fadd_rn(a, b); }
+    __device__ static float mul(float a, float b) { return __fmul_rn(a, b); }
+    __device__ static float div(float a, float b) { return __fdiv_rn(a, b); }
+    __device__ static float ln(float a) { return logf(a); }
+    __device__ static float wsum(float v) { return warp_sum(v); }
+};
+template <> struct Num<double> {
+    __device__ static double add(double a, double b) { return __dadd_rn(a, b); }
+    __device__ static double mul(double a, double b) { return __dmul_rn(a, b); }
+    __device__ static double div(double a, double b) { return __ddiv_rn(a, b); }
+    __device__ static double ln(double a) { return log(a); }
+    __device__ static double wsum(double v) { return warp_sum64(v); }
+};
+
+// Sum of v over the block's NW warps, identical in every thread: a butterfly per warp,
+// then the warps' sums in warp order (red holds one value per warp; the call ends with a
+// barrier, and `red` may be reused after the next barrier).
+template <typename T, int NW>
+__device__ __forceinline__ T block_sum(T v, T *red) {
+    v = Num<T>::wsum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    T s = T(0);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s = Num<T>::add(s, red[w]);
+    return s;
+}
+
+// Rank of expert e under the order of the keys rk (desc: larger first, else smaller
+// first; equal keys: lower id first), i.e. the number of experts before it. `per`
+// consecutive threads (a power of two dividing 32) share e: thread `part` counts the
+// experts q = part (mod per), so that at each step a warp reads `per` consecutive words,
+// and the counts are added with shuffles.
+template <typename T>
+__device__ __forceinline__ int rank_of(const T *rk, int e, int E, int per, int part, bool desc) {
+    const T me = rk[e];
+    int r = 0;
+#pragma unroll 8
+    for (int q = part; q < E; q += per) {
+        const T o = rk[q];
+        r += ((desc ? o > me : o < me) || (o == me && q < e)) ? 1 : 0;
+    }
+    for (int off = 1; off < per; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+struct PhaseB {
+    int m, removed;
+    bool sure;  // fp32 pass: every decision is certain to equal the fp64 definition's
+};
+
+// Phase B of one tree in precision T, on a whole block of NW warps: the set size from the
+// effective rank exp(H(D / sum D)) (or fixed_B), the root anchor + fill in (D desc, id asc)
+// order among the pool, residency-aware pruning in (D asc, id asc) order. D[E] holds the
+// demand; inU / inA the natural union and the anchor; writes inS. rk, red, cut are
+// scratch. Returns the size, the number pruned and, for T = float, whether the decisions
+// are certain.
+//
+// The fp32 certificate. dD bounds the relative error of every fp32 D_e against the exact
+// demand (computed by the caller from the logit range and the number of roundings). Then
+//  - q_e = D_e / sum D is within dq = 2 dD + 21 u (sum: 20 roundings of positive terms);
+//  - each term q ln q is within q (dq |ln q| + dq) + 3u q |ln q| (logf: 1 ulp; the
+//    product: 1 rounding), so H (a block sum of same-sign terms, 20 roundings) is within
+//    dH = (dq + 23 u) H + dq, and r = expf(H) (2 ulp) within dr = dH + 4u, taken with 5%
+//    and 8u of slack for second-order terms and the rounding of the bounds themselves;
+//  - the size rule is m = clamp(ceil(r (1 - 1e-9))): it is certain when the rule gives the
+//    same m over [r (1 - dr), r (1 + dr)];
+//  - a cut (fill: last taken vs first left; prune: last removed vs next) is certain when
+//    the two demands stay ordered after moving each by dD + 2u towards the other.
+template <typename T, int NW>
+__device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const int *inU,
+                          const int *inA, int *inS, const uint8_t *resident, T *rk,
+                          T (*red)[NW], T *cut, float dD) {
+    using F = Num<T>;
+    constexpr bool exact = sizeof(T) == sizeof(double);
+    constexpr int NT = NW * 32;
+    const int tid = threadIdx.x;
+    const T De = tid < E ? D[tid] : T(0);
+    if (tid < 4) cut[tid] = T(-1);
+    const T sumD = block_sum<T, NW>(De, red[0]);
+    const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
+    T term = T(0);
+    if (tid < E) {
+        const T q = F::div(De, sumD);
+        term = q > T(0) ? F::mul(q, F::ln(q)) : T(0);
+    }
+    const T H = -block_sum<T, NW>(term, red[1]);
+    bool sure = true;
+    int m;
+    if (a.mode == MOE_ROUTE_ACCEPT) {
+        if constexpr (exact) {
+            const double r = exp(H);
+            const double rn = rint(r);
+            m = (fabs(r - rn) <= kSnap * r) ? (int)rn : (int)ceil(r);
+            m = min(max(m, k), pool);
+        } else {
+            const float r = expf(H);
+            const float dq = 2.f * dD + 21.f * kU;
+            const float dH = (dq + 23.f * kU) * fmaxf(H, 0.f) + dq;
+            const float dr = (dH + 4.f * kU) * 1.05f + 8.f * kU;
+            const int lo = min(max((int)ceilf(r * (1.f - dr)), k), pool);
+            const int hi = min(max((int)ceilf(r * (1.f + dr)), k), pool);
+            sure = lo == hi && isfinite(r);
+            m = hi;
+        }
+    } else {
+        m = min(max(a.fixed_B, k), pool);
+    }
+    const int nA = a.anchor ? k : 0;
+    // fill: candidates (pool minus anchor) ranked by (D desc, id asc); demand is >= 0, so
+    // -1 marks a non-candidate. `per` threads share an expert.
+    if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? De : T(-1);
+    __syncthreads();
+    const int per = NT >= 4 * E ? 4 : 2;
+    const int e = tid / per, pe = tid % per;
+    const int ec = min(e, E - 1);
+    const int F_ = m - nA;
+    int in = 0;
+    {
+        const int rnk = rank_of<T>(rk, ec, E, per, pe, true);  // every thread
+        const bool cand = e < E && rk[ec] >= T(0);
+        if (e < E) in = inA[e] || (cand && rnk < F_);
+        if (!exact && cand && pe == 0) {
+            if (rnk == F_ - 1) cut[0] = rk[ec];
+            if (rnk == F_) cut[1] = rk[ec];
+        }
+        const int ncand = __syncthreads_count(cand && pe == 0);  // rk is rewritten below
+        if (!exact && F_ > 0 && F_ < ncand)
+            sure = sure && (float)cut[0] * (1.f - dD - 2.f * kU) >
+                               (float)cut[1] * (1.f + dD + 2.f * kU);
+    }
+    if (e < E && pe == 0) inS[e] = in;
+    int removed = 0;
+    if (a.prune && resident) {
+        // removable members (non-resident, not anchor) ranked by (D asc, id asc); +inf
+        // marks the others
+        int is_rem = 0;
+        if (e < E) {
+            is_rem = in && !inA[e] && !resident[e];
+            if (pe == 0) rk[e] = is_rem ? D[e] : T(INFINITY);
+        }
+        const int nrem = __syncthreads_count(is_rem && pe == 0);
+        const int fl = a.min_set > k ? a.min_set : k;
+        removed = min(min(max(m - fl, 0), a.budget), nrem);
+        const int rnk = rank_of<T>(rk, ec, E, per, pe, false);  // every thread
+        if (is_rem && pe == 0) {
+            if (rnk < removed) inS[e] = 0;
+            if (!exact) {
+                if (rnk == removed - 1) cut[2] = D[e];
+                if (rnk == removed) cut[3] = D[e];
+            }
+        }
+        __syncthreads();
+        if (!exact && removed > 0 && removed < nrem)
+            sure = sure && (float)cut[3] * (1.f - dD - 2.f * kU) >
+                               (float)cut[2] * (1.f + dD + 2.f * kU);
+    }
+    __syncthreads();  // inS complete
+    return PhaseB{m, removed, sure};
+}
+
+// Relative error bound of the fp32 demand of a tree of N nodes whose logit ranges are at
+// most A, VPL logits per lane: per term, the commitment (1 rounding), the argument
+// l - max (|l - max| u), expf (2 ulp = 4u), the node's normaliser (its VPL - 1 + 5
+// additions and its terms' errors), the quotient and the product (1 rounding each); then
+// at most N + 8 additions of positive terms into D_e. 5% slack for second-order terms.
+__device__ __forceinline__ float demand_bound(float A, int N, int VPL) {
+    return kU * (2.f * A + (float)VPL + 15.f + (float)N + 8.f) * 1.05f;
 }
 
 // Loads the E logits of one node into v[] (lane holds experts lane + 32 i).
@@ -204,14 +416,13 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         prefetch_root_experts(pf, logits, E, k, (int)blockIdx.x - ((int)gridDim.x - pf.ctas));
         return;
     }
-    extern __shared__ float dyn[];  // staged logits, mx, nz, cN, nat, demand terms
+    // nz64 [N] (fp64 normalisers, the fp64 pass), staged logits, mx, nz, cN, nat, demand terms
+    extern __shared__ double dyn64[];
     __shared__ float D[kMaxE];
-    __shared__ float term[kMaxE];
-    __shared__ float rk[kMaxE];  // rank keys
+    __shared__ double D64[kMaxE], rkb[kMaxE], redb[2][kWarps], cutb[4];
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
     __shared__ int natRoot[kMaxK];
-    __shared__ float s_sumD;
-    __shared__ int s_m;
+    __shared__ int s_range;  // largest node logit range (a non-negative float's bits)
 
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -221,14 +432,16 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
     int *idxb = idx_out + (size_t)b * N * k;
     float *gb = gates_out + (size_t)b * N * k;
     const bool staged = N * E <= kStageFloats;
-    float *stage = dyn;
-    float *mx = dyn + (staged ? N * E : 0);  // [N] softmax maxima
-    float *nz = mx + N;                       // [N] softmax normalisers
-    float *cN = nz + N;                       // [N] commitment of each node
+    double *nz64 = dyn64;
+    float *stage = reinterpret_cast<float *>(dyn64 + N);
+    float *mx = stage + (staged ? N * E : 0);  // [N] softmax maxima
+    float *nz = mx + N;                        // [N] softmax normalisers
+    float *cN = nz + N;                        // [N] commitment of each node
     int *nat = reinterpret_cast<int *>(cN + N);  // [N][k] natural choices
 
     if (staged) {
-        if ((reinterpret_cast<uintptr_t>(Lg) & 15u) == 0) {
+        if ((reinterpret_cast<uintptr_t>(Lg) & 15u) == 0 &&
+            (reinterpret_cast<uintptr_t>(stage) & 15u) == 0) {
             const int n4 = (N * E) / 4;
             const float4 *src = reinterpret_cast<const float4 *>(Lg);
             float4 *dst = reinterpret_cast<float4 *>(stage);
@@ -243,10 +456,11 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         inSel[e] = 0;
         inA[e] = 0;
     }
+    if (tid == 0) s_range = 0;
     __syncthreads();
     const float *L = staged ? stage : Lg;
 
-    // ---- phase A: natural top-k, natural union, softmax max / normaliser ----
+    // ---- phase A: natural top-k, natural union, softmax max / normaliser, logit range ----
     for (int n = warp; n < N; n += kWarps) {
         float v[kVPL];
         load_row(L + (size_t)n * E, E, v);
@@ -261,10 +475,12 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         for (int i = 0; i < kVPL; ++i)
             if (lane + 32 * i < E) s += expf(v[i] - m);
         s = warp_sum(s);
+        const float range = node_range(v, E, m);
         if (lane == 0) {
             mx[n] = m;
             nz[n] = s;
             cN[n] = commitment(a, dep[n]);
+            atomicMax(&s_range, __float_as_int(range));
         }
     }
     __syncthreads();
@@ -295,87 +511,42 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
             D[e] = acc;
         }
     }
+    if (a.anchor && tid < k) inA[natRoot[tid]] = 1;
     __syncthreads();
 
-    // ---- phase B: size, anchor + fill, prune ----
-    const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
-    if (tid == 0) {
-        float sum = 0.f;
-#pragma unroll 16
-        for (int e = 0; e < E; ++e) sum = __fadd_rn(sum, D[e]);
-        s_sumD = sum;
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        const float q = __fdiv_rn(D[e], s_sumD);
-        term[e] = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int m;
-        if (a.mode == MOE_ROUTE_ACCEPT) {
-            float H = 0.f;
-#pragma unroll 16
-            for (int e = 0; e < E; ++e) H = __fsub_rn(H, term[e]);
-            const float r = expf(H);
-            const float rn = rintf(r);
-            m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
-        } else {
-            m = a.fixed_B;
-        }
-        if (m < k) m = k;
-        if (m > pool) m = pool;
-        s_m = m;
-        if (a.anchor)
-            for (int j = 0; j < k; ++j) inA[natRoot[j]] = 1;
-    }
-    __syncthreads();
-    const int nA = a.anchor ? k : 0;
-    const int m = s_m;
-    // fill: candidates (pool minus anchor) ranked by (D desc, id asc); demand is >= 0,
-    // so -1 marks a non-candidate
-    for (int e = tid; e < E; e += kThreads)
-        rk[e] = (!inA[e] && (a.pool_all || inU[e])) ? D[e] : -1.f;
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        int in = inA[e];
-        const float De = rk[e];
-        if (De >= 0.f) {
-            int rank = 0;
-#pragma unroll 8
-            for (int q = 0; q < E; ++q) {
-                const float Dq = rk[q];
-                rank += (Dq > De || (Dq == De && q < e)) ? 1 : 0;
+    // ---- phase B: size, anchor + fill, prune; fp32 with its certificate, else fp64 ----
+    const float A = __int_as_float(s_range);
+    PhaseB pb = phase_b<float, kWarps>(a, E, k, D, inU, inA, inS, resident,
+                                       reinterpret_cast<float *>(rkb),
+                                       reinterpret_cast<float(*)[kWarps]>(&redb[0][0]),
+                                       reinterpret_cast<float *>(cutb),
+                                       demand_bound(A, N, kVPL));
+    const bool exact_pass = !pb.sure || !(A <= kMaxRange);
+    if (exact_pass) {
+        // fp64 normaliser of every node, then a thread per expert adds its terms in order
+        for (int n = warp; n < N; n += kWarps) {
+            double s = 0.0;
+#pragma unroll
+            for (int i = 0; i < kVPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) s = __dadd_rn(s, exp((double)L[(size_t)n * E + e] - (double)mx[n]));
             }
-            in = rank < m - nA;
-        }
-        inS[e] = in;
-    }
-    __syncthreads();
-    int removed = 0;
-    if (a.prune && resident) {
-        // removable members (non-resident, not anchor) ranked by (D asc, id asc); +inf
-        // marks the others
-        int is_rem = 0;
-        if (tid < E) {
-            is_rem = inS[tid] && !inA[tid] && !resident[tid];
-            rk[tid] = is_rem ? D[tid] : INFINITY;
-        }
-        const int nrem = __syncthreads_count(is_rem);
-        const int fl = a.min_set > k ? a.min_set : k;
-        removed = min(min(max(m - fl, 0), a.budget), nrem);
-        if (is_rem) {
-            const float De = rk[tid];
-            int rank = 0;
-#pragma unroll 8
-            for (int q = 0; q < E; ++q) {
-                const float Dq = rk[q];
-                rank += (Dq < De || (Dq == De && q < tid)) ? 1 : 0;
-            }
-            if (rank < removed) inS[tid] = 0;
+            s = warp_sum64(s);
+            if (lane == 0) nz64[n] = s;
         }
         __syncthreads();
+        for (int e = tid; e < E; e += kThreads) {
+            double acc = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const double ex = exp((double)L[(size_t)n * E + e] - (double)mx[n]);
+                acc = __dadd_rn(acc, __dmul_rn(commitment64(a, dep[n]), __ddiv_rn(ex, nz64[n])));
+            }
+            D64[e] = acc;
+        }
+        __syncthreads();
+        pb = phase_b<double, kWarps>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb, 0.f);
     }
+    const int m = pb.m, removed = pb.removed;
 
     // ---- phase C: restricted top-k and gates ----
     unsigned allowed = 0;
@@ -401,6 +572,7 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
         info_out[b * MOE_INFO_FIELDS + 1] = u_sel;
         info_out[b * MOE_INFO_FIELDS + 2] = m;
         info_out[b * MOE_INFO_FIELDS + 3] = removed;
+        info_out[b * MOE_INFO_FIELDS + 4] = exact_pass ? 1 : 0;
     }
     if (elig_out)
         for (int e = tid; e < E; e += kThreads) elig_out[(size_t)b * E + e] = (uint8_t)inS[e];
@@ -416,9 +588,10 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
 // anchor / fill / prune phase, with sum D and H as block reductions and the ranks counted
 // by two or four threads per expert; meanwhile the other CTAs write their nodes' natural
 // routing, which stands for every node whose natural top-k lies in the eligible set. Every
-// CTA then reads the eligible set back and re-routes the nodes that need it. The demand
-// and its entropy are summed in a different order than in the one-CTA kernel (partials
-// per CTA, tree reductions), a difference at the level of fp32 rounding.
+// CTA then reads the eligible set back and re-routes the nodes that need it. When CTA 0's
+// fp32 phase B cannot certify its decisions, every CTA adds its nodes' fp64 demand terms
+// (from the logit rows it holds in shared memory), CTA 0 adds the partials in CTA order
+// and runs phase B again in fp64, before the re-routing.
 namespace cg = cooperative_groups;
 constexpr int kCC = 8;                  // CTAs per tree
 constexpr int kCW = 16;                 // warps per CTA
@@ -435,37 +608,6 @@ __device__ __forceinline__ void cluster_barrier(bool release) {
     else
         asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Rank of expert e under the order of the keys rk (desc: larger first, else smaller
-// first; equal keys: lower id first), i.e. the number of experts before it. `per`
-// consecutive threads (a power of two dividing 32) share e: thread `part` counts the
-// experts q = part (mod per), so that at each step a warp reads `per` consecutive words
-// (distinct banks), and the counts are added with shuffles.
-__device__ __forceinline__ int rank_of(const float *rk, int e, int E, int per, int part,
-                                       bool desc) {
-    const float me = rk[e];
-    int r = 0;
-#pragma unroll 8
-    for (int q = part; q < E; q += per) {
-        const float o = rk[q];
-        r += ((desc ? o > me : o < me) || (o == me && q < e)) ? 1 : 0;
-    }
-    for (int off = 1; off < per; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-    return r;
-}
-
-// Sum of v over the block's threads, identical in every thread: a butterfly per warp,
-// then the warps' sums in warp order (red holds one float per warp; the call ends with
-// a barrier, and `red` may be reused after the next barrier).
-__device__ __forceinline__ float block_sum(float v, float *red) {
-    v = warp_sum(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) s = __fadd_rn(s, red[w]);
-    return s;
 }
 
 // The permute step for a block of one tree, on CTA 0 of the selection cluster ("MoE and
@@ -578,16 +720,20 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         prefetch_root_experts(pf, logits, E, k, (int)blockIdx.x - ((int)gridDim.x - pf.ctas));
         return;
     }
-    // wt [slots][E], lrow [slots][E] (this CTA's logit rows), nat_all [N][k] (CTA 0),
-    // nat_loc [slots][k], nat_val [slots][k] (their logits), fin_all [N][k] (CTA 0: the
-    // final choices, for the permute step)
-    extern __shared__ float cdyn[];
-    __shared__ float part[kCC][kMaxE];  // CTA 0: partial demand of every CTA
-    __shared__ int selAll[kCC][kMaxE];  // CTA 0: experts chosen by every CTA's nodes
-    __shared__ float D[kMaxE], rk[kMaxE];
-    __shared__ float red[2][kCW];
+    // w64 [slots][E] (fp64 demand terms, the fp64 pass), wt [slots][E], lrow [slots][E]
+    // (this CTA's logit rows), nat_all [N][k] (CTA 0), nat_loc [slots][k], nat_val
+    // [slots][k] (their logits), fin_all [N][k] (CTA 0: the final choices, for the permute
+    // step)
+    extern __shared__ double cdyn64[];
+    __shared__ float part[kCC][kMaxE];    // CTA 0: partial demand of every CTA
+    __shared__ double part64[kCC][kMaxE]; // CTA 0: the same in fp64 (the fp64 pass)
+    __shared__ float rangeAll[kCC];       // CTA 0: largest node logit range of every CTA
+    __shared__ int selAll[kCC][kMaxE];    // CTA 0: experts chosen by every CTA's nodes
+    __shared__ float D[kMaxE];
+    __shared__ double D64[kMaxE], rkb[kMaxE], redb[2][kCW], cutb[4];
     __shared__ int inU[kMaxE], inS[kMaxE], inA[kMaxE], inSel[kMaxE];
-    __shared__ int s_m, s_removed;
+    __shared__ int s_m, s_removed, s_exact;
+    __shared__ float wrange[kCW];  // largest node logit range of each warp
     // CTA 0, permute step: bit n of rmask[e][n / 32] = node n chose e; offsets per expert
     __shared__ uint32_t rmask[kMaxE][kClusterMaxN / 32];
     __shared__ int soff[kMaxE + 1];
@@ -602,7 +748,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / kCC;
     const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
-    float *wt = cdyn;
+    double *w64 = cdyn64;
+    float *wt = reinterpret_cast<float *>(w64 + (size_t)slots * E);
     float *lrow = wt + (size_t)slots * E;
     int *nat_all = reinterpret_cast<int *>(lrow + (size_t)slots * E);
     int *nat_loc = nat_all + (size_t)N * k;
@@ -627,6 +774,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
     // ---- phase A: this CTA's nodes ----
+    float my_range = 0.f;  // uniform over the warp
     for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
         const int slot = t * kCW + warp;
         const int dn = dep[n];  // in flight with the logits
@@ -656,8 +804,15 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             const int e = lane + 32 * i;
             if (e < E) wt[slot * E + e] = __fmul_rn(cn, __fdiv_rn(ex[i], s));
         }
+        my_range = fmaxf(my_range, node_range(v, E, m));
     }
+    if (lane == 0) wrange[warp] = my_range;
     __syncthreads();
+    if (tid == 0) {
+        float A = 0.f;
+        for (int w = 0; w < kCW; ++w) A = fmaxf(A, wrange[w]);
+        cl.map_shared_rank(rangeAll, 0)[rank] = A;
+    }
     if (tid < E) {  // partial demand of this CTA's nodes, node order
         float acc = 0.f;
         for (int t = 0; t * kCC * kCW < N; ++t) {
@@ -678,61 +833,24 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     // stands unless phase C re-routes the node ----
     if (rank == 0) {
         for (int i = tid; i < N * k; i += kCThreads) inU[nat_all[i]] = 1;
-        float De = 0.f;
         if (tid < E) {
+            float De = 0.f;
             for (int r = 0; r < kCC; ++r) De = __fadd_rn(De, part[r][tid]);
             D[tid] = De;
         }
-        // sum D and H = -sum q ln q, each a block reduction (every thread gets the value)
-        const float sumD = block_sum(De, red[0]);
-        const int pool = __syncthreads_count(tid < E && (a.pool_all || inU[tid]));
-        float term = 0.f;
-        if (tid < E) {
-            const float q = __fdiv_rn(De, sumD);
-            term = q > 0.f ? __fmul_rn(q, logf(q)) : 0.f;
-        }
-        const float H = -block_sum(term, red[1]);
-        int m;
-        if (a.mode == MOE_ROUTE_ACCEPT) {
-            const float r = expf(H);
-            const float rn = rintf(r);
-            m = (fabsf(r - rn) <= kSnap * r) ? (int)rn : (int)ceilf(r);
-        } else {
-            m = a.fixed_B;
-        }
-        m = min(max(m, k), pool);
         if (a.anchor && tid < k) inA[nat_all[tid]] = 1;
+        float A = 0.f;
+        for (int r = 0; r < kCC; ++r) A = fmaxf(A, rangeAll[r]);
         __syncthreads();
-        const int nA = a.anchor ? k : 0;
-        if (tid < E) rk[tid] = (!inA[tid] && (a.pool_all || inU[tid])) ? D[tid] : -1.f;
-        __syncthreads();
-        // fill: candidates (pool minus anchor) ranked by (D desc, id asc); demand is >= 0,
-        // so -1 marks a non-candidate. `per` threads share an expert.
-        const int per = E <= kCThreads / 4 ? 4 : 2;
-        const int e = tid / per, pe = tid % per;
-        int in = 0;
-        {
-            const int rnk = rank_of(rk, min(e, E - 1), E, per, pe, true);  // every thread
-            if (e < E) in = inA[e] || (rk[e] >= 0.f && rnk < m - nA);
-        }
-        __syncthreads();  // rk is read above and rewritten below
-        if (e < E && pe == 0) inS[e] = in;
-        int removed = 0;
-        if (a.prune && resident) {
-            int is_rem = 0;
-            if (e < E) {
-                is_rem = in && !inA[e] && !resident[e];
-                if (pe == 0) rk[e] = is_rem ? D[e] : INFINITY;
-            }
-            const int nrem = __syncthreads_count(is_rem && pe == 0);
-            const int fl = a.min_set > k ? a.min_set : k;
-            removed = min(min(max(m - fl, 0), a.budget), nrem);
-            const int rnk = rank_of(rk, min(e, E - 1), E, per, pe, false);  // every thread
-            if (is_rem && pe == 0 && rnk < removed) inS[e] = 0;
-        }
+        const PhaseB pb = phase_b<float, kCW>(a, E, k, D, inU, inA, inS, resident,
+                                              reinterpret_cast<float *>(rkb),
+                                              reinterpret_cast<float(*)[kCW]>(&redb[0][0]),
+                                              reinterpret_cast<float *>(cutb),
+                                              demand_bound(A, N, VPL));
         if (tid == 0) {
-            s_m = m;
-            s_removed = removed;
+            s_m = pb.m;
+            s_removed = pb.removed;
+            s_exact = (!pb.sure || !(A <= kMaxRange)) ? 1 : 0;
         }
     } else {
         for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
@@ -742,9 +860,59 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                          idxb + (size_t)n * k, gb + (size_t)n * k);
         }
     }
-    // only CTA 0's writes (the eligible set) must be visible past this barrier: the other
-    // CTAs arrive without waiting for their global stores
+    // only CTA 0's writes (the eligible set, the verdict) must be visible past this
+    // barrier: the other CTAs arrive without waiting for their global stores
     cluster_barrier(rank == 0);
+
+    // ---- the fp64 pass, when CTA 0 could not certify the fp32 decisions (uniform over
+    // the cluster) ----
+    const int exact_pass = rank == 0 ? s_exact : *cl.map_shared_rank(&s_exact, 0);
+    if (exact_pass) {
+        for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
+            const int slot = t * kCW + warp;
+            const double top = (double)nat_val[slot * k];  // the node's largest logit
+            const double cn = commitment64(a, dep[n]);
+            double ex[VPL], s = 0.0;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                ex[i] = e < E ? exp((double)lrow[slot * E + e] - top) : 0.0;
+                s = __dadd_rn(s, ex[i]);
+            }
+            s = warp_sum64(s);
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) w64[slot * E + e] = __dmul_rn(cn, __ddiv_rn(ex[i], s));
+            }
+        }
+        __syncthreads();
+        if (tid < E) {  // this CTA's nodes in node order, into CTA 0
+            double acc = 0.0;
+            for (int t = 0; t * kCC * kCW < N; ++t) {
+                const int cnt = min(kCW, max(0, N - t * kCC * kCW - rank * kCW));
+                for (int w = 0; w < cnt; ++w)
+                    acc = __dadd_rn(acc, w64[(size_t)(t * kCW + w) * E + tid]);
+            }
+            cl.map_shared_rank(&part64[0][0], 0)[rank * kMaxE + tid] = acc;
+        }
+        cluster_barrier(true);
+        if (rank == 0) {
+            if (tid < E) {
+                double De = 0.0;
+                for (int r = 0; r < kCC; ++r) De = __dadd_rn(De, part64[r][tid]);
+                D64[tid] = De;
+            }
+            __syncthreads();
+            const PhaseB pb =
+                phase_b<double, kCW>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb, 0.f);
+            if (tid == 0) {
+                s_m = pb.m;
+                s_removed = pb.removed;
+            }
+        }
+        cluster_barrier(rank == 0);
+    }
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
     if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
@@ -752,6 +920,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         if (tid == 0 && info_out) {
             info_out[b * MOE_INFO_FIELDS + 2] = s_m;
             info_out[b * MOE_INFO_FIELDS + 3] = s_removed;
+            info_out[b * MOE_INFO_FIELDS + 4] = exact_pass;
         }
         if (elig_out && tid < E) elig_out[(size_t)b * E + tid] = (uint8_t)inS[tid];
     }
@@ -896,6 +1065,7 @@ select_natural_kernel(const float *__restrict__ logits, int N, int E, int k,
             info_out[b * MOE_INFO_FIELDS + 1] = u;
             info_out[b * MOE_INFO_FIELDS + 2] = E;
             info_out[b * MOE_INFO_FIELDS + 3] = 0;
+            info_out[b * MOE_INFO_FIELDS + 4] = 0;
         }
         if (elig_out)
             for (int e = tid; e < E; e += kNW * 32) elig_out[(size_t)b * E + e] = 1;
@@ -958,8 +1128,9 @@ cudaError_t launch_cluster(const moe_layer_desc &L, const SelectArgs &a, const f
                            float *gates, uint8_t *elig, int *info, WeightPrefetch pf,
                            PermuteOut po, std::atomic<size_t> &smem_set, cudaStream_t s) {
     const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
-    // wt and lrow [slots][E]; nat_all and fin_all [N][k]; nat_loc and nat_val [slots][k]
-    const size_t smem =
+    // w64 [slots][E] doubles; wt and lrow [slots][E]; nat_all and fin_all [N][k]; nat_loc
+    // and nat_val [slots][k]
+    const size_t smem = (size_t)slots * L.E * sizeof(double) +
         ((size_t)2 * slots * L.E + (size_t)2 * N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
     cudaError_t err = allow_smem(select_cluster_kernel<VPL>, smem_set, smem);
     if (err != cudaSuccess) return err;
@@ -1020,8 +1191,9 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
         return err;
     }
     const bool staged = N * L.E <= kStageFloats;
-    // staged: logits and demand terms [N][E] each; always: mx, nz, cN [N] and nat [N][k]
-    const size_t smem =
+    // nz64 [N] doubles; staged: logits and demand terms [N][E] each; always: mx, nz, cN [N]
+    // and nat [N][k]
+    const size_t smem = (size_t)N * sizeof(double) +
         ((staged ? 2 * (size_t)N * L.E : 0) + 3 * (size_t)N + (size_t)N * L.k) * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     cudaError_t err = allow_smem(select_kernel, single_smem_set, smem);

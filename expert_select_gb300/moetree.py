@@ -24,7 +24,7 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_ROUTE_NATURAL, MOE_ROUTE_ACCEPT, MOE_ROUTE_FIXED_B = 0, 1, 2
 MOE_FFN_AUTO, MOE_FFN_SIMT, MOE_FFN_TCGEN05 = 0, 1, 2
 MOE_MAX_DEPTHS = 16
-MOE_INFO_FIELDS = 4
+MOE_INFO_FIELDS = 5
 
 # Every function declared in include/moetree.h.
 EXPORTS = (
@@ -33,6 +33,7 @@ EXPORTS = (
     "moe_workspace_check", "moe_residency_create", "moe_residency_destroy",
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
     "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward", "moe_draft_select",
+    "moe_tree_route", "moe_tree_block_stats", "moe_noalloc_check",
 )
 
 
@@ -61,6 +62,16 @@ class TreeOutputs(C.Structure):
 class OffloadStats(C.Structure):
     _fields_ = [("needed", C.c_int), ("hits", C.c_int), ("uploads", C.c_int),
                 ("passes", C.c_int), ("h2d_bytes", C.c_longlong)]
+
+
+class TreeStats(C.Structure):
+    _fields_ = [("trees", C.c_int), ("assignments", C.c_int), ("union_experts", C.c_int),
+                ("max_per_expert", C.c_int), ("reuse", C.c_double),
+                ("union_nat_mean", C.c_double), ("union_sel_mean", C.c_double),
+                ("m_mean", C.c_double), ("pruned_mean", C.c_double), ("exact_trees", C.c_int)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class RunOpts(C.Structure):
@@ -100,6 +111,9 @@ def lib() -> C.CDLL:
             "moe_offload_forward": ([P, P, P, P, P, P, P, P, P, P, P, I, P, I, I, P, P, P, P, P,
                                      P, P], I),
             "moe_draft_select": ([P, I, P, P, P, P, C.c_float, I, P, P, P, P, P, P, P], I),
+            "moe_tree_route": ([P, P, P, P, P, I, I, P, P, P, P, P, P, P], I),
+            "moe_tree_block_stats": ([P, I, I, P, P, P, P, P], I),
+            "moe_noalloc_check": ([P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -170,6 +184,21 @@ def moe_tree_select(L, P, logits, depth, B, N, resident, topk_idx, gates, eligib
         _ptr(gates), _ptr(eligible), _ptr(info), _stream(stream)))
 
 
+def moe_tree_route(L, P, x, W_r, depth, B, N, resident, logits, topk_idx, gates, eligible=None,
+                   info=None, stream=None):
+    return _check("moe_tree_route", lib().moe_tree_route(
+        C.byref(L), C.byref(P), _ptr(x), _ptr(W_r), _ptr(depth), B, N, _ptr(resident),
+        _ptr(logits), _ptr(topk_idx), _ptr(gates), _ptr(eligible), _ptr(info), _stream(stream)))
+
+
+def moe_tree_block_stats(L, B, N, info=None, counts=None, ws=None, stream=None) -> TreeStats:
+    """Counters of the last block (union, reuse, per-tree set sizes); waits for the stream."""
+    st = TreeStats()
+    _check("moe_tree_block_stats", lib().moe_tree_block_stats(
+        C.byref(L), B, N, _ptr(info), _ptr(counts), _ptr(ws), C.byref(st), _stream(stream)))
+    return st
+
+
 def moe_expert_permute(L, topk_idx, counts, offsets, perm, ws, stream=None):
     return _check("moe_expert_permute", lib().moe_expert_permute(
         C.byref(L), _ptr(topk_idx), topk_idx.shape[0], _ptr(counts), _ptr(offsets), _ptr(perm),
@@ -232,6 +261,15 @@ def moe_workspace_check(ws, stream=None) -> int:
     st = lib().moe_workspace_check(_ptr(ws), C.byref(flags), _stream(stream))
     if st not in (MOE_OK, MOE_ERR_DEVICE_CHECK):
         raise MoeError("moe_workspace_check", st)
+    return flags.value
+
+
+def moe_noalloc_check(stream=None) -> int:
+    """Reads and clears the check word of moe_tree_forward_noalloc's built-in scratch."""
+    flags = C.c_int(0)
+    st = lib().moe_noalloc_check(C.byref(flags), _stream(stream))
+    if st not in (MOE_OK, MOE_ERR_DEVICE_CHECK):
+        raise MoeError("moe_noalloc_check", st)
     return flags.value
 
 

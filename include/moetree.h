@@ -103,8 +103,9 @@ typedef struct {
 } moe_select_params;
 
 /* Per-tree counters written by selection, int32 [B][MOE_INFO_FIELDS] in device memory:
- * natural union, selected union, eligible-set size m before pruning, pruned count. */
-#define MOE_INFO_FIELDS 4
+ * natural union, selected union, eligible-set size m before pruning, pruned count, and
+ * 1 if the tree's decisions needed the fp64 pass (see moe_tree_select), else 0. */
+#define MOE_INFO_FIELDS 5
 
 /* Optional device outputs of moe_tree_forward; any member may be NULL. */
 typedef struct {
@@ -150,17 +151,24 @@ moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void 
 
 /* Expert selection for B trees of N nodes from router logits ("AcceptMoE" news
  * article, section 02; AcceptMoE abstract). Per tree: natural top-k of every node,
- * demand D_e = sum_n c(depth_n) softmax(logits_n)_e (fp32, nodes in order), set
- * size m = max(k, ceil(exp(H(D / sum D)))) capped at the pool (FIXED_B: fixed_B),
- * root anchor + fill by (D desc, id asc), optional residency-aware pruning, then
- * each node's top-k restricted to the eligible set, gates = softmax over the k
- * chosen logits. NATURAL mode: plain top-k with the same renormalised gates.
+ * demand D_e = sum_n c(depth_n) softmax(logits_n)_e (nodes in order), set size
+ * m = max(k, ceil(exp(H(D / sum D)))) capped at the pool, an exp(H) within 1e-9
+ * (relative) of an integer counting as that integer (FIXED_B: m = fixed_B), root anchor
+ * + fill by (D desc, id asc), optional residency-aware pruning, then each node's top-k
+ * restricted to the eligible set, gates = softmax over the k chosen logits. NATURAL
+ * mode: plain top-k with the same renormalised gates.
+ * The demand, entropy and exp(H) are defined in fp64. The kernels compute them in fp32
+ * with a bound on their own rounding error and keep the fp32 decisions only where that
+ * bound proves them equal to the fp64 ones; any other tree is recomputed in fp64
+ * (info[b][4] = 1). Given the same logits, the results are those of the fp64 definition
+ * up to ties closer than fp64 rounding.
  *   logits   [B*N, E] device fp32, node n of tree b at row b*N + n, node 0 = root.
  *   depth    [B*N] device int32, draft depth of each node (root 0).
  *   resident [E] device uint8 (1 = expert resident) or NULL; required if P->prune.
  *   topk_idx [B*N, k] device int32, descending logit order, ties to the lower id.
  *   gates    [B*N, k] device fp32.
- *   eligible [B, E] device uint8 or NULL; info [B, 4] device int32 or NULL. */
+ *   eligible [B, E] device uint8 or NULL; info [B, MOE_INFO_FIELDS] device int32 or
+ *   NULL. */
 moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
                            const float *logits, const int *depth, int B, int N,
                            const uint8_t *resident, int *topk_idx, float *gates,
@@ -202,6 +210,41 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
                             const moe_tree_outputs *out, void *workspace,
                             const moe_run_opts *opts, moe_stream_t stream);
 
+/* Router and selection from hidden states: moe_router_logits followed by
+ * moe_tree_select on the same stream, for callers that hold x and W_r rather than
+ * logits. `logits` [B*N, E] device fp32 is written (the selection reads it); the other
+ * arguments are those of the two calls. */
+moe_status moe_tree_route(const moe_layer_desc *L, const moe_select_params *P, const void *x,
+                          const void *W_r, const int *depth, int B, int N,
+                          const uint8_t *resident, float *logits, int *topk_idx, float *gates,
+                          uint8_t *eligible, int *info, moe_stream_t stream);
+
+/* Counters of one verification block ("MoE and speculative decoding" blog, measurement
+ * section: unique experts, assignments per expert, and the reuse of the union
+ * 1 - |union of E(x_i)| / sum |E(x_i)|; "AcceptMoE" news article, section 02: the set
+ * size and what pruning removed). */
+typedef struct {
+    int trees;               /* B */
+    int assignments;         /* R * k routed (row, expert) pairs */
+    int union_experts;       /* experts with at least one assignment in the block */
+    int max_per_expert;      /* the largest per-expert count */
+    double reuse;            /* 1 - union_experts / assignments */
+    double union_nat_mean;   /* per tree: natural union (the pages' Standard SD) */
+    double union_sel_mean;   /* per tree: union after selection */
+    double m_mean;           /* per tree: eligible-set size before pruning */
+    double pruned_mean;      /* per tree: experts removed by residency-aware pruning */
+    int exact_trees;         /* trees whose decisions took the fp64 pass */
+} moe_tree_stats;
+
+/* Reads the counters of the last block routed with these arrays: info [B,
+ * MOE_INFO_FIELDS] and counts [E] (device), as written by moe_tree_forward /
+ * moe_tree_select + moe_expert_permute. NULL info or counts: the copies inside
+ * `workspace` (the one the forward call used; info/counts must not have been redirected
+ * by moe_tree_outputs then). Waits for `stream`; allocates nothing. */
+moe_status moe_tree_block_stats(const moe_layer_desc *L, int B, int N, const int *info,
+                                const int *counts, const void *workspace, moe_tree_stats *stats,
+                                moe_stream_t stream);
+
 /* moe_tree_forward without a `workspace` argument, for callers that cannot allocate
  * device memory when they run the layer: an engine whose free HBM is already reserved
  * for its KV cache, a plug-in that is handed only input/output device pointers, or a
@@ -218,8 +261,10 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
  *     contents; what must start at zero is cleared by the call itself. Calls whose work
  *     overlaps on the GPU (different streams, or different host threads without
  *     ordering) race on the array: order them on one stream.
- *   - Calls no allocating routine. Other arguments, results and errors are those of
- *     moe_tree_forward. */
+ *   - Calls no allocating routine. Other arguments and results are those of
+ *     moe_tree_forward. Kernel-side checks (a skipped expert id or slot, a bounded wait
+ *     that gave up) land in the built-in array's check word: read and clear it with
+ *     moe_noalloc_check. */
 moe_status moe_tree_forward_noalloc(const moe_layer_desc *L, const moe_select_params *P,
                                     const void *x, const void *W_r, const void *W_gate,
                                     const void *W_up, const void *W_down,
@@ -227,6 +272,14 @@ moe_status moe_tree_forward_noalloc(const moe_layer_desc *L, const moe_select_pa
                                     const uint8_t *resident, void *y,
                                     const moe_tree_outputs *out, const moe_run_opts *opts,
                                     moe_stream_t stream);
+
+/* The check word of moe_tree_forward_noalloc's built-in scratch on the current device,
+ * read and cleared like moe_workspace_check (waits for `stream`; no allocation). Each
+ * call of the layer starts the word afresh, so it reports the kernels of the last call:
+ * *flags = 0 when they reported no problem (also when the entry point has not run on
+ * this device or the word was read since); bits as in moe_workspace_check. Returns
+ * MOE_ERR_DEVICE_CHECK when *flags != 0. */
+moe_status moe_noalloc_check(int *flags, moe_stream_t stream);
 
 /* Cost-aware choice of the draft tree to verify ("Fewer experts, faster decoding:
  * cost-aware speculative decoding for MoE" (EcoSpec, arXiv 2607.12696), section 1 and

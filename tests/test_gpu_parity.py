@@ -2,14 +2,18 @@
 CPU oracle on the same seeded inputs.
 
 Bars: expert indices, eligible sets, set sizes, per-expert counts and the
-permutation are bit-exact; router logits within 1e-4 of the row's largest
-|logit|; gates within 1e-6; bf16 layer outputs within 2e-2 * max|ref| (fp32 layers
-within 1e-4 * max|ref|).
+permutation are bit-exact given the same fp32 router logits; router logits within
+1e-4 of the row's largest |logit|; gates within 1e-6; bf16 layer outputs within
+2e-2 * max|ref| (fp32 layers within 1e-4 * max|ref|).
 
-Where floating point decides an integer, both sides decide in fp32 (the oracle's
-precision="fp32" mode). A decision whose oracle margin is below 1e-5 (relative)
-is a tie at that precision: there both answers are correct, and the test checks
-that the device's answer is a valid one instead of comparing it.
+Decisions are compared with the oracle's fp64 definition of demand, entropy and
+effective rank. The device decides in fp32 when its rounding bound certifies the
+result and recomputes the tree in fp64 otherwise, so every tree must match. Only a
+tree whose fp64 decision margin is below TIE64 (1e-11, where CUDA's and the C
+library's fp64 exp and the two summation orders may disagree) is excused from the
+exact comparison; for such a tree the test checks that the device's answer is one
+of the valid ones (a size the margins allow, a demand-ordered fill, and the
+restricted top-k over the device's own eligible set).
 """
 import math
 
@@ -23,8 +27,9 @@ from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
 
-TIE = 1e-5
+TIE64 = 1e-11
 DEV = "cuda"
+NF = M.MOE_INFO_FIELDS
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,42 +62,68 @@ def _assert_close_rows(got, ref, shape):
 def _select_gpu(shape, P, logits, depth, B, N, resident=None):
     L = _desc(shape)
     R = B * N
-    lg = torch.from_numpy(logits).to(DEV)
+    lg = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(DEV)
     dp = torch.from_numpy(np.ascontiguousarray(depth.reshape(-1).astype(np.int32))).to(DEV)
     idx = torch.empty(R, shape.k, dtype=torch.int32, device=DEV)
     gates = torch.empty(R, shape.k, dtype=torch.float32, device=DEV)
     elig = torch.empty(B, shape.E, dtype=torch.uint8, device=DEV)
-    info = torch.empty(B, 4, dtype=torch.int32, device=DEV)
+    info = torch.empty(B, NF, dtype=torch.int32, device=DEV)
     res = None if resident is None else torch.from_numpy(resident).to(DEV)
     M.moe_tree_select(L, P, lg, dp, B, N, res, idx, gates, elig, info)
     _sync()
     return idx.cpu().numpy(), gates.cpu().numpy(), elig.cpu().numpy(), info.cpu().numpy()
 
 
-def _oracle_tree_ambiguous(o):
-    return (o["margin_rank"] < TIE or o["margin_fill"] < TIE or o["margin_prune"] < TIE)
+def _fp64_tied(o):
+    return min(o["margin_rank"], o["margin_fill"], o["margin_prune"]) < TIE64
+
+
+def _check_valid(shape, kw, l, o, gidx, ggates, gelig_b, ginfo_b):
+    """A valid selection for a tree whose fp64 margins tie: the size is one the rank
+    margin allows, the anchor is in, the fill is demand-ordered up to the tie, pruned
+    experts are non-resident non-anchor members, and the routing is the restricted
+    top-k over the device's own eligible set."""
+    k = shape.k
+    S = set(np.flatnonzero(gelig_b).tolist())
+    nat, _ = O.topk(l[:1], k)
+    A = set(nat[0].tolist()) if kw.get("anchor", True) else set()
+    assert A <= S
+    m_ok = {o["m"]} if o["margin_rank"] >= TIE64 else {o["m"] - 1, o["m"], o["m"] + 1}
+    assert ginfo_b[2] in m_ok and ginfo_b[2] >= k
+    D = o["D"]
+    pool = set(range(shape.E)) if kw.get("pool_all") else set(O.topk(l, k)[0].ravel().tolist())
+    if not kw.get("prune"):
+        assert len(S) == ginfo_b[2]
+        inside, outside = S - A, (pool - A) - S
+        if inside and outside:
+            assert min(D[e] for e in inside) >= max(D[e] for e in outside) * (1 - 1e-9)
+    else:
+        assert ginfo_b[3] <= kw.get("budget", 8)
+        assert len(S) == ginfo_b[2] - ginfo_b[3]
+    ridx, rg = O.restricted_route(l, gelig_b, k)
+    np.testing.assert_array_equal(gidx, ridx)
+    np.testing.assert_allclose(ggates, rg, atol=1e-6)
 
 
 def _check_selection(shape, kw, logits, depth, gidx, ggates, gelig, ginfo, N, B):
-    """Compares one block's selection tree by tree; returns the number of trees
-    compared exactly."""
-    exact = 0
+    """Compares one block's selection tree by tree with the fp64 oracle; returns the
+    number of trees excused as fp64 ties (validity-checked instead)."""
+    tied = 0
+    okw = {k: v for k, v in kw.items() if k != "c"}
     for b in range(B):
         sl = slice(b * N, (b + 1) * N)
-        o = O.select_tree(logits[sl], depth[b], shape.k, kw["c"],
-                          **{k: v for k, v in kw.items() if k != "c"})
-        if _oracle_tree_ambiguous(o):
-            S = set(np.flatnonzero(gelig[b]).tolist())
-            nat, _ = O.topk(logits[sl][:1], shape.k)
-            assert set(nat[0].tolist()) <= S and len(S) >= shape.k
-            assert set(np.unique(gidx[sl]).tolist()) <= S
+        o = O.select_tree(logits[sl], depth[b], shape.k, kw["c"], **okw)
+        if _fp64_tied(o):
+            tied += 1
+            _check_valid(shape, kw, logits[sl], o, gidx[sl], ggates[sl], gelig[b], ginfo[b])
             continue
-        exact += 1
         np.testing.assert_array_equal(gelig[b], o["eligible"])
         np.testing.assert_array_equal(gidx[sl], o["idx"])
         np.testing.assert_allclose(ggates[sl], o["gates"], atol=1e-6)
-        assert ginfo[b].tolist() == [o["union_nat"], o["union_sel"], o["m"], o["pruned"]]
-    return exact
+        assert ginfo[b, :4].tolist() == [o["union_nat"], o["union_sel"], o["m"], o["pruned"]]
+        if kw["mode"] == O.NATURAL:
+            assert ginfo[b, 4] == 0
+    return tied
 
 
 # ------------------------------------------------------------------- router
@@ -164,8 +195,143 @@ def test_selection_bit_exact(case):
     okw = dict(kw, c=c)
     if resident is not None:
         okw["resident"] = resident
-    exact = _check_selection(shape, okw, logits, depth, gidx, gg, ge, gi, N, B)
-    assert exact >= max(1, B - 1)
+    tied = _check_selection(shape, okw, logits, depth, gidx, gg, ge, gi, N, B)
+    assert tied == 0  # no fp64 ties on these seeded trees: every tree compared exactly
+
+
+# ------------------------------------------- near ties: the fp64 pass of the selector
+
+def _tree_of(N, seed):
+    """An EAGLE-3-shaped 65-node tree, or a random tree of N nodes (N > 256 takes the
+    one-CTA selector)."""
+    if N == 65:
+        t = W.eagle_tree(seed)
+        return t.parent, t.depth
+    rng = np.random.default_rng(seed)
+    parent = np.array([-1] + [int(rng.integers(0, n)) for n in range(1, N)], np.int32)
+    depth = np.zeros(N, np.int32)
+    for n in range(1, N):
+        depth[n] = depth[parent[n]] + 1
+    return parent, depth
+
+
+def _tie_columns(l, D, keep, copy, up):
+    """Expert `copy` gets expert `keep`'s logits at every node, then one fp32 ulp up (or
+    down) at the node where `keep` weighs most: the two demands then differ by ~1e-8
+    relative, below what fp32 resolves and far above fp64's rounding."""
+    l2 = l.copy()
+    l2[:, copy] = l2[:, keep]
+    n0 = int(np.argmax(l[:, keep] - l.max(axis=1)))
+    l2[n0, copy] = np.nextafter(l2[n0, keep], np.float32(np.inf if up else -np.inf))
+    return l2
+
+
+def _near_tie_fill(l, depth, k, c, kw):
+    """Moves the fill cut onto a near-tie (pool = all experts, so the natural union does
+    not move with the edit); returns logits whose fp64 fill margin is below 1e-6."""
+    for _ in range(8):
+        o = O.select_tree(l, depth, k, c, **kw)
+        if 1e-11 < o["margin_fill"] < 1e-6:
+            return l, o
+        A = set(O.topk(l[:1], k)[0][0].tolist())
+        cand = sorted(set(range(l.shape[1])) - A, key=lambda e: (-o["D"][e], e))
+        F = o["m"] - k
+        l = _tie_columns(l, o["D"], cand[F - 1], cand[F], up=False)
+    pytest.fail("could not build a fill near-tie")
+
+
+@pytest.mark.parametrize("E,N,mode", [(32, 65, O.FIXED_B), (128, 65, O.ACCEPT),
+                                      (256, 65, O.FIXED_B), (64, 300, O.ACCEPT)])
+def test_fp64_pass_decides_a_fill_near_tie(E, N, mode):
+    """Two experts whose demands differ by ~1e-8 sit on either side of the fill cut: the
+    fp32 pass cannot order them, takes the fp64 pass (info[4] = 1), and the eligible set
+    equals the fp64 oracle's."""
+    shape = W.LayerShape(d=64, E=E, k=4, f=64, dtype="fp32")
+    parent, depth = _tree_of(N, 7 + E)
+    l = W.synthetic_logits(8 + E, parent[None], E, 3.0)
+    kw = dict(mode=mode, pool_all=True, fixed_B=14)
+    l, o = _near_tie_fill(l, depth, shape.k, W.C_EAGLE, kw)
+    omode = {O.ACCEPT: M.MOE_ROUTE_ACCEPT, O.FIXED_B: M.MOE_ROUTE_FIXED_B}[mode]
+    P = M.select_params(omode, W.C_EAGLE, pool_all=True, fixed_B=14)
+    gidx, gg, ge, gi = _select_gpu(shape, P, l, depth[None], 1, N)
+    assert gi[0, 4] == 1
+    assert _check_selection(shape, dict(kw, c=W.C_EAGLE), l, depth[None], gidx, gg, ge, gi,
+                            N, 1) == 0
+
+
+@pytest.mark.parametrize("E,N", [(64, 65), (64, 300)])
+def test_fp64_pass_decides_a_prune_near_tie(E, N):
+    """The last expert pruning removes and the next one differ by ~1e-8 in demand."""
+    shape = W.LayerShape(d=64, E=E, k=4, f=64, dtype="fp32")
+    parent, depth = _tree_of(N, 30 + N)
+    l = W.synthetic_logits(31 + N, parent[None], E, 3.0)
+    res = W.residency_mask(5, E, E // 2)
+    kw = dict(mode=O.FIXED_B, pool_all=True, fixed_B=24, prune=True, resident=res, budget=3,
+              min_set=4)
+    for _ in range(8):
+        o = O.select_tree(l, depth, shape.k, W.C_EAGLE, **kw)
+        if 1e-11 < o["margin_prune"] < 1e-6:
+            break
+        base = O.select_tree(l, depth, shape.k, W.C_EAGLE, **dict(kw, prune=False))
+        A = set(O.topk(l[:1], shape.k)[0][0].tolist())
+        S = set(np.flatnonzero(base["eligible"]).tolist())
+        rem = sorted([e for e in S - A if not res[e]], key=lambda e: (base["D"][e], e))
+        r = o["pruned"]
+        assert 0 < r < len(rem)
+        l = _tie_columns(l, base["D"], rem[r - 1], rem[r], up=True)
+    else:
+        pytest.fail("could not build a prune near-tie")
+    P = M.select_params(M.MOE_ROUTE_FIXED_B, W.C_EAGLE, pool_all=True, fixed_B=24, prune=True,
+                        reroute_budget=3, min_set=4)
+    gidx, gg, ge, gi = _select_gpu(shape, P, l, depth[None], 1, N, res)
+    assert gi[0, 4] == 1
+    assert _check_selection(shape, dict(kw, c=W.C_EAGLE), l, depth[None], gidx, gg, ge, gi,
+                            N, 1) == 0
+
+
+@pytest.mark.parametrize("E,N,side", [(128, 65, 1.0), (128, 65, -1.0), (64, 300, 1.0)])
+def test_fp64_pass_decides_a_size_near_integer(E, N, side):
+    """Logits scaled so that exp(H) lies 4e-8 (relative) above an integer n (set size
+    n + 1: beyond the 1e-9 snap) or below it (size n): fp32 cannot tell, fp64 can."""
+    shape = W.LayerShape(d=64, E=E, k=4, f=64, dtype="fp32")
+    parent, depth = _tree_of(N, 50 + N)
+    base = W.synthetic_logits(51 + N, parent[None], E, 3.0).astype(np.float64)
+    kw = dict(mode=O.ACCEPT, pool_all=True)
+    r_of = lambda a: O.select_tree((base * a).astype(np.float32), depth, shape.k,  # noqa: E731
+                                   W.C_EAGLE, **kw)["r"]
+    n = round(r_of(1.0))
+    target = n * (1.0 + side * 4e-8)
+    lo, hi = 0.7, 1.4  # exp(H) falls as the logits sharpen
+    assert r_of(lo) > target > r_of(hi)
+    for _ in range(80):
+        mid = 0.5 * (lo + hi)
+        if r_of(mid) > target:
+            lo = mid
+        else:
+            hi = mid
+    l = (base * lo).astype(np.float32)
+    o = O.select_tree(l, depth, shape.k, W.C_EAGLE, **kw)
+    assert 1e-11 < o["margin_rank"] < 1e-6 and abs(o["r"] / n - 1) < 1e-6
+    assert o["m"] == (n + 1 if side > 0 else n)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, pool_all=True)
+    gidx, gg, ge, gi = _select_gpu(shape, P, l, depth[None], 1, N)
+    assert gi[0, 4] == 1
+    assert _check_selection(shape, dict(kw, c=W.C_EAGLE), l, depth[None], gidx, gg, ge, gi,
+                            N, 1) == 0
+
+
+def test_fp32_certificate_decides_ordinary_trees():
+    """64 peaked EAGLE-3-shaped trees (set sizes in the pages' 23-34 range): all match the
+    fp64 oracle and the fp32 pass decides nearly all of them on its own."""
+    shape = W.QWEN3_30B_A3B
+    parent, depth = W.tree_block(606, 64, "eagle")
+    N = parent.shape[1]
+    logits = W.synthetic_logits(607, parent, shape.E, 4.5)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth, 64, N)
+    assert _check_selection(shape, dict(mode=O.ACCEPT, c=W.C_EAGLE), logits, depth, gidx, gg,
+                            ge, gi, N, 64) == 0
+    assert gi[:, 4].sum() <= 3, gi[:, 4].sum()
 
 
 def test_selection_large_tree_single_cta_path():
@@ -183,10 +349,10 @@ def test_selection_large_tree_single_cta_path():
         P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=True, reroute_budget=8,
                             min_set=6)
         gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth[None], 1, N, res)
-        exact = _check_selection(shape, dict(mode=O.ACCEPT, prune=True, budget=8, min_set=6,
-                                             resident=res, c=W.C_EAGLE),
-                                 logits, depth[None], gidx, gg, ge, gi, N, 1)
-        assert exact == 1
+        tied = _check_selection(shape, dict(mode=O.ACCEPT, prune=True, budget=8, min_set=6,
+                                            resident=res, c=W.C_EAGLE),
+                                logits, depth[None], gidx, gg, ge, gi, N, 1)
+        assert tied == 0
 
 
 @pytest.mark.parametrize("B,N,E,k", [(1, 411, 128, 8), (3, 1000, 64, 4), (2, 3000, 256, 16),
@@ -205,9 +371,9 @@ def test_selection_natural_any_tree_size(B, N, E, k):
     logits = W.synthetic_logits(N + 7 * B, parent, E, 3.0)
     P = M.select_params(M.MOE_ROUTE_NATURAL, [1.0])
     gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth, B, N)
-    exact = _check_selection(shape, dict(mode=O.NATURAL, c=[1.0]), logits, depth, gidx, gg, ge,
-                             gi, N, B)
-    assert exact == B
+    tied = _check_selection(shape, dict(mode=O.NATURAL, c=[1.0]), logits, depth, gidx, gg, ge,
+                            gi, N, B)
+    assert tied == 0
 
 
 def test_selection_root_only_and_all_experts():
@@ -222,6 +388,7 @@ def test_selection_root_only_and_all_experts():
         o = O.select_tree(logits, depth[0], shape.k, W.C_TINY)
         np.testing.assert_array_equal(gidx, o["idx"])
         np.testing.assert_array_equal(ge[0], o["eligible"])
+        assert gi[0, :4].tolist() == [o["union_nat"], o["union_sel"], o["m"], o["pruned"]]
 
 
 def test_worked_examples_through_device():
@@ -247,6 +414,59 @@ def test_worked_examples_through_device():
         assert int((c > 0).sum()) == union
         for e, v in counts.items():
             assert c[e] == v
+        # the block counters: union, assignments and reuse = 1 - union / assignments
+        st = M.moe_tree_block_stats(L, 1, N, torch.from_numpy(gi).to(DEV), cnt)
+        assert (st.union_experts, st.assignments, st.trees) == (union, 2 * N, 1)
+        assert st.reuse == pytest.approx(1 - union / (2 * N))
+        assert st.max_per_expert == max(counts.values())
+        assert st.union_nat_mean == st.union_sel_mean == union and st.exact_trees == 0
+
+
+def test_tree_route_equals_router_then_select():
+    """moe_tree_route (hidden states in) gives bit for bit what moe_router_logits followed
+    by moe_tree_select give, and the selection equals the fp64 oracle's on those logits;
+    the block counters read from the workspace match the forward call's outputs."""
+    shape = W.QWEN3_30B_A3B
+    B = 4
+    parent, depth = W.tree_block(515, B, "eagle")
+    N = parent.shape[1]
+    R = B * N
+    x = W.hidden_states(516, parent, shape.d, torch.bfloat16).to(DEV)
+    wr = W.router_weight(517, shape, std=0.1, device=DEV)
+    L = _desc(shape)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    dp = torch.from_numpy(depth.reshape(-1).copy()).to(DEV)
+    outs = []
+    for fused in (True, False):
+        lg = torch.empty(R, shape.E, device=DEV)
+        idx = torch.empty(R, shape.k, dtype=torch.int32, device=DEV)
+        g = torch.empty(R, shape.k, device=DEV)
+        el = torch.empty(B, shape.E, dtype=torch.uint8, device=DEV)
+        inf = torch.empty(B, NF, dtype=torch.int32, device=DEV)
+        if fused:
+            M.moe_tree_route(L, P, x, wr, dp, B, N, None, lg, idx, g, el, inf)
+        else:
+            M.moe_router_logits(L, x, wr, lg)
+            M.moe_tree_select(L, P, lg, dp, B, N, None, idx, g, el, inf)
+        _sync()
+        outs.append([t.cpu().numpy() for t in (lg, idx, g, el, inf)])
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    lg, idx, g, el, inf = outs[0]
+    assert _check_selection(shape, dict(mode=O.ACCEPT, c=W.C_EAGLE), lg, depth, idx, g, el, inf,
+                            N, B) == 0
+    # the same block through the whole layer, counters read back from the workspace
+    wg, wu, wd = _weights(shape, 518)
+    ws = M.workspace(L, B, N)
+    y = torch.empty(R, shape.d, dtype=torch.bfloat16, device=DEV)
+    M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dp, B, N, None, y, ws)
+    st = M.moe_tree_block_stats(L, B, N, ws=ws)
+    cnt = np.bincount(idx.ravel(), minlength=shape.E)
+    assert st.assignments == R * shape.k and st.union_experts == int((cnt > 0).sum())
+    assert st.max_per_expert == int(cnt.max())
+    assert st.union_sel_mean == pytest.approx(inf[:, 1].mean())
+    assert st.m_mean == pytest.approx(inf[:, 2].mean())
+    assert st.reuse == pytest.approx(1 - st.union_experts / st.assignments)
 
 
 # ------------------------------------------------------------------ permute
@@ -478,7 +698,7 @@ def _run_forward(shape, B, kind, std, mode, seed, path=M.MOE_FFN_AUTO, prune=Non
                topk_idx=torch.empty(R, shape.k, dtype=torch.int32, device=DEV),
                gates=torch.empty(R, shape.k, device=DEV),
                eligible=torch.empty(B, shape.E, dtype=torch.uint8, device=DEV),
-               info=torch.empty(B, 4, dtype=torch.int32, device=DEV),
+               info=torch.empty(B, NF, dtype=torch.int32, device=DEV),
                counts=torch.empty(shape.E, dtype=torch.int32, device=DEV),
                offsets=torch.empty(shape.E + 1, dtype=torch.int32, device=DEV),
                perm=torch.empty(R * shape.k, dtype=torch.int32, device=DEV))
@@ -496,6 +716,11 @@ def _run_forward(shape, B, kind, std, mode, seed, path=M.MOE_FFN_AUTO, prune=Non
 
 @pytest.mark.parametrize("case", FORWARD_CASES, ids=[c[0] for c in FORWARD_CASES])
 def test_tree_forward_against_oracle(case):
+    """The whole layer. The router's logits are compared with the oracle's (its own fp64
+    matmul); every later step is compared with the oracle fed the device's fp32 logits,
+    exactly (per tree, fp64 ties excused as in the selection tests); the layer output on
+    sampled rows is compared with the oracle's experts and combine on those choices. The
+    oracle's routing from its own logits must also agree on nearly every row."""
     _, shape, B, kind, std, mode, rows = case
     run = _run_forward(shape, B, kind, std, mode, seed=300 + B)
     got, N = run["got"], run["N"]
@@ -503,33 +728,36 @@ def test_tree_forward_against_oracle(case):
     omode = {M.MOE_ROUTE_NATURAL: O.NATURAL, M.MOE_ROUTE_ACCEPT: O.ACCEPT}[mode]
     sample = list(range(R)) if rows is None else \
         sorted(np.random.default_rng(3).choice(R, rows, replace=False).tolist())
-    ref = O.forward(run["x"], run["wr"], run["wg"].cpu(), run["wu"].cpu(), run["wd"].cpu(),
-                    run["depth"], shape.k, run["c"], rows=sample, mode=omode)
-    scale = np.abs(ref["logits"]).max(axis=1, keepdims=True)
-    assert (np.abs(got["logits"] - ref["logits"]) <= 1e-4 * scale).all()
-    # decisions: exact unless the oracle's own margin says the inputs are tied at fp32
-    topk_tied = ref["margin_topk"] < TIE * scale.min() or \
-        ref["margin_restricted"] < TIE * scale.min()
-    ambiguous = topk_tied or ref["margin_rank"] < TIE or ref["margin_fill"] < TIE
-    if not ambiguous:
-        np.testing.assert_array_equal(got["topk_idx"], ref["idx"])
-        np.testing.assert_array_equal(got["eligible"], ref["eligible"])
-        np.testing.assert_array_equal(got["counts"], ref["counts"])
-        np.testing.assert_array_equal(got["offsets"], ref["offsets"])
-        np.testing.assert_array_equal(got["perm"], ref["perm"])
-        np.testing.assert_allclose(got["gates"], ref["gates"], atol=1e-5)
-        assert got["info"][:, 0].tolist() == ref["union_nat"].tolist()
-        assert got["info"][:, 1].tolist() == ref["union_sel"].tolist()
-        _assert_close_rows(got["y"][sample], ref["y"], shape)
-    else:
-        same = [i for i, r in enumerate(sample) if (got["topk_idx"][r] == ref["idx"][r]).all()]
-        assert len(same) >= len(sample) // 2
-        _assert_close_rows(got["y"][[sample[i] for i in same]], ref["y"][same], shape)
+    # 1. router logits against the oracle's own
+    ref_l = O.router(run["x"], run["wr"])
+    scale = np.abs(ref_l).max(axis=1, keepdims=True)
+    assert (np.abs(got["logits"] - ref_l) <= 1e-4 * scale).all()
+    # 2. selection, permute and counters from the device's logits, tree by tree
+    depth = run["depth"]
+    kw = dict(mode=omode, c=run["c"])
+    tied = _check_selection(shape, kw, got["logits"], depth, got["topk_idx"], got["gates"],
+                            got["eligible"], got["info"], N, B)
+    assert tied == 0
+    rc, ro, rp = O.permute(got["topk_idx"], shape.E)
+    np.testing.assert_array_equal(got["counts"], rc)
+    np.testing.assert_array_equal(got["offsets"], ro)
+    np.testing.assert_array_equal(got["perm"], rp)
+    sel = O.select_block(got["logits"], depth, shape.k, run["c"], mode=omode)
+    np.testing.assert_array_equal(got["topk_idx"], sel["idx"])
+    # 3. the layer output on sampled rows: the oracle's experts and combine
+    y_ref = O.moe_combine(run["x"], run["wg"].cpu(), run["wu"].cpu(), run["wd"].cpu(),
+                          sel["idx"], sel["gates"], rows=sample)
+    _assert_close_rows(got["y"][sample], y_ref, shape)
+    # 4. the oracle end to end from its own logits: the same routing on nearly every row
+    # (rows may differ only where the two logit computations straddle a near-tie)
+    own = O.select_block(ref_l.astype(np.float32), depth, shape.k, run["c"], mode=omode)
+    same = (np.sort(own["idx"], axis=1) == np.sort(got["topk_idx"], axis=1)).all(axis=1)
+    assert same.mean() >= 0.98, same.mean()
     # invariants that hold at any size
     for b in range(B):
         S = set(np.flatnonzero(got["eligible"][b]).tolist())
-        sel = set(np.unique(got["topk_idx"][b * N:(b + 1) * N]).tolist())
-        assert sel <= S and len(S) >= shape.k
+        chosen = set(np.unique(got["topk_idx"][b * N:(b + 1) * N]).tolist())
+        assert chosen <= S and len(S) >= shape.k
         assert got["info"][b, 1] <= got["info"][b, 0]
 
 
@@ -566,15 +794,11 @@ def test_residual_chain_of_layers_against_oracle():
     for l, (wr, wg, wu, wd) in enumerate(layers):
         ref = O.forward(xo, wr.cpu(), wg.cpu(), wu.cpu(), wd.cpu(), t.depth, shape.k, W.C_EAGLE,
                         mode=O.ACCEPT)
-        if l == 0:  # identical inputs: exact unless the oracle reports a tie
-            tied = ref["margin_topk"] < 1e-4 or ref["margin_restricted"] < 1e-4 or \
-                ref["margin_rank"] < TIE or ref["margin_fill"] < TIE
-            if not tied:
-                np.testing.assert_array_equal(got_idx[l], ref["idx"])
-        else:  # inputs differ by the bf16 rounding of the previous layer's output
-            same = sum(set(got_idx[l][r].tolist()) == set(ref["idx"][r].tolist())
-                       for r in range(N))
-            assert same >= 0.9 * N
+        # identical inputs for the first layer, inputs that differ by the bf16 rounding of
+        # the previous layer's output afterwards: the routing agrees on nearly every row
+        same = sum(set(got_idx[l][r].tolist()) == set(ref["idx"][r].tolist())
+                   for r in range(N))
+        assert same >= (0.98 if l == 0 else 0.9) * N
         xo = (xo.double() + torch.from_numpy(ref["y"])).to(torch.bfloat16)
     ref_x = xo.double().numpy()
     got = x.double().cpu().numpy()

@@ -41,7 +41,7 @@ def test_status_strings_and_version():
     assert M.status_str(0) == "ok"
     assert "slot" in M.status_str(M.MOE_ERR_NOSLOT)
     assert M.status_str(12345) == "unknown status"
-    assert M.lib().moe_abi_version() == 100
+    assert M.lib().moe_abi_version() == 200
 
 
 def test_workspace_bytes():
@@ -104,6 +104,19 @@ def test_draft_select_and_other_entry_points_reject_bad_arguments():
     assert lib.moe_tree_forward_noalloc(C.byref(L), nul, nul, nul, nul, nul, nul, nul, nul, 1, 65,
                                         nul, nul, nul, nul, nul) == M.MOE_ERR_ARG
     P = M.select_params(M.MOE_ROUTE_ACCEPT, [1.0])
+    # router + selection from hidden states: missing outputs, misaligned x
+    assert lib.moe_tree_route(C.byref(L), C.byref(P), f, f, f, 1, 65, nul, nul, f, f, nul, nul,
+                              nul) == M.MOE_ERR_ARG
+    assert lib.moe_tree_route(C.byref(L), C.byref(P), odd, f, f, 1, 65, nul, f, f, f, nul, nul,
+                              nul) == M.MOE_ERR_ARG
+    # block counters: no output struct, or neither arrays nor a workspace to read them from
+    st = M.TreeStats()
+    assert lib.moe_tree_block_stats(C.byref(L), 1, 65, f, f, nul, nul, nul) == M.MOE_ERR_ARG
+    assert lib.moe_tree_block_stats(C.byref(L), 1, 65, nul, f, nul, C.byref(st),
+                                    nul) == M.MOE_ERR_ARG
+    assert lib.moe_tree_block_stats(C.byref(L), 0, 65, f, f, nul, C.byref(st),
+                                    nul) == M.MOE_ERR_ARG
+    assert lib.moe_noalloc_check(nul, nul) == M.MOE_ERR_ARG
     Ls = M.layer_desc(2048, 128, 8, 768, "bf16", slots=48)
     # no residency table
     assert lib.moe_offload_forward(C.byref(Ls), C.byref(P), f, f, f, f, f, f, f, f, nul, 0, f,

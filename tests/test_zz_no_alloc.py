@@ -79,3 +79,26 @@ def test_noalloc_rejects_requests_beyond_its_scratch(layer):
     with pytest.raises(M.MoeError) as ei:
         M.moe_tree_forward_noalloc(L, P, x, wr, wg, wu, wd, None, dep, B, N, None, y)
     assert ei.value.status == M.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_kernel_checks(layer):
+    """The built-in scratch's check word is readable (and cleared) through
+    moe_noalloc_check: an expert mapped to a slot outside the weight pool is skipped by
+    the expert kernel and flagged (bit 0); a clean call reports 0."""
+    shape, wr, wg, wu, wd = layer
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    t, x, dep = _tree(13, shape)
+    R = t.N
+    y = torch.empty(R, shape.d, dtype=torch.bfloat16, device=DEV)
+    M.moe_tree_forward_noalloc(L, P, x, wr, wg, wu, wd, None, dep, 1, R, None, y)
+    assert M.moe_noalloc_check() == 0
+    slot = torch.arange(shape.E, dtype=torch.int32, device=DEV)
+    idx = torch.empty(R, shape.k, dtype=torch.int32, device=DEV)
+    M.moe_tree_forward_noalloc(L, P, x, wr, wg, wu, wd, slot, dep, 1, R, None, y,
+                               M.tree_outputs(topk_idx=idx))
+    torch.cuda.synchronize()
+    slot[int(idx[0, 0].item())] = 10 ** 6  # the root's first expert: beyond the pool
+    M.moe_tree_forward_noalloc(L, P, x, wr, wg, wu, wd, slot, dep, 1, R, None, y)
+    assert M.moe_noalloc_check() & 1
+    assert M.moe_noalloc_check() == 0  # cleared by the read
