@@ -186,7 +186,30 @@ struct moe_residency {
     std::vector<int> expert_in;   // [layer][slots], -1 = free
     std::vector<long long> used;  // [layer][slots], last-use tick
     long long tick = 0;
+    // Timing events of the offloaded layer, per layer: pairs recorded on the compute
+    // stream just before and just after each wait for an upload, and how many pairs the
+    // last call on that layer used (created on first use, reused by later calls).
+    std::vector<std::vector<cudaEvent_t>> wait_ev;
+    std::vector<int> n_wait;
+    ~moe_residency() {
+        for (auto &v : wait_ev)
+            for (cudaEvent_t e : v)
+                if (e) cudaEventDestroy(e);
+    }
 };
+
+// Event `which` (0: before the wait, 1: after it) of the i-th upload wait of `layer`.
+cudaEvent_t moe::residency_wait_event(moe_residency *t, int layer, int i, int which) {
+    auto &v = t->wait_ev[layer];
+    while ((int)v.size() < 2 * (i + 1)) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        v.push_back(e);
+    }
+    return v[2 * i + which];
+}
+
+void moe::residency_set_waits(moe_residency *t, int layer, int n) { t->n_wait[layer] = n; }
 
 extern "C" {
 
@@ -358,6 +381,9 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
                         at<int>(workspace, w.active), at<int>(workspace, w.rowtiles),
                         at<int>(workspace, w.flags), 1};
     bool permuted = false;
+    if (opts && opts->select_begin &&
+        cudaEventRecord((cudaEvent_t)opts->select_begin, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, pf, po,
                       &permuted, s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -389,6 +415,8 @@ moe_status moe_residency_create(int n_layers, int E, int slots, moe_residency **
     t->slot_of.assign((size_t)n_layers * E, -1);
     t->expert_in.assign((size_t)n_layers * slots, -1);
     t->used.assign((size_t)n_layers * slots, 0);
+    t->wait_ev.resize(n_layers);
+    t->n_wait.assign(n_layers, 0);
     *table = t;
     return MOE_OK;
 }
@@ -488,6 +516,25 @@ moe_status moe_expert_upload(const moe_layer_desc *L, const void *host_gate, con
                 return MOE_ERR_CUDA;
     }
     if (done && cudaEventRecord((cudaEvent_t)done, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_offload_upload_wait(moe_residency *t, int layer, double timeout_s,
+                                   double *wait_ms, int *waits) {
+    if (!t || layer < 0 || layer >= t->n_layers || !wait_ms || timeout_s < 0)
+        return MOE_ERR_ARG;
+    double sum = 0.0;
+    const int n = t->n_wait[layer];
+    for (int i = 0; i < n; ++i) {
+        cudaEvent_t a = t->wait_ev[layer][2 * i], b = t->wait_ev[layer][2 * i + 1];
+        const moe_status st = moe_event_wait((moe_event_t)b, timeout_s);
+        if (st != MOE_OK) return st;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return MOE_ERR_CUDA;
+        sum += ms;
+    }
+    *wait_ms = sum;
+    if (waits) *waits = n;
     return MOE_OK;
 }
 

@@ -137,6 +137,9 @@ cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host,
                            uint8_t *res_dev, cudaStream_t s);
 
 // ---- host helpers shared by the entry points (api.cu, offload.cu) ----
+// Timing events of the offloaded layer's upload waits, kept in the residency table.
+cudaEvent_t residency_wait_event(moe_residency *t, int layer, int i, int which);
+void residency_set_waits(moe_residency *t, int layer, int n);
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 template <typename T>

@@ -152,6 +152,8 @@ extern "C" moe_status moe_offload_forward(
 
     // 3b. missing experts in chunks, uploads on the side stream
     size_t next = 0;
+    int n_wait = 0;
+    residency_set_waits(table, layer, 0);
     while (next < missing.size()) {
         const size_t left = missing.size() - next;
         const size_t room = slots > (int)prev.size() ? slots - prev.size() : 0;
@@ -179,7 +181,14 @@ extern "C" moe_status moe_offload_forward(
             return st;
         uploads += n_up;
         h2d += (long long)n_up * 3 * (long long)mat_bytes;
+        // the compute stream's wait for this upload, bracketed by timing events: the
+        // second completes when both the work before it and the upload are done
+        cudaEvent_t w0 = residency_wait_event(table, layer, n_wait, 0);
+        cudaEvent_t w1 = residency_wait_event(table, layer, n_wait, 1);
+        if (!w0 || !w1 || cudaEventRecord(w0, s) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaStreamWaitEvent(s, ev_up, 0) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaEventRecord(w1, s) != cudaSuccess) return MOE_ERR_CUDA;
+        residency_set_waits(table, layer, ++n_wait);
         if ((st = pass_run(chunk)) != MOE_OK) return st;
         ev_prev2 = ev_prev;
         ev_prev = events.make();

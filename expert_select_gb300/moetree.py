@@ -33,7 +33,7 @@ EXPORTS = (
     "moe_workspace_check", "moe_residency_create", "moe_residency_destroy",
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
     "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward", "moe_draft_select",
-    "moe_tree_route", "moe_tree_block_stats", "moe_noalloc_check",
+    "moe_tree_route", "moe_tree_block_stats", "moe_noalloc_check", "moe_offload_upload_wait",
 )
 
 
@@ -76,7 +76,7 @@ class TreeStats(C.Structure):
 
 class RunOpts(C.Structure):
     _fields_ = [("ffn_path", C.c_int), ("ffn_begin", C.c_void_p), ("ffn_end", C.c_void_p),
-                ("residual", C.c_int)]
+                ("residual", C.c_int), ("select_begin", C.c_void_p)]
 
 
 _lib = None
@@ -114,6 +114,7 @@ def lib() -> C.CDLL:
             "moe_tree_route": ([P, P, P, P, P, I, I, P, P, P, P, P, P, P], I),
             "moe_tree_block_stats": ([P, I, I, P, P, P, P, P], I),
             "moe_noalloc_check": ([P, P], I),
+            "moe_offload_upload_wait": ([P, I, C.c_double, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -213,10 +214,12 @@ def _event(ev):
     return C.c_void_p(ev.cuda_event)
 
 
-def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None, residual=False) -> RunOpts:
+def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None, residual=False,
+             select_begin=None) -> RunOpts:
     """Options for the forward entry points. `begin`/`end` are torch.cuda.Event
-    objects recorded around the grouped-expert kernel; `residual` returns x + MoE(x)."""
-    return RunOpts(ffn_path, _event(begin), _event(end), int(residual))
+    objects recorded around the grouped-expert kernel, `select_begin` one recorded before
+    the selection launch; `residual` returns x + MoE(x)."""
+    return RunOpts(ffn_path, _event(begin), _event(end), int(residual), _event(select_begin))
 
 
 def moe_expert_forward(L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, y, ws,
@@ -311,6 +314,14 @@ class Residency:
             self.h, layer, nd.ctypes.data_as(C.c_void_p), len(nd), ue.ctypes.data_as(C.c_void_p),
             us.ctypes.data_as(C.c_void_p), C.byref(n_up), C.byref(hits)))
         return ue[:n_up.value].copy(), us[:n_up.value].copy(), hits.value
+
+    def upload_wait(self, layer: int, timeout_s: float = 10.0):
+        """(ms the compute stream waited for uploads, number of waits) in the last
+        moe_offload_forward call on `layer`."""
+        ms, n = C.c_double(0), C.c_int(0)
+        _check("moe_offload_upload_wait", lib().moe_offload_upload_wait(
+            self.h, layer, float(timeout_s), C.byref(ms), C.byref(n)))
+        return ms.value, n.value
 
     def publish(self, layer: int, slot_dev=None, res_dev=None, stream=None):
         _check("moe_residency_publish", lib().moe_residency_publish(

@@ -121,14 +121,19 @@ typedef struct {
 
 /* Run options; pass NULL for defaults. If both events are non-NULL they are
  * recorded on the stream immediately before and after the grouped-expert kernel
- * (for timing the dominant kernel with CUDA events). With `residual` set the layer
- * returns y = x + MoE(x) instead of MoE(x), for a residual stack of layers; y may then
- * be the same buffer as x. */
+ * (for timing the dominant kernel with CUDA events). `select_begin`, if non-NULL, is
+ * recorded just before the selection launch of moe_tree_forward (whose extra CTAs
+ * start streaming the root's experts into L2), so that select_begin .. ffn_end times
+ * the whole expert stage. An event between two launches keeps the second from
+ * starting early, so timed calls run slightly slower than untimed ones. With `residual`
+ * set the layer returns y = x + MoE(x) instead of MoE(x), for a residual stack of
+ * layers; y may then be the same buffer as x. */
 typedef struct {
     int ffn_path; /* moe_ffn_path */
     moe_event_t ffn_begin;
     moe_event_t ffn_end;
     int residual;
+    moe_event_t select_begin;
 } moe_run_opts;
 
 /* Text for a status code. Never NULL. */
@@ -381,6 +386,15 @@ moe_status moe_offload_forward(const moe_layer_desc *L, const moe_select_params 
                                const moe_tree_outputs *out, moe_offload_stats *stats,
                                void *workspace, const moe_run_opts *opts, moe_stream_t stream,
                                moe_stream_t side);
+
+/* Time the compute stream of the last moe_offload_forward call on `layer` spent waiting
+ * for expert uploads ("AcceptMoE" news article, section 03: the share of runtime spent
+ * waiting on expert loads): the sum over that call's upload waits of the time between
+ * the stream reaching the wait and the upload completing (0 for a wait the upload had
+ * already met). Waits (bounded by timeout_s per event -> MOE_ERR_TIMEOUT) for those
+ * events; *waits (may be NULL) = the number of upload waits. Host only. */
+moe_status moe_offload_upload_wait(moe_residency *table, int layer, double timeout_s,
+                                   double *wait_ms, int *waits);
 
 /* Host poll of cudaEventQuery(ev) for at most timeout_s seconds. MOE_ERR_TIMEOUT if
  * the event has not completed by then. */

@@ -13,6 +13,7 @@ import torch
 
 from expert_select_gb300 import moetree as M
 from expert_select_gb300 import workload as W
+from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -90,6 +91,10 @@ def test_offload_matches_resident_layer(shape, slots, mode, prune, router_std):
         assert st.h2d_bytes == st.uploads * expert_bytes
         if union > slots:
             assert st.passes >= 2
+        # one timed wait per pass that needed uploads; a wait lasts >= 0 ms
+        wait_ms, waits = table.upload_wait(1)
+        assert waits == st.passes - (1 if st.hits > 0 else 0)
+        assert wait_ms >= 0.0 and (waits > 0 or wait_ms == 0.0)
         total_up += st.uploads
         slot_map, res_after = table.query(1)
         needed = np.flatnonzero(cnt_ref.cpu().numpy())
@@ -121,3 +126,48 @@ def test_residual_option_adds_the_input():
     ref = x.double() + y.double()
     err = (yr.double() - ref).abs().max().item()
     assert err <= 2e-2 * ref.abs().max().item()
+
+
+def test_offload_gptoss_shape_against_oracle():
+    """A GPT-OSS-120B-shaped offloaded layer (d = f = 2880, top-4, bf16; 32 experts, 12
+    slots, AcceptMoE with residency-aware pruning, router std 0.1), two blocks in a row:
+    the routing equals the fp64 oracle's on the device's logits and the residency the
+    table had before each call, and sampled rows of y equal the oracle's experts and
+    combine within the bf16 bar."""
+    shape = W.LayerShape(d=2880, E=32, k=4, f=2880, dtype="bf16")
+    slots = 12
+    wg, wu, wd = W.expert_weights(15, shape, device=DEV)
+    hg, hu, hd = (w.cpu().pin_memory() for w in (wg, wu, wd))
+    del wg, wu, wd
+    pg = torch.zeros(slots, shape.f, shape.d, dtype=torch.bfloat16, device=DEV)
+    pu = torch.zeros_like(pg)
+    pd = torch.zeros(slots, shape.d, shape.f, dtype=torch.bfloat16, device=DEV)
+    wr = W.router_weight(16, shape, std=0.1, device=DEV)
+    Ls = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16", slots=slots)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=True, reroute_budget=8, min_set=4)
+    table = M.Residency(n_layers=1, E=shape.E, slots=slots)
+    side = torch.cuda.Stream()
+    for step in range(2):
+        t = W.eagle_tree(70 + step)
+        N = t.N
+        x = W.hidden_states(80 + step, t.parent, shape.d, torch.bfloat16).to(DEV)
+        dep = torch.from_numpy(t.depth.copy()).to(DEV)
+        _, res_before = table.query(0)
+        lg = torch.empty(N, shape.E, device=DEV)
+        idx = torch.empty(N, shape.k, dtype=torch.int32, device=DEV)
+        g = torch.empty(N, shape.k, device=DEV)
+        y = torch.empty(N, shape.d, dtype=torch.bfloat16, device=DEV)
+        ws = M.workspace(Ls, 1, N)
+        st = M.moe_offload_forward(Ls, P, x, wr, hg, hu, hd, pg, pu, pd, table, 0, dep, 1, N, y,
+                                   ws, M.tree_outputs(logits=lg, topk_idx=idx, gates=g),
+                                   side_stream=side)
+        torch.cuda.synchronize()
+        assert M.moe_workspace_check(ws) == 0
+        assert st.uploads > 0 and st.hits + st.uploads == st.needed
+        sel = O.select_tree(lg.cpu().numpy(), t.depth, shape.k, W.C_EAGLE, mode=O.ACCEPT,
+                            prune=True, resident=res_before, budget=8, min_set=4)
+        np.testing.assert_array_equal(idx.cpu().numpy(), sel["idx"])
+        rows = [0, 17, 40, 64]
+        ref = O.moe_combine(x.cpu(), hg, hu, hd, sel["idx"], sel["gates"], rows=rows)
+        got = y.float().cpu().numpy()[rows]
+        assert np.abs(got - ref).max() <= 2e-2 * np.abs(ref).max()

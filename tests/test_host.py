@@ -179,6 +179,9 @@ def test_residency_plan_follows_lru():
 
 def test_residency_errors():
     R = M.Residency(n_layers=1, E=8, slots=3)
+    assert R.upload_wait(0) == (0.0, 0)  # no offloaded call yet: no waits
+    with pytest.raises(M.MoeError):
+        R.upload_wait(1)
     with pytest.raises(M.MoeError) as ei:
         R.plan(0, [0, 1, 2, 3])
     assert ei.value.status == M.MOE_ERR_NOSLOT
