@@ -316,8 +316,34 @@ def run_gpu(args):
             M.moe_tree_forward(L, P, xs[j], w_r, wg, wu, wd, None, deps[j], 1, N, None, y, ws,
                                out, opts)
 
+    def runner(n, routing, w_r=wr):
+        """A callable running n steps of the layer: by default CUDA graphs of the steps,
+        captured here after the eager warm-up (the host then launches one graph instead of
+        five kernels per step, and the programmatic launch edges between consecutive
+        kernels stay inside the graph); with --no-graph the eager loop. Graphs hold up to
+        256 steps (a multiple of the 64 trees, so replays walk the same tree sequence)."""
+        if args.no_graph:
+            return lambda: loop(n, routing, w_r=w_r)
+        full, rest = divmod(n, 256)
+        graphs = []
+        for m in ([256] if full else []) + ([rest] if rest else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                loop(m, routing, w_r=w_r)
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+
+        def run():
+            for _ in range(full):
+                graphs[0].replay()
+            if rest:
+                graphs[-1].replay()
+        run()  # one untimed replay: the graphs' own first launch
+        torch.cuda.synchronize(dev)
+        return run
+
     def timed(n, routing, **kw):
-        return _timed(lambda: loop(n, routing, **kw), dev, world)
+        return _timed(runner(n, routing, **kw), dev, world)
 
     def counters(n, routing, **kw):
         """Per-step union (experts with assignments) and per-tree counters of the first n
@@ -468,7 +494,9 @@ def run_gpu(args):
         "warmup": Wm, "ms_per_step": round(sec / K * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded EAGLE-3-shaped trees, N(0,0.02) weights)",
-        "config": dict(workload_config(shape, routing, wr_std), parallelism=f"replicas{world}"),
+        "config": dict(workload_config(shape, routing, wr_std), parallelism=f"replicas{world}",
+                       launch="eager" if args.no_graph else
+                       "CUDA graphs of the timed steps (captured after the eager warm-up)"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
@@ -1034,6 +1062,8 @@ def main(argv=None):
     ap.add_argument("--ffn-path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--cpu-trees", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps eagerly instead of from CUDA graphs")
     ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched", "budget",
                                            "efficiency", "ecospec"],
                     default="layer", help="layer: the Qwen3-shaped layer (default line)")
