@@ -1051,6 +1051,75 @@ def run_ecospec(args):
                      "router_std": args.router_std}, sweep=rows))
 
 
+def run_crossover(args):
+    """The grouped-expert stage alone (moe_expert_forward) on the CUDA-core and tensor-core
+    paths, with exactly r rows routed to each of 64 experts (r = 1 .. 256), Qwen3-shaped
+    bf16 experts: where the batch regime turns from memory-bound to compute-bound (MoESD
+    notes, section 5.1) and which path wins at each rows-per-expert count. Events bracket
+    the expert launches of each call (CUDA cores: gate/up and down; tensor cores: the token
+    gather and the expert kernel)."""
+    import torch
+    from expert_select_gb300 import moetree as M
+    from expert_select_gb300 import workload as W
+    world, rank, local, dev = _setup_gpu()
+    shape = W.QWEN3_30B_A3B
+    n_exp = 64
+    wg, wu, wd = W.expert_weights(SEED + 8000, shape, device=dev)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    peak, _ = measured_peaks()
+    tflops_peak = 1895.9
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            tflops_peak = float(json.load(fh)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        pass
+    K, Wm = args.steps, args.warmup
+    s = torch.cuda.current_stream(dev)
+    rows = []
+    for r in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        R = n_exp * r // shape.k
+        t = torch.arange(R, device=dev).view(R, 1) * shape.k + torch.arange(shape.k, device=dev)
+        idx = (t % n_exp).int().contiguous()  # every expert gets exactly r rows
+        gates = torch.full((R, shape.k), 1.0 / shape.k, device=dev)
+        x = W.hidden_states(SEED + 8001 + r, np.arange(-1, R - 1, dtype=np.int32), shape.d,
+                            torch.bfloat16).to(dev)
+        y = torch.empty_like(x)
+        ws = M.workspace(L, 1, R, device=dev)
+        A = R * shape.k
+        bytes_ = n_exp * shape.expert_bytes + 2 * R * shape.d * 2
+        flops = 2.0 * A * 3 * shape.d * shape.f
+        res = {"rows_per_expert": r, "rows": R}
+        for name, path in (("cuda_cores", M.MOE_FFN_SIMT), ("tcgen05", M.MOE_FFN_TCGEN05)):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            for a, b in ev:
+                a.record(s)
+                b.record(s)
+            for _ in range(Wm):
+                M.moe_expert_forward(L, x, wg, wu, wd, None, idx, gates, y, ws, M.run_opts(path))
+            torch.cuda.synchronize(dev)
+            for i in range(K):
+                M.moe_expert_forward(L, x, wg, wu, wd, None, idx, gates, y, ws,
+                                     M.run_opts(path, ev[i][0], ev[i][1]))
+            torch.cuda.synchronize(dev)
+            ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+            res[name] = {"ms": round(ms, 4),
+                         "gbs": round(bytes_ / ms / 1e6, 1),
+                         "hbm_frac": round(bytes_ / ms / 1e6 / peak, 4),
+                         "tflops": round(flops / ms / 1e9, 1),
+                         "tensor_frac": round(flops / ms / 1e9 / tflops_peak, 4)}
+        res["faster"] = "tcgen05" if res["tcgen05"]["ms"] < res["cuda_cores"]["ms"] else \
+            "cuda_cores"
+        rows.append(res)
+    if rank == 0:
+        print(_line("grouped SwiGLU expert stage: CUDA cores vs tcgen05 by rows per expert",
+                    rows[-1]["tcgen05"]["tflops"], "TFLOP/s", world, K, Wm,
+                    rows[-1]["tcgen05"]["ms"] * K / 1e3,
+                    {"workload": "qwen3-30b-a3b-experts-64-active-rows-per-expert-sweep",
+                     "experts": n_exp, "l2": "604 MB of expert weights per call (> L2)"},
+                    sweep=rows, hbm_peak=peak, bf16_tflops_peak=tflops_peak))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1065,7 +1134,7 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of from CUDA graphs")
     ap.add_argument("--workload", choices=["layer", "stack48", "offload", "batched", "budget",
-                                           "efficiency", "ecospec"],
+                                           "efficiency", "ecospec", "crossover"],
                     default="layer", help="layer: the Qwen3-shaped layer (default line)")
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--slots", type=int, default=48)
@@ -1086,6 +1155,8 @@ def main(argv=None):
         run_efficiency(args)
     elif args.workload == "ecospec":
         run_ecospec(args)
+    elif args.workload == "crossover":
+        run_crossover(args)
     else:
         run_gpu(args)
 
