@@ -102,13 +102,16 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 
 struct Unit {
     int phase, rt, m, e, row0, ntok, slot;  // row0: the row tile's first permuted row
+    int group;                              // tiles of this expert (they share its weights)
 };
 
-// Row tile rt -> {expert, first permuted row, tokens, code}; code is the expert's slot, -1
-// for an expert outside this launch's expert pass, -2 for a slot outside the pool.
+// Row tile rt -> {expert, first permuted row, tokens | index in the expert's group << 12 |
+// group size << 22, code}; code is the expert's slot, -1 for an expert outside this
+// launch's expert pass, -2 for a slot outside the pool. (tokens <= 256, groups < 1024.)
 __device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
     const int *t = p.rowtiles + kRowTileHeader + 4 * rt;
     const int e = t[0], row0 = t[1], ntok = t[2];
+    const int jg = (t[3] >> 16) & 1023, g = max(1, min(t[3] & 0xffff, 1023));
     int code;
     if (p.pass && !p.pass[e]) {
         code = -1;
@@ -116,29 +119,38 @@ __device__ __forceinline__ int4 row_tile(const Params &p, int rt) {
         const int sl = p.slot ? p.slot[e] : e;
         code = (sl >= 0 && sl < p.slots && ntok > 0) ? sl : -2;
     }
-    return make_int4(e, row0, ntok, code);
+    return make_int4(e, row0, ntok | (jg << 12) | (g << 22), code);
 }
 
-// Ticket u -> unit: tickets [0, U1) are phase 1 (row-tile major), the rest phase 2. The
-// row tile's entry comes from the shared-memory table when it holds it (tbl != nullptr).
-// Returns 0 for a unit to compute, 1 for one outside this launch's expert pass, 2 for an
-// expert whose slot is outside the pool (skipped and flagged).
+__device__ __forceinline__ int4 tile_at(const Params &p, int rt, const int4 *tbl) {
+    return (tbl && rt < p.tbl_cap) ? tbl[rt] : row_tile(p, rt);
+}
+
+// Ticket u -> unit. Tickets [0, U1) are phase 1, the rest phase 2; within a phase the
+// tickets of an expert's row tiles [f, f + g) form one block of g * mt tickets taken weight
+// tile by weight tile: ticket f * mt + m * g + j is weight tile m of row tile f + j, so the
+// g tiles that read the same weights are handed out together and run at the same time
+// (the second read of those weights hits L2). The row tile's entry comes from the
+// shared-memory table when it holds it (tbl != nullptr). Returns 0 for a unit to compute,
+// 1 for one outside this launch's expert pass, 2 for an expert whose slot is outside the
+// pool (skipped and flagged).
 __device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w,
                                       const int4 *tbl) {
-    if (u < U1) {
-        w.phase = 1;
-        w.rt = u / p.mt1;
-        w.m = u - w.rt * p.mt1;
-    } else {
-        const int v = u - U1;
-        w.phase = 2;
-        w.rt = v / p.mt2;
-        w.m = v - w.rt * p.mt2;
-    }
-    const int4 t = (tbl && w.rt < p.tbl_cap) ? tbl[w.rt] : row_tile(p, w.rt);
+    const bool ph1 = u < U1;
+    const int v = ph1 ? u : u - U1, mt = ph1 ? p.mt1 : p.mt2;
+    const int rt0 = v / mt;  // a tile of the right group (the order within differs)
+    int4 t = tile_at(p, rt0, tbl);
+    const int jg = (t.z >> 12) & 1023, g = ((unsigned)t.z >> 22) & 1023;
+    const int f = rt0 - jg;
+    const int local = v - f * mt;
+    w.phase = ph1 ? 1 : 2;
+    w.m = local / g;
+    w.rt = f + (local - w.m * g);
+    if (w.rt != rt0) t = tile_at(p, w.rt, tbl);
     w.e = t.x;
     w.row0 = t.y;
-    w.ntok = t.z;
+    w.ntok = t.z & 4095;
+    w.group = g;
     w.slot = t.w;
     return t.w >= 0 ? 0 : (t.w == -1 ? 1 : 2);
 }
@@ -235,7 +247,9 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol = evict_first_policy();
+            // weights read by one row tile stream through L2 once (evict first); weights
+            // that the sibling tiles of a group read at the same time stay in L2 for them
+            const uint64_t pol_once = evict_first_policy(), pol_shared = evict_normal_policy();
             int s = 0, qs = 0;
             uint32_t ph = 0, qph = 0;
             bool ok = mbar_wait(tbl_bar, 0, abort_flag, p.flags);
@@ -288,6 +302,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     const uint32_t fb = full + 8 * s;
                     mbar_expect_tx(fb, kABytes + bb);
                     const uint32_t a = sA + (uint32_t)s * kABytes;
+                    const uint64_t pol = w.group > 1 ? pol_shared : pol_once;
                     if (w.phase == 1) {
                         tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
                         tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, w.m * 64, w.slot, fb,

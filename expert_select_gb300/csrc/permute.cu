@@ -9,9 +9,9 @@
 //   offsets[e] + prefix[e][block] + popc(mask[e][block] & lanes_below(row)).
 // The masks and prefixes live in shared memory: (R/32) x E x 8 bytes (133 KB at 4160
 // rows and 128 experts). The same kernel also writes the active-expert list and the list
-// of row tiles (at most 64 or 256 tokens of one expert) that the grouped expert kernels
-// walk; the tile height is the largest expert's token count rounded up to 16, at most
-// 256. Up to 2048 assignments it keeps the expert ids in shared memory and places the
+// of row tiles that the tensor-core expert kernel walks: an expert with c tokens takes
+// ceil(c / 256) tiles of near-equal size (sizes differ by at most one), and the tile height
+// is the largest tile rounded up to 16. Up to 2048 assignments it keeps the expert ids in shared memory and places the
 // assignments itself; past that it leaves the masks and prefixes in the workspace and a
 // second, many-CTA kernel places the assignments.
 #include "common.cuh"
@@ -102,17 +102,19 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         const int lane = tid & 31, warp = tid >> 5;
         const int nw = (E + 31) >> 5;
         const int c = tid < E ? cnt[tid] : 0;
+        // an expert's tiles: ceil(c / kMaxRowTile) of near-equal size
+        const int nt = (c + kMaxRowTile - 1) / kMaxRowTile;
+        const int tmax = nt > 0 ? (c + nt - 1) / nt : 0;  // its largest tile
         if (warp < nw) {
-            const int wm = __reduce_max_sync(0xffffffffu, c);
+            const int wm = __reduce_max_sync(0xffffffffu, tmax);
             if (lane == 0) wred[3][warp] = wm;
         }
         __syncthreads();
-        // row-tile height: the largest expert's tokens rounded up to 16 (every expert in
-        // one tile), at most kMaxRowTile (larger experts split into tiles of that many)
+        // row-tile height: the largest tile rounded up to 16
         int cmax = 0;
         for (int w = 0; w < nw; ++w) cmax = max(cmax, wred[3][w]);
         const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
-        const int a = c > 0, nt = (c + rt_size - 1) / rt_size;
+        const int a = c > 0;
         int ci = c, ai = a, ti = nt;  // inclusive scans within the warp
         if (warp < nw) {
 #pragma unroll
@@ -143,13 +145,16 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
             int t_ex = ti - nt;
             off[tid] = c_ex;
             if (a) active[1 + a_ex] = tid;
-            // row tiles of at most rt_size tokens of one expert, for the tensor-core kernel
-            for (int n0 = 0; n0 < c; n0 += rt_size) {
+            // the expert's row tiles for the tensor-core kernel: nt near-equal tiles, each
+            // knowing its index in the expert's group and the group's size
+            for (int j = 0, n0 = 0; j < nt; ++j) {
+                const int sz = c / nt + (j < c % nt ? 1 : 0);
                 int *t = rowtiles + kRowTileHeader + 4 * t_ex++;
                 t[0] = tid;
                 t[1] = c_ex + n0;  // first permuted row of the tile
-                t[2] = min(rt_size, c - n0);
-                t[3] = 0;
+                t[2] = sz;
+                t[3] = rowtile_group(j, nt);
+                n0 += sz;
             }
             if (tid == E - 1) {
                 off[E] = ci;

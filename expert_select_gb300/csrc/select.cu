@@ -680,7 +680,7 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
             t[0] = tid;
             t[1] = c_ex + n0;  // first permuted row of the tile
             t[2] = min(rt_size, c - n0);
-            t[3] = 0;
+            t[3] = rowtile_group(0, 1);  // N <= 256 nodes: one tile per expert
         }
         if (tid == E - 1) {
             soff[E] = ci;

@@ -99,6 +99,12 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t evict_normal_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
