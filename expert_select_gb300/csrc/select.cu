@@ -865,8 +865,14 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
     cluster_barrier(rank == 0);
 
     // ---- the fp64 pass, when CTA 0 could not certify the fp32 decisions (uniform over
-    // the cluster) ----
-    const int exact_pass = rank == 0 ? s_exact : *cl.map_shared_rank(&s_exact, 0);
+    // the cluster). The other CTAs read CTA 0's verdict and eligible set together (one
+    // round trip); after an fp64 pass they read the set again. ----
+    int exact_pass = s_exact;
+    if (rank != 0) {
+        const int *inS0 = cl.map_shared_rank(inS, 0);
+        if (tid < E) inS[tid] = inS0[tid];
+        exact_pass = *cl.map_shared_rank(&s_exact, 0);
+    }
     if (exact_pass) {
         for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
             const int slot = t * kCW + warp;
@@ -912,10 +918,10 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             }
         }
         cluster_barrier(rank == 0);
+        if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
     }
 
     // ---- phase C: this CTA's nodes, restricted to the eligible set ----
-    if (rank != 0 && tid < E) inS[tid] = cl.map_shared_rank(inS, 0)[tid];
     if (rank == 0) {  // the set's size and the block's eligibility mask
         if (tid == 0 && info_out) {
             info_out[b * MOE_INFO_FIELDS + 2] = s_m;
