@@ -649,6 +649,7 @@ def run_stack48(args):
     x = torch.empty_like(xs[0])
     K, Wm = args.steps, args.warmup
     counts = torch.zeros(K, NL, shape.E, dtype=torch.int32, device=dev)
+    info = torch.zeros(K, NL, M.MOE_INFO_FIELDS, dtype=torch.int32, device=dev)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(NL)] for _ in range(K)]
     s = torch.cuda.current_stream(dev)
@@ -661,7 +662,7 @@ def run_stack48(args):
     def step(i, record):
         x.copy_(xs[i % TREES])
         for l, (wr, wg, wu, wd) in enumerate(layers):
-            out = M.tree_outputs(counts=counts[i, l]) if record else None
+            out = M.tree_outputs(counts=counts[i, l], info=info[i, l]) if record else None
             opts = M.run_opts(args.ffn_path, ev[i][l][0], ev[i][l][1], residual=True) if record \
                 else M.run_opts(args.ffn_path, residual=True)
             M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, deps[i % TREES], 1, N, None, x,
@@ -689,6 +690,7 @@ def run_stack48(args):
                               "kernel": "grouped SwiGLU experts"},
                     union={"mean": float(union.mean()), "min": int(union.min()),
                            "max": int(union.max())},
+                    fp64_pass_frac=round(float(info[:, :, 4].float().mean().item()), 4),
                     clocks=clk.summary()))
 
 

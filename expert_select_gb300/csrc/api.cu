@@ -71,9 +71,11 @@ bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
     a->budget = P->reroute_budget;
     a->min_set = P->min_set;
     a->fixed_B = P->fixed_B;
+    a->cmax = 0.f;
     for (int t = 0; t < MOE_MAX_DEPTHS; ++t) {
         a->c64[t] = (P->mode != MOE_ROUTE_NATURAL && t < P->n_c) ? P->c_by_depth[t] : 0.0;
         a->c[t] = (float)a->c64[t];
+        a->cmax = std::max(a->cmax, a->c[t]);
     }
     (void)k;
     return true;

@@ -61,6 +61,7 @@ struct SelectArgs {
     int mode, n_c, pool_all, anchor, prune, budget, min_set, fixed_B;
     float c[MOE_MAX_DEPTHS];     // the commitment table rounded to fp32 (the fast pass)
     double c64[MOE_MAX_DEPTHS];  // as given (the exact pass)
+    float cmax;                  // the largest entry
 };
 // L2 prefetch of expert weights during routing (AcceptMoE and fixed-size selection). The
 // root's natural top-k is the anchor that AcceptMoE keeps in every eligible set, and with

@@ -141,12 +141,17 @@ __device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w,
     const int rt0 = v / mt;  // a tile of the right group (the order within differs)
     int4 t = tile_at(p, rt0, tbl);
     const int jg = (t.z >> 12) & 1023, g = ((unsigned)t.z >> 22) & 1023;
-    const int f = rt0 - jg;
-    const int local = v - f * mt;
     w.phase = ph1 ? 1 : 2;
-    w.m = local / g;
-    w.rt = f + (local - w.m * g);
-    if (w.rt != rt0) t = tile_at(p, w.rt, tbl);
+    if (g <= 1) {  // an expert in one tile (every expert of small blocks)
+        w.rt = rt0;
+        w.m = v - rt0 * mt;
+    } else {
+        const int f = rt0 - jg;
+        const int local = v - f * mt;
+        w.m = local / g;
+        w.rt = f + (local - w.m * g);
+        if (w.rt != rt0) t = tile_at(p, w.rt, tbl);
+    }
     w.e = t.x;
     w.row0 = t.y;
     w.ntok = t.z & 4095;
@@ -294,6 +299,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 const int brow = w.row0;
                 const int kchunks = (w.phase == 1 ? p.d : p.f) / kBK;
                 const CUtensorMap *bmap = w.phase == 1 ? &maps.bx[bxi] : &maps.bh[bxi];
+                const uint64_t pol = w.group > 1 ? pol_shared : pol_once;
                 for (int kc = 0; kc < kchunks; ++kc) {
                     if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.flags)) {
                         ok = false;
@@ -302,7 +308,6 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     const uint32_t fb = full + 8 * s;
                     mbar_expect_tx(fb, kABytes + bb);
                     const uint32_t a = sA + (uint32_t)s * kABytes;
-                    const uint64_t pol = w.group > 1 ? pol_shared : pol_once;
                     if (w.phase == 1) {
                         tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
                         tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, w.m * 64, w.slot, fb,

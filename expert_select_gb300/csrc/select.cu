@@ -63,9 +63,10 @@ static_assert(kThreads >= kMaxE, "block-wide counts take one expert per thread")
 // j after fp64 rounding.
 constexpr double kSnap = 1e-9;
 constexpr float kU = 5.9604645e-8f;  // 2^-24, the unit roundoff of fp32
-// Logit ranges above this make exp() underflow in fp32 (and the relative error bound
-// meaningless): such trees always take the fp64 pass.
-constexpr float kMaxRange = 80.f;
+// Terms whose exponent lies below about -87 underflow in fp32 (denormal or zero): their
+// error is not relative but below 2^-126 in absolute value. The certificate adds
+// kUnderflow * N * max(c) to every demand's error.
+constexpr float kUnderflow = 2.4e-38f;  // 2^-125, twice the smallest normal fp32
 
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t u = __float_as_uint(v + 0.f);  // -0 -> +0
@@ -226,11 +227,12 @@ struct PhaseB {
 //  - the size rule is m = clamp(ceil(r (1 - 1e-9))): it is certain when the rule gives the
 //    same m over [r (1 - dr), r (1 + dr)];
 //  - a cut (fill: last taken vs first left; prune: last removed vs next) is certain when
-//    the two demands stay ordered after moving each by dD + 2u towards the other.
+//    the two demands stay ordered after moving each by dD + 2u (relative) and dA
+//    (absolute: terms that underflowed in fp32) towards the other.
 template <typename T, int NW>
 __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const int *inU,
                           const int *inA, int *inS, const uint8_t *resident, T *rk,
-                          T (*red)[NW], T *cut, float dD) {
+                          T (*red)[NW], T *cut, float dD, float dA) {
     using F = Num<T>;
     constexpr bool exact = sizeof(T) == sizeof(double);
     constexpr int NT = NW * 32;
@@ -256,7 +258,9 @@ __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const i
         } else {
             const float r = expf(H);
             const float dq = 2.f * dD + 21.f * kU;
-            const float dH = (dq + 23.f * kU) * fmaxf(H, 0.f) + dq;
+            // + the underflowed terms: each q moves by at most dA / sum D, and |ln q| < 100
+            const float dH = (dq + 23.f * kU) * fmaxf(H, 0.f) + dq +
+                             (float)E * 100.f * dA / fmaxf((float)sumD, 1e-30f);
             const float dr = (dH + 4.f * kU) * 1.05f + 8.f * kU;
             const int lo = min(max((int)ceilf(r * (1.f - dr)), k), pool);
             const int hi = min(max((int)ceilf(r * (1.f + dr)), k), pool);
@@ -286,8 +290,8 @@ __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const i
         }
         const int ncand = __syncthreads_count(cand && pe == 0);  // rk is rewritten below
         if (!exact && F_ > 0 && F_ < ncand)
-            sure = sure && (float)cut[0] * (1.f - dD - 2.f * kU) >
-                               (float)cut[1] * (1.f + dD + 2.f * kU);
+            sure = sure && (float)cut[0] * (1.f - dD - 2.f * kU) - dA >
+                               (float)cut[1] * (1.f + dD + 2.f * kU) + dA;
     }
     if (e < E && pe == 0) inS[e] = in;
     int removed = 0;
@@ -312,11 +316,21 @@ __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const i
         }
         __syncthreads();
         if (!exact && removed > 0 && removed < nrem)
-            sure = sure && (float)cut[3] * (1.f - dD - 2.f * kU) >
-                               (float)cut[2] * (1.f + dD + 2.f * kU);
+            sure = sure && (float)cut[3] * (1.f - dD - 2.f * kU) - dA >
+                               (float)cut[2] * (1.f + dD + 2.f * kU) + dA;
     }
     __syncthreads();  // inS complete
     return PhaseB{m, removed, sure};
+}
+
+// The fp64 phase B, kept out of line: it runs for few trees, and the selection kernels
+// are short enough that the instruction fetch of their common path shows.
+template <int NW>
+__device__ __noinline__ PhaseB phase_b_exact(const SelectArgs &a, int E, int k, const double *D,
+                                             const int *inU, const int *inA, int *inS,
+                                             const uint8_t *resident, double *rk,
+                                             double (*red)[NW], double *cut) {
+    return phase_b<double, NW>(a, E, k, D, inU, inA, inS, resident, rk, red, cut, 0.f, 0.f);
 }
 
 // Relative error bound of the fp32 demand of a tree of N nodes whose logit ranges are at
@@ -326,6 +340,13 @@ __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const i
 // at most N + 8 additions of positive terms into D_e. 5% slack for second-order terms.
 __device__ __forceinline__ float demand_bound(float A, int N, int VPL) {
     return kU * (2.f * A + (float)VPL + 15.f + (float)N + 8.f) * 1.05f;
+}
+
+// Absolute error bound of the fp32 demand from terms that underflow: at most one
+// kUnderflow per node, times the largest commitment (computed on the host: indexing the
+// table here would copy the whole argument block to local memory).
+__device__ __forceinline__ float demand_floor(const SelectArgs &a, int N) {
+    return kUnderflow * (float)N * a.cmax;
 }
 
 // Loads the E logits of one node into v[] (lane holds experts lane + 32 i).
@@ -520,8 +541,8 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
                                        reinterpret_cast<float *>(rkb),
                                        reinterpret_cast<float(*)[kWarps]>(&redb[0][0]),
                                        reinterpret_cast<float *>(cutb),
-                                       demand_bound(A, N, kVPL));
-    const bool exact_pass = !pb.sure || !(A <= kMaxRange);
+                                       demand_bound(A, N, kVPL), demand_floor(a, N));
+    const bool exact_pass = !pb.sure || !isfinite(A);
     if (exact_pass) {
         // fp64 normaliser of every node, then a thread per expert adds its terms in order
         for (int n = warp; n < N; n += kWarps) {
@@ -535,16 +556,19 @@ select_kernel(SelectArgs a, const float *__restrict__ logits, const int *__restr
             if (lane == 0) nz64[n] = s;
         }
         __syncthreads();
+        for (int n = warp; n < N; n += kWarps)  // c_n / sum_n once per node
+            if (lane == 0) nz64[n] = __ddiv_rn(commitment64(a, dep[n]), nz64[n]);
+        __syncthreads();
         for (int e = tid; e < E; e += kThreads) {
             double acc = 0.0;
             for (int n = 0; n < N; ++n) {
                 const double ex = exp((double)L[(size_t)n * E + e] - (double)mx[n]);
-                acc = __dadd_rn(acc, __dmul_rn(commitment64(a, dep[n]), __ddiv_rn(ex, nz64[n])));
+                acc = __dadd_rn(acc, __dmul_rn(nz64[n], ex));
             }
             D64[e] = acc;
         }
         __syncthreads();
-        pb = phase_b<double, kWarps>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb, 0.f);
+        pb = phase_b_exact<kWarps>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb);
     }
     const int m = pb.m, removed = pb.removed;
 
@@ -708,6 +732,48 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
     for (int p = soff[E] + tid; p < A; p += kCThreads) po.perm[p] = -1;
 }
 
+// The fp64 demand terms of one CTA's nodes in the cluster kernel (the fp64 pass, out of
+// line): a warp per node takes exp(l - max) in fp64 from the logit rows the CTA holds, the
+// node's sum, and c_n / sum_n once per node (one fp64 divide instead of one per expert;
+// the product differs from c_n * (ex / sum_n) by an fp64 rounding); then a thread per
+// expert adds the CTA's nodes in node order and stores the partial into part0[rank][e]
+// (CTA 0's shared memory).
+template <int VPL>
+__device__ __noinline__ void cluster_exact_terms(const SelectArgs &a, const int *dep, int N,
+                                                 int E, int k, int rank, const float *lrow,
+                                                 const float *nat_val, double *w64,
+                                                 double *part0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
+        const int slot = t * kCW + warp;
+        const double top = (double)nat_val[slot * k];  // the node's largest logit
+        const double cn = commitment64(a, dep[n]);
+        double ex[VPL], s = 0.0;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            ex[i] = e < E ? exp((double)lrow[slot * E + e] - top) : 0.0;
+            s = __dadd_rn(s, ex[i]);
+        }
+        s = warp_sum64(s);
+        const double scale = __ddiv_rn(cn, s);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) w64[slot * E + e] = __dmul_rn(scale, ex[i]);
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        double acc = 0.0;
+        for (int t = 0; t * kCC * kCW < N; ++t) {
+            const int cnt = min(kCW, max(0, N - t * kCC * kCW - rank * kCW));
+            for (int w = 0; w < cnt; ++w) acc = __dadd_rn(acc, w64[(size_t)(t * kCW + w) * E + tid]);
+        }
+        part0[rank * kMaxE + tid] = acc;
+    }
+}
+
 template <int VPL>
 __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(kCThreads, 1)
 select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
@@ -846,11 +912,11 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
                                               reinterpret_cast<float *>(rkb),
                                               reinterpret_cast<float(*)[kCW]>(&redb[0][0]),
                                               reinterpret_cast<float *>(cutb),
-                                              demand_bound(A, N, VPL));
+                                              demand_bound(A, N, VPL), demand_floor(a, N));
         if (tid == 0) {
             s_m = pb.m;
             s_removed = pb.removed;
-            s_exact = (!pb.sure || !(A <= kMaxRange)) ? 1 : 0;
+            s_exact = (!pb.sure || !isfinite(A)) ? 1 : 0;
         }
     } else {
         for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
@@ -874,34 +940,8 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
         exact_pass = *cl.map_shared_rank(&s_exact, 0);
     }
     if (exact_pass) {
-        for (int n = rank * kCW + warp, t = 0; n < N; n += kCC * kCW, ++t) {
-            const int slot = t * kCW + warp;
-            const double top = (double)nat_val[slot * k];  // the node's largest logit
-            const double cn = commitment64(a, dep[n]);
-            double ex[VPL], s = 0.0;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const int e = lane + 32 * i;
-                ex[i] = e < E ? exp((double)lrow[slot * E + e] - top) : 0.0;
-                s = __dadd_rn(s, ex[i]);
-            }
-            s = warp_sum64(s);
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E) w64[slot * E + e] = __dmul_rn(cn, __ddiv_rn(ex[i], s));
-            }
-        }
-        __syncthreads();
-        if (tid < E) {  // this CTA's nodes in node order, into CTA 0
-            double acc = 0.0;
-            for (int t = 0; t * kCC * kCW < N; ++t) {
-                const int cnt = min(kCW, max(0, N - t * kCC * kCW - rank * kCW));
-                for (int w = 0; w < cnt; ++w)
-                    acc = __dadd_rn(acc, w64[(size_t)(t * kCW + w) * E + tid]);
-            }
-            cl.map_shared_rank(&part64[0][0], 0)[rank * kMaxE + tid] = acc;
-        }
+        cluster_exact_terms<VPL>(a, dep, N, E, k, rank, lrow, nat_val, w64,
+                                 cl.map_shared_rank(&part64[0][0], 0));
         cluster_barrier(true);
         if (rank == 0) {
             if (tid < E) {
@@ -911,7 +951,7 @@ select_cluster_kernel(SelectArgs a, const float *__restrict__ logits,
             }
             __syncthreads();
             const PhaseB pb =
-                phase_b<double, kCW>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb, 0.f);
+                phase_b_exact<kCW>(a, E, k, D64, inU, inA, inS, resident, rkb, redb, cutb);
             if (tid == 0) {
                 s_m = pb.m;
                 s_removed = pb.removed;

@@ -320,6 +320,24 @@ def test_fp64_pass_decides_a_size_near_integer(E, N, side):
                             N, 1) == 0
 
 
+@pytest.mark.parametrize("scale", [20.0, 40.0])
+def test_wide_logit_ranges(scale):
+    """Logit ranges of 150-300 within a node (as deep in a residual stack of layers): the
+    far tails of each softmax underflow in fp32, which the certificate bounds in absolute
+    terms. Every tree matches the fp64 oracle, and the fp32 pass still decides most."""
+    shape = W.QWEN3_30B_A3B
+    B = 16
+    parent, depth = W.tree_block(616, B, "eagle")
+    N = parent.shape[1]
+    logits = W.synthetic_logits(617, parent, shape.E, scale)
+    assert float((logits.max(1) - logits.min(1)).max()) > 150
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth, B, N)
+    assert _check_selection(shape, dict(mode=O.ACCEPT, c=W.C_EAGLE), logits, depth, gidx, gg,
+                            ge, gi, N, B) == 0
+    assert gi[:, 4].sum() <= B // 2, gi[:, 4]
+
+
 def test_fp32_certificate_decides_ordinary_trees():
     """64 peaked EAGLE-3-shaped trees (set sizes in the pages' 23-34 range): all match the
     fp64 oracle and the fp32 pass decides nearly all of them on its own."""
@@ -591,6 +609,47 @@ def test_expert_forward(case):
     ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64),
                         rows=sample.tolist())
     _assert_close_rows(y.float().cpu().numpy()[sample], ref, shape)
+
+
+@pytest.mark.parametrize("path", [M.MOE_FFN_SIMT, M.MOE_FFN_TCGEN05])
+def test_expert_forward_at_the_largest_width(path):
+    """d = f = 6144, the largest hidden and SwiGLU width the layer accepts (the CUDA-core
+    kernel stages 8 token rows of 6144 fp32 values in shared memory; the tensor-core kernel
+    streams 96 k-chunks per unit), 4 experts, top-2, ragged 9 rows; sampled rows against
+    the oracle."""
+    shape = W.LayerShape(d=6144, E=4, k=2, f=6144, dtype="bf16")
+    L = _desc(shape)
+    R = 9
+    wg, wu, wd = _weights(shape, 91)
+    x = W.hidden_states(92, np.arange(-1, R - 1, dtype=np.int32), shape.d, torch.bfloat16)
+    idx = W.random_assignments(93, R, shape.E, shape.k, 0.5)
+    gates = W.random_gates(94, R, shape.k)
+    y = torch.empty(R, shape.d, dtype=torch.bfloat16, device=DEV)
+    ws = M.workspace(L, 1, R)
+    M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, torch.from_numpy(idx).to(DEV),
+                         torch.from_numpy(gates).to(DEV), y, ws, M.run_opts(path))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    rows = [0, 4, 8]
+    ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64),
+                        rows=rows)
+    _assert_close_rows(y.float().cpu().numpy()[rows], ref, shape)
+
+
+def test_selection_cluster_at_its_largest_tree():
+    """256 nodes (the largest tree the 8-CTA cluster takes), E = 256, k = 16: the launch
+    with the most shared memory (logit rows, fp32 and fp64 demand terms of 32 nodes per
+    CTA); AcceptMoE with pruning against the fp64 oracle, one tree exact per tree."""
+    shape = W.LayerShape(d=64, E=256, k=16, f=64, dtype="fp32")
+    N = 256
+    parent, depth = _tree_of(N, 256)
+    logits = W.synthetic_logits(257, parent[None], shape.E, 3.0)
+    res = W.residency_mask(9, shape.E, 96)
+    kw = dict(mode=O.ACCEPT, prune=True, budget=8, min_set=24, resident=res, c=W.C_EAGLE)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=True, reroute_budget=8,
+                        min_set=24)
+    gidx, gg, ge, gi = _select_gpu(shape, P, logits, depth[None], 1, N, res)
+    assert _check_selection(shape, kw, logits, depth[None], gidx, gg, ge, gi, N, 1) == 0
 
 
 @pytest.mark.parametrize("shape,R,skew", [(SMALL_BF16, 65, 1.0), (W.QWEN3_30B_A3B, 65, 1.0),
