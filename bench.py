@@ -626,7 +626,9 @@ def _line(metric, value, unit, world, K, Wm, sec, config, **extra):
 
 def run_stack48(args):
     """48 independent Qwen3-shaped layers resident in HBM (~58 GB of experts), one fresh
-    65-node tree per step through all layers with a residual chain x <- x + MoE_l(x)."""
+    65-node tree per step through all layers with a pre-norm residual chain
+    x <- x + MoE_l(rmsnorm(x)), as the target model's blocks are built (without the norm
+    the residual stream of random layers grows until bf16 overflows)."""
     import torch
     from expert_select_gb300 import moetree as M
     from expert_select_gb300 import workload as W
@@ -663,8 +665,9 @@ def run_stack48(args):
         x.copy_(xs[i % TREES])
         for l, (wr, wg, wu, wd) in enumerate(layers):
             out = M.tree_outputs(counts=counts[i, l], info=info[i, l]) if record else None
-            opts = M.run_opts(args.ffn_path, ev[i][l][0], ev[i][l][1], residual=True) if record \
-                else M.run_opts(args.ffn_path, residual=True)
+            opts = M.run_opts(args.ffn_path, ev[i][l][0], ev[i][l][1], residual=True,
+                              norm_input=True) if record \
+                else M.run_opts(args.ffn_path, residual=True, norm_input=True)
             M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, deps[i % TREES], 1, N, None, x,
                                ws, out, opts)
 
@@ -681,6 +684,7 @@ def run_stack48(args):
                     whole_job_rate(K, world, sec), "tree-blocks/s", world, K, Wm, sec,
                     {"workload": f"qwen3-30b-a3b-{NL}-layer-stack-resident", "layers": NL,
                      "routing": args.routing, "router_std": args.router_std,
+                     "block": "x + MoE(rmsnorm(x))",
                      "expert_bytes_resident_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1),
                      "l2": "inputs larger than L2 (0.7 GB of union weights per layer)"},
                     per_layer_blocks_per_s=round(whole_job_rate(K, world, sec) * NL, 1),
@@ -764,7 +768,8 @@ def run_offload(args):
             for l, (wr, host, pools) in enumerate(layers):
                 st = M.moe_offload_forward(Ls, P, x, wr, *host, *pools, table, l,
                                            deps[i % TREES], 1, N, x, ws,
-                                           opts=M.run_opts(residual=True), side_stream=side)
+                                           opts=M.run_opts(residual=True, norm_input=True),
+                                           side_stream=side)
                 if keep:
                     stats.append((st.needed, st.hits, st.uploads, st.h2d_bytes, st.passes))
             if keep:  # the compute stream's upload waits of this step, layer by layer
@@ -798,6 +803,7 @@ def run_offload(args):
                     K / main_r["tree_blocks_per_s"],
                     {"workload": f"gpt-oss-120b-{NL}-layer-offload-{slots}-slots",
                      "layers": NL, "slots": slots, "router_std": args.router_std,
+                     "block": "x + MoE(rmsnorm(x))",
                      "routing": "acceptmoe + residency-aware pruning (budget 8, min 16)",
                      "host_store_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1)},
                     modes=results, h2d_link_gbs=round(link_gbs, 1), setup_s=round(setup_s, 1)))

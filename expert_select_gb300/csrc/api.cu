@@ -43,6 +43,7 @@ Workspace workspace_layout(const moe_layer_desc &L, int B, int N) {
     w.xp = take(A * L.d * elem_size(L.dtype));
     w.h = take(A * L.f * 4);
     w.o = take(A * L.d * 4);
+    w.xn = take(R * L.d * elem_size(L.dtype));
     w.total = off;
     return w;
 }
@@ -148,18 +149,31 @@ moe_status run_combine(const moe_layer_desc &L, const void *residual, const floa
 }
 
 // permute (unless the selection did it) -> experts -> combine, shared by
-// moe_expert_forward and moe_tree_forward.
+// moe_expert_forward and moe_tree_forward. The experts read x; the combine adds `residual`
+// (may be null).
 static moe_status run_experts(const moe_layer_desc &L, const void *x, const void *Wg,
                               const void *Wu, const void *Wd, const int *slot, const int *idx,
                               const float *gates, int R, void *y, void *ws, const Workspace &w,
                               int *counts, int *offsets, int *perm, const moe_run_opts *opts,
-                              bool after_router, bool permuted, cudaStream_t s) {
+                              bool after_router, bool permuted, const void *residual,
+                              cudaStream_t s) {
     moe_status st = MOE_OK;
     if (!permuted) st = run_permute(L, idx, R, ws, w, counts, offsets, perm, after_router, s);
     if (st != MOE_OK) return st;
     st = run_ffn(L, x, Wg, Wu, Wd, slot, nullptr, R, ws, w, counts, offsets, perm, opts, s);
     if (st != MOE_OK) return st;
-    return run_combine(L, (opts && opts->residual) ? x : nullptr, gates, R, y, ws, w, s);
+    return run_combine(L, residual, gates, R, y, ws, w, s);
+}
+
+// The input the router and experts read: x, or its pre-norm written into the workspace.
+const void *layer_input(const moe_layer_desc &L, const void *x, int R, void *ws,
+                        const Workspace &w, const moe_run_opts *opts, cudaStream_t s,
+                        moe_status *st) {
+    *st = MOE_OK;
+    if (!opts || !opts->norm_input) return x;
+    void *xn = at<void>(ws, w.xn);
+    if (launch_rmsnorm(L, x, R, xn, s) != cudaSuccess) *st = MOE_ERR_CUDA;
+    return xn;
 }
 
 }  // namespace moe
@@ -228,7 +242,7 @@ const char *moe_status_str(int status) {
     }
 }
 
-int moe_abi_version(void) { return 200; }
+int moe_abi_version(void) { return 201; }
 
 size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N) {
     if (!desc_ok(L) || B < 1 || N < 1) return 0;
@@ -240,6 +254,13 @@ moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void 
     if (!desc_ok(L) || R < 0 || (R > 0 && (!x || !W_r || !logits))) return MOE_ERR_ARG;
     if (R > 0 && (!aligned16(x) || !aligned16(W_r))) return MOE_ERR_ARG;
     return cuda_status(launch_router(*L, x, W_r, R, logits, nullptr, (cudaStream_t)stream));
+}
+
+moe_status moe_rms_norm(const moe_layer_desc *L, const void *x, int R, void *xn,
+                        moe_stream_t stream) {
+    if (!desc_ok(L) || R < 0 || (R > 0 && (!x || !xn))) return MOE_ERR_ARG;
+    if (R > 0 && (!aligned16(x) || !aligned16(xn))) return MOE_ERR_ARG;
+    return cuda_status(launch_rmsnorm(*L, x, R, xn, (cudaStream_t)stream));
 }
 
 moe_status moe_tree_select(const moe_layer_desc *L, const moe_select_params *P,
@@ -344,9 +365,14 @@ moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void
         return MOE_ERR_ARG;
     if (!permute_fits(R, L->E)) return MOE_ERR_UNSUPPORTED;
     const Workspace w = workspace_layout(*L, 1, R);
-    return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, R, y,
+    cudaStream_t s = (cudaStream_t)stream;
+    moe_status st;
+    const void *xin = layer_input(*L, x, R, workspace, w, opts, s, &st);
+    if (st != MOE_OK) return st;
+    return run_experts(*L, xin, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, R, y,
                        workspace, w, at<int>(workspace, w.counts), at<int>(workspace, w.offsets),
-                       at<int>(workspace, w.perm), opts, false, false, (cudaStream_t)stream);
+                       at<int>(workspace, w.perm), opts, false, false,
+                       (opts && opts->residual) ? x : nullptr, s);
 }
 
 moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P, const void *x,
@@ -375,8 +401,11 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
     int *offsets = o.offsets ? o.offsets : at<int>(workspace, w.offsets);
     int *perm = o.perm ? o.perm : at<int>(workspace, w.perm);
 
-    if (launch_router(*L, x, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord, s) !=
-        cudaSuccess)
+    moe_status sn;
+    const void *xin = layer_input(*L, x, R, workspace, w, opts, s, &sn);
+    if (sn != MOE_OK) return sn;
+    if (launch_router(*L, xin, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord,
+                      s) != cudaSuccess)
         return MOE_ERR_CUDA;
     const WeightPrefetch pf = weight_prefetch(*L, B, W_gate, W_up, W_down, slot_of_expert);
     const PermuteOut po{counts, offsets, perm, at<int>(workspace, w.pos),
@@ -389,8 +418,9 @@ moe_status moe_tree_forward(const moe_layer_desc *L, const moe_select_params *P,
     if (launch_select(*L, a, logits, depth, B, N, resident, idx, gates, elig, info, pf, po,
                       &permuted, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    return run_experts(*L, x, W_gate, W_up, W_down, slot_of_expert, idx, gates, R, y, workspace,
-                       w, counts, offsets, perm, opts, true, permuted, s);
+    return run_experts(*L, xin, W_gate, W_up, W_down, slot_of_expert, idx, gates, R, y,
+                       workspace, w, counts, offsets, perm, opts, true, permuted,
+                       (opts && opts->residual) ? x : nullptr, s);
 }
 
 moe_status moe_workspace_check(void *workspace, int *flags, moe_stream_t stream) {

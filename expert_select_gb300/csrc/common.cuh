@@ -46,6 +46,7 @@ struct Workspace {
     size_t xp;        // layer dtype [A, d]  x rows gathered in permuted order
     size_t h;         // f32 [A, f]  SwiGLU activations (bf16 [A, f] on the tensor-core path)
     size_t o;         // f32 [A, d]  expert outputs in permuted order
+    size_t xn;        // layer dtype [R, d]  the normalised input (moe_run_opts.norm_input)
     size_t total;
 };
 
@@ -140,6 +141,11 @@ cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *p
 cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,
                            uint8_t *res_dev, cudaStream_t s);
 
+// Pre-norm (moe_run_opts.norm_input): xn[r] = x[r] / sqrt(mean_i x[r, i]^2 + kNormEps).
+constexpr double kNormEps = 1e-6;
+cudaError_t launch_rmsnorm(const moe_layer_desc &L, const void *x, int R, void *xn,
+                           cudaStream_t s);
+
 // ---- host helpers shared by the entry points (api.cu, offload.cu) ----
 // Timing events of the offloaded layer's upload waits, kept in the residency table.
 cudaEvent_t residency_wait_event(moe_residency *t, int layer, int i, int which);
@@ -168,6 +174,10 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
                    const Workspace &w, const int *counts, const int *offsets, const int *perm,
                    const moe_run_opts *opts, cudaStream_t s);
 int resolve_ffn_path(const moe_layer_desc &L, const moe_run_opts *opts);  // -1: unsupported
+// x, or (opts->norm_input) its pre-norm written into the workspace by a launch on s.
+const void *layer_input(const moe_layer_desc &L, const void *x, int R, void *ws,
+                        const Workspace &w, const moe_run_opts *opts, cudaStream_t s,
+                        moe_status *st);
 moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
                        void *y, void *ws, const Workspace &w, cudaStream_t s);
 

@@ -1,0 +1,84 @@
+// Pre-norm of the layer input: every row scaled to unit root-mean-square,
+//   xn[r] = x[r] / sqrt(mean_i x[r, i]^2 + eps),
+// as the blocks of the target models put a normalisation in front of the MoE layer (a
+// stack of layers without one lets the residual stream grow until it overflows). No
+// learned weight. The mean of squares and the scale are computed in fp64 (the squares of
+// fp32 / bf16 values are exact in fp64), and each element x * scale is rounded once to the
+// layer dtype.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kNormWarps = 8;
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// Stores v[q] * scale, q < 8, rounded once (nearest, ties to even) to T, as 16-byte stores.
+template <typename T> __device__ __forceinline__ void store_scaled(T *p, const float v[8],
+                                                                  double scale);
+template <>
+__device__ __forceinline__ void store_scaled<__nv_bfloat16>(__nv_bfloat16 *p, const float v[8],
+                                                            double scale) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = __bfloat16_as_ushort(__double2bfloat16((double)v[2 * q] * scale));
+        const uint32_t hi = __bfloat16_as_ushort(__double2bfloat16((double)v[2 * q + 1] * scale));
+        w[q] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ void store_scaled<float>(float *p, const float v[8], double scale) {
+    float o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = __double2float_rn((double)v[q] * scale);
+    reinterpret_cast<float4 *>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+// A warp per row: 8-element slices per lane, the sum of squares in fp64.
+template <typename T>
+__global__ void __launch_bounds__(kNormWarps * 32)
+rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict__ xn) {
+    pdl_wait();
+    const int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= R) return;  // no block-wide barrier follows
+    const T *xr = x + (size_t)row * d;
+    double s = 0.0;
+    for (int c = lane * 8; c < d; c += 256) {
+        float v[8];
+        Vec8<T>::load(xr + c, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s = __dadd_rn(s, __dmul_rn((double)v[q], (double)v[q]));
+    }
+    s = warp_sum_d(s);
+    const double scale = 1.0 / sqrt(s / (double)d + eps);
+    T *out = xn + (size_t)row * d;
+    for (int c = lane * 8; c < d; c += 256) {
+        float v[8];
+        Vec8<T>::load(xr + c, v);
+        store_scaled<T>(out + c, v, scale);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const moe_layer_desc &L, const void *x, int R, void *xn,
+                           cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    const dim3 grid((R + kNormWarps - 1) / kNormWarps);
+    if (L.dtype == MOE_DTYPE_BF16)
+        return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, grid, dim3(kNormWarps * 32), 0, s,
+                          (const __nv_bfloat16 *)x, R, L.d, kNormEps, (__nv_bfloat16 *)xn);
+    return launch_pdl(rmsnorm_kernel<float>, grid, dim3(kNormWarps * 32), 0, s, (const float *)x,
+                      R, L.d, kNormEps, (float *)xn);
+}
+
+}  // namespace moe

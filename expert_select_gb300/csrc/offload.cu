@@ -98,8 +98,11 @@ extern "C" moe_status moe_offload_forward(
     // 1. residency before uploads, routing, selection, permutation
     if (launch_publish(E, slot_host.data(), res_host.data(), slot_dev, res_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_router(*L, x, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord, s) !=
-        cudaSuccess)
+    moe_status sn;
+    const void *xin = layer_input(*L, x, R, workspace, w, opts, s, &sn);
+    if (sn != MOE_OK) return sn;
+    if (launch_router(*L, xin, W_r, R, logits, at<int>(workspace, w.flags) + kRouterCheckWord,
+                      s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_select(*L, a, logits, depth, B, N, a.prune ? res_dev : nullptr, idx, gates, elig,
                       info, WeightPrefetch{}, PermuteOut{}, nullptr, s) != cudaSuccess)
@@ -132,7 +135,7 @@ extern "C" moe_status moe_offload_forward(
         if (launch_publish(E, sl, mask.data(), slot_dev, pass_dev, s) != cudaSuccess)
             return MOE_ERR_CUDA;
         ++passes;
-        return run_ffn(*L, x, slot_gate, slot_up, slot_down, slot_dev, pass_dev, R, workspace, w,
+        return run_ffn(*L, xin, slot_gate, slot_up, slot_down, slot_dev, pass_dev, R, workspace, w,
                        counts, offsets, perm, opts, s);
     };
 

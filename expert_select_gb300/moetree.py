@@ -34,6 +34,7 @@ EXPORTS = (
     "moe_residency_query", "moe_residency_plan", "moe_residency_publish", "moe_expert_upload",
     "moe_event_wait", "moe_tree_forward_noalloc", "moe_offload_forward", "moe_draft_select",
     "moe_tree_route", "moe_tree_block_stats", "moe_noalloc_check", "moe_offload_upload_wait",
+    "moe_rms_norm",
 )
 
 
@@ -76,7 +77,7 @@ class TreeStats(C.Structure):
 
 class RunOpts(C.Structure):
     _fields_ = [("ffn_path", C.c_int), ("ffn_begin", C.c_void_p), ("ffn_end", C.c_void_p),
-                ("residual", C.c_int), ("select_begin", C.c_void_p)]
+                ("residual", C.c_int), ("select_begin", C.c_void_p), ("norm_input", C.c_int)]
 
 
 _lib = None
@@ -95,6 +96,7 @@ def lib() -> C.CDLL:
             "moe_abi_version": ([], I),
             "moe_workspace_bytes": ([P, I, I], S),
             "moe_router_logits": ([P, P, P, I, P, P], I),
+            "moe_rms_norm": ([P, P, I, P, P], I),
             "moe_tree_select": ([P, P, P, P, I, I, P, P, P, P, P, P], I),
             "moe_expert_permute": ([P, P, I, P, P, P, P, P], I),
             "moe_expert_forward": ([P, P, P, P, P, P, P, P, I, P, P, P, P], I),
@@ -178,6 +180,11 @@ def moe_router_logits(L, x, W_r, logits, stream=None):
         C.byref(L), _ptr(x), _ptr(W_r), x.shape[0], _ptr(logits), _stream(stream)))
 
 
+def moe_rms_norm(L, x, xn, stream=None):
+    return _check("moe_rms_norm", lib().moe_rms_norm(
+        C.byref(L), _ptr(x), x.shape[0], _ptr(xn), _stream(stream)))
+
+
 def moe_tree_select(L, P, logits, depth, B, N, resident, topk_idx, gates, eligible=None,
                     info=None, stream=None):
     return _check("moe_tree_select", lib().moe_tree_select(
@@ -215,11 +222,13 @@ def _event(ev):
 
 
 def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None, residual=False,
-             select_begin=None) -> RunOpts:
+             select_begin=None, norm_input=False) -> RunOpts:
     """Options for the forward entry points. `begin`/`end` are torch.cuda.Event
     objects recorded around the grouped-expert kernel, `select_begin` one recorded before
-    the selection launch; `residual` returns x + MoE(x)."""
-    return RunOpts(ffn_path, _event(begin), _event(end), int(residual), _event(select_begin))
+    the selection launch; `residual` returns x + MoE(x); `norm_input` routes and computes
+    the experts on the RMS pre-norm of x (the residual still adds x)."""
+    return RunOpts(ffn_path, _event(begin), _event(end), int(residual), _event(select_begin),
+                   int(norm_input))
 
 
 def moe_expert_forward(L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, y, ws,

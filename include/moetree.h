@@ -127,13 +127,19 @@ typedef struct {
  * the whole expert stage. An event between two launches keeps the second from
  * starting early, so timed calls run slightly slower than untimed ones. With `residual`
  * set the layer returns y = x + MoE(x) instead of MoE(x), for a residual stack of
- * layers; y may then be the same buffer as x. */
+ * layers; y may then be the same buffer as x. With `norm_input` set the router and the
+ * experts read the pre-norm x_n[r] = x[r] / sqrt(mean_i x[r, i]^2 + 1e-6) (no learned
+ * weight; mean and scale in fp64, each element rounded once to the layer dtype, written
+ * into the workspace) instead of x, as the pre-norm blocks of the target models do; the
+ * residual still adds x itself: y = x + MoE(x_n). Used by moe_tree_forward,
+ * moe_expert_forward and moe_offload_forward. */
 typedef struct {
     int ffn_path; /* moe_ffn_path */
     moe_event_t ffn_begin;
     moe_event_t ffn_end;
     int residual;
     moe_event_t select_begin;
+    int norm_input;
 } moe_run_opts;
 
 /* Text for a status code. Never NULL. */
@@ -153,6 +159,16 @@ size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N);
  *   x [R, d] and W_r [E, d] device, layer dtype; logits [R, E] device fp32. */
 moe_status moe_router_logits(const moe_layer_desc *L, const void *x, const void *W_r, int R,
                              float *logits, moe_stream_t stream);
+
+/* Pre-norm of the layer input, the RMS normalisation the target models (Qwen3, GPT-OSS)
+ * apply before the MoE layer, without a learned weight: per row
+ * xn[r, i] = x[r, i] / sqrt(mean_i x[r, i]^2 + 1e-6); the mean and scale are computed in
+ * fp64, each element is rounded once (nearest, ties to even) to the layer dtype. The
+ * layer calls apply it themselves when moe_run_opts.norm_input is set; this call exposes
+ * it on its own.
+ *   x, xn [R, d] device, layer dtype, 16-byte aligned, must not overlap. */
+moe_status moe_rms_norm(const moe_layer_desc *L, const void *x, int R, void *xn,
+                        moe_stream_t stream);
 
 /* Expert selection for B trees of N nodes from router logits ("AcceptMoE" news
  * article, section 02; AcceptMoE abstract). Per tree: natural top-k of every node,

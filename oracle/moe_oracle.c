@@ -60,6 +60,58 @@ static double elem(const void *p, int dtype, size_t i) {
     return (double)f;
 }
 
+/* Nearest bf16 to v, ties to the even significand, as raw bits. bf16 keeps 8
+ * significant bits and fp32's exponent range: normal numbers from 2^-126, subnormals in
+ * steps of 2^-133, largest finite (2 - 2^-7) * 2^127. Written from that definition:
+ * v = m * 2^e with 1/2 <= |m| < 1, so the quantum at v is 2^(e-8) (never below 2^-133);
+ * nearbyint rounds to nearest even in the default rounding mode. */
+ORC_API uint16_t oracle_round_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    const double a = fabs(v);
+    double r;
+    if (a == 0.0 || isinf(a)) {
+        r = a;
+    } else {
+        int e;
+        frexp(a, &e);
+        int qexp = e - 8;
+        if (qexp < -133) qexp = -133;
+        r = ldexp(nearbyint(ldexp(a, -qexp)), qexp);
+        if (r > ldexp(255.0, 120)) r = INFINITY; /* past (2 - 2^-7) * 2^127 */
+    }
+    /* r is a bf16 value (or inf), so it is exact in fp32 and its low 16 bits are 0 */
+    const float f = (float)r;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* Pre-norm of the layer input (the RMS normalisation the target models put in front of
+ * the MoE layer, without a learned weight): xn[r, i] = x[r, i] / sqrt(mean_i x[r, i]^2 +
+ * eps), all in fp64, each element then rounded once to the input dtype (nearest, ties
+ * to even). xn64 [R, d] (may be NULL) receives the values before that rounding. */
+ORC_API void oracle_rmsnorm(const void *x, int dtype, int R, int d, double eps, double *xn64,
+                            void *xn) {
+    for (int n = 0; n < R; ++n) {
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) {
+            const double v = elem(x, dtype, (size_t)n * d + i);
+            ss += v * v;
+        }
+        const double scale = 1.0 / sqrt(ss / d + eps);
+        for (int i = 0; i < d; ++i) {
+            const size_t at = (size_t)n * d + i;
+            const double v = elem(x, dtype, at) * scale;
+            if (xn64) xn64[at] = v;
+            if (dtype == 0)
+                ((float *)xn)[at] = (float)v;
+            else
+                ((uint16_t *)xn)[at] = oracle_round_bf16(v);
+        }
+    }
+}
+
 /* [LAYER] router scores l = W_r x, one row per token; no bias. */
 ORC_API void oracle_router(const void *x, const void *Wr, int dtype, int R, int d, int E,
                            double *logits) {

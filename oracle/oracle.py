@@ -60,6 +60,10 @@ def lib():
         _lib.oracle_moe_combine.restype = None
         _lib.oracle_draft_select.argtypes = [i, i, i, P, P, P, C.c_float, i, P, P]
         _lib.oracle_draft_select.restype = i
+        _lib.oracle_round_bf16.argtypes = [C.c_double]
+        _lib.oracle_round_bf16.restype = C.c_uint16
+        _lib.oracle_rmsnorm.argtypes = [P, i, i, i, C.c_double, P, P]
+        _lib.oracle_rmsnorm.restype = None
     return _lib
 
 
@@ -83,6 +87,26 @@ def _raw(t):
     if a.dtype == np.uint16:
         return a, 1
     return a.astype(np.float32, copy=False), 0
+
+
+NORM_EPS = 1e-6
+
+
+def round_bf16(v: float) -> int:
+    """Raw bits of the bf16 nearest to v (ties to even)."""
+    return int(lib().oracle_round_bf16(float(v)))
+
+
+def rmsnorm(x, eps: float = NORM_EPS, unrounded: bool = False):
+    """Pre-norm x / sqrt(mean(x^2) + eps) per row in fp64, rounded once to x's dtype:
+    a uint16 array of bf16 bits for bf16 input (accepted by router / moe_combine as
+    bf16), fp32 otherwise. With `unrounded`, also the fp64 values before rounding."""
+    xa, dt = _raw(x)
+    R, d = xa.shape
+    out = np.empty((R, d), dtype=np.uint16 if dt == 1 else np.float32)
+    x64 = np.empty((R, d), dtype=np.float64) if unrounded else None
+    lib().oracle_rmsnorm(_p(xa), dt, R, d, eps, _p(x64), _p(out))
+    return (out, x64) if unrounded else out
 
 
 def router(x, Wr) -> np.ndarray:
@@ -212,9 +236,13 @@ def moe_combine(x, Wg, Wu, Wd, idx: np.ndarray, gates: np.ndarray,
 
 
 def forward(x, Wr, Wg, Wu, Wd, depth: np.ndarray, k: int, c: Sequence[float],
-            rows: Optional[Sequence[int]] = None, **select_kw) -> Dict:
-    """The whole layer: router (fp64, rounded to fp32 for the decisions) ->
-    per-tree selection -> permute -> gated expert outputs for `rows`."""
+            rows: Optional[Sequence[int]] = None, norm_input: bool = False,
+            **select_kw) -> Dict:
+    """The whole layer: (optionally the RMS pre-norm of x) -> router (fp64, rounded to
+    fp32 for the decisions) -> per-tree selection -> permute -> gated expert outputs for
+    `rows` (without the residual)."""
+    if norm_input:
+        x = rmsnorm(x)
     logits64 = router(x, Wr)
     l32 = logits64.astype(np.float32)
     E = l32.shape[1]

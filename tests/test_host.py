@@ -41,7 +41,7 @@ def test_status_strings_and_version():
     assert M.status_str(0) == "ok"
     assert "slot" in M.status_str(M.MOE_ERR_NOSLOT)
     assert M.status_str(12345) == "unknown status"
-    assert M.lib().moe_abi_version() == 200
+    assert M.lib().moe_abi_version() == 201
 
 
 def test_workspace_bytes():
@@ -78,6 +78,9 @@ def test_bad_arguments_rejected_before_any_launch():
     # misaligned (not 16-byte) pointers are rejected on the host
     odd = C.c_void_p(0x1004)
     assert lib.moe_router_logits(C.byref(L), odd, odd, 4, odd, nul) == M.MOE_ERR_ARG
+    assert lib.moe_rms_norm(C.byref(L), nul, 4, nul, nul) == M.MOE_ERR_ARG
+    assert lib.moe_rms_norm(C.byref(L), odd, 4, odd, nul) == M.MOE_ERR_ARG
+    assert lib.moe_rms_norm(C.byref(L), nul, -1, nul, nul) == M.MOE_ERR_ARG
     assert lib.moe_event_wait(nul, 1.0) == M.MOE_ERR_ARG
 
 

@@ -590,3 +590,84 @@ def test_draft_select_invariants(seed):
     s0, u0 = O.draft_select(cand.parent, cand.logp, fp, E, 0.0, 65)
     s1, u1 = O.draft_select(cand.parent, cand.logp, fp, E, 1e6, 65)
     assert u1 <= u0
+
+
+# ---------------------------------------------------------------- pre-norm
+
+def _bf16_value(bits: int) -> float:
+    return float(torch.tensor([bits], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+                 .double()[0]) if bits < 0x8000 else -_bf16_value(bits & 0x7FFF)
+
+
+def test_round_bf16_is_nearest_with_ties_to_even():
+    """Brute force over the two neighbours: the result is never farther from v than the
+    bf16 values one step either side, across normal and subnormal magnitudes; on the
+    exact midpoint between two bf16 values the even significand wins."""
+    rng = np.random.default_rng(0)
+    mags = np.ldexp(rng.uniform(0.5, 1.0, 4000), rng.integers(-140, 128, 4000))
+    vals = np.concatenate([mags, -mags[:1000]])
+    for v in vals:
+        b = O.round_bf16(v)
+        got = _bf16_value(b)
+        assert math.copysign(1.0, got) == math.copysign(1.0, v) or got == 0.0
+        mag = b & 0x7FFF
+        for nb in (mag - 1, mag + 1):
+            if 0 <= nb < 0x7F80:
+                alt = math.copysign(_bf16_value(nb), v)
+                assert abs(v - got) <= abs(v - alt), (v, hex(b), hex(nb))
+    # midpoints between consecutive bf16 values (exact in fp64)
+    for mag in list(range(1, 200)) + list(range(0x3F00, 0x3F40)) + list(range(0x7F00, 0x7F7F)):
+        lo, hi = _bf16_value(mag), _bf16_value(mag + 1)
+        mid = (lo + hi) / 2
+        want = mag if mag % 2 == 0 else mag + 1
+        assert O.round_bf16(mid) == want
+        assert O.round_bf16(-mid) == 0x8000 | want
+        assert O.round_bf16(np.nextafter(mid, 0)) == mag
+        assert O.round_bf16(np.nextafter(mid, np.inf)) == mag + 1
+
+
+def test_round_bf16_matches_torch_on_fp32_inputs():
+    """For values that are fp32 numbers a single rounding to bf16 is what torch's
+    fp32 -> bf16 conversion (nearest, ties to even) does."""
+    rng = np.random.default_rng(1)
+    f = np.concatenate([rng.standard_normal(3000).astype(np.float32),
+                        (rng.standard_normal(1000) * 1e-38).astype(np.float32),
+                        np.float32([0.0, -0.0, 1.00390625, 1.01171875, 3.4e38])])
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([O.round_bf16(float(v)) for v in f], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+    # past the largest finite bf16 by at least half a step: infinity
+    assert O.round_bf16(2.0 ** 128) == 0x7F80
+    assert O.round_bf16(-(2.0 ** 128)) == 0xFF80
+    assert O.round_bf16(float(np.ldexp(511, 119))) == 0x7F80   # the midpoint rounds up to inf
+    assert O.round_bf16(float(np.ldexp(509, 119))) == 0x7F7E   # midpoint, even side
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_rmsnorm_closed_form(dtype):
+    """The unrounded pre-norm is x / sqrt(mean(x^2) + eps) (torch fp64); each row's mean
+    square is then m / (m + eps); the stored values are that rounded once to the dtype;
+    a row scaled by a power of two (eps negligible) normalises to the same output."""
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(7, 96, generator=g) * torch.tensor([1e-3, 0.02, 1, 30, 1, 1, 1])[:, None])
+    x = x.to(dtype)
+    x[5] = 0.0
+    out, x64 = O.rmsnorm(x, unrounded=True)
+    xd = x.double()
+    ms = (xd ** 2).mean(1, keepdim=True)
+    ref = xd / torch.sqrt(ms + O.NORM_EPS)
+    np.testing.assert_allclose(x64, ref.numpy(), rtol=1e-14, atol=0)
+    assert np.all(x64[5] == 0.0)
+    got_ms = (x64 ** 2).mean(1)
+    want_ms = (ms / (ms + O.NORM_EPS)).numpy()[:, 0]
+    np.testing.assert_allclose(got_ms, want_ms, rtol=1e-12)
+    if dtype == torch.bfloat16:
+        assert out.dtype == np.uint16
+        want = np.array([O.round_bf16(v) for v in x64.ravel()], dtype=np.uint16)
+        np.testing.assert_array_equal(out.ravel(), want)
+    else:
+        np.testing.assert_array_equal(out, x64.astype(np.float32))
+    x2 = x.clone()
+    x2[3] = x[3] * 4.0
+    out2 = O.rmsnorm(x2)
+    np.testing.assert_array_equal(out2[3], out[3])
