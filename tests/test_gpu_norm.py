@@ -243,3 +243,36 @@ def test_normed_residual_chain_stays_bounded():
     assert torch.isfinite(x.float()).all()
     rms = x.double().pow(2).mean().sqrt().item()
     assert rms <= 25 * max(rms0, 1.0), (rms, rms0)
+
+
+def test_normed_fp32_layer_against_oracle():
+    """The fp32 layer (CUDA-core router and experts) with the pre-norm and the residual:
+    routing bit-exact from the device's logits, every row of y within 1e-4 * max|ref|."""
+    shape = W.TINY
+    t = W.eagle_tree(81, steps=3, topk=4, draft_tokens=20)
+    N = t.N
+    x = (W.hidden_states(82, t.parent, shape.d, torch.float32) * 3.0)
+    wr, wg, wu, wd = _layer(shape, 83, 0.3)
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "fp32")
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_TINY)
+    dep = torch.from_numpy(t.depth.copy()).to(DEV)
+    ws = M.workspace(L, 1, N)
+    lg = torch.empty(N, shape.E, device=DEV)
+    idx = torch.empty(N, shape.k, dtype=torch.int32, device=DEV)
+    gates = torch.empty(N, shape.k, device=DEV)
+    y = torch.empty(N, shape.d, device=DEV)
+    M.moe_tree_forward(L, P, x.to(DEV), wr, wg, wu, wd, None, dep, 1, N, None, y, ws,
+                       M.tree_outputs(logits=lg, topk_idx=idx, gates=gates),
+                       M.run_opts(norm_input=True, residual=True))
+    torch.cuda.synchronize()
+    assert M.moe_workspace_check(ws) == 0
+    xn = O.rmsnorm(x)
+    ref_l = O.router(xn, wr.cpu())
+    got_l = lg.cpu().numpy()
+    assert (np.abs(got_l - ref_l) <= 1e-4 * np.abs(ref_l).max(axis=1, keepdims=True)).all()
+    sel = O.select_tree(got_l, t.depth, shape.k, W.C_TINY, mode=O.ACCEPT)
+    np.testing.assert_array_equal(idx.cpu().numpy(), sel["idx"])
+    ref = x.double().numpy() + O.moe_combine(xn, wg.cpu(), wu.cpu(), wd.cpu(), sel["idx"],
+                                             sel["gates"])
+    got = y.double().cpu().numpy()
+    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()

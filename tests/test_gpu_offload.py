@@ -1,6 +1,7 @@
 """GPU tests of the offloaded layer (moe_offload_forward) and of the residual option.
 
-The offloaded layer computes every expert with the same kernels as the resident layer,
+The offloaded layer computes every expert with the same kernels as the resident layer
+(with or without the pre-norm and the residual),
 only addressed through slots that uploads fill, in one or more passes; so its output
 must equal moe_tree_forward on the same inputs bit for bit, given the residency mask the
 table had before the call (pruning reads that mask). The counters must add up: every
@@ -39,14 +40,16 @@ def _params(mode, prune):
                            min_set=4)
 
 
-@pytest.mark.parametrize("shape,slots,mode,prune,router_std", [
-    (SHAPE_TC, 8, "natural", False, 0.02),
-    (SHAPE_TC, 8, "accept", False, 0.3),
-    (SHAPE_TC, 12, "accept", True, 0.3),
-    (SHAPE_TC, 30, "natural", False, 0.02),
-    (SHAPE_SIMT, 4, "accept", True, 0.3),
+@pytest.mark.parametrize("shape,slots,mode,prune,router_std,norm", [
+    (SHAPE_TC, 8, "natural", False, 0.02, False),
+    (SHAPE_TC, 8, "accept", False, 0.3, False),
+    (SHAPE_TC, 12, "accept", True, 0.3, False),
+    (SHAPE_TC, 12, "accept", True, 0.3, True),
+    (SHAPE_TC, 30, "natural", False, 0.02, False),
+    (SHAPE_SIMT, 4, "accept", True, 0.3, False),
+    (SHAPE_SIMT, 4, "accept", True, 0.3, True),
 ])
-def test_offload_matches_resident_layer(shape, slots, mode, prune, router_std):
+def test_offload_matches_resident_layer(shape, slots, mode, prune, router_std, norm):
     E, k = shape.E, shape.k
     wg, wu, wd = W.expert_weights(5, shape, device=DEV)
     hg, hu, hd = (w.cpu().pin_memory() for w in (wg, wu, wd))
@@ -73,14 +76,16 @@ def test_offload_matches_resident_layer(shape, slots, mode, prune, router_std):
         cnt_ref = torch.empty(E, dtype=torch.int32, device=DEV)
         y_ref = torch.empty(N, shape.d, dtype=shape.torch_dtype, device=DEV)
         ws = M.workspace(L, 1, N)
+        opts = M.run_opts(norm_input=norm, residual=norm)
         M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dep, 1, N, res_dev, y_ref, ws,
-                           M.tree_outputs(topk_idx=idx_ref, counts=cnt_ref))
+                           M.tree_outputs(topk_idx=idx_ref, counts=cnt_ref), opts)
         # the offloaded layer
         idx = torch.empty_like(idx_ref)
         y = torch.full_like(y_ref, float("nan"))
         ws2 = M.workspace(Ls, 1, N)
         st = M.moe_offload_forward(Ls, P, x, wr, hg, hu, hd, pg, pu, pd, table, 1, dep, 1, N,
-                                   y, ws2, M.tree_outputs(topk_idx=idx), side_stream=side)
+                                   y, ws2, M.tree_outputs(topk_idx=idx), opts=opts,
+                                   side_stream=side)
         torch.cuda.synchronize()
         assert M.moe_workspace_check(ws2) == 0
         assert torch.equal(idx, idx_ref)

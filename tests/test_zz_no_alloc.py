@@ -41,6 +41,28 @@ def _outputs(shape, R):
                 counts=torch.empty(shape.E, dtype=torch.int32, device=DEV))
 
 
+def test_noalloc_prenorm_residual_equals_workspace_forward(layer):
+    """The pre-norm residual block (norm_input + residual, y written over x) through the
+    built-in scratch equals the same call with a caller workspace bit for bit."""
+    shape, wr, wg, wu, wd = layer
+    L = M.layer_desc(shape.d, shape.E, shape.k, shape.f, "bf16")
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    t, x, dep = _tree(31, shape)
+    R = t.N
+    opts = M.run_opts(residual=True, norm_input=True)
+    y_ref = x.clone()
+    y_na = x.clone()
+    ws = M.workspace(L, 1, R)
+    M.moe_tree_forward(L, P, y_ref, wr, wg, wu, wd, None, dep, 1, R, None, y_ref, ws, None, opts)
+    M.moe_tree_forward_noalloc(L, P, y_na, wr, wg, wu, wd, None, dep, 1, R, None, y_na, None,
+                               opts)
+    torch.cuda.synchronize()
+    assert M.moe_workspace_check(ws) == 0
+    assert M.moe_noalloc_check() == 0
+    assert torch.equal(y_na, y_ref)
+    assert not torch.equal(y_na, x)
+
+
 def test_noalloc_matches_workspace_forward_twice(layer):
     """Two calls in a row (different trees) through the built-in scratch give the
     same routing as moe_tree_forward with a caller workspace, and outputs within
