@@ -1,0 +1,120 @@
+"""Seeded random layer configurations through the whole layer, against the oracle.
+
+Each case draws a layer (dtype, d, f, E, k), a block of B draft trees of one random
+shape, a routing rule (natural, AcceptMoE, fixed size; with or without the root anchor;
+with or without residency-aware pruning on a random residency mask), a router scale and
+an expert path, then runs moe_tree_forward once and checks, as the whole-layer parity
+tests do: router logits within 1e-4 of the row's largest |logit|; the selection tree by
+tree against the fp64 oracle on the device's logits (a tree whose fp64 decision margin is
+a tie is checked for validity instead); counts and offsets exactly; every row of y against
+the oracle's experts and combine on the device's routing (2e-2 * max|ref| for bf16, 1e-4
+for fp32). The cases cover expert counts that are not multiples of 32, k from 1 to 16,
+blocks of one to three trees and trees of 2 to 65 nodes.
+"""
+import numpy as np
+import pytest
+import torch
+
+from expert_select_gb300 import moetree as M
+from expert_select_gb300 import workload as W
+from oracle import oracle as O
+from test_gpu_parity import _check_selection
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+NF = M.MOE_INFO_FIELDS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from expert_select_gb300 import build
+    build.build()
+    M.lib()
+
+
+def _draw(seed):
+    rng = np.random.default_rng(7000 + seed)
+    dtype = "bf16" if rng.random() < 0.7 else "fp32"
+    d = int(rng.choice([64, 128, 192, 256, 384]))
+    f = int(rng.choice([64, 128, 192, 256]))
+    E = int(rng.choice([8, 16, 24, 32, 48, 64, 100, 128, 160, 256]))
+    k = int(rng.integers(1, min(16, E) + 1))
+    B = int(rng.choice([1, 1, 2, 3]))
+    steps = int(rng.integers(1, 6))
+    topk = int(rng.integers(2, 11))
+    most = topk + (steps - 1) * topk * topk
+    tokens = int(min(rng.integers(1, 65), most))
+    mode = str(rng.choice(["natural", "accept", "fixed"]))
+    anchor = bool(rng.random() < 0.8)
+    prune = mode != "natural" and bool(rng.random() < 0.4)
+    std = float(rng.choice([0.02, 0.1, 0.3]))
+    path = M.MOE_FFN_SIMT if (dtype == "fp32" or rng.random() < 0.25) else M.MOE_FFN_AUTO
+    fixed_B = int(rng.integers(k, E + 1))
+    min_set = int(rng.integers(k, max(k, 20) + 1))
+    budget = int(rng.integers(0, 10))
+    resident = (rng.random(E) < 0.5).astype(np.uint8)
+    return dict(dtype=dtype, d=d, f=f, E=E, k=k, B=B, steps=steps, topk=topk, tokens=tokens,
+                mode=mode, anchor=anchor, prune=prune, std=std, path=path, fixed_B=fixed_B,
+                min_set=min_set, budget=budget, resident=resident)
+
+
+@pytest.mark.parametrize("seed", list(range(64)))
+def test_random_layer_against_oracle(seed):
+    c = _draw(seed)
+    shape = W.LayerShape(d=c["d"], E=c["E"], k=c["k"], f=c["f"], dtype=c["dtype"])
+    E, k, B = c["E"], c["k"], c["B"]
+    trees = [W.eagle_tree(8000 + 17 * seed + b, steps=c["steps"], topk=c["topk"],
+                          draft_tokens=c["tokens"]) for b in range(B)]
+    N = trees[0].N
+    assert all(t.N == N for t in trees)
+    depth = np.stack([t.depth for t in trees]).astype(np.int32)
+    R = B * N
+    x = torch.cat([W.hidden_states(8100 + 17 * seed + b, t.parent, shape.d, shape.torch_dtype)
+                   for b, t in enumerate(trees)])
+    wr = W.router_weight(8200 + seed, shape, std=c["std"], device=DEV)
+    wg, wu, wd = W.expert_weights(8300 + seed, shape, device=DEV)
+    mode = {"natural": M.MOE_ROUTE_NATURAL, "accept": M.MOE_ROUTE_ACCEPT,
+            "fixed": M.MOE_ROUTE_FIXED_B}[c["mode"]]
+    P = M.select_params(mode, W.C_EAGLE, anchor=c["anchor"], prune=c["prune"],
+                        reroute_budget=c["budget"], min_set=c["min_set"],
+                        fixed_B=c["fixed_B"] if c["mode"] == "fixed" else 0)
+    L = M.layer_desc(shape.d, E, k, shape.f, shape.dtype)
+    out = dict(logits=torch.empty(R, E, device=DEV),
+               topk_idx=torch.empty(R, k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(R, k, device=DEV),
+               eligible=torch.empty(B, E, dtype=torch.uint8, device=DEV),
+               info=torch.empty(B, NF, dtype=torch.int32, device=DEV),
+               counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV))
+    res = torch.from_numpy(c["resident"]).to(DEV) if c["prune"] else None
+    y = torch.full((R, shape.d), float("nan"), dtype=shape.torch_dtype, device=DEV)
+    ws = M.workspace(L, B, N)
+    M.moe_tree_forward(L, P, x.to(DEV), wr, wg, wu, wd, None,
+                       torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
+                       M.tree_outputs(**out), M.run_opts(c["path"]))
+    torch.cuda.synchronize()
+    assert M.moe_workspace_check(ws) == 0
+    got = {key: v.cpu().numpy() for key, v in out.items()}
+    # 1. the router against the oracle's own fp64 logits
+    ref_l = O.router(x, wr.cpu())
+    assert (np.abs(got["logits"] - ref_l) <= 1e-4 * np.abs(ref_l).max(axis=1, keepdims=True)).all()
+    # 2. the selection, tree by tree, from the device's logits
+    omode = {"natural": O.NATURAL, "accept": O.ACCEPT, "fixed": O.FIXED_B}[c["mode"]]
+    kw = dict(mode=omode, c=W.C_EAGLE, anchor=c["anchor"])
+    if c["mode"] == "fixed":
+        kw["fixed_B"] = c["fixed_B"]
+    if c["prune"]:
+        kw.update(prune=True, resident=c["resident"], budget=c["budget"], min_set=c["min_set"])
+    _check_selection(shape, kw, got["logits"], depth, got["topk_idx"], got["gates"],
+                     got["eligible"], got["info"], N, B)
+    # 3. the counting sort of the device's routing
+    rc, ro, _ = O.permute(got["topk_idx"], E)
+    np.testing.assert_array_equal(got["counts"], rc)
+    np.testing.assert_array_equal(got["offsets"], ro)
+    # 4. every row of y: the oracle's experts and combine on the device's routing
+    ref_y = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"])
+    tol = 2e-2 if shape.dtype == "bf16" else 1e-4
+    err = np.abs(y.double().cpu().numpy() - ref_y).max()
+    assert err <= tol * np.abs(ref_y).max(), (c, err)
