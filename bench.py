@@ -465,6 +465,67 @@ def run_gpu(args):
     peaked["acceptmoe_vs_natural"] = round(peaked["acceptmoe"]["value"] /
                                            peaked["natural"]["value"], 3)
 
+    # two independent one-tree blocks in flight (a serving engine verifying two requests'
+    # trees at once): the trees alternate between two streams with their own workspaces,
+    # and the expert kernel is capped below one CTA per SM so that one stream's routing
+    # kernels find SMs while the other's experts stream. Reported beside the headline, not
+    # instead of it: each call is still the one-tree layer.
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cap = max(1, nsm - args.pair_free_sms)
+    s2 = torch.cuda.Stream(dev)
+    ws2 = M.workspace(L, 1, N, device=dev)
+    y2 = torch.empty_like(y)
+
+    def pair_loop(n, routing, w_r):
+        P = M.select_params(routing_mode[routing], W.C_EAGLE)
+        opts = M.run_opts(args.ffn_path, ffn_max_ctas=cap)
+        cur = torch.cuda.current_stream(dev)
+        s2.wait_stream(cur)
+        for i in range(n):
+            j = i % TREES
+            if i % 2 == 0:
+                M.moe_tree_forward(L, P, xs[j], w_r, wg, wu, wd, None, deps[j], 1, N, None, y,
+                                   ws, None, opts, cur)
+            else:
+                M.moe_tree_forward(L, P, xs[j], w_r, wg, wu, wd, None, deps[j], 1, N, None, y2,
+                                   ws2, None, opts, s2)
+        cur.wait_stream(s2)
+
+    def pair_runner(n, routing, w_r):
+        if args.no_graph:
+            return lambda: pair_loop(n, routing, w_r)
+        full, rest = divmod(n, 256)
+        graphs = []
+        for m_ in ([256] if full else []) + ([rest] if rest else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                pair_loop(m_, routing, w_r)
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+
+        def run():
+            for _ in range(full):
+                graphs[0].replay()
+            if rest:
+                graphs[-1].replay()
+        run()
+        torch.cuda.synchronize(dev)
+        return run
+
+    pair = {"ffn_ctas": cap, "streams": 2}
+    for label, r_, w_r, u_ref in (("acceptmoe_std_0.02", routing, wr, union),
+                                  ("acceptmoe_std_0.1", "acceptmoe", wr_peaked, None),
+                                  ("natural_std_0.1", "natural", wr_peaked, None)):
+        pair_loop(Wm, r_, w_r)
+        torch.cuda.synchronize(dev)
+        sec_pair = _timed(pair_runner(Kv, r_, w_r), dev, world)
+        u_pair = u_ref[:Kv] if u_ref is not None else counters(Kv, r_, w_r=w_r)[0]
+        pb = (u_pair * shape.expert_bytes + shape.E * shape.d * 2 + 3 * N * shape.d * 2 +
+              2 * assignments * shape.f * 2).mean()
+        pair[label] = {"value": round(whole_job_rate(Kv, world, sec_pair), 2),
+                       "union_mean": round(float(u_pair.mean()), 2),
+                       "whole_step_hbm_frac": round(float(pb / (sec_pair / Kv) / 1e9 / peak), 4)}
+
     # router, select, combine + the grouped-expert launches; the permute step runs inside
     # the selection launch for a block of one tree of up to 256 nodes, else in its own
     # kernel (and a second, placing kernel past 2048 assignments)
@@ -534,6 +595,7 @@ def run_gpu(args):
                   f"{other}_union_mean": float(u_o.mean()),
                   f"{other}_value": round(whole_job_rate(Kv, world, sec_o), 2)},
         "router_std_0.1": peaked,
+        "two_blocks_in_flight": pair,
     }
     print(json.dumps(line))
 
@@ -1161,6 +1223,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--slots", type=int, default=48)
     ap.add_argument("--batches", default="1,4,16,64")
+    ap.add_argument("--pair-free-sms", type=int, default=16,
+                    help="SMs the expert kernel leaves free when two blocks are in flight")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

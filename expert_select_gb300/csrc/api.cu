@@ -122,6 +122,7 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
     fa.xp = at<void>(ws, w.xp);
     fa.h = at<void>(ws, w.h);
     fa.o = at<float>(ws, w.o);
+    fa.max_ctas = opts ? opts->ffn_max_ctas : 0;
 
     const int path = resolve_ffn_path(L, opts);
     if (path < 0) return MOE_ERR_UNSUPPORTED;
@@ -242,7 +243,7 @@ const char *moe_status_str(int status) {
     }
 }
 
-int moe_abi_version(void) { return 201; }
+int moe_abi_version(void) { return 202; }
 
 size_t moe_workspace_bytes(const moe_layer_desc *L, int B, int N) {
     if (!desc_ok(L) || B < 1 || N < 1) return 0;

@@ -125,6 +125,7 @@ struct FfnArgs {
     int R, d, f, E, k, dtype;
     int slots;           // expert slots in the weight pools
     int *flags;
+    int max_ctas;        // tensor-core path: CTAs at most (0: one per SM)
     int *sched;          // tensor-core path: ticket + row-tile counters
     void *xp;            // gathered x (tensor-core path)
     void *h;             // activations

@@ -620,7 +620,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.sched = a.sched;
     p.h = (__nv_bfloat16 *)a.h;
     p.o = a.o;
-    return launch_pdl(ffn_tc_kernel, dim3(nsm), dim3(kThreads), smem, s, m, p);
+    const int ctas = a.max_ctas > 0 ? std::min(nsm, a.max_ctas) : nsm;
+    return launch_pdl(ffn_tc_kernel, dim3(ctas), dim3(kThreads), smem, s, m, p);
 }
 
 }  // namespace moe

@@ -77,7 +77,8 @@ class TreeStats(C.Structure):
 
 class RunOpts(C.Structure):
     _fields_ = [("ffn_path", C.c_int), ("ffn_begin", C.c_void_p), ("ffn_end", C.c_void_p),
-                ("residual", C.c_int), ("select_begin", C.c_void_p), ("norm_input", C.c_int)]
+                ("residual", C.c_int), ("select_begin", C.c_void_p), ("norm_input", C.c_int),
+                ("ffn_max_ctas", C.c_int)]
 
 
 _lib = None
@@ -222,13 +223,14 @@ def _event(ev):
 
 
 def run_opts(ffn_path: int = MOE_FFN_AUTO, begin=None, end=None, residual=False,
-             select_begin=None, norm_input=False) -> RunOpts:
+             select_begin=None, norm_input=False, ffn_max_ctas: int = 0) -> RunOpts:
     """Options for the forward entry points. `begin`/`end` are torch.cuda.Event
     objects recorded around the grouped-expert kernel, `select_begin` one recorded before
     the selection launch; `residual` returns x + MoE(x); `norm_input` routes and computes
-    the experts on the RMS pre-norm of x (the residual still adds x)."""
+    the experts on the RMS pre-norm of x (the residual still adds x); `ffn_max_ctas` caps
+    the tensor-core expert kernel's CTAs (0: one per SM)."""
     return RunOpts(ffn_path, _event(begin), _event(end), int(residual), _event(select_begin),
-                   int(norm_input))
+                   int(norm_input), int(ffn_max_ctas))
 
 
 def moe_expert_forward(L, x, W_gate, W_up, W_down, slot_of_expert, topk_idx, gates, y, ws,

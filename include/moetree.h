@@ -140,6 +140,9 @@ typedef struct {
     int residual;
     moe_event_t select_begin;
     int norm_input;
+    int ffn_max_ctas; /* tensor-core expert kernel: CTAs at most (0: one per SM). Fewer
+                         leave SMs free for another stream's routing kernels, so that two
+                         independent blocks can be in flight at once */
 } moe_run_opts;
 
 /* Text for a status code. Never NULL. */

@@ -1075,3 +1075,41 @@ def test_topk_with_exact_ties(E, k):
         P = M.select_params(mode, W.C_EAGLE, **kw)
         gidx, _, _, _ = _select_gpu(shape, P, logits, depth, 1, N)
         np.testing.assert_array_equal(gidx, ref)
+
+
+@pytest.mark.parametrize("cap", [1, 64, 136])
+def test_two_streams_with_capped_expert_kernel(cap):
+    """Two one-tree blocks in flight on two streams, each with its own workspace and the
+    tensor-core expert kernel capped at `cap` CTAs, give the same routing and y bit for bit
+    as the same trees run one at a time with one CTA per SM."""
+    shape = W.QWEN3_30B_A3B
+    L = _desc(shape)
+    P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE)
+    wr = W.router_weight(960, shape, std=0.1, device=DEV)
+    wg, wu, wd = _weights(shape, 961)
+    trees = [W.eagle_tree(962 + i) for i in range(6)]
+    xs = [W.hidden_states(970 + i, t.parent, shape.d, torch.bfloat16).to(DEV)
+          for i, t in enumerate(trees)]
+    deps = [torch.from_numpy(t.depth.copy()).to(DEV) for t in trees]
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    wss = [M.workspace(L, 1, 65), M.workspace(L, 1, 65)]
+    ys = [torch.empty(t.N, shape.d, dtype=torch.bfloat16, device=DEV) for t in trees]
+    idx = [torch.empty(t.N, shape.k, dtype=torch.int32, device=DEV) for t in trees]
+    opts = M.run_opts(M.MOE_FFN_TCGEN05, ffn_max_ctas=cap)
+    streams[1].wait_stream(streams[0])
+    for i, t in enumerate(trees):
+        M.moe_tree_forward(L, P, xs[i], wr, wg, wu, wd, None, deps[i], 1, t.N, None, ys[i],
+                           wss[i % 2], M.tree_outputs(topk_idx=idx[i]), opts, streams[i % 2])
+    streams[0].wait_stream(streams[1])
+    _sync()
+    for w_ in wss:
+        assert M.moe_workspace_check(w_) == 0
+    ws = M.workspace(L, 1, 65)
+    for i, t in enumerate(trees):
+        y = torch.empty_like(ys[i])
+        i2 = torch.empty_like(idx[i])
+        M.moe_tree_forward(L, P, xs[i], wr, wg, wu, wd, None, deps[i], 1, t.N, None, y, ws,
+                           M.tree_outputs(topk_idx=i2), M.run_opts(M.MOE_FFN_TCGEN05))
+        _sync()
+        assert torch.equal(i2, idx[i]), i
+        assert torch.equal(y, ys[i]), i

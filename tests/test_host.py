@@ -41,7 +41,7 @@ def test_status_strings_and_version():
     assert M.status_str(0) == "ok"
     assert "slot" in M.status_str(M.MOE_ERR_NOSLOT)
     assert M.status_str(12345) == "unknown status"
-    assert M.lib().moe_abi_version() == 201
+    assert M.lib().moe_abi_version() == 202
 
 
 def test_workspace_bytes():
