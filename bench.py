@@ -1223,7 +1223,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--slots", type=int, default=48)
     ap.add_argument("--batches", default="1,4,16,64")
-    ap.add_argument("--pair-free-sms", type=int, default=16,
+    ap.add_argument("--pair-free-sms", type=int, default=8,
                     help="SMs the expert kernel leaves free when two blocks are in flight")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
