@@ -753,6 +753,31 @@ def run_stack48(args):
     torch.cuda.synchronize(dev)
     ffn_s = sum(a.elapsed_time(b) for row in ev for a, b in row) / 1e3
     union = (counts.cpu().numpy() > 0).sum(axis=2)  # [K, NL]
+
+    # two trees in flight (two requests): even trees on this stream, odd ones on a second,
+    # each with its own hidden state and workspace, the expert kernel capped to leave
+    # --pair-free-sms SMs to the other tree's routing kernels
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cap = max(1, nsm - args.pair_free_sms)
+    s2 = torch.cuda.Stream(dev)
+    x2 = torch.empty_like(x)
+    ws2 = M.workspace(L, 1, N, device=dev)
+    popts = M.run_opts(args.ffn_path, residual=True, norm_input=True, ffn_max_ctas=cap)
+
+    def pair_steps(n):
+        s2.wait_stream(s)
+        for i in range(n):
+            st, xb, wsb = (s, x, ws) if i % 2 == 0 else (s2, x2, ws2)
+            with torch.cuda.stream(st):
+                xb.copy_(xs[i % TREES])
+            for wr, wg, wu, wd in layers:
+                M.moe_tree_forward(L, P, xb, wr, wg, wu, wd, None, deps[i % TREES], 1, N, None,
+                                   xb, wsb, None, popts, st)
+        s.wait_stream(s2)
+
+    pair_steps(Wm)
+    torch.cuda.synchronize(dev)
+    sec_pair = _timed(lambda: pair_steps(K), dev, world)
     algo = float((union * shape.expert_bytes).sum() + K * NL * 2 * N * shape.d * 2)
     peak, kind = measured_peaks()
     if rank == 0:
@@ -764,6 +789,8 @@ def run_stack48(args):
                      "expert_bytes_resident_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1),
                      "l2": "inputs larger than L2 (0.7 GB of union weights per layer)"},
                     per_layer_blocks_per_s=round(whole_job_rate(K, world, sec) * NL, 1),
+                    two_blocks_in_flight={"value": round(whole_job_rate(K, world, sec_pair), 3),
+                                          "streams": 2, "ffn_ctas": cap},
                     roofline={"bound": "hbm", "achieved": round(algo / ffn_s / 1e9, 1),
                               "peak": peak, "unit": "GB/s",
                               "frac": round(algo / ffn_s / 1e9 / peak, 4), "peak_kind": kind,
