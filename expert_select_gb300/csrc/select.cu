@@ -281,17 +281,22 @@ __device__ PhaseB phase_b(const SelectArgs &a, int E, int k, const T *D, const i
     const int F_ = m - nA;
     int in = 0;
     {
-        const int rnk = rank_of<T>(rk, ec, E, per, pe, true);  // every thread
         const bool cand = e < E && rk[ec] >= T(0);
-        if (e < E) in = inA[e] || (cand && rnk < F_);
-        if (!exact && cand && pe == 0) {
-            if (rnk == F_ - 1) cut[0] = rk[ec];
-            if (rnk == F_) cut[1] = rk[ec];
+        const int ncand = __syncthreads_count(cand && pe == 0);
+        if (F_ > 0 && F_ < ncand) {  // uniform: rank the candidates, keep the first F_
+            const int rnk = rank_of<T>(rk, ec, E, per, pe, true);  // every thread
+            if (e < E) in = inA[e] || (cand && rnk < F_);
+            if (!exact && cand && pe == 0) {
+                if (rnk == F_ - 1) cut[0] = rk[ec];
+                if (rnk == F_) cut[1] = rk[ec];
+            }
+            __syncthreads();  // rk is rewritten below
+            if (!exact)
+                sure = sure && (float)cut[0] * (1.f - dD - 2.f * kU) - dA >
+                                   (float)cut[1] * (1.f + dD + 2.f * kU) + dA;
+        } else if (e < E) {  // every candidate fits (or none does): no ranking needed
+            in = inA[e] || (cand && F_ > 0);
         }
-        const int ncand = __syncthreads_count(cand && pe == 0);  // rk is rewritten below
-        if (!exact && F_ > 0 && F_ < ncand)
-            sure = sure && (float)cut[0] * (1.f - dD - 2.f * kU) - dA >
-                               (float)cut[1] * (1.f + dD + 2.f * kU) + dA;
     }
     if (e < E && pe == 0) inS[e] = in;
     int removed = 0;
