@@ -817,7 +817,9 @@ def run_offload(args):
     mode: H2D bytes, hit rate, and the share of the step the compute stream spent waiting
     for uploads ("AcceptMoE" news article, section 03: 65-78% under Standard SD, 27-35%
     with AcceptMoE, on an RTX 5090 over PCIe). Each step ends with a host read of that
-    step's wait events."""
+    step's wait events. The three modes run interleaved, step by step (each with its own
+    residency table and slot pools, in rotating order), so that the host link of a shared
+    machine, whose rate drifts over minutes, affects them alike."""
     import torch
     from expert_select_gb300 import moetree as M
     from expert_select_gb300 import workload as W
@@ -828,6 +830,9 @@ def run_offload(args):
     seed = SEED + 3000 + 7919 * rank
     xs_h, deps_h = make_trees(TREES, shape, seed)
     xs, deps = xs_h.to(dev), deps_h.to(dev).int()
+    modes = (("natural", M.MOE_ROUTE_NATURAL, False),
+             ("acceptmoe", M.MOE_ROUTE_ACCEPT, False),
+             ("acceptmoe+prune", M.MOE_ROUTE_ACCEPT, True))
     t0 = time.perf_counter()
     layers = []
     for l in range(NL):
@@ -837,9 +842,10 @@ def run_offload(args):
         for h, w in zip(host, (wg, wu, wd)):
             h.copy_(w)
         del wg, wu, wd
-        pools = [torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
-                 torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
-                 torch.empty(slots, shape.d, shape.f, dtype=torch.bfloat16, device=dev)]
+        pools = [[torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
+                  torch.empty(slots, shape.f, shape.d, dtype=torch.bfloat16, device=dev),
+                  torch.empty(slots, shape.d, shape.f, dtype=torch.bfloat16, device=dev)]
+                 for _ in modes]
         layers.append((wr, host, pools))
     torch.cuda.empty_cache()
     setup_s = time.perf_counter() - t0
@@ -857,41 +863,49 @@ def run_offload(args):
     x = torch.empty_like(xs[0])
     side = torch.cuda.Stream(dev)
     K, Wm = args.steps, args.warmup
-    results = {}
-    for name, mode, prune in (("natural", M.MOE_ROUTE_NATURAL, False),
-                              ("acceptmoe", M.MOE_ROUTE_ACCEPT, False),
-                              ("acceptmoe+prune", M.MOE_ROUTE_ACCEPT, True)):
+    opts = M.run_opts(residual=True, norm_input=True)
+    state = []
+    for name, mode, prune in modes:
         P = M.select_params(mode, W.C_EAGLE, prune=prune, reroute_budget=8, min_set=16)
-        table = M.Residency(n_layers=NL, E=shape.E, slots=slots)
-        stats = []
-        waits = []
+        state.append({"name": name, "P": P, "stats": [], "waits": [], "sec": 0.0,
+                      "table": M.Residency(n_layers=NL, E=shape.E, slots=slots)})
 
-        def step(i, keep):
-            x.copy_(xs[i % TREES])
-            for l, (wr, host, pools) in enumerate(layers):
-                st = M.moe_offload_forward(Ls, P, x, wr, *host, *pools, table, l,
-                                           deps[i % TREES], 1, N, x, ws,
-                                           opts=M.run_opts(residual=True, norm_input=True),
-                                           side_stream=side)
-                if keep:
-                    stats.append((st.needed, st.hits, st.uploads, st.h2d_bytes, st.passes))
-            if keep:  # the compute stream's upload waits of this step, layer by layer
-                waits.append(sum(table.upload_wait(l)[0] for l in range(NL)))
+    def step(m, i, keep):
+        st_ = state[m]
+        x.copy_(xs[i % TREES])
+        for l, (wr, host, pools) in enumerate(layers):
+            st = M.moe_offload_forward(Ls, st_["P"], x, wr, *host, *pools[m], st_["table"], l,
+                                       deps[i % TREES], 1, N, x, ws, opts=opts,
+                                       side_stream=side)
+            if keep:
+                st_["stats"].append((st.needed, st.hits, st.uploads, st.h2d_bytes, st.passes))
+        if keep:  # the compute stream's upload waits of this step, layer by layer
+            st_["waits"].append(sum(st_["table"].upload_wait(l)[0] for l in range(NL)))
 
-        for i in range(Wm):
-            step(i, False)
-        sec = _timed(lambda: [step(i, True) for i in range(K)], dev, world)
-        a = np.array(stats, dtype=np.float64)
-        results[name] = {"tree_blocks_per_s": round(K / sec, 3),
-                         "ms_per_step": round(sec / K * 1e3, 3),
-                         "needed_per_layer": round(float(a[:, 0].mean()), 2),
-                         "hit_rate": round(float(a[:, 1].sum() / a[:, 0].sum()), 4),
-                         "uploads_per_layer": round(float(a[:, 2].mean()), 2),
-                         "h2d_gb_per_step": round(float(a[:, 3].sum()) / K / 1e9, 3),
-                         "passes_per_layer": round(float(a[:, 4].mean()), 2),
-                         "upload_wait_ms_per_step": round(float(np.mean(waits)), 3),
-                         "upload_wait_frac": round(float(np.sum(waits) / 1e3 / sec), 4)}
-        table.close()
+    for i in range(Wm):
+        for m in range(len(modes)):
+            step(m, i, False)
+    for i in range(K):
+        for j in range(len(modes)):
+            m = (i + j) % len(modes)
+            state[m]["sec"] += _timed(lambda: step(m, i, True), dev, world)
+    results = {}
+    for st_ in state:
+        a = np.array(st_["stats"], dtype=np.float64)
+        sec, waits = st_["sec"], st_["waits"]
+        h2d = float(a[:, 3].sum()) / K
+        results[st_["name"]] = {
+            "tree_blocks_per_s": round(K / sec, 3),
+            "ms_per_step": round(sec / K * 1e3, 3),
+            "needed_per_layer": round(float(a[:, 0].mean()), 2),
+            "hit_rate": round(float(a[:, 1].sum() / a[:, 0].sum()), 4),
+            "uploads_per_layer": round(float(a[:, 2].mean()), 2),
+            "h2d_gb_per_step": round(h2d / 1e9, 3),
+            "passes_per_layer": round(float(a[:, 4].mean()), 2),
+            "upload_wait_ms_per_step": round(float(np.mean(waits)), 3),
+            "upload_wait_frac": round(float(np.sum(waits) / 1e3 / sec), 4),
+            "upload_gbs_while_waiting": round(h2d / max(float(np.mean(waits)) / 1e3, 1e-9) / 1e9, 1)}
+        st_["table"].close()
     nat = results["natural"]
     for name in ("acceptmoe", "acceptmoe+prune"):
         r = results[name]
@@ -908,6 +922,7 @@ def run_offload(args):
                      "layers": NL, "slots": slots, "router_std": args.router_std,
                      "block": "x + MoE(rmsnorm(x))",
                      "routing": "acceptmoe + residency-aware pruning (budget 8, min 16)",
+                     "modes_interleaved": True,
                      "host_store_gb": round(NL * shape.E * shape.expert_bytes / 1e9, 1)},
                     modes=results, h2d_link_gbs=round(link_gbs, 1), setup_s=round(setup_s, 1)))
 
