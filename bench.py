@@ -1249,7 +1249,9 @@ def run_crossover(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 5000; 200 for stack48 and offload, the "
+                         "verification steps those workloads are defined over)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--routing", choices=["acceptmoe", "natural"], default="acceptmoe")
@@ -1268,6 +1270,8 @@ def main(argv=None):
     ap.add_argument("--pair-free-sms", type=int, default=8,
                     help="SMs the expert kernel leaves free when two blocks are in flight")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 200 if args.workload in ("stack48", "offload") else 5000
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)
