@@ -636,6 +636,43 @@ def test_expert_forward_at_the_largest_width(path):
     _assert_close_rows(y.float().cpu().numpy()[rows], ref, shape)
 
 
+def _assignments_with_counts(counts, R, k):
+    """int32 [R, k] routing in which expert e takes exactly counts[e] assignments (sum =
+    R * k, no count above R / 2 when k = 2), every row's experts distinct: the sorted list
+    of expert ids, row r taking entries r, r + R, ... of it."""
+    flat = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    assert flat.size == R * k
+    idx = np.stack([flat[j * R:(j + 1) * R] for j in range(k)], axis=1)
+    assert all(len(set(row)) == k for row in idx.tolist())
+    return np.ascontiguousarray(idx)
+
+
+@pytest.mark.parametrize("counts", [
+    [256, 257, 384, 385, 700, 17, 0, 201],     # one tile of 256, equal tiles from 257 on
+    [16, 300, 1000, 384, 96, 368, 0, 36],      # a hot expert in four tiles
+    [256, 1, 512, 1, 255, 1, 510, 0]])         # full tiles next to one-token tiles
+def test_expert_forward_exact_expert_loads(counts):
+    """Experts with exactly the given numbers of tokens on the tensor-core path, around the
+    256-token row-tile limit: a full 256-token tile (N = 256), experts of 257 tokens and
+    more in near-equal tiles that share their weight loads, a hot expert in four tiles,
+    one-token tiles, an expert with no tokens; every row against the oracle."""
+    shape = W.LayerShape(d=256, E=8, k=2, f=192, dtype="bf16")
+    R = sum(counts) // 2
+    L = _desc(shape)
+    wg, wu, wd = _weights(shape, 51)
+    x = W.hidden_states(52, np.arange(-1, R - 1, dtype=np.int32), shape.d, torch.bfloat16)
+    idx = _assignments_with_counts(counts, R, 2)
+    gates = W.random_gates(54, R, 2)
+    y = torch.full((R, shape.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = M.workspace(L, 1, R)
+    M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, torch.from_numpy(idx).to(DEV),
+                         torch.from_numpy(gates).to(DEV), y, ws, M.run_opts(M.MOE_FFN_TCGEN05))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64))
+    _assert_close_rows(y.float().cpu().numpy(), ref, shape)
+
+
 def test_selection_cluster_at_its_largest_tree():
     """256 nodes (the largest tree the 8-CTA cluster takes), E = 256, k = 16: the launch
     with the most shared memory (logit rows, fp32 and fp64 demand terms of 32 nodes per
