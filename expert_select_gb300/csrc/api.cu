@@ -121,7 +121,7 @@ moe_status run_ffn(const moe_layer_desc &L, const void *x, const void *Wg, const
     fa.sched = at<int>(ws, w.sched);
     fa.xp = at<void>(ws, w.xp);
     fa.h = at<void>(ws, w.h);
-    fa.o = at<float>(ws, w.o);
+    fa.o = at<void>(ws, w.o);
     fa.max_ctas = opts ? opts->ffn_max_ctas : 0;
 
     const int path = resolve_ffn_path(L, opts);
@@ -145,7 +145,7 @@ int resolve_ffn_path(const moe_layer_desc &L, const moe_run_opts *opts) {
 
 moe_status run_combine(const moe_layer_desc &L, const void *residual, const float *gates, int R,
                        void *y, void *ws, const Workspace &w, cudaStream_t s) {
-    return cuda_status(launch_combine(L, at<float>(ws, w.o), at<int>(ws, w.pos), gates, residual,
+    return cuda_status(launch_combine(L, at<void>(ws, w.o), at<int>(ws, w.pos), gates, residual,
                                       R, y, s));
 }
 

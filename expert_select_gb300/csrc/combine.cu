@@ -1,6 +1,7 @@
 // Unpermute + weighted combine ("MoE and speculative decoding" blog, pipeline step
 // "unpermute + weighted combine"): y[r] = sum_j gates[r, j] O[pos(r, j)], slots in
-// ascending j, fp32 accumulation, rounded once to the layer dtype. With a residual
+// ascending j, fp32 accumulation, rounded once to the layer dtype. The expert outputs O
+// arrive in the layer dtype (bf16 layers: rounded once from the experts' fp32 sums). With a residual
 // input the sum starts from it (y = x + MoE(x), as in a stack of layers).
 //
 // Also holds the small kernel that publishes a residency table to the device.
@@ -39,11 +40,24 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
 
+// The same through the read-only cache (for the expert outputs, never written here).
+template <typename TO>
+__device__ __forceinline__ float4 ldg4(const TO *p);
+template <>
+__device__ __forceinline__ float4 ldg4<float>(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+template <>
+__device__ __forceinline__ float4 ldg4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+
 // `res` (may be null, may alias y) is added first: y = res + sum_j g_j O_j, over the slots
 // in ascending j. A thread per 4 columns of a row.
 template <typename TO>
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
+combine_kernel(const TO *__restrict__ o, const int *__restrict__ pos,
                const float *__restrict__ gates, const TO *res, int d, int k, TO *y) {
     pdl_wait();
     const int r = blockIdx.x;
@@ -54,7 +68,7 @@ combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
         const int p = pos[r * k + j];
         if (p < 0) continue;
         const float g = gates[r * k + j];
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(o + (size_t)p * d + c));
+        const float4 v = ldg4<TO>(o + (size_t)p * d + c);
         acc.x = fmaf(g, v.x, acc.x);
         acc.y = fmaf(g, v.y, acc.y);
         acc.z = fmaf(g, v.z, acc.z);
@@ -69,7 +83,7 @@ combine_kernel(const float *__restrict__ o, const int *__restrict__ pos,
 // blocks keep the kernel above: its fewer registers let more threads stream.
 template <typename TO, int KMAX>
 __global__ void __launch_bounds__(kThreads)
-combine_small_kernel(const float *__restrict__ o, const int *__restrict__ pos,
+combine_small_kernel(const TO *__restrict__ o, const int *__restrict__ pos,
                      const float *__restrict__ gates, const TO *res, int d, int k, TO *y) {
     pdl_wait();
     const int r = blockIdx.x;
@@ -86,7 +100,7 @@ combine_small_kernel(const float *__restrict__ o, const int *__restrict__ pos,
     float4 v[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-        if (p[j] >= 0) v[j] = __ldg(reinterpret_cast<const float4 *>(o + (size_t)p[j] * d + c));
+        if (p[j] >= 0) v[j] = ldg4<TO>(o + (size_t)p[j] * d + c);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
         if (p[j] < 0) continue;
@@ -102,7 +116,7 @@ combine_small_kernel(const float *__restrict__ o, const int *__restrict__ pos,
 constexpr int kSmallCombine = 2048;
 
 template <typename TO>
-cudaError_t launch_combine_t(const float *o, const int *pos, const float *gates,
+cudaError_t launch_combine_t(const TO *o, const int *pos, const float *gates,
                              const TO *res, int R, int d, int k, TO *y, cudaStream_t s) {
     const dim3 grid(R, (d / 4 + kThreads - 1) / kThreads);
     if (R * k <= kSmallCombine) {
@@ -131,14 +145,15 @@ __global__ void publish_kernel(PublishArgs p, int E, int *slot, uint8_t *res) {
 
 }  // namespace
 
-cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
+cudaError_t launch_combine(const moe_layer_desc &L, const void *o, const int *pos,
                            const float *gates, const void *residual, int R, void *y,
                            cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
     if (L.dtype == MOE_DTYPE_BF16)
-        return launch_combine_t(o, pos, gates, (const __nv_bfloat16 *)residual, R, L.d, L.k,
-                                (__nv_bfloat16 *)y, s);
-    return launch_combine_t(o, pos, gates, (const float *)residual, R, L.d, L.k, (float *)y, s);
+        return launch_combine_t((const __nv_bfloat16 *)o, pos, gates,
+                                (const __nv_bfloat16 *)residual, R, L.d, L.k, (__nv_bfloat16 *)y, s);
+    return launch_combine_t((const float *)o, pos, gates, (const float *)residual, R, L.d, L.k,
+                            (float *)y, s);
 }
 
 cudaError_t launch_publish(int E, const int *slot_host, const uint8_t *res_host, int *slot_dev,

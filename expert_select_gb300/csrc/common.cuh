@@ -129,13 +129,13 @@ struct FfnArgs {
     int *sched;          // tensor-core path: ticket + row-tile counters
     void *xp;            // gathered x (tensor-core path)
     void *h;             // activations
-    float *o;            // expert outputs, permuted order
+    void *o;             // expert outputs, permuted order, in the layer dtype
 };
 cudaError_t launch_ffn_simt(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s);
 bool ffn_tc_supported(const moe_layer_desc &L);
 
-cudaError_t launch_combine(const moe_layer_desc &L, const float *o, const int *pos,
+cudaError_t launch_combine(const moe_layer_desc &L, const void *o, const int *pos,
                            const float *gates, const void *residual, int R, void *y,
                            cudaStream_t s);
 

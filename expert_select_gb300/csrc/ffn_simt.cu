@@ -85,6 +85,10 @@ template <> struct Raw8<float> {
     }
 };
 
+// Stores an fp32 result in the layer dtype (bf16: rounded to nearest even).
+__device__ __forceinline__ void store_as(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_as(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
 __device__ __forceinline__ float dot8(const float w[8], const float *x) {
     const float4 a = reinterpret_cast<const float4 *>(x)[0];
     const float4 b = reinterpret_cast<const float4 *>(x)[1];
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffn_down_simt(FfnArgs a) {
         }
         const float v = warp_transpose_sum32(acc);
         const int r = lane >> 3, t = lane & 7;
-        if (t < nt && i0 + r < d) a.o[(size_t)(off + t0 + t) * d + i0 + r] = v;
+        if (t < nt && i0 + r < d) store_as(static_cast<T *>(a.o) + (size_t)(off + t0 + t) * d + i0 + r, v);
     }
 }
 

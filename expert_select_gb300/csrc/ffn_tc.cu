@@ -1,7 +1,7 @@
 // Grouped SwiGLU experts on the 5th-generation tensor cores (tcgen05 + TMA + TMEM)
 // ("MoE and speculative decoding" blog, "grouped GEMM for active experts"):
 //   phase 1  h   = silu(X_e W_gate[e]^T) * (X_e W_up[e]^T)      (bf16 out)
-//   phase 2  O_e = h W_down[e]^T                                (fp32 out)
+//   phase 2  O_e = h W_down[e]^T                                (bf16 out)
 // for every expert e with assignments, X_e its token rows in permuted order.
 //
 // A verification block routes only ~4-20 tokens to an expert, so the weights are
@@ -79,8 +79,7 @@ struct Params {
     const uint8_t *pass;  // experts computed by this launch (null: all)
     int *flags;
     int *sched;    // [0] ticket counter, [1 + rt] finished phase-1 units of row tile rt
-    __nv_bfloat16 *h;
-    float *o;
+    __nv_bfloat16 *h, *o;
 };
 
 // Named barriers (bar.sync is warp-aligned: reconverge first): one per epilogue team of
@@ -454,11 +453,12 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
                     if (drow < p.d) {
-                        float *op = p.o + row0 * p.d + drow;
+                        __nv_bfloat16 *op = p.o + row0 * p.d + drow;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int tok = c0 + c;
-                            if (tok < w.ntok) op[(size_t)tok * p.d] = __uint_as_float(v[c]);
+                            if (tok < w.ntok)
+                                op[(size_t)tok * p.d] = __float2bfloat16_rn(__uint_as_float(v[c]));
                         }
                     }
                 }
@@ -619,7 +619,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.flags = a.flags;
     p.sched = a.sched;
     p.h = (__nv_bfloat16 *)a.h;
-    p.o = a.o;
+    p.o = (__nv_bfloat16 *)a.o;
     const int ctas = a.max_ctas > 0 ? std::min(nsm, a.max_ctas) : nsm;
     return launch_pdl(ffn_tc_kernel, dim3(ctas), dim3(kThreads), smem, s, m, p);
 }
