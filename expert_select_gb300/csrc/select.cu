@@ -1172,17 +1172,32 @@ WeightPrefetch sized(WeightPrefetch pf, int used, int avail, int per_slot) {
     return pf;
 }
 
+// Dynamic shared memory of the cluster kernel for N-node trees: w64 [slots][E] doubles; wt
+// and lrow [slots][E]; nat_all and fin_all [N][k]; nat_loc and nat_val [slots][k].
+size_t cluster_smem(const moe_layer_desc &L, int N) {
+    const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
+    return (size_t)slots * L.E * sizeof(double) +
+        ((size_t)2 * slots * L.E + (size_t)2 * N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
+}
+
+// Whether B clusters of the kernel for this layer run in at most three waves. The kernel's
+// shared-memory limit is raised first, so the occupancy query sees the launch as it will be.
+bool clusters_in_three_waves(const moe_layer_desc &L, int B, int N) {
+    const size_t smem = cluster_smem(L, N);
+    if (L.E <= 128)
+        return allow_smem(select_cluster_kernel<4>, cluster4_smem_set, smem) == cudaSuccess &&
+               B <= 3 * active_clusters(select_cluster_kernel<4>, kCThreads, smem);
+    return allow_smem(select_cluster_kernel<8>, cluster8_smem_set, smem) == cudaSuccess &&
+           B <= 3 * active_clusters(select_cluster_kernel<8>, kCThreads, smem);
+}
+
 // One 8-CTA cluster per tree (+ the prefetch CTAs), VPL logits per lane (E <= 32 VPL).
 template <int VPL>
 cudaError_t launch_cluster(const moe_layer_desc &L, const SelectArgs &a, const float *logits,
                            const int *depth, int B, int N, const uint8_t *resident, int *idx,
                            float *gates, uint8_t *elig, int *info, WeightPrefetch pf,
                            PermuteOut po, std::atomic<size_t> &smem_set, cudaStream_t s) {
-    const int slots = ((N + kCC * kCW - 1) / (kCC * kCW)) * kCW;
-    // w64 [slots][E] doubles; wt and lrow [slots][E]; nat_all and fin_all [N][k]; nat_loc
-    // and nat_val [slots][k]
-    const size_t smem = (size_t)slots * L.E * sizeof(double) +
-        ((size_t)2 * slots * L.E + (size_t)2 * N * L.k + (size_t)2 * slots * L.k) * sizeof(float);
+    const size_t smem = cluster_smem(L, N);
     cudaError_t err = allow_smem(select_cluster_kernel<VPL>, smem_set, smem);
     if (err != cudaSuccess) return err;
     if (pf.ctas > 0)
@@ -1230,7 +1245,12 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
         if (err == cudaSuccess && permuted) *permuted = po.counts != nullptr;
         return err;
     }
-    if (N <= kClusterMaxN) {
+    // trees of up to kClusterMaxN nodes take a cluster each while the clusters run in at
+    // most three waves; more trees than that take the one-CTA kernel, one CTA per tree in
+    // one wave. Measured on GB300 (65-node trees, Qwen3-30B-A3B-shaped layer): at 48 and 64
+    // trees per block (more than three waves of clusters) the one-CTA kernel made the block
+    // 1.2% and 2.5% faster, at 16-32 trees (one to three waves) up to 2.4% slower.
+    if (N <= kClusterMaxN && (B == 1 || clusters_in_three_waves(L, B, N))) {
         // a block of one tree: the cluster also performs the permute step
         const PermuteOut po = (B == 1 && po_in.counts) ? po_in : PermuteOut{};
         const cudaError_t err =
