@@ -9,7 +9,9 @@ tree against the fp64 oracle on the device's logits (a tree whose fp64 decision 
 a tie is checked for validity instead); counts and offsets exactly; every row of y against
 the oracle's experts and combine on the device's routing (2e-2 * max|ref| for bf16, 1e-4
 for fp32). The cases cover expert counts that are not multiples of 32, k from 1 to 16,
-blocks of one to three trees and trees of 2 to 65 nodes.
+blocks of one to three trees and trees of 2 to 65 nodes. A second set draws blocks of 4 to
+80 trees of one random shape (up to ~5000 rows), with the router and y checked on sampled
+rows.
 """
 import numpy as np
 import pytest
@@ -117,4 +119,86 @@ def test_random_layer_against_oracle(seed):
     ref_y = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"])
     tol = 2e-2 if shape.dtype == "bf16" else 1e-4
     err = np.abs(y.double().cpu().numpy() - ref_y).max()
+    assert err <= tol * np.abs(ref_y).max(), (c, err)
+
+
+def _draw_large(seed):
+    rng = np.random.default_rng(9000 + seed)
+    dtype = "bf16" if rng.random() < 0.85 else "fp32"
+    d = int(rng.choice([256, 512, 1024]))
+    f = int(rng.choice([128, 256, 384]))
+    E = int(rng.choice([32, 64, 100, 128, 160, 256]))
+    k = int(rng.integers(1, min(16, E) + 1))
+    B = int(rng.integers(4, 81))
+    steps = int(rng.integers(2, 6))
+    topk = int(rng.integers(4, 11))
+    tokens = int(min(rng.integers(16, 65), topk + (steps - 1) * topk * topk))
+    mode = str(rng.choice(["natural", "accept", "accept", "fixed"]))
+    prune = mode != "natural" and bool(rng.random() < 0.4)
+    return dict(dtype=dtype, d=d, f=f, E=E, k=k, B=B, steps=steps, topk=topk, tokens=tokens,
+                mode=mode, anchor=bool(rng.random() < 0.8), prune=prune,
+                std=float(rng.choice([0.02, 0.1, 0.3])),
+                fixed_B=int(rng.integers(k, E + 1)), min_set=int(rng.integers(k, max(k, 24) + 1)),
+                budget=int(rng.integers(0, 10)), resident=(rng.random(E) < 0.5).astype(np.uint8))
+
+
+@pytest.mark.parametrize("seed", list(range(48)))
+def test_random_large_block_against_oracle(seed):
+    """Blocks of 4 to 80 trees (up to ~5000 rows) of random layers: the tensor-core router,
+    the selection of many trees per launch (clusters, or one CTA per tree past three waves
+    of clusters), the many-CTA permute, experts with hundreds of tokens in several row
+    tiles; the same checks as above, y on 48 sampled rows."""
+    c = _draw_large(seed)
+    shape = W.LayerShape(d=c["d"], E=c["E"], k=c["k"], f=c["f"], dtype=c["dtype"])
+    E, B = c["E"], c["B"]
+    tree = W.eagle_tree(9100 + seed, steps=c["steps"], topk=c["topk"], draft_tokens=c["tokens"])
+    N = tree.N
+    depth = np.tile(tree.depth.astype(np.int32), (B, 1))
+    R = B * N
+    x = torch.cat([W.hidden_states(9200 + 131 * seed + b, tree.parent, shape.d,
+                                   shape.torch_dtype) for b in range(B)])
+    wr = W.router_weight(9300 + seed, shape, std=c["std"], device=DEV)
+    wg, wu, wd = W.expert_weights(9400 + seed, shape, device=DEV)
+    mode = {"natural": M.MOE_ROUTE_NATURAL, "accept": M.MOE_ROUTE_ACCEPT,
+            "fixed": M.MOE_ROUTE_FIXED_B}[c["mode"]]
+    P = M.select_params(mode, W.C_EAGLE, anchor=c["anchor"], prune=c["prune"],
+                        reroute_budget=c["budget"], min_set=c["min_set"],
+                        fixed_B=c["fixed_B"] if c["mode"] == "fixed" else 0)
+    L = M.layer_desc(shape.d, E, shape.k, shape.f, shape.dtype)
+    out = dict(logits=torch.empty(R, E, device=DEV),
+               topk_idx=torch.empty(R, shape.k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(R, shape.k, device=DEV),
+               eligible=torch.empty(B, E, dtype=torch.uint8, device=DEV),
+               info=torch.empty(B, NF, dtype=torch.int32, device=DEV),
+               counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV))
+    res = torch.from_numpy(c["resident"]).to(DEV) if c["prune"] else None
+    y = torch.full((R, shape.d), float("nan"), dtype=shape.torch_dtype, device=DEV)
+    ws = M.workspace(L, B, N)
+    M.moe_tree_forward(L, P, x.to(DEV), wr, wg, wu, wd, None,
+                       torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
+                       M.tree_outputs(**out), M.run_opts(M.MOE_FFN_AUTO))
+    torch.cuda.synchronize()
+    assert M.moe_workspace_check(ws) == 0
+    got = {key: v.cpu().numpy() for key, v in out.items()}
+    rows = np.random.default_rng(seed).choice(R, min(R, 256), replace=False)
+    ref_l = O.router(x[rows], wr.cpu())
+    assert (np.abs(got["logits"][rows] - ref_l) <=
+            1e-4 * np.abs(ref_l).max(axis=1, keepdims=True)).all()
+    omode = {"natural": O.NATURAL, "accept": O.ACCEPT, "fixed": O.FIXED_B}[c["mode"]]
+    kw = dict(mode=omode, c=W.C_EAGLE, anchor=c["anchor"])
+    if c["mode"] == "fixed":
+        kw["fixed_B"] = c["fixed_B"]
+    if c["prune"]:
+        kw.update(prune=True, resident=c["resident"], budget=c["budget"], min_set=c["min_set"])
+    _check_selection(shape, kw, got["logits"], depth, got["topk_idx"], got["gates"],
+                     got["eligible"], got["info"], N, B)
+    rc, ro, _ = O.permute(got["topk_idx"], E)
+    np.testing.assert_array_equal(got["counts"], rc)
+    np.testing.assert_array_equal(got["offsets"], ro)
+    sample = np.random.default_rng(seed + 1).choice(R, 48, replace=False).tolist()
+    ref_y = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"],
+                          rows=sample)
+    tol = 2e-2 if shape.dtype == "bf16" else 1e-4
+    err = np.abs(y.double().cpu().numpy()[sample] - ref_y).max()
     assert err <= tol * np.abs(ref_y).max(), (c, err)
