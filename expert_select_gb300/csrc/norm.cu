@@ -5,12 +5,18 @@
 // learned weight. The mean of squares and the scale are computed in fp64 (the squares of
 // fp32 / bf16 values are exact in fp64), and each element x * scale is rounded once to the
 // layer dtype.
+//
+// GB300's fp64 rate is a small fraction of its fp32 rate (~2 fp64 operations per clock per
+// SM), so the ~4 fp64 operations per element are spread over as many SMs as there are rows:
+// a CTA of 256 threads per row, 8 elements per thread per 2048 columns. (A warp per row put
+// a 65-row block on 9 SMs and took ~31 us; measured on GB300.)
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kNormWarps = 8;
+constexpr int kNormThreads = 256;
+constexpr int kNormWarps = kNormThreads / 32;
 
 __device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
@@ -42,26 +48,31 @@ __device__ __forceinline__ void store_scaled<float>(float *p, const float v[8], 
     reinterpret_cast<float4 *>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 
-// A warp per row: 8-element slices per lane, the sum of squares in fp64.
+// A CTA per row: 8-element slices per thread, the sum of squares in fp64 (per thread, then
+// over the warp, then over the CTA's warps in warp order).
 template <typename T>
-__global__ void __launch_bounds__(kNormWarps * 32)
+__global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict__ xn) {
     pdl_wait();
-    const int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= R) return;  // no block-wide barrier follows
+    __shared__ double part[kNormWarps];
+    const int row = blockIdx.x, tid = threadIdx.x;
     const T *xr = x + (size_t)row * d;
     double s = 0.0;
-    for (int c = lane * 8; c < d; c += 256) {
+    for (int c = tid * 8; c < d; c += kNormThreads * 8) {
         float v[8];
         Vec8<T>::load(xr + c, v);
 #pragma unroll
         for (int q = 0; q < 8; ++q) s = __dadd_rn(s, __dmul_rn((double)v[q], (double)v[q]));
     }
     s = warp_sum_d(s);
-    const double scale = 1.0 / sqrt(s / (double)d + eps);
+    if ((tid & 31) == 0) part[tid >> 5] = s;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < kNormWarps; ++w) tot = __dadd_rn(tot, part[w]);
+    const double scale = 1.0 / sqrt(tot / (double)d + eps);
     T *out = xn + (size_t)row * d;
-    for (int c = lane * 8; c < d; c += 256) {
+    for (int c = tid * 8; c < d; c += kNormThreads * 8) {
         float v[8];
         Vec8<T>::load(xr + c, v);
         store_scaled<T>(out + c, v, scale);
@@ -73,11 +84,11 @@ rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict_
 cudaError_t launch_rmsnorm(const moe_layer_desc &L, const void *x, int R, void *xn,
                            cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    const dim3 grid((R + kNormWarps - 1) / kNormWarps);
+    const dim3 grid(R);
     if (L.dtype == MOE_DTYPE_BF16)
-        return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, grid, dim3(kNormWarps * 32), 0, s,
+        return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, grid, dim3(kNormThreads), 0, s,
                           (const __nv_bfloat16 *)x, R, L.d, kNormEps, (__nv_bfloat16 *)xn);
-    return launch_pdl(rmsnorm_kernel<float>, grid, dim3(kNormWarps * 32), 0, s, (const float *)x,
+    return launch_pdl(rmsnorm_kernel<float>, grid, dim3(kNormThreads), 0, s, (const float *)x,
                       R, L.d, kNormEps, (float *)xn);
 }
 
