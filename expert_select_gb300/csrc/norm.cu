@@ -4,7 +4,7 @@
 // stack of layers without one lets the residual stream grow until it overflows). No
 // learned weight. The mean of squares and the scale are computed in fp64 (the squares of
 // fp32 / bf16 values are exact in fp64), and each element x * scale is rounded once to the
-// layer dtype.
+// layer dtype (bf16: through an fp32 product where that provably rounds the same).
 //
 // GB300's fp64 rate is a small fraction of its fp32 rate (~2 fp64 operations per clock per
 // SM), so the ~4 fp64 operations per element are spread over as many SMs as there are rows:
@@ -24,19 +24,40 @@ __device__ __forceinline__ double warp_sum_d(double v) {
     return v;
 }
 
+// bf16(fp64(v * scale)), rounded to nearest even, for v an fp32 value. The fp32 product
+// p = v * (float)scale lies within 2^-22.8 |p| of the fp64 product (one rounding of the
+// scale to fp32 and one of the product, 2^-24 relative each); bf16 rounding midpoints are
+// at least 2^-9 |p| apart, so when p is farther than 2^-21 |p| from the midpoint between
+// its two bf16 neighbours, both products round to the same bf16 value and p's rounding is
+// the answer. Otherwise (about one element in 4000, for zero, tiny or non-finite p, and for
+// a scale whose fp32 rounding is not a normal number far from the range ends) the product
+// is formed and rounded in fp64.
+__device__ __forceinline__ uint32_t scaled_bf16(float v, double scale, float scale_f) {
+    const float p = v * scale_f;
+    const float ap = fabsf(p);
+    if (scale_f >= 0x1p-100f && scale_f <= 0x1p+100f && ap >= 0x1p-100f && ap <= 0x1p+100f) {
+        const __nv_bfloat16 lo = __float2bfloat16_rd(p), hi = __float2bfloat16_ru(p);
+        const float flo = __bfloat162float(lo), fhi = __bfloat162float(hi);
+        if (flo == fhi) return __bfloat16_as_ushort(lo);  // p is a bf16 value
+        const float mid = 0.5f * (flo + fhi);              // exact: a 9-bit value
+        const float dist = fabsf(p - mid);                 // exact (Sterbenz)
+        if (dist > ap * 0x1p-21f) return __bfloat16_as_ushort(p < mid ? lo : hi);
+    }
+    return __bfloat16_as_ushort(__double2bfloat16((double)v * scale));
+}
+
 // Stores v[q] * scale, q < 8, rounded once (nearest, ties to even) to T, as 16-byte stores.
 template <typename T> __device__ __forceinline__ void store_scaled(T *p, const float v[8],
                                                                   double scale);
 template <>
 __device__ __forceinline__ void store_scaled<__nv_bfloat16>(__nv_bfloat16 *p, const float v[8],
                                                             double scale) {
+    const float scale_f = __double2float_rn(scale);
     uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t lo = __bfloat16_as_ushort(__double2bfloat16((double)v[2 * q] * scale));
-        const uint32_t hi = __bfloat16_as_ushort(__double2bfloat16((double)v[2 * q + 1] * scale));
-        w[q] = lo | (hi << 16);
-    }
+    for (int q = 0; q < 4; ++q)
+        w[q] = scaled_bf16(v[2 * q], scale, scale_f) |
+               (scaled_bf16(v[2 * q + 1], scale, scale_f) << 16);
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 template <>
@@ -62,7 +83,8 @@ rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict_
         float v[8];
         Vec8<T>::load(xr + c, v);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) s = __dadd_rn(s, __dmul_rn((double)v[q], (double)v[q]));
+        for (int q = 0; q < 8; ++q)  // v^2 is exact in fp64: one fused rounding per add
+            s = __fma_rn((double)v[q], (double)v[q], s);
     }
     s = warp_sum_d(s);
     if ((tid & 31) == 0) part[tid >> 5] = s;
