@@ -7,9 +7,8 @@
 // layer dtype (bf16: through an fp32 product where that provably rounds the same).
 //
 // GB300's fp64 rate is a small fraction of its fp32 rate (~2 fp64 operations per clock per
-// SM), so the ~4 fp64 operations per element are spread over as many SMs as there are rows:
-// a CTA of 256 threads per row, 8 elements per thread per 2048 columns. (A warp per row put
-// a 65-row block on 9 SMs and took ~31 us; measured on GB300.)
+// SM), so the fp64 work is spread over as many SMs as there are rows: a CTA of 256 threads
+// per row. (A warp per row put a 65-row block on 9 SMs and took ~31 us; measured on GB300.)
 #include "common.cuh"
 
 namespace moe {
@@ -18,10 +17,35 @@ namespace {
 constexpr int kNormThreads = 256;
 constexpr int kNormWarps = kNormThreads / 32;
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ double norm_warp_sum(double v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
+}
+
+// Adds v[q]^2, q < 8, to s (v^2 is exact in fp64: one rounding per fused add).
+__device__ __forceinline__ double norm_add_squares(double s, const float v[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s = __fma_rn((double)v[q], (double)v[q], s);
+    return s;
+}
+
+// The row's scale from each thread's partial sum; every thread of the CTA calls it (two
+// block barriers). Thread 0 alone adds the warps' partials and forms the scale (an fp64
+// square root and divide are dozens of fp64 operations), then shares it. part: kNormWarps
+// doubles of shared memory.
+__device__ __forceinline__ double norm_scale(double s, int d, double eps, double *part) {
+    s = norm_warp_sum(s);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+#pragma unroll
+        for (int w = 0; w < kNormWarps; ++w) tot = __dadd_rn(tot, part[w]);
+        part[0] = 1.0 / sqrt(tot / (double)d + eps);
+    }
+    __syncthreads();
+    return part[0];
 }
 
 // bf16(fp64(v * scale)), rounded to nearest even, for v an fp32 value. The fp32 product
@@ -69,8 +93,8 @@ __device__ __forceinline__ void store_scaled<float>(float *p, const float v[8], 
     reinterpret_cast<float4 *>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 
-// A CTA per row: 8-element slices per thread, the sum of squares in fp64 (per thread, then
-// over the warp, then over the CTA's warps in warp order).
+// A CTA per row: the 8-element groups at columns 8 t + 8 kNormThreads j to thread t, its
+// fp64 sum of squares over them, then over the warp, then the warps' partials in order.
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict__ xn) {
@@ -82,17 +106,9 @@ rmsnorm_kernel(const T *__restrict__ x, int R, int d, double eps, T *__restrict_
     for (int c = tid * 8; c < d; c += kNormThreads * 8) {
         float v[8];
         Vec8<T>::load(xr + c, v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)  // v^2 is exact in fp64: one fused rounding per add
-            s = __fma_rn((double)v[q], (double)v[q], s);
+        s = norm_add_squares(s, v);
     }
-    s = warp_sum_d(s);
-    if ((tid & 31) == 0) part[tid >> 5] = s;
-    __syncthreads();
-    double tot = 0.0;
-#pragma unroll
-    for (int w = 0; w < kNormWarps; ++w) tot = __dadd_rn(tot, part[w]);
-    const double scale = 1.0 / sqrt(tot / (double)d + eps);
+    const double scale = norm_scale(s, d, eps, part);
     T *out = xn + (size_t)row * d;
     for (int c = tid * 8; c < d; c += kNormThreads * 8) {
         float v[8];
