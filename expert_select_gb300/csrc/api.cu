@@ -82,7 +82,6 @@ bool select_args(const moe_select_params *P, int k, SelectArgs *a) {
     return true;
 }
 
-bool permute_fits(int R, int E) { return permute_smem_bytes(R, E) <= 227 * 1024; }
 
 moe_status run_permute(const moe_layer_desc &L, const int *idx, int R, void *ws,
                        const Workspace &w, int *counts, int *offsets, int *perm,
@@ -193,7 +192,7 @@ moe_status moe::tree_forward_check(const moe_layer_desc *L, const moe_select_par
         !aligned16(W_down) || !aligned16(y))
         return MOE_ERR_ARG;
     if (a.prune && !resident) return MOE_ERR_ARG;
-    if ((long long)B * N > (1 << 30) || !permute_fits(B * N, L->E)) return MOE_ERR_UNSUPPORTED;
+    if ((long long)B * N > (1 << 30)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -344,7 +343,6 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
                               int *offsets, int *perm, void *workspace, moe_stream_t stream) {
     if (!desc_ok(L) || R < 1 || !topk_idx || !counts || !offsets || !perm || !workspace)
         return MOE_ERR_ARG;
-    if (!permute_fits(R, L->E)) return MOE_ERR_UNSUPPORTED;
     const Workspace w = workspace_layout(*L, 1, R);
     return cuda_status(launch_permute(*L, topk_idx, R, counts, offsets, perm,
                                       at<int>(workspace, w.pos), at<int>(workspace, w.active),
@@ -364,7 +362,6 @@ moe_status moe_expert_forward(const moe_layer_desc *L, const void *x, const void
     if (!aligned16(x) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) ||
         !aligned16(y) || ((uintptr_t)workspace & 255u))
         return MOE_ERR_ARG;
-    if (!permute_fits(R, L->E)) return MOE_ERR_UNSUPPORTED;
     const Workspace w = workspace_layout(*L, 1, R);
     cudaStream_t s = (cudaStream_t)stream;
     moe_status st;

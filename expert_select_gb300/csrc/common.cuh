@@ -160,7 +160,6 @@ inline T *at(void *ws, size_t off) {
 
 bool desc_ok(const moe_layer_desc *L);
 bool select_args(const moe_select_params *P, int k, SelectArgs *a);
-bool permute_fits(int R, int E);
 bool aligned16(const void *p);
 // The argument checks of moe_tree_forward other than those of the workspace.
 moe_status tree_forward_check(const moe_layer_desc *L, const moe_select_params *P,

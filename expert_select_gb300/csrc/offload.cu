@@ -77,7 +77,6 @@ extern "C" moe_status moe_offload_forward(
     std::vector<uint8_t> res_host(E);
     if (moe_residency_query(table, layer, slot_host.data(), res_host.data()) != MOE_OK)
         return MOE_ERR_ARG;
-    if (!permute_fits(R, E)) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream, sd = (cudaStream_t)side;
     const Workspace w = workspace_layout(*L, B, N);
     moe_tree_outputs o{};

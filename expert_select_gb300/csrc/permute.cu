@@ -44,8 +44,11 @@ permute_masks_kernel(const int *__restrict__ idx, int R, int k, int E,
     for (int e = tid; e < E; e += kMaskThreads) gmask[(size_t)e * nb + b] = m[e];
 }
 
-// kMasksReady: permute_masks_kernel has built the masks in gmask.
-template <bool kMasksReady>
+// kMode 0: the CTA builds the masks in shared memory. 1: permute_masks_kernel has built
+// them in gmask and the CTA loads them into shared memory. 2: the same, but the [E][nb]
+// masks and prefixes would not fit in shared memory: the CTA scans the masks in place and
+// writes the prefixes beside them, keeping only the per-expert counts and offsets.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict__ counts,
                int *__restrict__ offsets, int *__restrict__ perm, int *__restrict__ pos,
@@ -54,9 +57,10 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
     pdl_wait();
     extern __shared__ uint32_t sm[];
     const int nb = (R + 31) >> 5;
-    uint32_t *mask = sm;                  // [E][nb]
-    uint32_t *pre = sm + (size_t)nb * E;  // [E][nb]
-    int *cnt = (int *)(pre + (size_t)nb * E);
+    constexpr bool kMasksReady = kMode != 0, kInPlace = kMode == 2;
+    uint32_t *mask = kInPlace ? gmask : sm;                              // [E][nb]
+    uint32_t *pre = kInPlace ? gmask + (size_t)nb * E : sm + (size_t)nb * E;  // [E][nb]
+    int *cnt = (int *)(kInPlace ? sm : pre + (size_t)nb * E);
     int *off = cnt + E;                   // [E + 1]
     int *sidx = off + E + 1;              // [A] the expert ids, when this CTA places them
     const int tid = threadIdx.x;
@@ -68,7 +72,8 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
 #pragma unroll
     for (int u = 0; u < 4; ++u)
         ev0[u] = !kMasksReady && tid + u * kThreads < A ? idx[tid + u * kThreads] : -1;
-    for (int i = tid; i < nb * E; i += kThreads) mask[i] = kMasksReady ? gmask[i] : 0u;
+    if (!kInPlace)
+        for (int i = tid; i < nb * E; i += kThreads) mask[i] = kMasksReady ? gmask[i] : 0u;
     if (tid == 0) {  // a fresh check word for this call, keeping what the router reported
         flags[0] = after_router ? flags[kRouterCheckWord] : 0;
         flags[kRouterCheckWord] = 0;
@@ -197,8 +202,9 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         if (e < E) counts[e] = cnt[e];
     }
     if (gmask) {  // large blocks: permute_scatter_kernel places the assignments
-        for (int i = tid; i < 2 * nb * E; i += kThreads)
-            if (!kMasksReady || i >= nb * E) gmask[i] = sm[i];
+        if (!kInPlace)
+            for (int i = tid; i < 2 * nb * E; i += kThreads)
+                if (!kMasksReady || i >= nb * E) gmask[i] = sm[i];
         return;
     }
     // a thread per assignment; a repeated expert keeps its first slot
@@ -269,16 +275,29 @@ size_t permute_smem_bytes(int R, int E) {
     return nb * E * 8 + (size_t)(2 * E + 1) * 4;
 }
 
+namespace {
+// Shared memory of the one-CTA scan of masks left in place: counts, offsets.
+size_t masks_ready_smem_bytes(int E) { return (size_t)(2 * E + 1) * 4; }
+constexpr size_t kPermuteSmemLimit = 227 * 1024;
+}  // namespace
+
 cudaError_t launch_permute(const moe_layer_desc &L, const int *idx, int R, int *counts,
                            int *offsets, int *perm, int *pos, int *active, int *rowtiles,
                            int *flags, uint32_t *rbmask, bool after_router, cudaStream_t s) {
     const int A = R * L.k;
     uint32_t *gm = A > kOneCtaAssignments ? rbmask : nullptr;
-    // + the staged expert ids when this CTA places the assignments (A <= 2048, so R <= 2048
-    // and the masks take at most 64 row blocks: the total stays far below the limit)
-    const size_t smem = permute_smem_bytes(R, L.E) + (gm ? 0 : (size_t)A * 4);
-    const bool masks_ready = A > kManyCtaMasks;
-    auto kernel = masks_ready ? permute_kernel<true> : permute_kernel<false>;
+    // past kManyCtaMasks assignments, or when the masks and prefixes would not fit in shared
+    // memory, a many-CTA kernel builds the masks and the one CTA scans them in place; else
+    // they live in shared memory, with the staged expert ids when this CTA places the
+    // assignments (A <= 2048, so R <= 2048 and the masks take at most 64 row blocks: the
+    // total stays far below the limit)
+    const bool in_place = gm && permute_smem_bytes(R, L.E) > kPermuteSmemLimit;
+    const bool masks_ready = A > kManyCtaMasks || in_place;
+    const size_t smem = in_place ? masks_ready_smem_bytes(L.E)
+                                 : permute_smem_bytes(R, L.E) + (gm ? 0 : (size_t)A * 4);
+    auto kernel = in_place      ? permute_kernel<2>
+                  : masks_ready ? permute_kernel<1>
+                                : permute_kernel<0>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -489,10 +489,15 @@ def test_tree_route_equals_router_then_select():
 
 # ------------------------------------------------------------------ permute
 
+# The last four: row-block masks and prefixes that would not fit in one CTA's shared memory
+# (E = 256 past ~3570 rows), built by the many-CTA mask kernel and scanned in place, both
+# below and above 8192 assignments, and a block that still fits beside them.
 @pytest.mark.parametrize("R,E,k,skew", [(1, 16, 2, 0.0), (9, 16, 2, 0.0), (65, 128, 8, 0.0),
                                         (65, 128, 8, 1.5), (520, 128, 4, 1.0),
                                         (4160, 128, 8, 0.8), (33, 256, 16, 0.5),
-                                        (200, 256, 16, 0.7), (7000, 128, 8, 0.3)])
+                                        (200, 256, 16, 0.7), (7000, 128, 8, 0.3),
+                                        (2100, 256, 2, 0.0), (5000, 256, 1, 0.0),
+                                        (3600, 256, 5, 0.4), (20000, 256, 2, 0.2)])
 def test_permute_bit_exact(R, E, k, skew):
     shape = W.LayerShape(d=64, E=E, k=k, f=64, dtype="fp32")
     L = _desc(shape)
@@ -587,6 +592,8 @@ EXPERT_CASES = [
     ("qwen-tc-4160rows", W.QWEN3_30B_A3B, 4160, 0.8, M.MOE_FFN_TCGEN05, 16),
     ("qwen-tc-600rows-hot", W.QWEN3_30B_A3B, 600, 2.0, M.MOE_FFN_TCGEN05, 16),
     ("gptoss-tc", GPTOSS32, 65, 0.7, M.MOE_FFN_TCGEN05, 24),
+    ("e256-4000rows", W.LayerShape(d=256, E=256, k=4, f=128, dtype="bf16"), 4000, 0.5,
+     M.MOE_FFN_TCGEN05, 24),
 ]
 
 
