@@ -11,7 +11,8 @@ the oracle's experts and combine on the device's routing (2e-2 * max|ref| for bf
 for fp32). The cases cover expert counts that are not multiples of 32, k from 1 to 16,
 blocks of one to three trees and trees of 2 to 65 nodes. A second set draws blocks of 4 to
 80 trees of one random shape (up to ~5000 rows), with the router and y checked on sampled
-rows.
+rows. A third set draws tree sizes from 1 to 1000 nodes, blocks of up to 100 trees, layer
+widths in steps of 64, and the pre-norm and residual options.
 """
 import numpy as np
 import pytest
@@ -20,7 +21,7 @@ import torch
 from expert_select_gb300 import moetree as M
 from expert_select_gb300 import workload as W
 from oracle import oracle as O
-from test_gpu_parity import _check_selection
+from test_gpu_parity import _check_selection, _tree_of
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -199,6 +200,99 @@ def test_random_large_block_against_oracle(seed):
     sample = np.random.default_rng(seed + 1).choice(R, 48, replace=False).tolist()
     ref_y = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"],
                           rows=sample)
+    tol = 2e-2 if shape.dtype == "bf16" else 1e-4
+    err = np.abs(y.double().cpu().numpy()[sample] - ref_y).max()
+    assert err <= tol * np.abs(ref_y).max(), (c, err)
+
+
+def _draw_wide(seed):
+    rng = np.random.default_rng(50000 + seed)
+    dtype = "bf16" if rng.random() < 0.8 else "fp32"
+    d = int(64 * rng.integers(1, 33))
+    f = int(64 * rng.integers(1, 17))
+    E = int(rng.integers(8, 257))
+    k = int(rng.integers(1, min(16, E) + 1))
+    big = rng.random() < 0.3
+    N = int(rng.integers(257, 1001)) if big else int(rng.integers(1, 257))
+    B = 1 if big else int(rng.integers(1, 101 if N <= 65 else 9))
+    mode = str(rng.choice(["natural", "accept", "accept", "fixed"]))
+    prune = mode != "natural" and bool(rng.random() < 0.4)
+    return dict(dtype=dtype, d=d, f=f, E=E, k=k, N=N, B=B, mode=mode,
+                anchor=bool(rng.random() < 0.8), prune=prune,
+                std=float(rng.choice([0.02, 0.1, 0.3, 1.0])),
+                fixed_B=int(rng.integers(k, E + 1)), min_set=int(rng.integers(k, max(k, 24) + 1)),
+                budget=int(rng.integers(0, 10)), resident=(rng.random(E) < 0.5).astype(np.uint8),
+                norm=bool(rng.random() < 0.3), residual=bool(rng.random() < 0.3),
+                path=M.MOE_FFN_SIMT if (dtype == "fp32" or rng.random() < 0.15) else M.MOE_FFN_AUTO)
+
+
+@pytest.mark.parametrize("seed", list(range(48)))
+def test_random_tree_sizes_and_options(seed):
+    """Trees of 1 to 1000 nodes (past 256 the one-CTA selector), blocks of up to 100 trees,
+    d up to 2048 and f up to 1024 in steps of 64, E from 8 to 256, both expert paths, the
+    pre-norm and residual options; the selection of every tree, counts and offsets
+    exactly, logits and y on sampled rows (y = x + MoE(rmsnorm(x)) with both options)."""
+    c = _draw_wide(seed)
+    shape = W.LayerShape(d=c["d"], E=c["E"], k=c["k"], f=c["f"], dtype=c["dtype"])
+    E, B, N = c["E"], c["B"], c["N"]
+    parent, depth1 = _tree_of(N, 60000 + seed)
+    depth = np.tile(depth1.astype(np.int32), (B, 1))
+    R = B * N
+    x = torch.cat([W.hidden_states(61000 + 97 * seed + b, parent, shape.d, shape.torch_dtype)
+                   for b in range(B)])
+    wr = W.router_weight(62000 + seed, shape, std=c["std"], device=DEV)
+    wg, wu, wd = W.expert_weights(63000 + seed, shape, device=DEV)
+    mode = {"natural": M.MOE_ROUTE_NATURAL, "accept": M.MOE_ROUTE_ACCEPT,
+            "fixed": M.MOE_ROUTE_FIXED_B}[c["mode"]]
+    P = M.select_params(mode, W.C_EAGLE, anchor=c["anchor"], prune=c["prune"],
+                        reroute_budget=c["budget"], min_set=c["min_set"],
+                        fixed_B=c["fixed_B"] if c["mode"] == "fixed" else 0)
+    L = M.layer_desc(shape.d, E, shape.k, shape.f, shape.dtype)
+    out = dict(logits=torch.empty(R, E, device=DEV),
+               topk_idx=torch.empty(R, shape.k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(R, shape.k, device=DEV),
+               eligible=torch.empty(B, E, dtype=torch.uint8, device=DEV),
+               info=torch.empty(B, NF, dtype=torch.int32, device=DEV),
+               counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV))
+    res = torch.from_numpy(c["resident"]).to(DEV) if c["prune"] else None
+    y = torch.full((R, shape.d), float("nan"), dtype=shape.torch_dtype, device=DEV)
+    ws = M.workspace(L, B, N)
+    xd = x.to(DEV)
+    M.moe_tree_forward(L, P, xd, wr, wg, wu, wd, None,
+                       torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
+                       M.tree_outputs(**out),
+                       M.run_opts(c["path"], residual=c["residual"], norm_input=c["norm"]))
+    torch.cuda.synchronize()
+    assert M.moe_workspace_check(ws) == 0
+    got = {key: v.cpu().numpy() for key, v in out.items()}
+    if c["norm"]:
+        xn = torch.empty_like(xd)
+        M.moe_rms_norm(L, xd, xn)
+        torch.cuda.synchronize()
+        xr = xn.cpu()
+    else:
+        xr = x
+    rows = np.random.default_rng(seed).choice(R, min(R, 128), replace=False)
+    ref_l = O.router(xr[rows], wr.cpu())
+    assert (np.abs(got["logits"][rows] - ref_l) <=
+            1e-4 * np.abs(ref_l).max(axis=1, keepdims=True)).all()
+    omode = {"natural": O.NATURAL, "accept": O.ACCEPT, "fixed": O.FIXED_B}[c["mode"]]
+    kw = dict(mode=omode, c=W.C_EAGLE, anchor=c["anchor"])
+    if c["mode"] == "fixed":
+        kw["fixed_B"] = c["fixed_B"]
+    if c["prune"]:
+        kw.update(prune=True, resident=c["resident"], budget=c["budget"], min_set=c["min_set"])
+    _check_selection(shape, kw, got["logits"], depth, got["topk_idx"], got["gates"],
+                     got["eligible"], got["info"], N, B)
+    rc, ro, _ = O.permute(got["topk_idx"], E)
+    np.testing.assert_array_equal(got["counts"], rc)
+    np.testing.assert_array_equal(got["offsets"], ro)
+    sample = np.random.default_rng(seed + 1).choice(R, min(R, 24), replace=False).tolist()
+    ref_y = O.moe_combine(xr, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"],
+                          rows=sample)
+    if c["residual"]:
+        ref_y = ref_y + x.double().numpy()[sample]
     tol = 2e-2 if shape.dtype == "bf16" else 1e-4
     err = np.abs(y.double().cpu().numpy()[sample] - ref_y).max()
     assert err <= tol * np.abs(ref_y).max(), (c, err)
