@@ -12,7 +12,8 @@ for fp32). The cases cover expert counts that are not multiples of 32, k from 1 
 blocks of one to three trees and trees of 2 to 65 nodes. A second set draws blocks of 4 to
 80 trees of one random shape (up to ~5000 rows), with the router and y checked on sampled
 rows. A third set draws tree sizes from 1 to 1000 nodes, blocks of up to 100 trees, layer
-widths in steps of 64, and the pre-norm and residual options.
+widths in steps of 64, and the pre-norm and residual options. Two more sets draw offloaded
+layers (against the resident layer, bit for bit) and draft selections (against the oracle).
 """
 import numpy as np
 import pytest
@@ -21,7 +22,7 @@ import torch
 from expert_select_gb300 import moetree as M
 from expert_select_gb300 import workload as W
 from oracle import oracle as O
-from test_gpu_parity import _check_selection, _tree_of
+from test_gpu_parity import _check_selection, _sel_tree_from_oracle, _tree_of
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -296,3 +297,100 @@ def test_random_tree_sizes_and_options(seed):
     tol = 2e-2 if shape.dtype == "bf16" else 1e-4
     err = np.abs(y.double().cpu().numpy()[sample] - ref_y).max()
     assert err <= tol * np.abs(ref_y).max(), (c, err)
+
+
+@pytest.mark.parametrize("seed", list(range(24)))
+def test_random_offloaded_layer_equals_resident(seed):
+    """The offloaded layer on random shapes, slot counts (k to E), routing rules, pruning,
+    pre-norm and residual, blocks of 1-3 trees over three steps: output and routing equal
+    to the resident layer's bit for bit, counters consistent."""
+    rng = np.random.default_rng(70000 + seed)
+    dtype = "bf16" if rng.random() < 0.7 else "fp32"
+    d = int(64 * rng.integers(1, 9)); f = int(64 * rng.integers(1, 5))
+    E = int(rng.integers(8, 97)); k = int(rng.integers(1, min(8, E) + 1))
+    slots = int(rng.integers(k, E + 1))
+    shape = W.LayerShape(d=d, E=E, k=k, f=f, dtype=dtype)
+    mode = str(rng.choice(["natural", "accept", "fixed"]))
+    prune = mode != "natural" and bool(rng.random() < 0.5)
+    norm = bool(rng.random() < 0.4)
+    std = float(rng.choice([0.02, 0.1, 0.3]))
+    if mode == "natural":
+        P = M.select_params(M.MOE_ROUTE_NATURAL, W.C_EAGLE)
+    elif mode == "accept":
+        P = M.select_params(M.MOE_ROUTE_ACCEPT, W.C_EAGLE, prune=prune,
+                            reroute_budget=int(rng.integers(0, 9)), min_set=int(rng.integers(k, k + 12)))
+    else:
+        P = M.select_params(M.MOE_ROUTE_FIXED_B, W.C_EAGLE, prune=prune,
+                            reroute_budget=int(rng.integers(0, 9)), min_set=int(rng.integers(k, k + 12)),
+                            fixed_B=int(rng.integers(k, E + 1)))
+    wg, wu, wd = W.expert_weights(71000 + seed, shape, device=DEV)
+    hg, hu, hd = (w.cpu().pin_memory() for w in (wg, wu, wd))
+    pg = torch.zeros(slots, f, d, dtype=shape.torch_dtype, device=DEV)
+    pu = torch.zeros_like(pg)
+    pd = torch.zeros(slots, d, f, dtype=shape.torch_dtype, device=DEV)
+    wr = W.router_weight(72000 + seed, shape, std=std, device=DEV)
+    L = M.layer_desc(d, E, k, f, dtype)
+    Ls = M.layer_desc(d, E, k, f, dtype, slots=slots)
+    table = M.Residency(n_layers=1, E=E, slots=slots)
+    side = torch.cuda.Stream()
+    B = int(rng.integers(1, 4))
+    for step in range(3):
+        t = W.eagle_tree(73000 + 7 * seed + step, steps=int(rng.integers(1, 6)), topk=int(rng.integers(2, 11)),
+                         draft_tokens=int(rng.integers(1, 65)))
+        N = t.N
+        x = torch.cat([W.hidden_states(74000 + 11 * seed + 3 * step + b, t.parent, d, shape.torch_dtype)
+                       for b in range(B)]).to(DEV)
+        dep = torch.from_numpy(np.tile(t.depth, B).astype(np.int32)).to(DEV)
+        _, res_before = table.query(0)
+        res_dev = torch.from_numpy(res_before.copy()).to(DEV)
+        idx_ref = torch.empty(B * N, k, dtype=torch.int32, device=DEV)
+        cnt_ref = torch.empty(E, dtype=torch.int32, device=DEV)
+        y_ref = torch.empty(B * N, d, dtype=shape.torch_dtype, device=DEV)
+        ws = M.workspace(L, B, N)
+        opts = M.run_opts(norm_input=norm, residual=norm)
+        M.moe_tree_forward(L, P, x, wr, wg, wu, wd, None, dep, B, N, res_dev, y_ref, ws,
+                           M.tree_outputs(topk_idx=idx_ref, counts=cnt_ref), opts)
+        idx = torch.empty_like(idx_ref)
+        y = torch.full_like(y_ref, float("nan"))
+        ws2 = M.workspace(Ls, B, N)
+        st = M.moe_offload_forward(Ls, P, x, wr, hg, hu, hd, pg, pu, pd, table, 0, dep, B, N,
+                                   y, ws2, M.tree_outputs(topk_idx=idx), opts=opts, side_stream=side)
+        torch.cuda.synchronize()
+        assert M.moe_workspace_check(ws2) == 0
+        assert torch.equal(idx, idx_ref)
+        assert torch.equal(y, y_ref), (seed, step)
+        union = int((cnt_ref > 0).sum())
+        assert st.needed == union and st.hits + st.uploads == union
+
+
+@pytest.mark.parametrize("seed", list(range(48)))
+def test_random_draft_selection_against_oracle(seed):
+    """EcoSpec-style draft selection on random candidate pools (up to ~3200 candidates),
+    E 4-256, k 1-16, lambda 0-5, gamma 1-300, with repeated and out-of-range footprint ids
+    in a fifth of the cases: selection, parents, depths and union bit-exact."""
+    rng = np.random.default_rng(80000 + seed)
+    steps = int(rng.integers(1, 10)); topk = int(rng.integers(1, 21))
+    cand = W.eagle_candidates(81000 + seed, steps=steps, topk=topk)
+    C = cand.C
+    E = int(rng.integers(4, 257)); k = int(rng.integers(1, min(16, E) + 1))
+    junk = rng.random() < 0.2
+    if junk:
+        fp = rng.integers(-3, E + 3, size=(C, k)).astype(np.int32)
+    else:
+        fp = np.stack([rng.choice(E, size=k, replace=False) for _ in range(C)]).astype(np.int32)
+    lam = float(rng.choice([0.0, 0.01, 0.1, 0.3, 1.0, 5.0]))
+    gamma = int(rng.integers(1, min(C, 300) + 1))
+    L = M.layer_desc(256, E, k, 128, "bf16")
+    sel = torch.empty(gamma, dtype=torch.int32, device=DEV)
+    spar, sdep = torch.empty_like(sel), torch.empty_like(sel)
+    nu = torch.empty(1, dtype=torch.int32, device=DEV)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)  # noqa: E731
+    M.moe_draft_select(L, td(cand.parent), td(cand.depth), td(cand.logp), td(fp), lam, gamma,
+                       sel, spar, sdep, n_union=nu)
+    torch.cuda.synchronize()
+    ref_sel, ref_u = O.draft_select(cand.parent, cand.logp, fp, E, lam, gamma)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    rp, rd = _sel_tree_from_oracle(cand, ref_sel)
+    np.testing.assert_array_equal(spar.cpu().numpy(), rp)
+    np.testing.assert_array_equal(sdep.cpu().numpy(), rd)
+    assert int(nu.item()) == ref_u
