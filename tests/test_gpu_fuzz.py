@@ -13,7 +13,8 @@ blocks of one to three trees and trees of 2 to 65 nodes. A second set draws bloc
 80 trees of one random shape (up to ~5000 rows), with the router and y checked on sampled
 rows. A third set draws tree sizes from 1 to 1000 nodes, blocks of up to 100 trees, layer
 widths in steps of 64, and the pre-norm and residual options. Two more sets draw offloaded
-layers (against the resident layer, bit for bit) and draft selections (against the oracle).
+layers (against the resident layer, bit for bit) and draft selections (against the oracle),
+and a last set routes junk expert ids through the experts.
 """
 import numpy as np
 import pytest
@@ -394,3 +395,48 @@ def test_random_draft_selection_against_oracle(seed):
     np.testing.assert_array_equal(spar.cpu().numpy(), rp)
     np.testing.assert_array_equal(sdep.cpu().numpy(), rd)
     assert int(nu.item()) == ref_u
+
+
+@pytest.mark.parametrize("seed", list(range(24)))
+def test_random_junk_routing_through_the_experts(seed):
+    """moe_expert_forward on routing with out-of-range ids (5% of slots) and repeated ids
+    (5% of rows), 1 to 3000 rows, both expert paths: the check bit is set exactly when a
+    slot is skipped, and y equals the oracle over the valid slots (the first slot of a
+    repeated id)."""
+    rng = np.random.default_rng(90000 + seed)
+    dtype = "bf16" if rng.random() < 0.7 else "fp32"
+    d = int(64 * rng.integers(1, 9)); f = int(64 * rng.integers(1, 5))
+    E = int(rng.integers(4, 257)); k = int(rng.integers(1, min(16, E) + 1))
+    R = int(rng.choice([1, 7, 65, 300, 1100, 3000]))
+    shape = W.LayerShape(d=d, E=E, k=k, f=f, dtype=dtype)
+    L = M.layer_desc(d, E, k, f, dtype)
+    idx = W.random_assignments(91000 + seed, R, E, k, float(rng.choice([0.0, 1.0])))
+    junk = rng.random(idx.shape) < 0.05
+    idx[junk] = rng.integers(-5, E + 5, size=int(junk.sum()))
+    if k > 1:  # some rows repeat their first id in a later slot
+        rep = rng.random(R) < 0.05
+        idx[rep, k - 1] = idx[rep, 0]
+    gates = W.random_gates(92000 + seed, R, k)
+    wg, wu, wd = W.expert_weights(93000 + seed, shape, device=DEV)
+    x = W.hidden_states(94000 + seed, np.arange(-1, R - 1, dtype=np.int32), d, shape.torch_dtype)
+    y = torch.full((R, d), float("nan"), dtype=shape.torch_dtype, device=DEV)
+    ws = M.workspace(L, 1, R)
+    path = M.MOE_FFN_SIMT if (dtype == "fp32" or rng.random() < 0.3) else M.MOE_FFN_TCGEN05
+    M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, torch.from_numpy(idx).to(DEV),
+                         torch.from_numpy(gates).to(DEV), y, ws, M.run_opts(path))
+    torch.cuda.synchronize()
+    # the valid slots: in range, and the first slot of a repeated id
+    valid = (idx >= 0) & (idx < E)
+    for j in range(1, k):
+        for q in range(j):
+            valid[:, j] &= idx[:, j] != idx[:, q]
+    bad = not valid.all()
+    chk = M.moe_workspace_check(ws)
+    assert chk == (1 if bad else 0), (chk, bad)
+    g = np.where(valid, gates, 0.0).astype(np.float64)
+    ii = np.where(valid, idx, 0).astype(np.int32)
+    rows = np.random.default_rng(seed).choice(R, min(R, 24), replace=False).tolist()
+    ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), ii, g, rows=rows)
+    tol = 2e-2 if dtype == "bf16" else 1e-4
+    err = np.abs(y.double().cpu().numpy()[rows] - ref).max()
+    assert err <= tol * max(np.abs(ref).max(), 1e-30), (seed, err)
