@@ -513,7 +513,7 @@ def run_gpu(args):
         return run
 
     pair = {"ffn_ctas": cap, "streams": 2}
-    for label, r_, w_r, u_ref in (("acceptmoe_std_0.02", routing, wr, union),
+    for label, r_, w_r, u_ref in ((f"{routing}_std_{args.router_std:g}", routing, wr, union),
                                   ("acceptmoe_std_0.1", "acceptmoe", wr_peaked, None),
                                   ("natural_std_0.1", "natural", wr_peaked, None)):
         pair_loop(Wm, r_, w_r)

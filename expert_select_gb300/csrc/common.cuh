@@ -95,16 +95,23 @@ cudaError_t launch_select(const moe_layer_desc &L, const SelectArgs &a, const fl
                           const PermuteOut &po, bool *permuted, cudaStream_t s);
 
 // Row tiles of the tensor-core expert kernel: at most kMaxRowTile tokens of one expert
-// (its MMA N is at most 256). An expert with c tokens takes ceil(c / kMaxRowTile) tiles of
-// near-equal size (at most E + A / kMaxRowTile tiles in all); the height is the largest
-// tile rounded up to 16, and the expert kernel sizes its per-stage token buffer to it:
-// small blocks leave shared memory for more stages of weight bytes in flight. Each tile
-// entry is (expert, first permuted row, tokens, group) with group = rowtile_group(j, g):
-// the tile is the j-th of the expert's g tiles (the expert kernel hands the g tiles of one
-// weight tile out together, so they read the weights from HBM once).
+// (its MMA N is at most 256), or at most kPairRowTile when no expert has more than
+// 2 * kPairRowTile tokens: then every tile has 128 tokens or fewer and the expert kernel
+// can run two weight tiles over one tile of token rows. An expert with c tokens takes
+// ceil(c / limit) tiles of near-equal size (at most E + A / kPairRowTile tiles in all); the
+// height is the largest tile rounded up to 16, and the expert kernel sizes its per-stage
+// token buffer to it: small blocks leave shared memory for more stages of weight bytes in
+// flight. Each tile entry is (expert, first permuted row, tokens, group) with group =
+// rowtile_group(j, g): the tile is the j-th of the expert's g tiles (the expert kernel hands
+// the g tiles of one weight tile out together, so they read the weights from HBM once).
 constexpr int kMaxRowTile = 256;
+constexpr int kPairRowTile = 128;
 constexpr int kRowTileHeader = 4;  // count, height, two unused ints
-inline int max_rowtiles(int E, int A) { return E + (A + kMaxRowTile - 1) / kMaxRowTile + 1; }
+inline int max_rowtiles(int E, int A) { return E + (A + kPairRowTile - 1) / kPairRowTile + 1; }
+// The tile limit of a block whose largest expert has cmax tokens.
+__host__ __device__ inline int rowtile_limit(int cmax) {
+    return cmax <= 2 * kPairRowTile ? kPairRowTile : kMaxRowTile;
+}
 __host__ __device__ inline int rowtile_group(int j, int g) { return (j << 16) | g; }
 
 // The kernel starts the call's check word: the router's word is carried into it when the

@@ -28,9 +28,12 @@
 // tokens, slot) into shared memory, so looking up a unit between two units costs no
 // global round trip. Two 256-column accumulators alternate so the epilogue of one unit
 // overlaps the MMAs of the next. A unit is one weight tile x one row tile (<= 256
-// tokens of one expert). A phase-2 unit needs the whole h of its row tile: the epilogue
-// that finishes a phase-1 unit publishes it with a release increment of the row tile's
-// counter, and the producer of a phase-2 unit waits for the count with acquire loads
+// tokens of one expert); when every row tile of a launch has 32 to 128 tokens a unit is
+// two weight tiles x one row tile instead, whose two MMAs per k-step share the stage's
+// token rows and fill the two 128-column halves of one accumulator, so each token row
+// crosses into shared memory half as often. A phase-2 unit needs the whole h of its row
+// tile: the epilogue that finishes a phase-1 unit publishes it with a release increment of
+// the row tile's counter, and the producer of a phase-2 unit waits for the count with acquire loads
 // before its TMA reads h. Tickets are handed out in order, so every phase-1 unit is
 // owned by a running CTA before any CTA waits on one: no deadlock even when fewer CTAs
 // than SMs are resident.
@@ -75,6 +78,8 @@ struct Params {
     int smem;      // dynamic shared memory of the launch (bytes)
     int tbl_cap;   // row tiles described in the shared-memory table (the rest: global reads)
     int slots;     // expert slots in the weight pool
+    int pair_min;    // row-tile heights from this up to 128 tokens take weight-tile pairs,
+    int pair_units;  // when the launch has at least this many single-tile units per CTA
     const int *rowtiles, *slot;
     const uint8_t *pass;  // experts computed by this launch (null: all)
     int *flags;
@@ -101,6 +106,7 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 
 struct Unit {
     int phase, rt, m, e, row0, ntok, slot;  // row0: the row tile's first permuted row
+    int nm;                                 // weight tiles m, m + 1, ... of this unit (1 or 2)
     int group;                              // tiles of this expert (they share its weights)
 };
 
@@ -125,32 +131,38 @@ __device__ __forceinline__ int4 tile_at(const Params &p, int rt, const int4 *tbl
     return (tbl && rt < p.tbl_cap) ? tbl[rt] : row_tile(p, rt);
 }
 
-// Ticket u -> unit. Tickets [0, U1) are phase 1, the rest phase 2; within a phase the
-// tickets of an expert's row tiles [f, f + g) form one block of g * mt tickets taken weight
-// tile by weight tile: ticket f * mt + m * g + j is weight tile m of row tile f + j, so the
-// g tiles that read the same weights are handed out together and run at the same time
-// (the second read of those weights hits L2). The row tile's entry comes from the
+// Ticket u -> unit. A unit is W consecutive weight tiles (W = 1, or 2 when the launch pairs
+// them) of one row tile: mu = ceil(mt / W) units per row tile and phase, the last one short
+// when W does not divide mt. Tickets [0, U1) are phase 1, the rest phase 2; within a phase the
+// tickets of an expert's row tiles [f, f + g) form one block of g * mu tickets taken unit
+// by unit: ticket f * mu + i * g + j is unit i of row tile f + j, so the g tiles that read
+// the same weights are handed out together and run at the same time (the second read of
+// those weights hits L2). The row tile's entry comes from the
 // shared-memory table when it holds it (tbl != nullptr). Returns 0 for a unit to compute,
 // 1 for one outside this launch's expert pass, 2 for an expert whose slot is outside the
 // pool (skipped and flagged).
-__device__ __forceinline__ int decode(const Params &p, int U1, int u, Unit &w,
+__device__ __forceinline__ int decode(const Params &p, int U1, int u, int W, Unit &w,
                                       const int4 *tbl) {
     const bool ph1 = u < U1;
     const int v = ph1 ? u : u - U1, mt = ph1 ? p.mt1 : p.mt2;
-    const int rt0 = v / mt;  // a tile of the right group (the order within differs)
+    const int mu = (mt + W - 1) / W;
+    const int rt0 = v / mu;  // a tile of the right group (the order within differs)
     int4 t = tile_at(p, rt0, tbl);
     const int jg = (t.z >> 12) & 1023, g = ((unsigned)t.z >> 22) & 1023;
     w.phase = ph1 ? 1 : 2;
+    int i;
     if (g <= 1) {  // an expert in one tile (every expert of small blocks)
         w.rt = rt0;
-        w.m = v - rt0 * mt;
+        i = v - rt0 * mu;
     } else {
         const int f = rt0 - jg;
-        const int local = v - f * mt;
-        w.m = local / g;
-        w.rt = f + (local - w.m * g);
+        const int local = v - f * mu;
+        i = local / g;
+        w.rt = f + (local - i * g);
         if (w.rt != rt0) t = tile_at(p, w.rt, tbl);
     }
+    w.m = i * W;
+    w.nm = min(W, mt - w.m);
     w.e = t.x;
     w.row0 = t.y;
     w.ntok = t.z & 4095;
@@ -229,15 +241,26 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     pdl_wait();
     const uint32_t tmem = *tmem_slot;
     const int n_rt = p.rowtiles[0];
-    // the ring: as many stages as fit of 16 KB weights + a token buffer of the row-tile
-    // height (every row tile of this launch has at most that many tokens)
-    const uint32_t b_bytes = (uint32_t)p.rowtiles[1] * 128u;
+    // the ring: as many stages as fit of W 16 KB weight tiles + a token buffer of the
+    // row-tile height (every row tile of this launch has at most that many tokens). With
+    // row tiles of pair_min to 128 tokens a unit takes two weight tiles (W = 2): two MMAs
+    // per k-step read the same token tile into the two halves of one accumulator, so the
+    // token rows cross into shared memory once per two weight tiles. Only with enough units
+    // per CTA: a small union in units twice as long leaves CTAs idle at the end.
+    const int height = p.rowtiles[1];
+    const uint32_t b_bytes = (uint32_t)height * 128u;
     const uint32_t ring = (base + kCtlBytes + 2 * 2 * kSgFloats * 4 +
                            (uint32_t)p.tbl_cap * 16u + 1023u) & ~1023u;
-    const int S = max(1, min(kMaxStages, (int)((raw + (uint32_t)p.smem - ring) /
-                                               (kABytes + b_bytes))));
-    const uint32_t sA = ring, sB = ring + (uint32_t)S * kABytes;
-    const int U1 = n_rt * p.mt1, U = U1 + n_rt * p.mt2;
+    const uint32_t avail = raw + (uint32_t)p.smem - ring;
+    const int W = (p.pair_min > 0 && height >= p.pair_min && height <= kAccCols / 2 &&
+                   n_rt * (p.mt1 + p.mt2) >= p.pair_units * (int)gridDim.x &&
+                   avail >= 2u * (2u * kABytes + b_bytes))
+                      ? 2
+                      : 1;
+    const uint32_t a_bytes = (uint32_t)W * kABytes;  // weight bytes of a stage
+    const int S = max(1, min(kMaxStages, (int)(avail / (a_bytes + b_bytes))));
+    const uint32_t sA = ring, sB = ring + (uint32_t)S * a_bytes;
+    const int U1 = n_rt * ((p.mt1 + W - 1) / W), U = U1 + n_rt * ((p.mt2 + W - 1) / W);
     // the epilogue warps copy the row-tile list into shared memory (expert, first row,
     // tokens, slot), so that a unit's lookup costs no global round trips
     if (warp >= 2) {
@@ -269,7 +292,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                const int dc = decode(p, U1, u, w, tbl);
+                const int dc = decode(p, U1, u, W, w, tbl);
                 if (dc != 0) {
                     if (dc == 2) atomicOr(p.flags, FLAG_BAD_EXPERT);
                     continue;
@@ -305,14 +328,17 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                         break;
                     }
                     const uint32_t fb = full + 8 * s;
-                    mbar_expect_tx(fb, kABytes + bb);
-                    const uint32_t a = sA + (uint32_t)s * kABytes;
-                    if (w.phase == 1) {
-                        tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
-                        tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, w.m * 64, w.slot, fb,
-                                    pol);
-                    } else {
-                        tma_load_3d(a, &maps.wd, kc * kBK, w.m * kM, w.slot, fb, pol);
+                    mbar_expect_tx(fb, (uint32_t)w.nm * kABytes + bb);
+                    for (int t = 0; t < w.nm; ++t) {
+                        const uint32_t a = sA + (uint32_t)s * a_bytes + (uint32_t)t * kABytes;
+                        const int m = w.m + t;
+                        if (w.phase == 1) {
+                            tma_load_3d(a, &maps.wg, kc * kBK, m * 64, w.slot, fb, pol);
+                            tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, m * 64, w.slot, fb,
+                                        pol);
+                        } else {
+                            tma_load_3d(a, &maps.wd, kc * kBK, m * kM, w.slot, fb, pol);
+                        }
                     }
                     tma_load_2d(sB + (uint32_t)s * b_bytes, bmap, kc * kBK, brow, fb);
                     issued |= 1u << s;
@@ -340,7 +366,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (u < 0) break;
                 Unit w;
-                if (decode(p, U1, u, w, tbl) != 0) continue;
+                if (decode(p, U1, u, W, w, tbl) != 0) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -355,11 +381,15 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a = sA + (uint32_t)s * kABytes, b = sB + (uint32_t)s * b_bytes;
+                    const uint32_t b = sB + (uint32_t)s * b_bytes;
+                    // weight tile t of the unit accumulates into columns [128 t, 128 t + N)
+                    for (int t = 0; t < w.nm; ++t) {
+                        const uint32_t a = sA + (uint32_t)s * a_bytes + (uint32_t)t * kABytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        mma_bf16(d_tmem, sw128_desc(a + 32u * k), sw128_desc(b + 32u * k), idesc,
-                                 (kc | k) != 0);
+                        for (int k = 0; k < kBK / 16; ++k)
+                            mma_bf16(d_tmem + (uint32_t)t * (kAccCols / 2), sw128_desc(a + 32u * k),
+                                     sw128_desc(b + 32u * k), idesc, (kc | k) != 0);
+                    }
                     mma_issued = true;
                     mma_commit(empty + 8 * s);
                     if (++s == S) {
@@ -398,7 +428,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int u = epi_u[turn];
             if (u < 0) break;
             Unit w;
-            if (decode(p, U1, u, w, tbl) != 0) continue;
+            if (decode(p, U1, u, W, w, tbl) != 0) continue;
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             ++it;
@@ -408,16 +438,21 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (!epi_ok[acc]) break;  // uniform over the eight warps
             tc_fence_after();
             const int N = (w.ntok + 15) & ~15;
-            const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
+            // one weight tile per unit: the two teams take alternate 16-column chunks of the
+            // accumulator; a pair of weight tiles: team t takes all of tile t's columns
+            const int sub = W == 2 ? team : 0;           // the weight tile this team stores
+            const int c_first = W == 2 ? 0 : team * 16, c_step = W == 2 ? 16 : 32;
+            const int m = w.m + sub;
+            const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols + sub * (kAccCols / 2)) +
+                                   ((uint32_t)(q * 32) << 16);
             const size_t row0 = (size_t)w.row0;
-            // the two teams take alternate 16-column chunks of the accumulator
             if (w.phase == 1) {
                 // within a team the gate warps (quadrants 0, 1) hand silu(gate) to the up
                 // warps (quadrants 2, 3) through a double-buffered exchange buffer: one
                 // team barrier per chunk (a buffer is rewritten two chunks later, after
                 // the up warps have passed the barrier in between)
                 int j = 0;
-                for (int c0 = team * 16; c0 < N; c0 += 32, ++j) {
+                for (int c0 = c_first; sub < w.nm && c0 < N; c0 += c_step, ++j) {
                     float *buf = sg + (j & 1) * kSgFloats;
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
@@ -431,7 +466,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     team_bar(team);
                     if (q >= 2) {
                         const int i = row - 64;
-                        __nv_bfloat16 *hp = p.h + row0 * p.f + (size_t)w.m * 64 + i;
+                        __nv_bfloat16 *hp = p.h + row0 * p.f + (size_t)m * 64 + i;
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int tok = c0 + c;
@@ -445,11 +480,11 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 epi_bar();
                 if (threadIdx.x == 64) {
                     __threadfence();
-                    atomicAdd(p.sched + 1 + w.rt, 1);
+                    atomicAdd(p.sched + 1 + w.rt, w.nm);
                 }
             } else {
-                const int drow = w.m * kM + row;
-                for (int c0 = team * 16; c0 < N; c0 += 32) {
+                const int drow = m * kM + row;
+                for (int c0 = c_first; sub < w.nm && c0 < N; c0 += c_step) {
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
                     if (drow < p.d) {
@@ -555,6 +590,14 @@ int sm_count() {
 // exchange buffers.
 constexpr size_t kFixedSmem = 1024 + kCtlBytes + 2 * 2 * kSgFloats * sizeof(float);
 constexpr size_t kSmemBudget = 227 * 1024;
+// Row tiles of at least this many tokens (and at most 128) take weight-tile pairs: below
+// it the token rows are a small part of a stage and single tiles balance the CTAs better.
+// A launch on every SM pairs only with this many single-tile units per CTA (a union of ~26
+// experts of the Qwen3-shaped layer has about 5, and units twice as long would leave CTAs
+// idle at the end); a launch held to fewer CTAs runs beside other work, which fills the
+// SMs its CTAs leave at the end, and pairs at any unit count.
+constexpr int kPairMinRows = 32;
+constexpr int kPairMinUnitsPerCta = 8;
 
 }  // namespace
 
@@ -575,9 +618,13 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     // picks an expert at most once), rounded up to 16; the kernel sizes its stages from
     // the height the permute kernel chose
     const int box_cap = ((std::min(a.R, kMaxRowTile) + 15) / 16) * 16;
-    // the row-tile table takes what two stages of the tallest tiles leave; row tiles past
-    // it are read from global memory
-    const size_t two_stages = 2 * (kABytes + (size_t)box_cap * 128);
+    // the row-tile table takes what two stages of the tallest tiles leave (a stage of two
+    // weight tiles when the tiles can pair); row tiles past it are read from global memory
+    const size_t two_stages =
+        2 * std::max(kABytes + (size_t)box_cap * 128,
+                     box_cap >= kPairMinRows
+                         ? 2 * kABytes + (size_t)std::min(box_cap, kAccCols / 2) * 128
+                         : 0);
     const int tbl_cap = (int)std::min<size_t>((size_t)max_rowtiles(a.E, A),
                                               (kSmemBudget - kFixedSmem - two_stages) / 16);
     const size_t smem = kSmemBudget;
@@ -613,6 +660,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.smem = (int)smem;
     p.tbl_cap = tbl_cap;
     p.slots = S;
+    p.pair_min = kPairMinRows;
+    p.pair_units = a.max_ctas > 0 && a.max_ctas < nsm ? 0 : kPairMinUnitsPerCta;
     p.rowtiles = a.rowtiles;
     p.slot = a.slot;
     p.pass = a.pass;

@@ -10,8 +10,9 @@
 // The masks and prefixes live in shared memory: (R/32) x E x 8 bytes (133 KB at 4160
 // rows and 128 experts). The same kernel also writes the active-expert list and the list
 // of row tiles that the tensor-core expert kernel walks: an expert with c tokens takes
-// ceil(c / 256) tiles of near-equal size (sizes differ by at most one), and the tile height
-// is the largest tile rounded up to 16. Up to 2048 assignments it keeps the expert ids in shared memory and places the
+// ceil(c / 128) tiles of near-equal size (sizes differ by at most one) when no expert has
+// more than 256 tokens, else ceil(c / 256), and the tile height is the largest tile
+// rounded up to 16. Up to 2048 assignments it keeps the expert ids in shared memory and places the
 // assignments itself; past that it leaves the masks and prefixes in the workspace and a
 // second, many-CTA kernel places the assignments. Past 8192 assignments a many-CTA kernel
 // also builds the masks beforehand (a CTA per row block), and the one CTA only loads them.
@@ -134,8 +135,17 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         const int lane = tid & 31, warp = tid >> 5;
         const int nw = (E + 31) >> 5;
         const int c = tid < E ? cnt[tid] : 0;
-        // an expert's tiles: ceil(c / kMaxRowTile) of near-equal size
-        const int nt = (c + kMaxRowTile - 1) / kMaxRowTile;
+        // the tile limit from the largest count, then an expert's tiles: ceil(c / limit)
+        // of near-equal size
+        if (warp < nw) {
+            const int wm = __reduce_max_sync(0xffffffffu, c);
+            if (lane == 0) wred[2][warp] = wm;
+        }
+        __syncthreads();
+        int cbig = 0;
+        for (int w = 0; w < nw; ++w) cbig = max(cbig, wred[2][w]);
+        const int lim = rowtile_limit(cbig);
+        const int nt = (c + lim - 1) / lim;
         const int tmax = nt > 0 ? (c + nt - 1) / nt : 0;  // its largest tile
         if (warp < nw) {
             const int wm = __reduce_max_sync(0xffffffffu, tmax);
@@ -145,7 +155,7 @@ permute_kernel(const int *__restrict__ idx, int R, int k, int E, int *__restrict
         // row-tile height: the largest tile rounded up to 16
         int cmax = 0;
         for (int w = 0; w < nw; ++w) cmax = max(cmax, wred[3][w]);
-        const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
+        const int rt_size = min(lim, max(16, (cmax + 15) & ~15));
         const int a = c > 0;
         int ci = c, ai = a, ti = nt;  // inclusive scans within the warp
         if (warp < nw) {

@@ -644,8 +644,8 @@ __device__ __forceinline__ void cluster_barrier(bool release) {
 // results as the permute kernel: a stable counting sort of the assignments (n, j) by
 // (expert, node, slot). rmask[e] holds the nodes that chose e (a node chooses an expert
 // at most once, so within an expert the order is node order) and fin_all[n][j] the choices.
-// Writes counts, offsets, the active-expert list, the row tiles (height: the largest
-// expert's count rounded up to 16, at most kMaxRowTile), perm and pos, and starts the
+// Writes counts, offsets, the active-expert list, the row tiles (split and sized as the
+// permute kernel splits and sizes them), perm and pos, and starts the
 // call's check word (keeping router_word, the router's, read by thread 0 long before).
 __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
                              const uint32_t (*rmask)[kClusterMaxN / 32], int *soff,
@@ -670,8 +670,20 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
     __syncthreads();
     int cmax = 0;
     for (int w = 0; w < nw; ++w) cmax = max(cmax, wsc[3][w]);
-    const int rt_size = min(kMaxRowTile, max(16, (cmax + 15) & ~15));
-    const int act = c > 0, nt = (c + rt_size - 1) / rt_size;
+    // as in the permute kernel: ceil(c / limit) tiles of near-equal size, the height the
+    // largest tile of any expert rounded up to 16 (an expert of limit tokens can have a
+    // larger tile than one of more)
+    const int lim = rowtile_limit(cmax);
+    const int act = c > 0, nt = (c + lim - 1) / lim;
+    const int tmax = nt > 0 ? (c + nt - 1) / nt : 0;
+    if (warp < nw) {
+        const int wm = __reduce_max_sync(0xffffffffu, tmax);
+        if (lane == 0) wsc[2][warp] = wm;
+    }
+    __syncthreads();
+    int hmax = 0;
+    for (int w = 0; w < nw; ++w) hmax = max(hmax, wsc[2][w]);
+    const int rt_size = min(lim, max(16, (hmax + 15) & ~15));
     int ci = c, ai = act, ti = nt;  // inclusive scans within the warp
     if (warp < nw) {
 #pragma unroll
@@ -685,10 +697,10 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
                 ti += t2;
             }
         }
-        if (lane == 31) {
+        if (lane == 31) {  // wsc[2] may still be read above: the tile totals go to wsc[3]
             wsc[0][warp] = ci;
             wsc[1][warp] = ai;
-            wsc[2][warp] = ti;
+            wsc[3][warp] = ti;
         }
     }
     __syncthreads();
@@ -696,7 +708,7 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
         for (int w = 0; w < warp; ++w) {
             ci += wsc[0][w];
             ai += wsc[1][w];
-            ti += wsc[2][w];
+            ti += wsc[3][w];
         }
         const int c_ex = ci - c;
         int t_ex = ti - nt;
@@ -704,12 +716,14 @@ __device__ void permute_tree(const PermuteOut &po, const int *fin_all,
         po.counts[tid] = c;
         po.offsets[tid] = c_ex;
         if (act) po.active[1 + ai - act] = tid;
-        for (int n0 = 0; n0 < c; n0 += rt_size) {
+        for (int j = 0, n0 = 0; j < nt; ++j) {
+            const int sz = c / nt + (j < c % nt ? 1 : 0);
             int *t = po.rowtiles + kRowTileHeader + 4 * t_ex++;
             t[0] = tid;
             t[1] = c_ex + n0;  // first permuted row of the tile
-            t[2] = min(rt_size, c - n0);
-            t[3] = rowtile_group(0, 1);  // N <= 256 nodes: one tile per expert
+            t[2] = sz;
+            t[3] = rowtile_group(j, nt);
+            n0 += sz;
         }
         if (tid == E - 1) {
             soff[E] = ci;

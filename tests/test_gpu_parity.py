@@ -591,6 +591,7 @@ EXPERT_CASES = [
     ("qwen-tc-skewed", W.QWEN3_30B_A3B, 65, 3.0, M.MOE_FFN_TCGEN05, 24),
     ("qwen-tc-4160rows", W.QWEN3_30B_A3B, 4160, 0.8, M.MOE_FFN_TCGEN05, 16),
     ("qwen-tc-600rows-hot", W.QWEN3_30B_A3B, 600, 2.0, M.MOE_FFN_TCGEN05, 16),
+    ("qwen-tc-260rows", W.QWEN3_30B_A3B, 260, 1.0, M.MOE_FFN_TCGEN05, 32),
     ("gptoss-tc", GPTOSS32, 65, 0.7, M.MOE_FFN_TCGEN05, 24),
     ("e256-4000rows", W.LayerShape(d=256, E=256, k=4, f=128, dtype="bf16"), 4000, 0.5,
      M.MOE_FFN_TCGEN05, 24),
@@ -677,6 +678,79 @@ def test_expert_forward_exact_expert_loads(counts):
     _sync()
     assert M.moe_workspace_check(ws) == 0
     ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64))
+    _assert_close_rows(y.float().cpu().numpy(), ref, shape)
+
+
+@pytest.mark.parametrize("counts,d,f", [
+    ([128, 120, 33, 1, 0, 96, 65, 113], 320, 192),  # tallest tile 128: pairs fill 512 columns
+    ([32, 32, 17, 31, 16, 32, 30, 10], 320, 192),   # tallest tile 32: the smallest paired
+    ([128, 120, 33, 1, 0, 96, 65, 113], 256, 128),  # weight tiles in even counts
+    ([31, 31, 17, 31, 16, 31, 30, 13], 320, 192),   # tallest tile 31 (32 rows): paired
+    ([129, 128, 200, 230, 1, 0, 150, 200], 320, 192)])  # no expert past 256: 128-token split
+@pytest.mark.parametrize("max_ctas", [0, 8])
+def test_expert_forward_weight_tile_pairs(counts, d, f, max_ctas):
+    """Row tiles of 32 to 128 tokens, where a unit of the tensor-core kernel takes two weight
+    tiles that share the token rows: an odd number of weight tiles per phase (f = 192: 3
+    tiles of 64 gate/up rows; d = 320: 3 tiles of 128 down rows, the last one 64 rows), so
+    the last unit of each row tile holds one tile; the tallest tile at 128 tokens, where
+    the second accumulator's second half ends at the last TMEM column; experts of 129-256
+    tokens in two tiles of at most 128 (an expert of 128 tokens keeps one tile of 128,
+    taller than the 65 + 64 of its neighbour of 129); every row against the oracle. On 8
+    CTAs the kernel pairs at any number of units; on every SM these few units stay single
+    (both must agree with the oracle)."""
+    shape = W.LayerShape(d=d, E=8, k=2, f=f, dtype="bf16")
+    R = sum(counts) // 2
+    L = _desc(shape)
+    wg, wu, wd = _weights(shape, 55)
+    x = W.hidden_states(56, np.arange(-1, R - 1, dtype=np.int32), shape.d, torch.bfloat16)
+    idx = _assignments_with_counts(counts, R, 2)
+    gates = W.random_gates(57, R, 2)
+    y = torch.full((R, shape.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = M.workspace(L, 1, R)
+    M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, torch.from_numpy(idx).to(DEV),
+                         torch.from_numpy(gates).to(DEV), y, ws,
+                         M.run_opts(M.MOE_FFN_TCGEN05, ffn_max_ctas=max_ctas))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64))
+    _assert_close_rows(y.float().cpu().numpy(), ref, shape)
+
+
+@pytest.mark.parametrize("seed,max_ctas", [(0, 0), (15, 0), (0, 16)])
+def test_one_tree_of_256_nodes_with_hot_experts(seed, max_ctas):
+    """One tree of 256 nodes over 8 experts, top-2 (the selection cluster's own permute step
+    builds the row tiles): experts of 140-173 tokens split in two near-equal tiles of at most
+    128 tokens, which the tensor-core kernel on 16 CTAs runs in weight-tile pairs; counts,
+    offsets and every row of y against the oracle."""
+    shape = W.LayerShape(d=256, E=8, k=2, f=192, dtype="bf16")
+    N, E, k = 256, 8, 2
+    parent, depth = _tree_of(N, 70000 + seed)
+    x = W.hidden_states(71000 + seed, parent, shape.d, torch.bfloat16)
+    wr = W.router_weight(72000 + seed, shape, std=0.3)
+    wg, wu, wd = _weights(shape, 73)
+    L = _desc(shape)
+    P = M.select_params(M.MOE_ROUTE_NATURAL, W.C_EAGLE)
+    out = dict(logits=torch.empty(N, E, device=DEV),
+               topk_idx=torch.empty(N, k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(N, k, device=DEV),
+               eligible=torch.empty(1, E, dtype=torch.uint8, device=DEV),
+               info=torch.empty(1, NF, dtype=torch.int32, device=DEV),
+               counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV))
+    y = torch.full((N, shape.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = M.workspace(L, 1, N)
+    M.moe_tree_forward(L, P, x.to(DEV), wr.to(DEV), wg, wu, wd, None,
+                       torch.from_numpy(depth.astype(np.int32)).to(DEV), 1, N, None, y, ws,
+                       M.tree_outputs(**out),
+                       M.run_opts(M.MOE_FFN_TCGEN05, ffn_max_ctas=max_ctas))
+    _sync()
+    assert M.moe_workspace_check(ws) == 0
+    got = {key: v.cpu().numpy() for key, v in out.items()}
+    assert 128 < got["counts"].max() <= 256  # the case this test is for
+    rc, ro, _ = O.permute(got["topk_idx"], E)
+    np.testing.assert_array_equal(got["counts"], rc)
+    np.testing.assert_array_equal(got["offsets"], ro)
+    ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), got["topk_idx"], got["gates"])
     _assert_close_rows(y.float().cpu().numpy(), ref, shape)
 
 
