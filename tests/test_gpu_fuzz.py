@@ -12,7 +12,9 @@ for fp32). The cases cover expert counts that are not multiples of 32, k from 1 
 blocks of one to three trees and trees of 2 to 65 nodes. A second set draws blocks of 4 to
 80 trees of one random shape (up to ~5000 rows), with the router and y checked on sampled
 rows. A third set draws tree sizes from 1 to 1000 nodes, blocks of up to 100 trees, layer
-widths in steps of 64, and the pre-norm and residual options. Two more sets draw offloaded
+widths in steps of 64, and the pre-norm and residual options. In these three sets half the
+cases hold the tensor-core expert kernel to 8-151 CTAs, where it pairs weight tiles over
+row tiles of 32-128 tokens at any number of units. Two more sets draw offloaded
 layers (against the resident layer, bit for bit) and draft selections (against the oracle),
 and a last set routes junk expert ids through the experts.
 """
@@ -39,6 +41,14 @@ def _lib():
     M.lib()
 
 
+def _cta_cap(rng):
+    """The tensor-core expert kernel's CTA cap for a case: half the cases run on 8-151 CTAs,
+    where the kernel takes weight-tile pairs at any number of units (on every SM the few
+    units of a small layer stay single), the rest on one CTA per SM. Drawn last, so the
+    other draws of a seed stay as they were."""
+    return int(rng.integers(8, 152)) if rng.random() < 0.5 else 0
+
+
 def _draw(seed):
     rng = np.random.default_rng(7000 + seed)
     dtype = "bf16" if rng.random() < 0.7 else "fp32"
@@ -60,9 +70,10 @@ def _draw(seed):
     min_set = int(rng.integers(k, max(k, 20) + 1))
     budget = int(rng.integers(0, 10))
     resident = (rng.random(E) < 0.5).astype(np.uint8)
+    cap = _cta_cap(rng)
     return dict(dtype=dtype, d=d, f=f, E=E, k=k, B=B, steps=steps, topk=topk, tokens=tokens,
                 mode=mode, anchor=anchor, prune=prune, std=std, path=path, fixed_B=fixed_B,
-                min_set=min_set, budget=budget, resident=resident)
+                min_set=min_set, budget=budget, resident=resident, cap=cap)
 
 
 @pytest.mark.parametrize("seed", list(range(64)))
@@ -98,7 +109,7 @@ def test_random_layer_against_oracle(seed):
     ws = M.workspace(L, B, N)
     M.moe_tree_forward(L, P, x.to(DEV), wr, wg, wu, wd, None,
                        torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
-                       M.tree_outputs(**out), M.run_opts(c["path"]))
+                       M.tree_outputs(**out), M.run_opts(c["path"], ffn_max_ctas=c["cap"]))
     torch.cuda.synchronize()
     assert M.moe_workspace_check(ws) == 0
     got = {key: v.cpu().numpy() for key, v in out.items()}
@@ -142,7 +153,8 @@ def _draw_large(seed):
                 mode=mode, anchor=bool(rng.random() < 0.8), prune=prune,
                 std=float(rng.choice([0.02, 0.1, 0.3])),
                 fixed_B=int(rng.integers(k, E + 1)), min_set=int(rng.integers(k, max(k, 24) + 1)),
-                budget=int(rng.integers(0, 10)), resident=(rng.random(E) < 0.5).astype(np.uint8))
+                budget=int(rng.integers(0, 10)), resident=(rng.random(E) < 0.5).astype(np.uint8),
+                cap=_cta_cap(rng))
 
 
 @pytest.mark.parametrize("seed", list(range(48)))
@@ -180,7 +192,7 @@ def test_random_large_block_against_oracle(seed):
     ws = M.workspace(L, B, N)
     M.moe_tree_forward(L, P, x.to(DEV), wr, wg, wu, wd, None,
                        torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
-                       M.tree_outputs(**out), M.run_opts(M.MOE_FFN_AUTO))
+                       M.tree_outputs(**out), M.run_opts(M.MOE_FFN_AUTO, ffn_max_ctas=c["cap"]))
     torch.cuda.synchronize()
     assert M.moe_workspace_check(ws) == 0
     got = {key: v.cpu().numpy() for key, v in out.items()}
@@ -225,7 +237,8 @@ def _draw_wide(seed):
                 fixed_B=int(rng.integers(k, E + 1)), min_set=int(rng.integers(k, max(k, 24) + 1)),
                 budget=int(rng.integers(0, 10)), resident=(rng.random(E) < 0.5).astype(np.uint8),
                 norm=bool(rng.random() < 0.3), residual=bool(rng.random() < 0.3),
-                path=M.MOE_FFN_SIMT if (dtype == "fp32" or rng.random() < 0.15) else M.MOE_FFN_AUTO)
+                path=M.MOE_FFN_SIMT if (dtype == "fp32" or rng.random() < 0.15) else M.MOE_FFN_AUTO,
+                cap=_cta_cap(rng))
 
 
 @pytest.mark.parametrize("seed", list(range(48)))
@@ -264,7 +277,8 @@ def test_random_tree_sizes_and_options(seed):
     M.moe_tree_forward(L, P, xd, wr, wg, wu, wd, None,
                        torch.from_numpy(depth.reshape(-1).copy()).to(DEV), B, N, res, y, ws,
                        M.tree_outputs(**out),
-                       M.run_opts(c["path"], residual=c["residual"], norm_input=c["norm"]))
+                       M.run_opts(c["path"], residual=c["residual"], norm_input=c["norm"],
+                                  ffn_max_ctas=c["cap"]))
     torch.cuda.synchronize()
     assert M.moe_workspace_check(ws) == 0
     got = {key: v.cpu().numpy() for key, v in out.items()}
