@@ -659,11 +659,14 @@ def _assignments_with_counts(counts, R, k):
     [256, 257, 384, 385, 700, 17, 0, 201],     # one tile of 256, equal tiles from 257 on
     [16, 300, 1000, 384, 96, 368, 0, 36],      # a hot expert in four tiles
     [256, 1, 512, 1, 255, 1, 510, 0]])         # full tiles next to one-token tiles
-def test_expert_forward_exact_expert_loads(counts):
+@pytest.mark.parametrize("max_ctas", [0, 8])
+def test_expert_forward_exact_expert_loads(counts, max_ctas):
     """Experts with exactly the given numbers of tokens on the tensor-core path, around the
     256-token row-tile limit: a full 256-token tile (N = 256), experts of 257 tokens and
     more in near-equal tiles that share their weight loads, a hot expert in four tiles,
-    one-token tiles, an expert with no tokens; every row against the oracle."""
+    one-token tiles, an expert with no tokens; every row against the oracle, on every SM
+    and on 8 CTAs (where the kernel's unit-count rule for weight-tile pairs no longer holds
+    back: only the tile heights do)."""
     shape = W.LayerShape(d=256, E=8, k=2, f=192, dtype="bf16")
     R = sum(counts) // 2
     L = _desc(shape)
@@ -674,7 +677,8 @@ def test_expert_forward_exact_expert_loads(counts):
     y = torch.full((R, shape.d), float("nan"), dtype=torch.bfloat16, device=DEV)
     ws = M.workspace(L, 1, R)
     M.moe_expert_forward(L, x.to(DEV), wg, wu, wd, None, torch.from_numpy(idx).to(DEV),
-                         torch.from_numpy(gates).to(DEV), y, ws, M.run_opts(M.MOE_FFN_TCGEN05))
+                         torch.from_numpy(gates).to(DEV), y, ws,
+                         M.run_opts(M.MOE_FFN_TCGEN05, ffn_max_ctas=max_ctas))
     _sync()
     assert M.moe_workspace_check(ws) == 0
     ref = O.moe_combine(x, wg.cpu(), wu.cpu(), wd.cpu(), idx, gates.astype(np.float64))
