@@ -23,15 +23,19 @@
 //   warp 1       TMEM allocator and MMA issuer (one lane)
 //   warps 2..9   epilogue, two teams of four (warps 2-5, 6-9) taking alternate
 //                16-column chunks of the accumulator: tcgen05.ld (each warp may read
-//                the 32 TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O
+//                the 32 TMEM lanes of its quadrant, warp % 4), apply SwiGLU or store O;
+//                each warp turns its 32 outputs x 16 tokens around in a 1 KB staging
+//                buffer and writes them as 16-byte pieces of the output rows
 // At the start the epilogue warps copy the row-tile list (expert, first permuted row,
 // tokens, slot) into shared memory, so looking up a unit between two units costs no
 // global round trip. Two 256-column accumulators alternate so the epilogue of one unit
 // overlaps the MMAs of the next. A unit is one weight tile x one row tile (<= 256
-// tokens of one expert); when every row tile of a launch has 32 to 128 tokens a unit is
-// two weight tiles x one row tile instead, whose two MMAs per k-step share the stage's
-// token rows and fill the two 128-column halves of one accumulator, so each token row
-// crosses into shared memory half as often. A phase-2 unit needs the whole h of its row
+// tokens of one expert); when every row tile of a launch has 32 or more tokens (and the
+// launch has enough units per CTA) a unit is two weight tiles x one row tile instead,
+// whose two MMAs per k-step share the stage's token rows, so each token row crosses into
+// shared memory half as often: tiles of up to 128 tokens fill the two 128-column halves of
+// one accumulator (two units still alternate), taller tiles one accumulator each (each
+// epilogue team then stores one tile). A phase-2 unit needs the whole h of its row
 // tile: the epilogue that finishes a phase-1 unit publishes it with a release increment of
 // the row tile's counter, and the producer of a phase-2 unit waits for the count with acquire loads
 // before its TMA reads h. Tickets are handed out in order, so every phase-1 unit is
@@ -61,6 +65,7 @@ constexpr uint32_t kABytes = kM * kBK * 2;  // 16 KB weight tile per stage
 constexpr int kBoxes = 16;                  // token-row boxes of 16, 32, 48, ..., 256 rows
 constexpr int kSgStride = 17;               // padded row of the silu(gate) exchange buffer
 constexpr int kSgFloats = 64 * kSgStride;   // one buffer; two per team (double-buffered)
+constexpr int kStageBytes = 16 * 64;        // per epilogue warp: 16 tokens x 32 bf16 outputs
 constexpr int kMaxStages = 12;              // pipeline stages at most
 constexpr int kCtlBytes = 512;              // barriers and slots (16 * kMaxStages + 152 bytes)
 
@@ -80,6 +85,8 @@ struct Params {
     int slots;     // expert slots in the weight pool
     int pair_min;    // row-tile heights from this up to 128 tokens take weight-tile pairs,
     int pair_units;  // when the launch has at least this many single-tile units per CTA
+    int pair_max;    // tallest row tile that takes pairs (up to 128 tokens: the halves of one
+                     // accumulator; up to 256: one accumulator per tile, both for one unit)
     const int *rowtiles, *slot;
     const uint8_t *pass;  // experts computed by this launch (null: all)
     int *flags;
@@ -102,6 +109,29 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Stores one warp's outputs of a 16-token chunk. Lane l holds output column col0 + l of
+// tokens c0 .. c0 + 15 (val[c], fp32); the warp writes them, rounded to bf16, into its
+// staging buffer in token-major order and reads them back as 16-byte pieces (token c,
+// columns col0 + 8 g .. + 8), so each store instruction writes 8 tokens x 64 contiguous
+// bytes instead of one 2-byte element per lane. out points at token c0's row, column col0;
+// ld is the row stride in elements; tokens from `left` on, or a column block past the
+// output's width (cols_ok false), are not written.
+__device__ __forceinline__ void store_chunk(uint8_t *stg, const float (&val)[16], int lane,
+                                            __nv_bfloat16 *out, size_t ld, int left,
+                                            bool cols_ok) {
+    __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(stg);
+    __syncwarp();  // the previous chunk's reads of the buffer are done
+#pragma unroll
+    for (int c = 0; c < 16; ++c) sb[c * 32 + lane] = __float2bfloat16_rn(val[c]);
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int piece = h * 32 + lane, c = piece >> 2, g = piece & 3;
+        const uint4 v = *reinterpret_cast<const uint4 *>(stg + c * 64 + g * 16);
+        if (cols_ok && c < left) *reinterpret_cast<uint4 *>(out + (size_t)c * ld + g * 8) = v;
+    }
 }
 
 struct Unit {
@@ -199,7 +229,10 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     volatile int *queue = ints + 6;     // [kQ]
     const uint32_t tbl_bar = ctl_s + 16 * kMaxStages + 144;  // the row-tile table is filled
     float *sg_all = reinterpret_cast<float *>(ctl + kCtlBytes);  // [team][2][64][kSgStride]
-    int4 *tbl = reinterpret_cast<int4 *>(sg_all + 2 * 2 * kSgFloats);  // [tbl_cap]
+    // per epilogue warp, its outputs of one 16-token chunk in token-major order, so that
+    // they leave for global memory as 16-byte pieces of the output rows
+    uint8_t *stage_all = reinterpret_cast<uint8_t *>(sg_all + 2 * 2 * kSgFloats);
+    int4 *tbl = reinterpret_cast<int4 *>(stage_all + kEpiWarps * kStageBytes);  // [tbl_cap]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -243,20 +276,26 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     const int n_rt = p.rowtiles[0];
     // the ring: as many stages as fit of W 16 KB weight tiles + a token buffer of the
     // row-tile height (every row tile of this launch has at most that many tokens). With
-    // row tiles of pair_min to 128 tokens a unit takes two weight tiles (W = 2): two MMAs
-    // per k-step read the same token tile into the two halves of one accumulator, so the
-    // token rows cross into shared memory once per two weight tiles. Only with enough units
-    // per CTA: a small union in units twice as long leaves CTAs idle at the end.
+    // row tiles of pair_min to pair_max tokens a unit takes two weight tiles (W = 2): two
+    // MMAs per k-step read the same token tile, so the token rows cross into shared memory
+    // once per two weight tiles. Only with enough units per CTA: a small union in units
+    // twice as long leaves CTAs idle at the end.
     const int height = p.rowtiles[1];
     const uint32_t b_bytes = (uint32_t)height * 128u;
-    const uint32_t ring = (base + kCtlBytes + 2 * 2 * kSgFloats * 4 +
+    const uint32_t ring = (base + kCtlBytes + 2 * 2 * kSgFloats * 4 + kEpiWarps * kStageBytes +
                            (uint32_t)p.tbl_cap * 16u + 1023u) & ~1023u;
     const uint32_t avail = raw + (uint32_t)p.smem - ring;
-    const int W = (p.pair_min > 0 && height >= p.pair_min && height <= kAccCols / 2 &&
+    const int W = (p.pair_min > 0 && height >= p.pair_min && height <= p.pair_max &&
                    n_rt * (p.mt1 + p.mt2) >= p.pair_units * (int)gridDim.x &&
                    avail >= 2u * (2u * kABytes + b_bytes))
                       ? 2
                       : 1;
+    // accumulators in rotation and the column offset of a unit's second weight tile: pairs
+    // over tiles of up to 128 tokens share one 256-column accumulator and two units
+    // alternate; taller pairs take both accumulators, so a unit's MMAs wait for the
+    // previous unit's epilogue (the ring keeps filling meanwhile)
+    const int nacc = (W == 2 && height > kAccCols / 2) ? 1 : 2;
+    const uint32_t sub_cols = nacc == 1 ? (uint32_t)kAccCols : (uint32_t)(kAccCols / 2);
     const uint32_t a_bytes = (uint32_t)W * kABytes;  // weight bytes of a stage
     const int S = max(1, min(kMaxStages, (int)(avail / (a_bytes + b_bytes))));
     const uint32_t sA = ring, sB = ring + (uint32_t)S * a_bytes;
@@ -367,8 +406,8 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                 if (u < 0) break;
                 Unit w;
                 if (decode(p, U1, u, W, w, tbl) != 0) continue;
-                const int acc = it & 1;
-                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                const int acc = nacc == 2 ? it & 1 : 0;
+                const uint32_t aph = (uint32_t)(nacc == 2 ? it >> 1 : it) & 1u;
                 ++it;
                 if (!mbar_wait(tempty + 8 * acc, aph ^ 1u, abort_flag, p.flags)) break;
                 tc_fence_after();
@@ -382,12 +421,12 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     }
                     tc_fence_after();
                     const uint32_t b = sB + (uint32_t)s * b_bytes;
-                    // weight tile t of the unit accumulates into columns [128 t, 128 t + N)
+                    // weight tile t of the unit accumulates into columns [t sub_cols, + N)
                     for (int t = 0; t < w.nm; ++t) {
                         const uint32_t a = sA + (uint32_t)s * a_bytes + (uint32_t)t * kABytes;
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
-                            mma_bf16(d_tmem + (uint32_t)t * (kAccCols / 2), sw128_desc(a + 32u * k),
+                            mma_bf16(d_tmem + (uint32_t)t * sub_cols, sw128_desc(a + 32u * k),
                                      sw128_desc(b + 32u * k), idesc, (kc | k) != 0);
                     }
                     mma_issued = true;
@@ -406,6 +445,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
         const int team = (warp - 2) >> 2;  // epilogue team: warps 2-5 or 6-9
         const int row = q * 32 + lane;     // accumulator row
         float *sg = sg_all + team * 2 * kSgFloats;
+        uint8_t *stg = stage_all + (warp - 2) * kStageBytes;
         int it = 0, qs = 0, turn = 0;
         uint32_t qph = 0;
         for (;; turn ^= 1) {
@@ -429,8 +469,8 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (u < 0) break;
             Unit w;
             if (decode(p, U1, u, W, w, tbl) != 0) continue;
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            const int acc = nacc == 2 ? it & 1 : 0;
+            const uint32_t aph = (uint32_t)(nacc == 2 ? it >> 1 : it) & 1u;
             ++it;
             if (threadIdx.x == 64)
                 epi_ok[acc] = mbar_wait(tfull + 8 * acc, aph, abort_flag, p.flags);
@@ -443,7 +483,7 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int sub = W == 2 ? team : 0;           // the weight tile this team stores
             const int c_first = W == 2 ? 0 : team * 16, c_step = W == 2 ? 16 : 32;
             const int m = w.m + sub;
-            const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols + sub * (kAccCols / 2)) +
+            const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + (uint32_t)sub * sub_cols +
                                    ((uint32_t)(q * 32) << 16);
             const size_t row0 = (size_t)w.row0;
             if (w.phase == 1) {
@@ -466,40 +506,40 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     team_bar(team);
                     if (q >= 2) {
                         const int i = row - 64;
-                        __nv_bfloat16 *hp = p.h + row0 * p.f + (size_t)m * 64 + i;
+                        float hv[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int tok = c0 + c;
-                            if (tok < w.ntok)
-                                hp[(size_t)tok * p.f] = __float2bfloat16_rn(
-                                    buf[i * kSgStride + c] * __uint_as_float(v[c]));
-                        }
+                        for (int c = 0; c < 16; ++c)
+                            hv[c] = buf[i * kSgStride + c] * __uint_as_float(v[c]);
+                        store_chunk(stg, hv, lane,
+                                    p.h + (row0 + (size_t)c0) * p.f + (size_t)m * 64 + (q - 2) * 32,
+                                    (size_t)p.f, w.ntok - c0, true);
                     }
                 }
-                // every h store of this unit precedes this barrier: publish them
+                // the accumulator is read: hand it back to the MMA issuer first, then
+                // publish h (every h store of this unit precedes the barrier)
+                tc_fence_before();
+                mbar_arrive(tempty + 8 * acc);
                 epi_bar();
                 if (threadIdx.x == 64) {
                     __threadfence();
                     atomicAdd(p.sched + 1 + w.rt, w.nm);
                 }
             } else {
-                const int drow = m * kM + row;
+                // this warp's 32 output columns: all inside d or all past it (d is a
+                // multiple of 64)
+                const int col0 = m * kM + q * 32;
                 for (int c0 = c_first; sub < w.nm && c0 < N; c0 += c_step) {
                     uint32_t v[16];
                     tmem_ld16(taddr + (uint32_t)c0, v);
-                    if (drow < p.d) {
-                        __nv_bfloat16 *op = p.o + row0 * p.d + drow;
+                    float ov[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int tok = c0 + c;
-                            if (tok < w.ntok)
-                                op[(size_t)tok * p.d] = __float2bfloat16_rn(__uint_as_float(v[c]));
-                        }
-                    }
+                    for (int c = 0; c < 16; ++c) ov[c] = __uint_as_float(v[c]);
+                    store_chunk(stg, ov, lane, p.o + (row0 + (size_t)c0) * p.d + col0,
+                                (size_t)p.d, w.ntok - c0, col0 < p.d);
                 }
+                tc_fence_before();
+                mbar_arrive(tempty + 8 * acc);
             }
-            tc_fence_before();
-            mbar_arrive(tempty + 8 * acc);
         }
     }
 
@@ -588,15 +628,18 @@ int sm_count() {
 
 // Shared memory besides the ring and the table: alignment slack, control block,
 // exchange buffers.
-constexpr size_t kFixedSmem = 1024 + kCtlBytes + 2 * 2 * kSgFloats * sizeof(float);
+constexpr size_t kFixedSmem =
+    1024 + kCtlBytes + 2 * 2 * kSgFloats * sizeof(float) + kEpiWarps * kStageBytes;
 constexpr size_t kSmemBudget = 227 * 1024;
-// Row tiles of at least this many tokens (and at most 128) take weight-tile pairs: below
-// it the token rows are a small part of a stage and single tiles balance the CTAs better.
+// Row tiles of at least kPairMinRows tokens (and at most kPairMaxRows) take weight-tile
+// pairs: below it the token rows are a small part of a stage and single tiles balance the
+// CTAs better.
 // A launch on every SM pairs only with this many single-tile units per CTA (a union of ~26
 // experts of the Qwen3-shaped layer has about 5, and units twice as long would leave CTAs
 // idle at the end); a launch held to fewer CTAs runs beside other work, which fills the
 // SMs its CTAs leave at the end, and pairs at any unit count.
 constexpr int kPairMinRows = 32;
+constexpr int kPairMaxRows = 256;
 constexpr int kPairMinUnitsPerCta = 8;
 
 }  // namespace
@@ -623,7 +666,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     const size_t two_stages =
         2 * std::max(kABytes + (size_t)box_cap * 128,
                      box_cap >= kPairMinRows
-                         ? 2 * kABytes + (size_t)std::min(box_cap, kAccCols / 2) * 128
+                         ? 2 * kABytes + (size_t)std::min(box_cap, kPairMaxRows) * 128
                          : 0);
     const int tbl_cap = (int)std::min<size_t>((size_t)max_rowtiles(a.E, A),
                                               (kSmemBudget - kFixedSmem - two_stages) / 16);
@@ -662,6 +705,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s) {
     p.slots = S;
     p.pair_min = kPairMinRows;
     p.pair_units = a.max_ctas > 0 && a.max_ctas < nsm ? 0 : kPairMinUnitsPerCta;
+    p.pair_max = kPairMaxRows;
     p.rowtiles = a.rowtiles;
     p.slot = a.slot;
     p.pass = a.pass;

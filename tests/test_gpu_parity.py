@@ -665,8 +665,8 @@ def test_expert_forward_exact_expert_loads(counts, max_ctas):
     256-token row-tile limit: a full 256-token tile (N = 256), experts of 257 tokens and
     more in near-equal tiles that share their weight loads, a hot expert in four tiles,
     one-token tiles, an expert with no tokens; every row against the oracle, on every SM
-    and on 8 CTAs (where the kernel's unit-count rule for weight-tile pairs no longer holds
-    back: only the tile heights do)."""
+    and on 8 CTAs, where these few units take weight-tile pairs (one accumulator per tile of
+    the pair over tiles taller than 128 tokens)."""
     shape = W.LayerShape(d=256, E=8, k=2, f=192, dtype="bf16")
     R = sum(counts) // 2
     L = _desc(shape)
