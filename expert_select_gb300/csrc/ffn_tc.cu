@@ -34,13 +34,15 @@
 // launch has enough units per CTA) a unit is two weight tiles x one row tile instead,
 // whose two MMAs per k-step share the stage's token rows, so each token row crosses into
 // shared memory half as often: tiles of up to 128 tokens fill the two 128-column halves of
-// one accumulator (two units still alternate), taller tiles one accumulator each (each
-// epilogue team then stores one tile). A phase-2 unit needs the whole h of its row
-// tile: the epilogue that finishes a phase-1 unit publishes it with a release increment of
-// the row tile's counter, and the producer of a phase-2 unit waits for the count with acquire loads
-// before its TMA reads h. Tickets are handed out in order, so every phase-1 unit is
-// owned by a running CTA before any CTA waits on one: no deadlock even when fewer CTAs
-// than SMs are resident.
+// one accumulator (two units still alternate), taller tiles one accumulator each. In
+// phase 1 a pair's first MMA takes the 128 gate rows of both weight tiles and the second
+// their 128 up rows, so every TMEM lane holds a gate row and its up row and each warp
+// forms h alone; in phase 2 each epilogue team stores one tile. A phase-2 unit needs the
+// whole h of its row tile: the epilogue that finishes a phase-1 unit publishes it with a
+// release increment of the row tile's counter, and the producer of a phase-2 unit waits
+// for the count with acquire loads before its TMA reads h. Tickets are handed out in
+// order, so every phase-1 unit is owned by a running CTA before any CTA waits on one: no
+// deadlock even when fewer CTAs than SMs are resident.
 //
 // Every wait is bounded: after 2 s a wait gives up, sets the workspace check bit
 // FLAG_WAIT_TIMEOUT and makes the CTA stop; the CTA then waits (again bounded) for
@@ -228,11 +230,13 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     volatile int *epi_u = ints + 4;     // [2]
     volatile int *queue = ints + 6;     // [kQ]
     const uint32_t tbl_bar = ctl_s + 16 * kMaxStages + 144;  // the row-tile table is filled
-    float *sg_all = reinterpret_cast<float *>(ctl + kCtlBytes);  // [team][2][64][kSgStride]
     // per epilogue warp, its outputs of one 16-token chunk in token-major order, so that
     // they leave for global memory as 16-byte pieces of the output rows
-    uint8_t *stage_all = reinterpret_cast<uint8_t *>(sg_all + 2 * 2 * kSgFloats);
+    uint8_t *stage_all = ctl + kCtlBytes;
     int4 *tbl = reinterpret_cast<int4 *>(stage_all + kEpiWarps * kStageBytes);  // [tbl_cap]
+    // the silu(gate) exchange buffers, [team][2][64][kSgStride]: only launches of single
+    // weight tiles have them (a pair keeps gate and up in the same TMEM lanes)
+    float *sg_all = reinterpret_cast<float *>(tbl + p.tbl_cap);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -282,14 +286,16 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     // twice as long leaves CTAs idle at the end.
     const int height = p.rowtiles[1];
     const uint32_t b_bytes = (uint32_t)height * 128u;
-    const uint32_t ring = (base + kCtlBytes + 2 * 2 * kSgFloats * 4 + kEpiWarps * kStageBytes +
-                           (uint32_t)p.tbl_cap * 16u + 1023u) & ~1023u;
-    const uint32_t avail = raw + (uint32_t)p.smem - ring;
+    const uint32_t pre = base + kCtlBytes + kEpiWarps * kStageBytes + (uint32_t)p.tbl_cap * 16u;
+    const uint32_t end = raw + (uint32_t)p.smem;
+    const uint32_t ring2 = (pre + 1023u) & ~1023u;
     const int W = (p.pair_min > 0 && height >= p.pair_min && height <= p.pair_max &&
                    n_rt * (p.mt1 + p.mt2) >= p.pair_units * (int)gridDim.x &&
-                   avail >= 2u * (2u * kABytes + b_bytes))
+                   end - ring2 >= 2u * (2u * kABytes + b_bytes))
                       ? 2
                       : 1;
+    const uint32_t ring = W == 2 ? ring2 : (pre + 2 * 2 * kSgFloats * 4 + 1023u) & ~1023u;
+    const uint32_t avail = end - ring;
     // accumulators in rotation and the column offset of a unit's second weight tile: pairs
     // over tiles of up to 128 tokens share one 256-column accumulator and two units
     // alternate; taller pairs take both accumulators, so a unit's MMAs wait for the
@@ -367,17 +373,29 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                         break;
                     }
                     const uint32_t fb = full + 8 * s;
-                    mbar_expect_tx(fb, (uint32_t)w.nm * kABytes + bb);
-                    for (int t = 0; t < w.nm; ++t) {
-                        const uint32_t a = sA + (uint32_t)s * a_bytes + (uint32_t)t * kABytes;
-                        const int m = w.m + t;
-                        if (w.phase == 1) {
-                            tma_load_3d(a, &maps.wg, kc * kBK, m * 64, w.slot, fb, pol);
-                            tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, m * 64, w.slot, fb,
-                                        pol);
-                        } else {
-                            tma_load_3d(a, &maps.wd, kc * kBK, m * kM, w.slot, fb, pol);
-                        }
+                    const uint32_t a = sA + (uint32_t)s * a_bytes;
+                    if (w.phase == 1 && W == 2) {
+                        // a pair: the gate rows of both tiles (128) in the stage's first
+                        // tile, their up rows in the second; a missing second tile (past f)
+                        // reads as zeros
+                        mbar_expect_tx(fb, 2u * kABytes + bb);
+                        tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
+                        tma_load_3d(a + kABytes / 2, &maps.wg, kc * kBK, w.m * 64 + 64, w.slot,
+                                    fb, pol);
+                        tma_load_3d(a + kABytes, &maps.wu, kc * kBK, w.m * 64, w.slot, fb, pol);
+                        tma_load_3d(a + kABytes + kABytes / 2, &maps.wu, kc * kBK,
+                                    w.m * 64 + 64, w.slot, fb, pol);
+                    } else if (w.phase == 1) {
+                        // one tile: 64 gate rows over the same 64 up rows
+                        mbar_expect_tx(fb, kABytes + bb);
+                        tma_load_3d(a, &maps.wg, kc * kBK, w.m * 64, w.slot, fb, pol);
+                        tma_load_3d(a + kABytes / 2, &maps.wu, kc * kBK, w.m * 64, w.slot, fb,
+                                    pol);
+                    } else {
+                        mbar_expect_tx(fb, (uint32_t)w.nm * kABytes + bb);
+                        for (int t = 0; t < w.nm; ++t)
+                            tma_load_3d(a + (uint32_t)t * kABytes, &maps.wd, kc * kBK,
+                                        (w.m + t) * kM, w.slot, fb, pol);
                     }
                     tma_load_2d(sB + (uint32_t)s * b_bytes, bmap, kc * kBK, brow, fb);
                     issued |= 1u << s;
@@ -421,8 +439,10 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
                     }
                     tc_fence_after();
                     const uint32_t b = sB + (uint32_t)s * b_bytes;
-                    // weight tile t of the unit accumulates into columns [t sub_cols, + N)
-                    for (int t = 0; t < w.nm; ++t) {
+                    // tile t of the stage accumulates into columns [t sub_cols, + N): in phase
+                    // 1 of a pair the gate and the up rows, else weight tile m + t
+                    const int ntiles = (W == 2 && w.phase == 1) ? 2 : w.nm;
+                    for (int t = 0; t < ntiles; ++t) {
                         const uint32_t a = sA + (uint32_t)s * a_bytes + (uint32_t)t * kABytes;
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
@@ -486,7 +506,33 @@ ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
             const uint32_t taddr = tmem + (uint32_t)(acc * kAccCols) + (uint32_t)sub * sub_cols +
                                    ((uint32_t)(q * 32) << 16);
             const size_t row0 = (size_t)w.row0;
-            if (w.phase == 1) {
+            if (w.phase == 1 && W == 2) {
+                // a pair: lane r of the accumulator holds gate row w.m * 64 + r in the first
+                // tile's columns and the same up row in the second's, so each warp forms
+                // h for its 32 rows by itself; the teams take alternate 16-token chunks
+                const uint32_t tg = tmem + (uint32_t)(acc * kAccCols) + ((uint32_t)(q * 32) << 16);
+                const int frow = w.m * 64 + q * 32;  // this warp's first h column
+                for (int c0 = team * 16; c0 < N; c0 += 32) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tg + (uint32_t)c0, g);
+                    tmem_ld16(tg + sub_cols + (uint32_t)c0, u);
+                    float hv[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float gv = __uint_as_float(g[c]);
+                        hv[c] = __fdividef(gv, 1.f + __expf(-gv)) * __uint_as_float(u[c]);
+                    }
+                    store_chunk(stg, hv, lane, p.h + (row0 + (size_t)c0) * p.f + frow,
+                                (size_t)p.f, w.ntok - c0, frow < p.f);
+                }
+                tc_fence_before();
+                mbar_arrive(tempty + 8 * acc);
+                epi_bar();
+                if (threadIdx.x == 64) {
+                    __threadfence();
+                    atomicAdd(p.sched + 1 + w.rt, w.nm);
+                }
+            } else if (w.phase == 1) {
                 // within a team the gate warps (quadrants 0, 1) hand silu(gate) to the up
                 // warps (quadrants 2, 3) through a double-buffered exchange buffer: one
                 // team barrier per chunk (a buffer is rewritten two chunks later, after
