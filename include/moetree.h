@@ -211,8 +211,10 @@ moe_status moe_expert_permute(const moe_layer_desc *L, const int *topk_idx, int 
  * decoding" blog, "grouped GEMM for active experts" and "unpermute + weighted
  * combine"): y[r] = sum_j gates[r, j] W_down[e] (silu(W_gate[e] x_r) * (W_up[e] x_r)),
  * e = topk_idx[r, j], slots summed in ascending j. Each expert with at least one
- * assignment streams its weights from HBM once per launch (a token count above 256
- * re-streams them once per 256 tokens).
+ * assignment streams its weights from HBM once per launch; an expert with more tokens
+ * than one row tile holds (128 when no expert of the call has more than 256, else 256)
+ * takes several row tiles, which read each weight tile at the same time, so their repeat
+ * reads mostly hit L2.
  *   x [R, d] device; y [R, d] device, layer dtype.
  *   W_gate, W_up [S, f, d] and W_down [S, d, f] device: a pool of S = L->slots (or E)
  *   expert slots.
